@@ -1,0 +1,534 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized projection path on GB300.
+
+Default run (N = 1): the 27B-class decode layer at B = 1 (hidden 5120; q, k,
+v, o projections, paired gate/up 5120 -> 2x17408, down 17408 -> 5120, each
+input produced by the fused RMSNorm + Q8_1 kernel) -- reported as HBM GB/s --
+and the same layer's 512-token prefill (all seven projections through the
+tensor-core GEMM) -- reported as effective int8-op TOPS -- in one JSON line.
+
+A step is one pass of the whole path over one batch: every RMSNorm+Q8_1 and
+every projection of the layer.  Inputs are synthetic (seeded generators of
+gemm_zq_rmsnorm_gb300.inputs), resident in HBM before timing.  L2 (129 MB)
+is defeated by rotating distinct copies of the weights (>= 3x L2 per
+rotation).  Steps are replayed from CUDA graphs; timing is CUDA events on the
+launching stream, W warm-up steps, K timed steps, max over ranks.
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_zq_rmsnorm_gb300 import inputs  # noqa: E402
+
+METRIC = "Q4_K GEMV HBM GB/s (B=1) & GEMM int8 TOPS (B=512), % of GB300 roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+def input_key(pname):
+    """Projections that read the same normalised input share one RMSNorm+Q8_1."""
+    return {"q_proj": "attn", "k_proj": "attn", "v_proj": "attn", "o_proj": "o",
+            "gate_up": "ffn", "down": "down"}.get(pname, pname)
+
+
+def layer_inputs(shapes):
+    seen = []
+    for (pname, K, N, paired) in shapes:
+        if input_key(pname) not in [k for k, _ in seen]:
+            seen.append((input_key(pname), K))
+    return seen
+
+
+def layer_algo_bytes(shapes, B, layers=1, extra=()):
+    """Algorithmic bytes of one step: each RMSNorm+Q8_1 (x read, Q8_1 written)
+    and each projection (weights once, its Q8_1 input once -- a pair reads it
+    once for both matrices at B = 1 --, fp32 outputs)."""
+    b = sum(norm_bytes(K, B) for _, K in layer_inputs(shapes))
+    for (pname, K, N, paired) in list(shapes) * layers + list(extra):
+        b += proj_bytes(K, N, B) * (2 if paired else 1) - (B * K * (1 + 4 / 32) if paired and B == 1 else 0)
+    return b
+
+
+def proj_bytes(K, N, B):
+    """Algorithmic bytes of one projection: weights once, Q8_1 input, fp32 y."""
+    return N * K * 144 // 256 + B * K * (1 + 4 / 32) + B * N * 4
+
+
+def norm_bytes(K, B):
+    return B * K * 4 + B * K * (1 + 4 / 32)
+
+
+class LayerWorkload:
+    """One decoder layer's projections at batch B with R rotating weight copies."""
+
+    def __init__(self, name, shapes, B, seed=0, min_rotation_bytes=3 * L2_BYTES, layers=1,
+                 extra=None):
+        import torch
+        import gemm_zq_rmsnorm_gb300 as zq
+        self.zq, self.torch = zq, torch
+        self.name, self.B = name, B
+        dev = "cuda"
+        self.extra = list(extra or [])
+        self.shapes = shapes + self.extra
+        # distinct inputs per projection input width; the norm runs once per
+        # distinct input (q/k/v share the attention input, gate/up the FFN one)
+        self.inputs_K = layer_inputs(shapes)
+        self.x = {k: torch.from_numpy(inputs.activations(seed + i, B, K)).to(dev)
+                  for i, (k, K) in enumerate(self.inputs_K)}
+        self.g = {k: torch.from_numpy(inputs.gamma(seed + i, K)).to(dev)
+                  for i, (k, K) in enumerate(self.inputs_K)}
+        self.a = {k: zq.empty_q8_1(B, K, dev) for k, K in self.inputs_K}
+        # weights: generate once per shape, clone to distinct device copies
+        self.layer_shapes = list(shapes)
+        per_copy = (sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in self.layer_shapes) * layers
+                    + sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in self.extra))
+        self.R = max(1, -(-min_rotation_bytes // per_copy))
+        self.layers = layers
+        base = {}
+        for si, (pname, K, N, paired) in enumerate(self.shapes):
+            w1 = torch.from_numpy(inputs.q4k_weights(seed + 17 * si, N, K)).to(dev)
+            w2 = torch.from_numpy(inputs.q4k_weights(seed + 17 * si, N, K, tag_offset=100)).to(dev) if paired else None
+            base[pname] = (w1, w2)
+
+        def clone(names):
+            return {k: (base[k][0].clone(), None if base[k][1] is None else base[k][1].clone()) for k in names}
+
+        lnames = [p for (p, _, _, _) in self.layer_shapes]
+        enames = [p for (p, _, _, _) in self.extra]
+        # W[copy] = (list over layers of {name: (W, W2)}, {extra name: (W, W2)})
+        self.W = []
+        for r in range(self.R):
+            layers_w = [({k: base[k] for k in lnames} if (r == 0 and li == 0) else clone(lnames))
+                        for li in range(layers)]
+            extra_w = {k: base[k] for k in enames} if r == 0 else clone(enames)
+            self.W.append((layers_w, extra_w))
+        self.y = {}
+        for (pname, K, N, paired) in self.shapes:
+            self.y[pname] = (torch.empty((B, N), dtype=torch.float32, device=dev),
+                             torch.empty((B, N), dtype=torch.float32, device=dev) if paired else None)
+        ws = max(zq.gemm_workspace_bytes(N, K, B) for (_, K, N, _) in self.shapes)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.key_of = {p: input_key(p) for (p, _, _, _) in self.layer_shapes}
+        for (p, K, N, _) in self.extra:
+            self.key_of[p] = [k for k, KK in self.inputs_K if KK == K][0]
+
+    def weights(self, r, pname, layer=0):
+        layers_w, extra_w = self.W[r]
+        return extra_w[pname] if pname in extra_w else layers_w[layer][pname]
+
+    def _proj(self, pname, K, N, paired, w1, w2, stream):
+        zq = self.zq
+        a = self.a[self.key_of[pname]]
+        y1, y2 = self.y[pname]
+        if self.B == 1:
+            if paired:
+                zq.q4k_gemv_pair(w1, w2, N, K, a, y1, y2, stream=stream)
+            else:
+                zq.q4k_gemv(w1, N, K, a, y1, stream=stream)
+        else:
+            zq.q4k_gemm(w1, N, K, a, self.B, y1, self.ws, stream=stream)
+            if paired:
+                zq.q4k_gemm(w2, N, K, a, self.B, y2, self.ws, stream=stream)
+
+    # one pass of the path
+    def run(self, r=0, stream=None):
+        for k, K in self.inputs_K:
+            self.zq.rmsnorm_q8_1(self.x[k], self.g[k], inputs.EPS, out=self.a[k], stream=stream)
+        layers_w, extra_w = self.W[r]
+        for li in range(self.layers):
+            for (pname, K, N, paired) in self.layer_shapes:
+                w1, w2 = layers_w[li][pname]
+                self._proj(pname, K, N, paired, w1, w2, stream)
+        for (pname, K, N, paired) in self.extra:
+            w1, w2 = extra_w[pname]
+            self._proj(pname, K, N, paired, w1, w2, stream)
+
+    def launches_per_step(self):
+        n = len(self.inputs_K)
+        for (pname, K, N, paired) in self.layer_shapes * self.layers + self.extra:
+            calls = 1 if (self.B == 1 or not paired) else 2
+            per = 1 if self.B == 1 else (2 if self.zq.gemm_workspace_bytes(N, K, self.B) else 1)
+            n += calls * per
+        return n
+
+    def algo_bytes(self):
+        return layer_algo_bytes(self.layer_shapes, self.B, self.layers, self.extra)
+
+    def algo_ops(self):
+        return sum(2 * self.B * N * K * (2 if p else 1) for (_, K, N, p) in self.layer_shapes * self.layers + self.extra)
+
+    def input_bytes(self):
+        return sum(self.B * K * 4 for _, K in self.inputs_K)
+
+    def output_bytes(self):
+        return sum(self.B * N * 4 * (2 if p else 1) for (_, K, N, p) in self.shapes)
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for nm, v in zip(names, r[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def time_graphs(torch, graphs, steps, warmup, stream):
+    """Replay graphs round-robin; W untimed, K timed; returns ms per step."""
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # uncaptured call first: sets per-device kernel attributes
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def bench_workload(torch, wl, steps, warmup, stream):
+    graphs = [capture(torch, lambda r=r: wl.run(r), stream) for r in range(wl.R)]
+    ms = time_graphs(torch, graphs, steps, warmup, stream)
+    return ms, graphs
+
+
+def bench_dominant(torch, wl, pname, steps, warmup, stream):
+    """Average duration of the workload's largest kernel alone (CUDA events
+    around back-to-back launches on its stream, rotating weight copies)."""
+    (_, K, N, paired) = [s for s in wl.shapes if s[0] == pname][0]
+    zq = wl.zq
+    a = wl.a[wl.key_of[pname]]
+
+    def one(r):
+        w1, w2 = wl.weights(r, pname)
+        y1, y2 = wl.y[pname]
+        if wl.B == 1:
+            if paired:
+                zq.q4k_gemv_pair(w1, w2, N, K, a, y1, y2)
+            else:
+                zq.q4k_gemv(w1, N, K, a, y1)
+        else:
+            zq.q4k_gemm(w1, N, K, a, wl.B, y1, wl.ws)
+
+    R = max(wl.R, -(-3 * L2_BYTES // (N * K * 144 // 256 * (2 if paired and wl.B == 1 else 1))))
+    R = min(R, wl.R)
+    graphs = [capture(torch, lambda r=r: one(r), stream) for r in range(R)]
+    ms = time_graphs(torch, graphs, max(steps * 4, 20), warmup, stream)
+    units = 2 if (paired and wl.B == 1) else 1
+    if wl.B == 1:
+        alg = proj_bytes(K, N, 1) * units - (K * (1 + 4 / 32) if units == 2 else 0)
+    else:
+        alg = 2 * wl.B * N * K
+    return ms, alg, (K, N, paired)
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_sample(wl_shapes, B, budget_s=12.0, seed=0):
+    """Time the CPU oracle on a bounded sample: RMSNorm+Q8_1 of every input and
+    a row sample of every projection; returns (seconds per full step, sample text)."""
+    import oracle
+    t_total, frac_used = 0.0, []
+    seen = {}
+    per_shape_budget = budget_s / max(1, len(wl_shapes))
+    for si, (pname, K, N, paired) in enumerate(wl_shapes):
+        key = input_key(pname)
+        if key not in seen:
+            x = inputs.activations(seed + si, B, K)
+            g = inputs.gamma(seed + si, K)
+            t0 = time.perf_counter()
+            q = oracle.rmsnorm_q8_1(x, g, inputs.EPS)
+            t_total += time.perf_counter() - t0
+            seen[key] = q
+        qs, d, s = seen[key]
+        ck = (seed + 17 * si, N, K)
+        if ck not in _ORACLE_CACHE:
+            _ORACLE_CACHE[ck] = inputs.q4k_weights(seed + 17 * si, N, K)
+        W = _ORACLE_CACHE[ck]
+        # calibrate on a few rows, then take as many as fit the budget
+        rows = np.arange(min(N, 8), dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.q4k_matmul(W, N, K, qs, d, s, rows=rows, want_scale=False)
+        dt = max(time.perf_counter() - t0, 1e-6) / len(rows)
+        n_rows = int(min(N, max(8, per_shape_budget / dt / (2 if paired else 1))))
+        rows = np.linspace(0, N - 1, n_rows).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.q4k_matmul(W, N, K, qs, d, s, rows=rows, want_scale=False)
+        dt = time.perf_counter() - t0
+        t_total += dt * (N / n_rows) * (2 if paired else 1)
+        frac_used.append(f"{pname} {n_rows}/{N} rows")
+    return t_total, "; ".join(frac_used)
+
+
+# ----------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="zq", choices=["zq", "reference"])
+    ap.add_argument("--workload", default="headline",
+                    choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference" or os.environ.get("ZQ_BENCH_DEBUG"), "W >= 3"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    stream = torch.cuda.Stream()
+    pk = peaks()
+    result = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    wl_dec = None
+    if args.workload in ("headline", "decode-27b"):
+        wl_dec = LayerWorkload("decode-27b-layer", inputs.LAYER_27B, 1)
+    elif args.workload == "decode-small":
+        wl_dec = LayerWorkload("decode-small-28L+lm_head", inputs.SMALL_DECODE[:-1], 1, layers=28,
+                               extra=[inputs.SMALL_DECODE[-1]])
+    elif args.workload == "tiny":
+        wl_dec = LayerWorkload("tiny-1024x1024", inputs.TINY, 1, min_rotation_bytes=3 * L2_BYTES)
+
+    out = dict(result)
+    if wl_dec is not None:
+        barrier()
+        with Clocks(local_rank) as clk:
+            ms, _ = bench_workload(torch, wl_dec, args.steps, args.warmup, stream)
+        ms = max_over_ranks(ms)
+        gbs = wl_dec.algo_bytes() / (ms * 1e-3) / 1e9 * world
+        dom = "gate_up" if any(s[0] == "gate_up" for s in wl_dec.shapes) else wl_dec.shapes[0][0]
+        dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl_dec, dom, args.steps, args.warmup, stream)
+        achieved = dalg / (dms * 1e-3) / 1e9
+        out.update({
+            "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5), "dtype": "u8",
+            "config": {"workload": wl_dec.name, "B": 1, "hidden": wl_dec.inputs_K[0][1],
+                       "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl_dec.shapes],
+                       "layers": wl_dec.layers, "weight_copies_rotated": wl_dec.R,
+                       "l2": f"inputs larger than L2: {wl_dec.R} rotating weight copies of the step",
+                       "algorithmic_bytes_per_step": int(wl_dec.algo_bytes())},
+            "roofline": {"bound": "hbm", "kernel": f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}",
+                         "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
+                         "traffic": None, "kernel_ms": round(dms, 5)},
+            "gpu_launches": wl_dec.launches_per_step() * args.steps,
+            "clocks": clk.summary(),
+        })
+        if not args.no_e2e:
+            out["e2e"] = e2e(torch, wl_dec, args.steps, args.warmup)
+        if rank == 0 and not args.no_cpu_baseline:
+            secs, sample = oracle_sample(wl_dec.shapes, 1, budget_s=10.0)
+            out["cpu_baseline"] = {"value": round(wl_dec.algo_bytes() / secs / 1e9, 4), "unit": "GB/s",
+                                   "cores": 1, "kind": "oracle",
+                                   "sample": f"RMSNorm+Q8_1 of every input, row samples: {sample}; "
+                                             f"scaled to one full step ({secs:.2f} s per step)"}
+
+    if args.workload in ("headline", "prefill-512", "chunk"):
+        Bs = [inputs.PREFILL_B] if args.workload != "chunk" else list(inputs.CHUNK_BATCHES)
+        sub = []
+        for B in Bs:
+            shapes = inputs.LAYER_27B if B == inputs.PREFILL_B else inputs.CHUNK_SHAPES
+            wl = LayerWorkload(f"prefill-{B}" if B == inputs.PREFILL_B else f"chunk-B{B}", shapes, B)
+            barrier()
+            with Clocks(local_rank) as clk:
+                ms, _ = bench_workload(torch, wl, max(3, args.steps // 5), args.warmup, stream)
+            ms = max_over_ranks(ms)
+            tops = wl.algo_ops() / (ms * 1e-3) / 1e12 * world
+            gbs = wl.algo_bytes() / (ms * 1e-3) / 1e9 * world
+            dom = "gate_up" if any(s[0] == "gate_up" for s in wl.shapes) else wl.shapes[0][0]
+            dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl, dom, max(3, args.steps // 5), args.warmup, stream)
+            ach = dalg / (dms * 1e-3) / 1e12
+            rec = {"workload": wl.name, "B": B, "value": round(tops, 2), "unit": "TOPS",
+                   "ms_per_step": round(ms, 4), "hbm_gbs": round(gbs, 1),
+                   "algorithmic_ops_per_step": int(wl.algo_ops()),
+                   "roofline": {"bound": "tensor", "kernel": f"q4k_gemm {dK}->{dN} B={B}",
+                                "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": round(ach / pk["bf16_tflops"], 4),
+                                "peak_source": pk["source"] + " bf16 dense burst (fp16 operands run at the bf16 rate; "
+                                               "int8 tcgen05 is not available on sm_103a)",
+                                "traffic": None, "kernel_ms": round(dms, 5)},
+                   "gpu_launches": wl.launches_per_step() * max(3, args.steps // 5), "clocks": clk.summary()}
+            sub.append(rec)
+            del wl
+            torch.cuda.empty_cache()
+        if wl_dec is None:
+            r0 = sub[0]
+            out.update({"value": r0["value"], "unit": "TOPS", "ms_per_step": r0["ms_per_step"], "dtype": "u8",
+                        "config": {"workload": r0["workload"], "B": r0["B"]}, "roofline": r0["roofline"],
+                        "gpu_launches": r0["gpu_launches"], "clocks": r0["clocks"]})
+            if len(sub) > 1:
+                out["more"] = sub[1:]
+        else:
+            out["prefill_b512"] = sub[0]
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+    return 0
+
+
+def e2e(torch, wl, steps, warmup):
+    """Same metric through the public API, host buffers: each step copies the
+    step's activations from pinned host memory, runs every call of the path
+    (no graph), and reads every output back to pinned host memory."""
+    hx = {k: wl.x[k].cpu().pin_memory() for k in wl.x}
+    hy = {p: (wl.y[p][0].cpu().pin_memory(), None if wl.y[p][1] is None else wl.y[p][1].cpu().pin_memory())
+          for p in wl.y}
+    s = torch.cuda.current_stream()
+
+    def step(r):
+        for k in hx:
+            wl.x[k].copy_(hx[k], non_blocking=True)
+        wl.run(r, stream=s)
+        for p in hy:
+            hy[p][0].copy_(wl.y[p][0], non_blocking=True)
+            if hy[p][1] is not None:
+                hy[p][1].copy_(wl.y[p][1], non_blocking=True)
+
+    for i in range(warmup):
+        step(i % wl.R)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        step(i % wl.R)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) / steps
+    ms = max(e0.elapsed_time(e1) / steps, wall * 1e3)
+    return {"value": round(wl.algo_bytes() / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(wl.input_bytes()),
+            "d2h_bytes_per_step": int(wl.output_bytes()), "graph": False}
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores (single thread)."""
+    shapes = inputs.LAYER_27B
+    per_step = []
+    # each step: a bounded sample of the decode layer, scaled to a full step
+    for i in range(args.warmup + args.steps):
+        secs, sample = oracle_sample(shapes, 1, budget_s=1.0, seed=0)
+        if i >= args.warmup:
+            per_step.append(secs)
+    secs = statistics.mean(per_step) if per_step else float("nan")
+    v = layer_algo_bytes(shapes, 1) / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "config": {"workload": "decode-27b-layer", "B": 1},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"per step: {sample}, scaled to a full step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

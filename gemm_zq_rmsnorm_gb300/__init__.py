@@ -1,0 +1,191 @@
+"""Python binding of libzq.so, the GB300 quantized-projection library.
+
+Argument marshalling only: every step of the path (RMSNorm + Q8_1 packing,
+Q4_K x Q8_1 mat-vec / paired mat-vec / batched GEMM) runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  There
+is no CPU fallback: if libzq.so is missing or the device is not sm_103, every
+call raises.
+
+The entry points mirror the C ABI of include/zq.h one to one.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzq.so")
+
+ZQ_OK = 0
+STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_ALIGN",
+                -4: "ZQ_ERR_CUDA", -5: "ZQ_ERR_DEVICE", -6: "ZQ_ERR_WORKSPACE"}
+
+EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
+           "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
+           "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums")
+
+
+class ZQError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Q8(ctypes.Structure):
+    _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p), ("s", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libzq.so (built by gemm_zq_rmsnorm_gb300/build.py); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libzq.so not found at {path}: build it with "
+                           "`python gemm_zq_rmsnorm_gb300/build.py` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    P, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "zq_rmsnorm_q8_1": ([P, P, i, i, f, _Q8, P], i),
+        "zq_q4k_gemv": ([P, i, i, _Q8, P, P], i),
+        "zq_q4k_gemv_pair": ([P, P, i, i, _Q8, P, P, P], i),
+        "zq_q4k_gemm": ([P, i, i, _Q8, i, P, P, sz, P], i),
+        "zq_q4k_gemm_workspace_bytes": ([i, i, i], sz),
+        "zq_q4k_bytes": ([i, i], sz),
+        "zq_q8_1_bytes": ([i, i], sz),
+        "zq_status_string": ([i], ctypes.c_char_p),
+        "zq_last_error": ([], ctypes.c_char_p),
+        "zq_version": ([], i),
+        "zq_debug_q4k_isums": ([P, i, i, _Q8, i, P, i, P, sz, P], i),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != ZQ_OK:
+        raise ZQError(status, load().zq_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclasses.dataclass
+class Q8_1:
+    """Planar Q8_1 activations: qs int8 [B][K], d/s binary16 [B][K/32]."""
+    qs: torch.Tensor
+    d: torch.Tensor
+    s: torch.Tensor
+
+    @property
+    def B(self) -> int:
+        return self.qs.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.qs.shape[1]
+
+    def _c(self) -> _Q8:
+        return _Q8(self.qs.data_ptr(), self.d.data_ptr(), self.s.data_ptr())
+
+    def rows(self, t0: int, t1: int) -> "Q8_1":
+        return Q8_1(self.qs[t0:t1], self.d[t0:t1], self.s[t0:t1])
+
+
+def empty_q8_1(B: int, K: int, device="cuda") -> Q8_1:
+    return Q8_1(torch.empty((B, K), dtype=torch.int8, device=device),
+                torch.empty((B, K // 32), dtype=torch.float16, device=device),
+                torch.empty((B, K // 32), dtype=torch.float16, device=device))
+
+
+def q4k_bytes(N: int, K: int) -> int:
+    return int(load().zq_q4k_bytes(N, K))
+
+
+def gemm_workspace_bytes(N: int, K: int, B: int) -> int:
+    return int(load().zq_q4k_gemm_workspace_bytes(N, K, B))
+
+
+def rmsnorm_q8_1(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: Q8_1 | None = None,
+                 stream=None) -> Q8_1:
+    """Fused RMSNorm + Q8_1 pack of x fp32 [B][K] (see zq_rmsnorm_q8_1)."""
+    lib = load()
+    B, K = x.shape
+    if out is None:
+        out = empty_q8_1(B, K, x.device)
+    _check(lib.zq_rmsnorm_q8_1(_ptr(x), _ptr(gamma), B, K, float(eps), out._c(), _stream(stream)))
+    return out
+
+
+def q4k_gemv(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    lib = load()
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=a.qs.device)
+    _check(lib.zq_q4k_gemv(_ptr(W), N, K, a._c(), _ptr(y), _stream(stream)))
+    return y
+
+
+def q4k_gemv_pair(Wg: torch.Tensor, Wu: torch.Tensor, N: int, K: int, a: Q8_1,
+                  y_gate: torch.Tensor | None = None, y_up: torch.Tensor | None = None,
+                  stream=None):
+    lib = load()
+    dev = a.qs.device
+    if y_gate is None:
+        y_gate = torch.empty(N, dtype=torch.float32, device=dev)
+    if y_up is None:
+        y_up = torch.empty(N, dtype=torch.float32, device=dev)
+    _check(lib.zq_q4k_gemv_pair(_ptr(Wg), _ptr(Wu), N, K, a._c(), _ptr(y_gate), _ptr(y_up),
+                                _stream(stream)))
+    return y_gate, y_up
+
+
+def q4k_gemm(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
+             y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    lib = load()
+    B = a.B if B is None else B
+    dev = a.qs.device
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=dev)
+    need = gemm_workspace_bytes(N, K, B)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.zq_q4k_gemm(_ptr(W), N, K, a._c(), B, _ptr(y), _ptr(workspace), wbytes,
+                           _stream(stream)))
+    return y
+
+
+def debug_q4k_isums(W: torch.Tensor, N: int, K: int, a: Q8_1, path: int = 0,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Exact sub-block integer sums [B][N][K/32] from the kernels' own inner
+    products (path 0: dp4a mat-vec; 1: prefill tensor cores; 2: chunk tensor cores)."""
+    lib = load()
+    B = a.B
+    dev = a.qs.device
+    isums = torch.empty((B, N, K // 32), dtype=torch.int32, device=dev)
+    need = gemm_workspace_bytes(N, K, B) if path else 0
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.zq_debug_q4k_isums(_ptr(W), N, K, a._c(), B, _ptr(isums), path, _ptr(workspace),
+                                  wbytes, _stream(stream)))
+    return isums

@@ -1,0 +1,234 @@
+// zq_api.cu -- the C ABI of libzq.so: argument, shape and alignment checks,
+// device checks, dispatch by batch size, status codes and error text.
+//
+// ZINC docs "ROCm backend", "Build and verify": the engine keeps its GPU
+// kernels behind a C ABI; every fused path is selectable, and a request the
+// build cannot serve fails instead of falling back (Zynfer README: forced
+// unsupported paths exit with an error).  Nothing here computes: every step of
+// the path runs in the kernels of the other translation units.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "zq_internal.cuh"
+
+namespace zq {
+
+namespace {
+thread_local std::string g_last_error;
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+bool g_checked[kMaxDevices];
+int g_dev_status[kMaxDevices];
+std::mutex g_mu;
+
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device check, once per device: the kernels are built for sm_103a only.
+int check_device(int *dev_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ZQ_ERR_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(ZQ_ERR_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_checked[dev]) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = sms;
+        g_dev_status[dev] = (major == 10 && minor == 3) ? ZQ_OK : ZQ_ERR_DEVICE;
+        g_checked[dev] = true;
+    }
+    *dev_out = dev;
+    if (g_dev_status[dev] != ZQ_OK)
+        return fail(ZQ_ERR_DEVICE, "device %d is not sm_103 (GB300); libzq is built for sm_103a only", dev);
+    return ZQ_OK;
+}
+
+int launched(cudaError_t e, const char *what)
+{
+    if (e != cudaSuccess) return fail(ZQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ZQ_OK;
+}
+
+int check_q8(const zq_q8_1 &a, const char *name)
+{
+    if (!a.qs || !a.d || !a.s) return fail(ZQ_ERR_ARG, "%s: null Q8_1 plane", name);
+    if (!aligned16(a.qs) || !aligned16(a.d) || !aligned16(a.s))
+        return fail(ZQ_ERR_ALIGN, "%s: Q8_1 planes must be 16-byte aligned", name);
+    return ZQ_OK;
+}
+
+int check_q4k(const void *W, int N, int K, const char *name)
+{
+    if (!W) return fail(ZQ_ERR_ARG, "%s: null weight pointer", name);
+    if (!aligned16(W)) return fail(ZQ_ERR_ALIGN, "%s: weights must be 16-byte aligned", name);
+    if (N < 1) return fail(ZQ_ERR_SHAPE, "%s: N = %d must be >= 1", name, N);
+    if (K < 256 || K % 256 != 0 || K > (1 << 22))
+        return fail(ZQ_ERR_SHAPE, "%s: K = %d must be a positive multiple of 256 (<= 2^22)", name, K);
+    return ZQ_OK;
+}
+
+}  // namespace
+
+int num_sms()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0) ? g_sms[dev] : 148;
+}
+
+}  // namespace zq
+
+using namespace zq;
+
+extern "C" {
+
+int zq_version(void) { return ZQ_VERSION; }
+
+const char *zq_last_error(void) { return g_last_error.c_str(); }
+
+const char *zq_status_string(int status)
+{
+    switch (status) {
+    case ZQ_OK: return "ok";
+    case ZQ_ERR_ARG: return "invalid argument";
+    case ZQ_ERR_SHAPE: return "unsupported shape";
+    case ZQ_ERR_ALIGN: return "misaligned pointer";
+    case ZQ_ERR_CUDA: return "CUDA error";
+    case ZQ_ERR_DEVICE: return "unsupported or missing device";
+    case ZQ_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+size_t zq_q4k_bytes(int N, int K)
+{
+    if (N < 1 || K < 256 || K % 256) return 0;
+    return (size_t)N * (size_t)(K / 256) * kQ4KBlockBytes;
+}
+
+size_t zq_q8_1_bytes(int B, int K)
+{
+    if (B < 1 || K < 32 || K % 32) return 0;
+    return (size_t)B * K + 2 * sizeof(uint16_t) * (size_t)B * (K / 32);
+}
+
+int zq_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float eps, zq_q8_1 out,
+                    void *stream)
+{
+    if (!x || !gamma) return fail(ZQ_ERR_ARG, "zq_rmsnorm_q8_1: null x or gamma");
+    if (!aligned16(x) || !aligned16(gamma))
+        return fail(ZQ_ERR_ALIGN, "zq_rmsnorm_q8_1: x and gamma must be 16-byte aligned");
+    if (!(eps >= 0.0f) || eps != eps) return fail(ZQ_ERR_ARG, "zq_rmsnorm_q8_1: eps must be >= 0");
+    if (B < 1 || B > (1 << 24)) return fail(ZQ_ERR_SHAPE, "zq_rmsnorm_q8_1: B = %d out of range", B);
+    if (K < 32 || K % 32 != 0 || K > (1 << 20))
+        return fail(ZQ_ERR_SHAPE, "zq_rmsnorm_q8_1: K = %d must be a multiple of 32 in [32, 2^20]", K);
+    int st = check_q8(out, "zq_rmsnorm_q8_1");
+    if (st) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_rmsnorm_q8_1(x, gamma, B, K, eps, out, (cudaStream_t)stream),
+                    "zq_rmsnorm_q8_1 launch");
+}
+
+int zq_q4k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream)
+{
+    int st = check_q4k(W, N, K, "zq_q4k_gemv");
+    if (st) return st;
+    if ((st = check_q8(a, "zq_q4k_gemv"))) return st;
+    if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemv: null y");
+    if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemv: y must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_gemv(W, nullptr, N, K, a, 1, y, nullptr, nullptr, (cudaStream_t)stream),
+                    "zq_q4k_gemv launch");
+}
+
+int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_1 a, float *y_gate,
+                     float *y_up, void *stream)
+{
+    int st = check_q4k(Wg, N, K, "zq_q4k_gemv_pair (gate)");
+    if (st) return st;
+    if ((st = check_q4k(Wu, N, K, "zq_q4k_gemv_pair (up)"))) return st;
+    if ((st = check_q8(a, "zq_q4k_gemv_pair"))) return st;
+    if (!y_gate || !y_up) return fail(ZQ_ERR_ARG, "zq_q4k_gemv_pair: null output");
+    if (!aligned16(y_gate) || !aligned16(y_up))
+        return fail(ZQ_ERR_ALIGN, "zq_q4k_gemv_pair: outputs must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_gemv(Wg, Wu, N, K, a, 1, y_gate, y_up, nullptr, (cudaStream_t)stream),
+                    "zq_q4k_gemv_pair launch");
+}
+
+size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B)
+{
+    if (N < 1 || K < 256 || K % 256 || B < 1) return 0;
+    return gemm_tc_workspace_bytes(N, K, B);
+}
+
+int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *workspace,
+                size_t workspace_bytes, void *stream)
+{
+    int st = check_q4k(W, N, K, "zq_q4k_gemm");
+    if (st) return st;
+    if ((st = check_q8(a, "zq_q4k_gemm"))) return st;
+    if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_q4k_gemm: B = %d must be in [1, 65536]", B);
+    if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemm: null y");
+    if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm: y must be 16-byte aligned");
+    const size_t need = gemm_tc_workspace_bytes(N, K, B);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(ZQ_ERR_WORKSPACE, "zq_q4k_gemm: workspace of %zu bytes required, got %zu", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (need && !aligned16(workspace))
+        return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm: workspace must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B == 1) return launched(launch_gemv(W, nullptr, N, K, a, 1, y, nullptr, nullptr, s), "zq_q4k_gemm (B=1)");
+    if (B <= 16) return launched(launch_gemm_tc_narrow(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (chunk)");
+    return launched(launch_gemm_tc_wide(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (prefill)");
+}
+
+int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B, int32_t *isums, int path,
+                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    int st = check_q4k(W, N, K, "zq_debug_q4k_isums");
+    if (st) return st;
+    if ((st = check_q8(a, "zq_debug_q4k_isums"))) return st;
+    if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_debug_q4k_isums: B = %d out of range", B);
+    if (!isums || !aligned16(isums)) return fail(ZQ_ERR_ARG, "zq_debug_q4k_isums: isums null or misaligned");
+    if (path < 0 || path > 2) return fail(ZQ_ERR_ARG, "zq_debug_q4k_isums: path %d unknown", path);
+    if (path == 1 && B < 17) return fail(ZQ_ERR_SHAPE, "zq_debug_q4k_isums: path 1 needs B >= 17");
+    if (path == 2 && (B < 2 || B > 16)) return fail(ZQ_ERR_SHAPE, "zq_debug_q4k_isums: path 2 needs 2 <= B <= 16");
+    if (path != 0) {
+        const size_t need = gemm_tc_workspace_bytes(N, K, B);
+        if (need && (!workspace || workspace_bytes < need))
+            return fail(ZQ_ERR_WORKSPACE, "zq_debug_q4k_isums: workspace of %zu bytes required", need);
+    }
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (path == 0) return launched(launch_gemv(W, nullptr, N, K, a, B, nullptr, nullptr, isums, s), "isums (dp4a)");
+    if (path == 1) return launched(launch_gemm_tc_wide(W, N, K, a, B, nullptr, isums, workspace, s), "isums (prefill)");
+    return launched(launch_gemm_tc_narrow(W, N, K, a, B, nullptr, isums, workspace, s), "isums (chunk)");
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// zq_internal.cuh -- helpers shared by the library's CUDA translation units.
+// Internal to libzq.so; nothing here is exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "zq.h"
+
+namespace zq {
+
+constexpr int kQ4KBlockBytes = 144;   // one 256-weight super-block
+constexpr int kQ4KBlockWeights = 256;
+
+// Host-side launch descriptions (defined in the kernel TUs, called by the API).
+cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K,
+                                float eps, zq_q8_1 out, cudaStream_t st);
+cudaError_t launch_gemv(const void *W, const void *W2, int N, int K, zq_q8_1 a,
+                        int B, float *y, float *y2, int32_t *isums,
+                        cudaStream_t st);
+cudaError_t launch_gemm_tc_wide(const void *W, int N, int K, zq_q8_1 a, int B,
+                                float *y, int32_t *isums, void *ws,
+                                cudaStream_t st);
+cudaError_t launch_gemm_tc_narrow(const void *W, int N, int K, zq_q8_1 a, int B,
+                                  float *y, int32_t *isums, void *ws,
+                                  cudaStream_t st);
+size_t gemm_tc_workspace_bytes(int N, int K, int B);
+
+int num_sms();
+
+// ------------------------------------------------------------------ device
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+{
+    // weights are read exactly once: do not keep them in L1
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cached_u4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float h2f(uint16_t h)
+{
+    return __half2float(__ushort_as_half(h));
+}
+
+// Six-bit scale and min of sub-block j from the 12 packed scale bytes, given
+// as three little-endian words s0 = S[0..3], s1 = S[4..7], s2 = S[8..11].
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2,
+                                              int j, uint32_t &sc, uint32_t &m)
+{
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63u;
+        m = (s1 >> (8 * j)) & 63u;
+    } else {
+        const int k = 8 * (j - 4);
+        const uint32_t b2 = (s2 >> k) & 0xFFu;
+        sc = (b2 & 15u) | (((s0 >> k) >> 6 & 3u) << 4);
+        m = (b2 >> 4) | (((s1 >> k) >> 6 & 3u) << 4);
+    }
+}
+
+}  // namespace zq

@@ -1,0 +1,171 @@
+/*
+ * zq.h -- C ABI of the GB300 (sm_103a) quantized-projection library libzq.so.
+ *
+ * The library computes one hot path of LLM inference on one GPU:
+ *   1. zq_rmsnorm_q8_1   RMSNorm of each token fused with Q8_1 packing of the
+ *                        normalised activations;
+ *   2. zq_q4k_gemv       Q4_K weight matrix x one Q8_1 token (decode, B = 1);
+ *   3. zq_q4k_gemv_pair  two Q4_K matrices (FFN gate and up) x one token,
+ *                        sharing one read of the activations;
+ *   4. zq_q4k_gemm       Q4_K matrix x B Q8_1 tokens (chunked prefill B = 2..16,
+ *                        full prefill e.g. B = 512) on the tensor cores.
+ *
+ * Sources: ZINC docs "ROCm backend", section "Build and verify" (RMS norm and
+ * Q8 activation packing in one per-token kernel; hot Q4_K projections on
+ * packed Q8 activations; paired Q4 gate/up projections; the engine's kernels
+ * sit behind a C ABI); MIInfer README, "Status" (Q4_K x Q8_1 MMVQ-style
+ * projections, Q4_K metadata staging, packed int8 dot4) and "Current phase"
+ * (token-batched B = 4 chunk projections; int8 GEMM and tensor-core prefill).
+ *
+ * ---------------------------------------------------------------- formats
+ * Q8_1 activations (planar, caller-owned device memory):
+ *   qs : int8     [B][K]     codes q, |q| <= 127
+ *   d  : binary16 [B][K/32]  per-32-block scale d = max|xh| / 127
+ *   s  : binary16 [B][K/32]  per-32-block d * sum(q)
+ *   q = round-half-away-from-zero(xh * (1/d)) computed in fp32 with the fp32 d;
+ *   the stored d and s are that fp32 d and s rounded to binary16 (RNE).
+ * Q4_K weights, N rows x K columns (K % 256 == 0), row-major, row n holding
+ * K/256 consecutive 144-byte super-blocks of 256 weights:
+ *   bytes 0..1 d, 2..3 dmin (binary16, little-endian);
+ *   bytes 4..15 S[12]: eight 6-bit scales sc[j] and mins m[j]:
+ *     j < 4 : sc = S[j] & 63,  m = S[j+4] & 63
+ *     j >= 4: sc = (S[j+4] & 15) | (S[j-4] >> 6) << 4,
+ *             m  = (S[j+4] >> 4) | (S[j]   >> 6) << 4
+ *   bytes 16..143: weight i (0..31) of sub-block j at byte 32*(j/2)+i,
+ *     low nibble for even j, high nibble for odd j;
+ *   weight = d*sc[j]*q - dmin*m[j].
+ * Output y (fp32, [B][N], token-major):
+ *   y[t][n] = sum_{b,j} d_b*sc_j*d8_{t,bj}*I_{t,n,b,j} - dmin_b*m_j*s8_{t,bj},
+ *   I = exact integer sum over the sub-block's 32 weights of q4*q8.
+ *
+ * ---------------------------------------------------------------- conventions
+ * - All tensor pointers are caller-owned DEVICE memory.  The library never
+ *   allocates device memory; it keeps no state except per-device launch
+ *   configuration set up on the first call, and a thread-local error string.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call is asynchronous on that stream; none synchronises.
+ * - Alignment: every tensor pointer must be 16-byte aligned.
+ * - Outputs must not alias inputs.
+ * - Every call returns ZQ_OK (0) or a negative status, checked on the host
+ *   before anything is launched (argument, shape and alignment errors launch
+ *   nothing).  zq_last_error() gives a one-line description of the last
+ *   failure on the calling thread.
+ * - Calls may be captured in a CUDA graph after one uncaptured call of the
+ *   same entry point on the device (the first call sets kernel attributes).
+ */
+#ifndef ZQ_H
+#define ZQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZQ_VERSION 1
+
+#if defined(__GNUC__)
+#define ZQ_API __attribute__((visibility("default")))
+#else
+#define ZQ_API
+#endif
+
+enum {
+    ZQ_OK = 0,
+    ZQ_ERR_ARG = -1,         /* null pointer, non-positive size, bad eps      */
+    ZQ_ERR_SHAPE = -2,       /* K not a multiple of 256 (32 for the norm),    */
+                             /* B or N out of range                           */
+    ZQ_ERR_ALIGN = -3,       /* a tensor pointer not 16-byte aligned          */
+    ZQ_ERR_CUDA = -4,        /* CUDA runtime error at launch                  */
+    ZQ_ERR_DEVICE = -5,      /* device is not sm_103 / no device              */
+    ZQ_ERR_WORKSPACE = -6    /* workspace missing or smaller than required    */
+};
+
+/* Planar Q8_1 activations of B tokens x K features (see "formats"). */
+typedef struct zq_q8_1 {
+    int8_t *qs;    /* [B][K]    */
+    uint16_t *d;   /* [B][K/32] binary16 bits */
+    uint16_t *s;   /* [B][K/32] binary16 bits */
+} zq_q8_1;
+
+/*
+ * Fused RMSNorm + Q8_1 packing (ZINC docs "ROCm backend", "Build and verify":
+ * normalisation and Q8 packing share one per-token kernel).
+ *   x     : fp32 [B][K] input activations
+ *   gamma : fp32 [K]    RMSNorm weight
+ *   eps   : >= 0, added to the mean square
+ *   out   : Q8_1 [B][K] (qs, d, s written)
+ * xh_k = (x_k * r) * gamma_k, r = 1 / sqrt(ss/K + eps); each step one IEEE
+ * fp32 operation, ss summed in this fixed order: per 32-block a fused
+ * multiply-add chain over its squares in index order; 256 slots, slot t
+ * summing the block partials b = t (mod 256) in increasing b; then the
+ * pairwise tree slot[t] += slot[t+off] for off = 128, 64, ..., 1.
+ * Shapes: B >= 1, K >= 32, K % 32 == 0, K <= 1048576.
+ */
+ZQ_API int zq_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float eps,
+                    zq_q8_1 out, void *stream);
+
+/*
+ * Decode mat-vec, one token (MIInfer README, "Status": Q4_K x Q8_1 MMVQ-style
+ * projection; ZINC docs "ROCm backend": packed Q8 activations for Q4_K).
+ *   W : Q4_K [N][K/256] super-blocks (N*K/256*144 bytes)
+ *   a : Q8_1 of one token (K features)
+ *   y : fp32 [N]
+ * Shapes: N >= 1, K >= 256, K % 256 == 0.
+ */
+ZQ_API int zq_q4k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream);
+
+/*
+ * Paired decode mat-vec for FFN gate and up (ZINC docs "ROCm backend":
+ * paired Q4 projections; MIInfer README, "Status": shared Q4_K x Q8_1 FFN
+ * gate/up path).  Both matrices are N x K Q4_K; one activation read serves
+ * both.  y_gate = Wg a, y_up = Wu a (fp32 [N] each).
+ */
+ZQ_API int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_1 a,
+                     float *y_gate, float *y_up, void *stream);
+
+/*
+ * Batched projection of B tokens (MIInfer README, "Current phase":
+ * token-batched chunk projections and tensor-core/int8 GEMM prefill).
+ *   W : Q4_K N x K;  a : Q8_1 of B tokens;  y : fp32 [B][N].
+ *   workspace / workspace_bytes : caller-owned device scratch of at least
+ *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0).
+ *     It holds the fp16 copy of the activation codes the tensor cores read;
+ *     its contents on entry do not matter and are not preserved.
+ * B = 1 runs the decode mat-vec.  2 <= B <= 16 runs the chunk path (tensor
+ * cores, weights unpacked once per tile and shared by the tokens); B >= 17
+ * runs the prefill path (tensor cores, 128-token tiles).
+ * Shapes: 1 <= B <= 65536, N >= 1, K % 256 == 0, K >= 256.
+ */
+ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace zq_q4k_gemm needs for this shape (0 if none). */
+ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
+
+/* Storage sizes: N x K Q4_K matrix; Q8_1 planes of B x K (qs + d + s). */
+ZQ_API size_t zq_q4k_bytes(int N, int K);
+ZQ_API size_t zq_q8_1_bytes(int B, int K);
+
+/* Status text, last error on this thread, library version (ZQ_VERSION). */
+ZQ_API const char *zq_status_string(int status);
+ZQ_API const char *zq_last_error(void);
+ZQ_API int zq_version(void);
+
+/*
+ * Test hook: exact sub-block integer sums I[t][n][K/32] (int32, device
+ * memory) computed by the kernels' own inner products.  path = 0: the packed
+ * dot4 (dp4a) inner product of the mat-vec kernels, any B; path = 1: the
+ * tensor-core prefill kernel (B >= 17), read back from its accumulators;
+ * path = 2: the tensor-core chunk kernel (2 <= B <= 16).  For paths 1 and 2
+ * the workspace rules of zq_q4k_gemm apply.
+ */
+ZQ_API int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B,
+                       int32_t *isums, int path, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZQ_H */

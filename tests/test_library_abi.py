@@ -1,0 +1,108 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every symbol
+include/zq.h declares, and rejects bad arguments on the host with the documented
+status before touching the device.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_zq_rmsnorm_gb300 as zq
+from gemm_zq_rmsnorm_gb300 import build as zqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(zq.LIB_PATH):
+        zqbuild.build()
+    return zq.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "zq.h")).read()
+    return sorted(set(re.findall(r"ZQ_API\s+[\w\s\*]*?\b(zq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(zq.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert lib.zq_version() == 1
+    for st, text in [(0, b"ok"), (-1, b"invalid argument"), (-2, b"unsupported shape"),
+                     (-3, b"misaligned pointer"), (-6, b"workspace missing or too small")]:
+        assert lib.zq_status_string(st) == text
+
+
+def test_size_helpers(lib):
+    assert lib.zq_q4k_bytes(5120, 17408) == 5120 * 68 * 144
+    assert lib.zq_q4k_bytes(10, 300) == 0
+    assert lib.zq_q8_1_bytes(2, 1024) == 2 * 1024 + 2 * 2 * 2 * 32
+
+
+# fake, never-dereferenced device addresses: validation fails before any use
+A16 = 0x10000
+A8 = 0x10008
+
+
+def q8(qs=A16, d=A16, s=A16):
+    return zq._Q8(qs, d, s)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, A16, 1, 1024, 1e-6, q8()), -1),            # null x
+    ((A16, A16, 1, 1000, 1e-6, q8()), -2),             # K % 32
+    ((A16, A16, 0, 1024, 1e-6, q8()), -2),             # B = 0
+    ((A16, A16, 1, 1024, -1.0, q8()), -1),             # negative eps
+    ((A8, A16, 1, 1024, 1e-6, q8()), -3),              # misaligned x
+    ((A16, A16, 1, 1024, 1e-6, q8(d=A8)), -3),         # misaligned d plane
+])
+def test_rmsnorm_rejects(lib, args, status):
+    assert lib.zq_rmsnorm_q8_1(*args, None) == status
+    assert lib.zq_last_error()
+
+
+@pytest.mark.parametrize("W,N,K,y,status", [
+    (None, 10, 1024, A16, -1), (A16, 0, 1024, A16, -2), (A16, 10, 1000, A16, -2),
+    (A16, 10, 0, A16, -2), (A8, 10, 1024, A16, -3), (A16, 10, 1024, A8, -3), (A16, 10, 1024, None, -1)])
+def test_gemv_rejects(lib, W, N, K, y, status):
+    assert lib.zq_q4k_gemv(W, N, K, q8(), y, None) == status
+
+
+def test_gemm_rejects(lib):
+    assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 0, A16, None, 0, None) == -2
+    assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 70000, A16, None, 0, None) == -2
+    need = lib.zq_q4k_gemm_workspace_bytes(64, 1024, 512)
+    if need:
+        assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 512, A16, None, 0, None) == -6
+        assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 512, A16, A16, need - 1, None) == -6
+    assert lib.zq_q4k_gemv_pair(A16, None, 64, 1024, q8(), A16, A16, None) == -1
+    assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 7, None, 0, None) == -1
+    assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 1, None, 0, None) == -2
+
+
+def test_valid_call_without_gpu_reports_device_error(lib):
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    st = lib.zq_q4k_gemv(A16, 64, 1024, q8(), A16, None)
+    assert st == -5, lib.zq_last_error()
+
+
+def test_binding_raises_without_device():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(Exception):
+        zq.rmsnorm_q8_1(torch.zeros(1, 64), torch.ones(64), 1e-6)
