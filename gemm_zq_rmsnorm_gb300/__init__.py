@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_AL
 
 EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
-           "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums")
+           "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
+           "zq_device_status")
 
 
 class ZQError(RuntimeError):
@@ -63,6 +64,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_last_error": ([], ctypes.c_char_p),
         "zq_version": ([], i),
         "zq_debug_q4k_isums": ([P, i, i, _Q8, i, P, i, P, sz, P], i),
+        "zq_device_status": ([P, i], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -172,6 +174,13 @@ def q4k_gemm(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
     _check(lib.zq_q4k_gemm(_ptr(W), N, K, a._c(), B, _ptr(y), _ptr(workspace), wbytes,
                            _stream(stream)))
     return y
+
+
+def device_status(clear: bool = False) -> int:
+    """Device-side error word (bit 0: a bounded wait in a pipelined kernel expired)."""
+    flags = ctypes.c_uint(0)
+    _check(load().zq_device_status(ctypes.byref(flags), int(clear)))
+    return int(flags.value)
 
 
 def debug_q4k_isums(W: torch.Tensor, N: int, K: int, a: Q8_1, path: int = 0,

@@ -1,0 +1,353 @@
+// q4k_gemv_stream.cu -- decode (B = 1) Q4_K x Q8_1 mat-vec and paired
+// mat-vec with the weights streamed through shared memory by bulk (TMA)
+// copies.
+//
+// MIInfer README, "Status": Q4_K x Q8_1 MMVQ-style projections (FFN down,
+// shared gate/up; Q4_K metadata staging; packed int8 dot4; activations reused
+// from on-chip memory).  ZINC docs "ROCm backend", "Build and verify": paired
+// Q4 projections.
+//
+// The mat-vec is bound by HBM bandwidth: N*K*144/256 weight bytes are read
+// exactly once.  To keep enough bytes in flight independently of register
+// pressure, one persistent CTA per SM runs a producer warp that issues 1-D
+// bulk copies of contiguous weight tiles (R whole rows, or a piece of one
+// long row; rows are contiguous, so a tile is one copy) into a ring of large
+// shared-memory stages, completing on mbarriers.  Sixteen consumer warps
+// decode each 144-byte super-block from shared memory -- four lanes per
+// block, lane p taking the 32 nibble bytes of sub-blocks 2p (low nibbles) and
+// 2p+1 (high nibbles) -- and form the two 32-wide integer sums with dp4a
+// against the Q8_1 activation row staged once per CTA.  Each lane applies
+// d*sc*d8*I - dmin*m*s8 in fp32, the four lanes of a block add up, and after
+// the stage the blocks of each row are summed in a fixed order into y.  The
+// paired kernel is the same launch over the rows of both matrices, sharing the
+// staged activations.
+#include "zq_async.cuh"
+#include "zq_internal.cuh"
+
+namespace zq {
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 3;
+constexpr int kStageMax = 64 * 1024;
+constexpr int kMaxBlk = kStageMax / kQ4KBlockBytes;   // 455 blocks per stage
+constexpr int kTasksPerStep = 8 * kConsumerWarps;      // blocks per warp-step
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxK = 32768;                           // activation staged in smem
+
+struct StreamParams {
+    const uint8_t *W[2];
+    float *y[2];
+    int N, K, nb;
+    uint32_t rowbytes;
+    int R;                // rows per group
+    int P;                // pieces per group (> 1 only when R == 1)
+    int CB;               // blocks per piece
+    int groups_per_mat;
+    int total_groups;
+    uint32_t nb_magic;    // ceil(2^32 / nb) for nb >= 2: task / nb = umulhi(task, nb_magic), task < 2^16
+    uint32_t stage_alloc; // bytes reserved per stage (multiple of 128)
+    const int8_t *qs;
+    const __half *d;
+    const __half *s;
+    unsigned int *status;
+};
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Activation codes are stored with 16 bytes of padding after every 64: the
+// 64-byte group g (sub-block pair) starts at 80*g.  The eight lanes of a
+// quarter-warp (two consecutive super-blocks x four pairs) then start in
+// eight different 16-byte bank groups.
+__host__ __device__ constexpr size_t act_bytes(int K) { return (size_t)K / 64 * 80; }
+
+struct SmemLayout {
+    size_t ring, act_qs, act_d, act_s, contrib, bars, total;
+    __host__ __device__ SmemLayout(int K, uint32_t stage_alloc)
+    {
+        ring = 0;
+        act_qs = ring + (size_t)kStages * stage_alloc;
+        act_d = align_up(act_qs + act_bytes(K), 16);
+        act_s = align_up(act_d + (size_t)K / 16, 16);
+        contrib = align_up(act_s + (size_t)K / 16, 16);
+        bars = align_up(contrib + (size_t)kStages * kMaxBlk * 4, 8);
+        total = bars + 2 * kStages * 8;
+    }
+};
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Scales and mins of sub-blocks 2p and 2p+1, packed as bytes 0 and 1 of the
+// returned words (branch-free; p = 0..3).
+__device__ __forceinline__ void q4k_pair_scales(const uint4 &hdr, int p, uint32_t &sc, uint32_t &mn)
+{
+    const uint32_t j = (uint32_t)(2 * p) & 3u;            // byte index within a 4-byte word
+    const uint32_t sel = j | ((j + 1) << 4);                // bytes j, j+1 -> bytes 0, 1
+    const uint32_t s0 = __byte_perm(hdr.y, 0, sel);         // S[j], S[j+1]
+    const uint32_t s1 = __byte_perm(hdr.z, 0, sel);         // S[4+j], S[5+j]
+    const uint32_t s2 = __byte_perm(hdr.w, 0, sel);         // S[8+j], S[9+j]
+    const uint32_t lo_sc = s0 & 0x3F3Fu, lo_mn = s1 & 0x3F3Fu;
+    const uint32_t hi_sc = (s2 & 0x0F0Fu) | ((s0 >> 2) & 0x3030u);
+    const uint32_t hi_mn = ((s2 >> 4) & 0x0F0Fu) | ((s1 >> 2) & 0x3030u);
+    sc = p < 2 ? lo_sc : hi_sc;
+    mn = p < 2 ? lo_mn : hi_mn;
+}
+
+// Contribution of this lane's pair of sub-blocks (2p, 2p+1; all 64 weights)
+// of one super-block b of a row to y.
+__device__ __forceinline__ float block_part(const uint8_t *blk, int p, int b, const uint8_t *aq,
+                                            const uint32_t *ad2, const uint32_t *as2)
+{
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * p);
+    const uint8_t *ap = aq + 80 * (4 * b + p);
+    const uint4 a00 = *reinterpret_cast<const uint4 *>(ap);
+    const uint4 a01 = *reinterpret_cast<const uint4 *>(ap + 16);
+    const uint4 a10 = *reinterpret_cast<const uint4 *>(ap + 32);
+    const uint4 a11 = *reinterpret_cast<const uint4 *>(ap + 48);
+    constexpr uint32_t LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+    int I0 = 0, I1 = 0;
+    I0 = dp4a_us(q0.x & LO, a00.x, I0);
+    I1 = dp4a_us(q0.x & HI, a10.x, I1);  // high nibbles in place: 16x the true products
+    I0 = dp4a_us(q0.y & LO, a00.y, I0);
+    I1 = dp4a_us(q0.y & HI, a10.y, I1);
+    I0 = dp4a_us(q0.z & LO, a00.z, I0);
+    I1 = dp4a_us(q0.z & HI, a10.z, I1);
+    I0 = dp4a_us(q0.w & LO, a00.w, I0);
+    I1 = dp4a_us(q0.w & HI, a10.w, I1);
+    I0 = dp4a_us(q1.x & LO, a01.x, I0);
+    I1 = dp4a_us(q1.x & HI, a11.x, I1);
+    I0 = dp4a_us(q1.y & LO, a01.y, I0);
+    I1 = dp4a_us(q1.y & HI, a11.y, I1);
+    I0 = dp4a_us(q1.z & LO, a01.z, I0);
+    I1 = dp4a_us(q1.z & HI, a11.z, I1);
+    I0 = dp4a_us(q1.w & LO, a01.w, I0);
+    I1 = dp4a_us(q1.w & HI, a11.w, I1);
+    uint32_t sc, mn;
+    q4k_pair_scales(hdr, p, sc, mn);
+    // exact integer scaling: |sc*I| <= 63*60960 < 2^22; I1 carries the factor 16
+    const int J0 = (int)(sc & 0xFFu) * I0;
+    const int J1 = (int)(sc >> 8) * (I1 >> 4);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));  // d, dmin
+    const uint32_t pair = (uint32_t)(4 * b + p);
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ad2[pair]));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&as2[pair]));
+    const float main = fmaf(d8.y, (float)J1, d8.x * (float)J0);
+    const float mins = fmaf((float)(mn >> 8), s8.y, (float)(mn & 0xFFu) * s8.x);
+    return fmaf(dd.x, main, -dd.y * mins);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const StreamParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const SmemLayout L(p.K, p.stage_alloc);
+    uint8_t *ring = smem + L.ring;
+    uint8_t *aq = smem + L.act_qs;
+    uint32_t *ad2 = reinterpret_cast<uint32_t *>(smem + L.act_d);
+    uint32_t *as2 = reinterpret_cast<uint32_t *>(smem + L.act_s);
+    float *contrib = reinterpret_cast<float *>(smem + L.contrib);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kStages;
+    __shared__ volatile int abort_s;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first_policy();
+            uint32_t it = 0;
+            for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
+                const int mat = g / p.groups_per_mat;
+                const int row0 = (g % p.groups_per_mat) * p.R;
+                const int rows = min(p.R, p.N - row0);
+                for (int pc = 0; pc < p.P; ++pc, ++it) {
+                    const uint32_t slot = it % kStages, round = it / kStages;
+                    if (round > 0 && !mbar_wait(&empty[slot], (round & 1) ^ 1, p.status)) return;
+                    const uint32_t bytes = (p.P == 1)
+                                               ? (uint32_t)rows * p.rowbytes
+                                               : (uint32_t)min(p.CB, p.nb - pc * p.CB) * kQ4KBlockBytes;
+                    const uint8_t *src = (mat ? p.W[1] : p.W[0]) + (size_t)row0 * p.rowbytes +
+                                         (size_t)pc * p.CB * kQ4KBlockBytes;
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    bulk_g2s_hint(ring + (size_t)slot * p.stage_alloc, src, bytes, &full[slot], policy);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    // stage the activation row: codes with the 80-byte group stride, scales
+    // and sums as they are (pairs of binary16 per 32-bit word)
+    {
+        const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs);
+        for (int c = tid; c < p.K / 16; c += kConsumers)
+            *reinterpret_cast<uint4 *>(aq + 80 * (c >> 2) + 16 * (c & 3)) = __ldg(gq + c);
+        const uint32_t *gd = reinterpret_cast<const uint32_t *>(p.d);
+        const uint32_t *gs = reinterpret_cast<const uint32_t *>(p.s);
+        for (int c = tid; c < p.K / 64; c += kConsumers) {
+            ad2[c] = __ldg(gd + c);
+            as2[c] = __ldg(gs + c);
+        }
+    }
+    named_bar(1, kConsumers);
+
+    const int grp = lane >> 2;          // block within the warp's step (8 per step)
+    const int pp = lane & 3;            // sub-block pair 2pp, 2pp+1
+    const unsigned gmask = 0xFu << (4 * grp);
+    uint32_t it = 0;
+    for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
+        const int mat = g / p.groups_per_mat;
+        const int row0 = (g % p.groups_per_mat) * p.R;
+        const int rows = min(p.R, p.N - row0);
+        float *yv = mat ? p.y[1] : p.y[0];
+        float row_acc = 0.0f;
+        for (int pc = 0; pc < p.P; ++pc, ++it) {
+            const uint32_t slot = it % kStages, round = it / kStages;
+            // one lane polls; then every lane observes the completed phase
+            // itself (acquire) before reading the stage
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&full[slot], round & 1, p.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok) ok = mbar_wait(&full[slot], round & 1, p.status);
+            if (!ok) abort_s = 1;
+            const uint8_t *stage = ring + (size_t)slot * p.stage_alloc;
+            float *cb = contrib + slot * kMaxBlk;
+            const int nblk = (p.P == 1) ? rows * p.nb : min(p.CB, p.nb - pc * p.CB);
+            const int bbase = pc * p.CB;
+            if (ok) {
+                // two independent blocks per lane per iteration
+                for (int t0 = warp * 8 + grp; t0 < nblk; t0 += 2 * kTasksPerStep) {
+                    const int t1 = t0 + kTasksPerStep;
+                    const bool has1 = t1 < nblk;
+                    int b0, b1;
+                    if (p.P == 1) {
+                        // nb == 1 has no 32-bit magic (it would be 2^32)
+                        const int r0 = p.nb == 1 ? t0 : (int)__umulhi((uint32_t)t0, p.nb_magic);
+                        const int r1 = p.nb == 1 ? t1 : (int)__umulhi((uint32_t)t1, p.nb_magic);
+                        b0 = t0 - r0 * p.nb;
+                        b1 = t1 - r1 * p.nb;
+                    } else {
+                        b0 = bbase + t0;
+                        b1 = bbase + t1;
+                    }
+                    float c0 = block_part(stage + (size_t)t0 * kQ4KBlockBytes, pp, b0, aq, ad2, as2);
+                    float c1 = has1 ? block_part(stage + (size_t)t1 * kQ4KBlockBytes, pp, b1, aq, ad2, as2)
+                                    : 0.0f;
+                    c0 += __shfl_xor_sync(gmask, c0, 1);
+                    c1 += __shfl_xor_sync(gmask, c1, 1);
+                    c0 += __shfl_xor_sync(gmask, c0, 2);
+                    c1 += __shfl_xor_sync(gmask, c1, 2);
+                    if (pp == 0) {
+                        cb[t0] = c0;
+                        if (has1) cb[t1] = c1;
+                    }
+                }
+            }
+            named_bar(1, kConsumers);
+            if (abort_s) return;
+            if (tid == 0) mbar_arrive(&empty[slot]);
+            if (p.P == 1) {
+                for (int r = warp; r < rows; r += kConsumerWarps) {
+                    float v = 0.0f;
+                    for (int q = lane; q < p.nb; q += 32) v += cb[r * p.nb + q];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    if (lane == 0) yv[row0 + r] = v;
+                }
+            } else if (warp == 0) {
+                float v = 0.0f;
+                for (int q = lane; q < nblk; q += 32) v += cb[q];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                row_acc += v;
+                if (pc == p.P - 1 && lane == 0) yv[row0] = row_acc;
+            }
+        }
+    }
+}
+
+size_t g_attr_bytes[64];
+
+}  // namespace
+
+bool gemv_stream_supported(int K) { return K <= kMaxK; }
+
+cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
+                               float *y2, unsigned int *status, cudaStream_t st)
+{
+    StreamParams p{};
+    p.W[0] = static_cast<const uint8_t *>(W);
+    p.W[1] = static_cast<const uint8_t *>(W2);
+    p.y[0] = y;
+    p.y[1] = y2;
+    p.N = N;
+    p.K = K;
+    p.nb = K / 256;
+    p.rowbytes = (uint32_t)p.nb * kQ4KBlockBytes;
+    const int nmat = W2 ? 2 : 1;
+    const int sms = num_sms();
+    // stage size: as large as shared memory allows (<= 64 KB), but small
+    // enough that every CTA gets >= 3 stages of work
+    const size_t fixed = SmemLayout(K, 0).total;
+    size_t cap = (kSmemLimit - fixed) / kStages / 128 * 128;
+    cap = cap > (size_t)kStageMax ? (size_t)kStageMax : cap;
+    const double total = (double)nmat * N * p.rowbytes;
+    size_t target = (size_t)(total / sms / 3);
+    target = target < 4096 ? 4096 : (target > cap ? cap : target);
+    if (p.rowbytes <= target) {
+        p.R = (int)(target / p.rowbytes);
+        p.P = 1;
+        p.CB = p.nb;
+        p.stage_alloc = (uint32_t)align_up((size_t)p.R * p.rowbytes, 128);
+    } else {
+        p.R = 1;
+        p.CB = (int)(target / kQ4KBlockBytes);
+        if (p.CB < 1) p.CB = 1;
+        p.P = (p.nb + p.CB - 1) / p.CB;
+        p.stage_alloc = (uint32_t)align_up((size_t)p.CB * kQ4KBlockBytes, 128);
+    }
+    p.nb_magic = p.nb >= 2 ? (uint32_t)((0x100000000ull + (uint64_t)p.nb - 1) / (uint64_t)p.nb) : 0u;
+    p.groups_per_mat = (N + p.R - 1) / p.R;
+    p.total_groups = p.groups_per_mat * nmat;
+    p.qs = a.qs;
+    p.d = reinterpret_cast<const __half *>(a.d);
+    p.s = reinterpret_cast<const __half *>(a.s);
+    p.status = status;
+    const SmemLayout L(K, p.stage_alloc);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_attr_bytes[dev] < L.total) {
+        cudaError_t e = cudaFuncSetAttribute(q4k_gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L.total);
+        if (e != cudaSuccess) return e;
+        g_attr_bytes[dev] = L.total;
+    }
+    const int grid = p.total_groups < sms ? p.total_groups : sms;
+    q4k_gemv_stream_kernel<<<grid, kThreads, L.total, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace zq

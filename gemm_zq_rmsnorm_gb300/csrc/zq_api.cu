@@ -14,6 +14,8 @@
 
 #include "zq_internal.cuh"
 
+__device__ unsigned int g_zq_device_status;
+
 namespace zq {
 
 namespace {
@@ -23,6 +25,7 @@ constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices];
 bool g_checked[kMaxDevices];
 int g_dev_status[kMaxDevices];
+unsigned int *g_status_word[kMaxDevices];
 std::mutex g_mu;
 
 int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -54,6 +57,14 @@ int check_device(int *dev_out)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         g_sms[dev] = sms;
         g_dev_status[dev] = (major == 10 && minor == 3) ? ZQ_OK : ZQ_ERR_DEVICE;
+        if (g_dev_status[dev] == ZQ_OK) {
+            void *w = nullptr;
+            if (cudaGetSymbolAddress(&w, g_zq_device_status) != cudaSuccess) {
+                cudaGetLastError();
+                return fail(ZQ_ERR_DEVICE, "device %d: cannot resolve the device status word", dev);
+            }
+            g_status_word[dev] = static_cast<unsigned int *>(w);
+        }
         g_checked[dev] = true;
     }
     *dev_out = dev;
@@ -87,6 +98,20 @@ int check_q4k(const void *W, int N, int K, const char *name)
 }
 
 }  // namespace
+
+unsigned int *device_status_word()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return (dev >= 0 && dev < kMaxDevices) ? g_status_word[dev] : nullptr;
+}
+
+cudaError_t launch_gemv_dispatch(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
+                                 float *y2, cudaStream_t st)
+{
+    if (gemv_stream_supported(K)) return launch_gemv_stream(W, W2, N, K, a, y, y2, device_status_word(), st);
+    return launch_gemv(W, W2, N, K, a, 1, y, y2, nullptr, st);
+}
 
 int num_sms()
 {
@@ -158,7 +183,7 @@ int zq_q4k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream)
     if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemv: y must be 16-byte aligned");
     int dev;
     if ((st = check_device(&dev))) return st;
-    return launched(launch_gemv(W, nullptr, N, K, a, 1, y, nullptr, nullptr, (cudaStream_t)stream),
+    return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, (cudaStream_t)stream),
                     "zq_q4k_gemv launch");
 }
 
@@ -174,7 +199,7 @@ int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_1 a, fl
         return fail(ZQ_ERR_ALIGN, "zq_q4k_gemv_pair: outputs must be 16-byte aligned");
     int dev;
     if ((st = check_device(&dev))) return st;
-    return launched(launch_gemv(Wg, Wu, N, K, a, 1, y_gate, y_up, nullptr, (cudaStream_t)stream),
+    return launched(launch_gemv_dispatch(Wg, Wu, N, K, a, y_gate, y_up, (cudaStream_t)stream),
                     "zq_q4k_gemv_pair launch");
 }
 
@@ -202,9 +227,22 @@ int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *w
     int dev;
     if ((st = check_device(&dev))) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    if (B == 1) return launched(launch_gemv(W, nullptr, N, K, a, 1, y, nullptr, nullptr, s), "zq_q4k_gemm (B=1)");
+    if (B == 1) return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, s), "zq_q4k_gemm (B=1)");
     if (B <= 16) return launched(launch_gemm_tc_narrow(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (chunk)");
     return launched(launch_gemm_tc_wide(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (prefill)");
+}
+
+int zq_device_status(unsigned int *flags, int clear)
+{
+    if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");
+    int dev, st;
+    if ((st = check_device(&dev))) return st;
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_zq_device_status, sizeof(unsigned int));
+    if (e == cudaSuccess && clear) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_zq_device_status, &zero, sizeof zero);
+    }
+    return launched(e, "zq_device_status");
 }
 
 int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B, int32_t *isums, int path,

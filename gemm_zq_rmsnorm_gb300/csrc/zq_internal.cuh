@@ -26,6 +26,13 @@ cudaError_t launch_gemm_tc_narrow(const void *W, int N, int K, zq_q8_1 a, int B,
                                   float *y, int32_t *isums, void *ws,
                                   cudaStream_t st);
 size_t gemm_tc_workspace_bytes(int N, int K, int B);
+bool gemv_stream_supported(int K);
+cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
+                               float *y2, unsigned int *status, cudaStream_t st);
+
+// Device-side error word of the current device (bit 0: a bounded wait in a
+// pipelined kernel expired).  Valid after the first successful device check.
+unsigned int *device_status_word();
 
 int num_sms();
 

@@ -148,6 +148,15 @@ ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
 ZQ_API size_t zq_q4k_bytes(int N, int K);
 ZQ_API size_t zq_q8_1_bytes(int B, int K);
 
+/*
+ * Device-side error word of the current device, copied to *flags (host
+ * memory; synchronous).  Bit 0 (ZQ_DEVICE_WAIT_EXPIRED): a bounded wait inside
+ * a pipelined kernel gave up -- that kernel's outputs are invalid.  The
+ * pipelined kernels never spin without a limit.  clear != 0 resets the word.
+ */
+#define ZQ_DEVICE_WAIT_EXPIRED 1u
+ZQ_API int zq_device_status(unsigned int *flags, int clear);
+
 /* Status text, last error on this thread, library version (ZQ_VERSION). */
 ZQ_API const char *zq_status_string(int status);
 ZQ_API const char *zq_last_error(void);
