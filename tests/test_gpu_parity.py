@@ -151,6 +151,46 @@ def test_isums_dp4a_bit_exact(B, K, N):
     assert np.array_equal(I.cpu().numpy(), oracle.q4k_isums(W, N, K, qs))
 
 
+@pytest.mark.parametrize("B,K,N", [(17, 256, 128), (130, 512, 200), (256, 1024, 256), (128, 768, 77)])
+def test_isums_tensor_core_bit_exact(B, K, N):
+    """The tensor-core path's per-sub-block sums, read back from TMEM, equal
+    the exact integer sums: fp16 operands and fp32 accumulation lose nothing."""
+    x, g, W = make_layer_inputs(50 + B, B, K, N)
+    qs, d, s = oracle_q8(x, g)
+    I = zq.debug_q4k_isums(to_dev(W), N, K, q8_from_oracle(qs, d, s), path=1)
+    torch.cuda.synchronize()
+    assert zq.device_status() == 0
+    assert np.array_equal(I.cpu().numpy(), oracle.q4k_isums(W, N, K, qs))
+
+
+@pytest.mark.parametrize("B,K,N", [(2, 256, 64), (4, 512, 130), (16, 1280, 200)])
+def test_isums_chunk_path_bit_exact(B, K, N):
+    x, g, W = make_layer_inputs(60 + B, B, K, N)
+    qs, d, s = oracle_q8(x, g)
+    I = zq.debug_q4k_isums(to_dev(W), N, K, q8_from_oracle(qs, d, s), path=2)
+    torch.cuda.synchronize()
+    assert np.array_equal(I.cpu().numpy(), oracle.q4k_isums(W, N, K, qs))
+
+
+def test_isums_extreme_codes_exact():
+    """Largest magnitudes: q4 = 15, sc = 63, q8 = +-127 -> |sc*I| = 63*60960."""
+    B, K, N = 128, 512, 128
+    f = inputs.q4k_fields(70, N, K)
+    f.q[...] = 15
+    f.sc[...] = 63
+    W = inputs.pack_q4k(f)
+    qs = np.where(np.arange(B * K).reshape(B, K) % 3 == 0, -127, 127).astype(np.int8)
+    qs[::2] = 127
+    d = np.full((B, K // 32), 0x2008, np.uint16)
+    s = np.full((B, K // 32), 0x3C00, np.uint16)
+    I = zq.debug_q4k_isums(to_dev(W), N, K, q8_from_oracle(qs, d, s), path=1)
+    torch.cuda.synchronize()
+    assert np.array_equal(I.cpu().numpy(), oracle.q4k_isums(W, N, K, qs))
+    y = run_gemm(W, N, K, q8_from_oracle(qs, d, s), B)
+    y_ref, S = oracle.q4k_matmul(W, N, K, qs, d, s)
+    assert_within(y, y_ref, S, "extreme codes")
+
+
 # ------------------------------------------------------------ batched GEMM
 def run_gemm(W, N, K, a, B):
     y = zq.q4k_gemm(to_dev(W), N, K, a, B)
