@@ -36,10 +36,13 @@ namespace {
 
 constexpr int BM = 128;               // tokens per tile (TMEM lanes)
 constexpr int BN = 128;               // weight rows per tile (TMEM columns)
-constexpr int kStages = 3;            // half super-block (K = 128) stages
+constexpr int kStages = 4;            // operand stages of K = 64 (two sub-blocks)
 constexpr int kAtomBytes = 128 * 128; // 128 rows x 64 fp16 (128 B), 128-byte swizzle
-constexpr int kStageBytes = 4 * kAtomBytes;  // A: 2 atoms, B: 2 atoms
+constexpr int kStageBytes = 2 * kAtomBytes;  // A atom + B atom
+constexpr int kRawSlots = 4;          // raw Q4_K tiles in flight (super-blocks)
+constexpr int kRawBytes = BN * kQ4KBlockBytes;  // 128 rows x 144 B
 constexpr int kMinBytes = 128 * 32;   // 128 rows x 16 fp16, 32-byte swizzle
+constexpr int kRing = 3;              // TMEM result buffers (sub-block or min products)
 constexpr int kWarps = 14;
 constexpr int kThreads = kWarps * 32;
 constexpr int kConvWarp0 = 2, kConvWarps = 4;
@@ -47,34 +50,34 @@ constexpr int kEpiWarp0 = 6, kEpiWarps = 8;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);   // 64 columns per epilogue thread
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD0 = 0, kColD1 = 128, kColMin = 256, kColAcc = 384;
+constexpr uint32_t kColAcc = 384;     // ring buffers at 0, 128, 256
 
 struct Smem {
     // offsets from the 1024-aligned base
-    static constexpr size_t stage(int s) { return (size_t)s * kStageBytes; }
-    static constexpr size_t a_atom(int s, int a) { return stage(s) + (size_t)a * kAtomBytes; }
-    static constexpr size_t b_atom(int s, int a) { return stage(s) + (size_t)(2 + a) * kAtomBytes; }
-    static constexpr size_t amin(int i) { return (size_t)kStages * kStageBytes + (size_t)i * 2 * kMinBytes; }
+    static constexpr size_t raw(int i) { return (size_t)i * kRawBytes; }
+    static constexpr size_t stage(int s) { return raw(kRawSlots) + (size_t)s * kStageBytes; }
+    static constexpr size_t a_atom(int s) { return stage(s); }
+    static constexpr size_t b_atom(int s) { return stage(s) + kAtomBytes; }
+    static constexpr size_t amin(int i) { return stage(kStages) + (size_t)i * 2 * kMinBytes; }
     static constexpr size_t bmin(int i) { return amin(i) + kMinBytes; }
     static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }
     static constexpr size_t bars() { return dd(2); }
-    static constexpr int kNumBars = 3 * kStages + 7 * 2 + 2;  // stage x3, seven pairs, two singles
+    static constexpr int kNumBars = 5 * kStages + 3 * 2 + 2 * kRing + 2 * 2;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }  // + alignment slack
 };
+static_assert(kRawSlots == kStages, "barrier block layout assumes equal counts");
+static_assert(Smem::total() <= 227 * 1024, "shared memory budget");
 
 struct Bars {
-    uint64_t *a_full, *b_full, *st_empty;      // [kStages]
-    uint64_t *amin_full, *bmin_full, *min_empty;  // [2]
-    uint64_t *mma_done, *epi_done;             // [2]
-    uint64_t *dd_full, *dd_free;               // [2]
-    uint64_t *min_done, *min_free;
+    uint64_t *a_full, *b_full, *st_empty, *raw_full, *raw_empty;  // [kStages]
+    uint64_t *amin_full, *bmin_full, *min_empty;                  // [2]
+    uint64_t *ring_full, *ring_empty;                             // [kRing]
+    uint64_t *dd_full, *dd_free;                                  // [2]
 };
 
 struct GemmParams {
-    const uint8_t *W;
     int N, K, B, nb;
-    uint32_t rowbytes;
     int t_tiles;
     const __half *d8;   // Q8_1 scales [B][K/32]
     float *y;           // [B][N]
@@ -97,6 +100,16 @@ __device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 of
     const uint32_t h1 = (p1 & m) | 0x64006400u;
     o0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h0), scale, off));
     o1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h1), scale, off));
+}
+
+// (c0, c1) += (a0, a1) * (b, b), one packed fp32x2 FMA
+__device__ __forceinline__ void ffma2(float &c0, float &c1, float a0, float a1, float b)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b));
 }
 
 // bounded wait that also gives up at once when another role already failed
@@ -127,26 +140,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 template <bool DEBUG>
 __global__ void __maxnreg__(128)
 q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_s,
-                     const GemmParams p)
+                     const __grid_constant__ CUtensorMap tmap_w, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     __shared__ volatile int abort_s;
 
-    uint64_t *barmem = reinterpret_cast<uint64_t *>(sm + Smem::bars());
+    uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
     Bars bar;
-    bar.a_full = barmem;
-    bar.b_full = barmem + kStages;
-    bar.st_empty = barmem + 2 * kStages;
-    bar.amin_full = barmem + 3 * kStages;
+    bar.a_full = bm;
+    bar.b_full = bm + kStages;
+    bar.st_empty = bm + 2 * kStages;
+    bar.raw_full = bm + 3 * kStages;
+    bar.raw_empty = bm + 4 * kStages;
+    bar.amin_full = bm + 5 * kStages;
     bar.bmin_full = bar.amin_full + 2;
     bar.min_empty = bar.amin_full + 4;
-    bar.mma_done = bar.amin_full + 6;
-    bar.epi_done = bar.mma_done + 2;
-    bar.dd_full = bar.mma_done + 4;
-    bar.dd_free = bar.mma_done + 6;
-    bar.min_done = bar.mma_done + 8;
-    bar.min_free = bar.mma_done + 9;
+    bar.ring_full = bar.amin_full + 6;
+    bar.ring_empty = bar.ring_full + kRing;
+    bar.dd_full = bar.ring_full + 2 * kRing;
+    bar.dd_free = bar.dd_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
     const int warp = threadIdx.x >> 5;
@@ -162,18 +175,20 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             mbar_init(&bar.a_full[s], 1);
             mbar_init(&bar.b_full[s], kConvWarps);
             mbar_init(&bar.st_empty[s], 1);
+            mbar_init(&bar.raw_full[s], 1);
+            mbar_init(&bar.raw_empty[s], kConvWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.amin_full[i], 1);
             mbar_init(&bar.bmin_full[i], kConvWarps);
             mbar_init(&bar.min_empty[i], 1);
-            mbar_init(&bar.mma_done[i], 1);
-            mbar_init(&bar.epi_done[i], kEpiWarps);
             mbar_init(&bar.dd_full[i], kConvWarps);
             mbar_init(&bar.dd_free[i], kEpiWarps);
         }
-        mbar_init(bar.min_done, 1);
-        mbar_init(bar.min_free, kEpiWarps);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&bar.ring_full[i], 1);
+            mbar_init(&bar.ring_empty[i], kEpiWarps);
+        }
         abort_s = 0;
         fence_mbar_init();
     }
@@ -188,19 +203,32 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
         if (lane == 0) {
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_s);
-            for (int q = 0; q < 2 * nb; ++q) {
-                const int b = q >> 1, h = q & 1;
-                const int slot = q % kStages, round = q / kStages;
-                if (round > 0 && !wait_ok(&bar.st_empty[slot], (round & 1) ^ 1, &abort_s, p.status)) break;
-                mbar_arrive_expect_tx(&bar.a_full[slot], 2 * kAtomBytes);
-                const int k0 = 256 * b + 128 * h;
-                tma_load_2d(sm + Smem::a_atom(slot, 0), &tmap_a, k0, t0, &bar.a_full[slot]);
-                tma_load_2d(sm + Smem::a_atom(slot, 1), &tmap_a, k0 + 64, t0, &bar.a_full[slot]);
-                if (h == 0) {
-                    const int mi = b & 1, use = b >> 1;
-                    if (use > 0 && !wait_ok(&bar.min_empty[mi], (use & 1) ^ 1, &abort_s, p.status)) break;
-                    mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
-                    tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * b, t0, &bar.amin_full[mi]);
+            prefetch_tmap(&tmap_w);
+            bool ok = true;
+            auto load_raw = [&](int bb) -> bool {
+                const int rs = bb % kRawSlots, use = bb / kRawSlots;
+                if (use > 0 && !wait_ok(&bar.raw_empty[rs], (use - 1) & 1, &abort_s, p.status)) return false;
+                mbar_arrive_expect_tx(&bar.raw_full[rs], kRawBytes);
+                tma_load_2d(sm + Smem::raw(rs), &tmap_w, kQ4KBlockBytes * bb, n0, &bar.raw_full[rs]);
+                return true;
+            };
+            for (int bb = 0; bb < nb && bb < kRawSlots - 1 && ok; ++bb) ok = load_raw(bb);
+            for (int b = 0; b < nb && ok; ++b) {
+                if (b + kRawSlots - 1 < nb && !(ok = load_raw(b + kRawSlots - 1))) break;
+                for (int i = 0; i < 4; ++i) {
+                    const int q = 4 * b + i;
+                    const int slot = q % kStages, round = q / kStages;
+                    if (round > 0 && !(ok = wait_ok(&bar.st_empty[slot], (round - 1) & 1, &abort_s, p.status)))
+                        break;
+                    mbar_arrive_expect_tx(&bar.a_full[slot], kAtomBytes);
+                    tma_load_2d(sm + Smem::a_atom(slot), &tmap_a, 256 * b + 64 * i, t0, &bar.a_full[slot]);
+                    if (i == 0) {
+                        const int mi = b & 1, use = b >> 1;
+                        if (use > 0 && !(ok = wait_ok(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status)))
+                            break;
+                        mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
+                        tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * b, t0, &bar.amin_full[mi]);
+                    }
                 }
             }
         }
@@ -208,80 +236,74 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
         // ---------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t base = smem_u32(sm);
-            for (int q = 0; q < 2 * nb; ++q) {
-                const int b = q >> 1, h = q & 1;
-                const int slot = q % kStages, round = q / kStages;
-                if (!wait_ok(&bar.a_full[slot], round & 1, &abort_s, p.status)) break;
-                if (!wait_ok(&bar.b_full[slot], round & 1, &abort_s, p.status)) break;
-                tc_fence_after();
-                bool fail = false;
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int s = 8 * b + 4 * h + jj;
-                    const int buf = s & 1, use = s >> 1;
-                    if (use > 0 && !wait_ok(&bar.epi_done[buf], (use - 1) & 1, &abort_s, p.status)) {
-                        fail = true;
-                        break;
-                    }
+            bool ok = true;
+            for (int b = 0; b < nb && ok; ++b) {
+                for (int i = 0; i < 4 && ok; ++i) {
+                    const int q = 4 * b + i;
+                    const int slot = q % kStages, round = q / kStages;
+                    ok = wait_ok(&bar.a_full[slot], round & 1, &abort_s, p.status) &&
+                         wait_ok(&bar.b_full[slot], round & 1, &abort_s, p.status);
+                    if (!ok) break;
                     tc_fence_after();
-                    const uint32_t a_at = base + (uint32_t)Smem::a_atom(slot, jj >> 1);
-                    const uint32_t b_at = base + (uint32_t)Smem::b_atom(slot, jj >> 1);
+                    const uint32_t a_at = base + (uint32_t)Smem::a_atom(slot);
+                    const uint32_t b_at = base + (uint32_t)Smem::b_atom(slot);
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int e = 9 * b + 2 * i + jj;
+                        const int buf = e % kRing, use = e / kRing;
+                        if (use > 0 && !(ok = wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status)))
+                            break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t off = (uint32_t)((jj & 1) * 64 + kk * 32);
-                        mma_f16(tmem + (buf ? kColD1 : kColD0), smem_desc(a_at + off, 16, 1024, kLayoutSw128),
-                                smem_desc(b_at + off, 16, 1024, kLayoutSw128), kIdesc, (uint32_t)kk);
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint32_t off = (uint32_t)(jj * 64 + kk * 32);
+                            mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(a_at + off, 16, 1024, kLayoutSw128),
+                                    smem_desc(b_at + off, 16, 1024, kLayoutSw128), kIdesc, (uint32_t)kk);
+                        }
+                        mma_commit(&bar.ring_full[buf]);
                     }
-                    mma_commit(&bar.mma_done[buf]);
+                    if (ok) mma_commit(&bar.st_empty[slot]);
                 }
-                if (fail) break;
-                mma_commit(&bar.st_empty[slot]);
-                if (h == 1) {
-                    const int mi = b & 1, use = b >> 1;
-                    if (!wait_ok(&bar.amin_full[mi], use & 1, &abort_s, p.status)) break;
-                    if (!wait_ok(&bar.bmin_full[mi], use & 1, &abort_s, p.status)) break;
-                    if (b > 0 && !wait_ok(bar.min_free, (b - 1) & 1, &abort_s, p.status)) break;
-                    tc_fence_after();
-                    mma_f16(tmem + kColMin,
-                            smem_desc(base + (uint32_t)Smem::amin(mi), 16, 256, kLayoutSw32),
-                            smem_desc(base + (uint32_t)Smem::bmin(mi), 16, 256, kLayoutSw32), kIdesc, 0u);
-                    mma_commit(bar.min_done);
-                    mma_commit(&bar.min_empty[mi]);
-                }
+                if (!ok) break;
+                // the super-block's min product: sum_j s8[t][bj] * m_j[n]
+                const int e = 9 * b + 8;
+                const int buf = e % kRing, use = e / kRing;
+                const int mi = b & 1, muse = b >> 1;
+                ok = wait_ok(&bar.amin_full[mi], muse & 1, &abort_s, p.status) &&
+                     wait_ok(&bar.bmin_full[mi], muse & 1, &abort_s, p.status) &&
+                     (use == 0 || wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(base + (uint32_t)Smem::amin(mi), 16, 256, kLayoutSw32),
+                        smem_desc(base + (uint32_t)Smem::bmin(mi), 16, 256, kLayoutSw32), kIdesc, 0u);
+                mma_commit(&bar.ring_full[buf]);
+                mma_commit(&bar.min_empty[mi]);
             }
         }
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------- converters
         const int r = (warp - kConvWarp0) * 32 + lane;   // row within the tile
-        const int row = n0 + r;
-        const bool valid = row < p.N;
-        const uint8_t *rowp = p.W + (size_t)(valid ? row : 0) * p.rowbytes;
-        for (int q = 0; q < 2 * nb; ++q) {
-            const int b = q >> 1, h = q & 1;
-            const int slot = q % kStages, round = q / kStages;
-            if (round > 0 && !warp_wait(&bar.st_empty[slot], (round & 1) ^ 1, &abort_s, p.status)) break;
-            const uint8_t *blk = rowp + (size_t)b * kQ4KBlockBytes;
-            uint4 hdr = make_uint4(0, 0, 0, 0), nib[4];
-            if (valid) {
-                hdr = ld_stream_u4(blk);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) nib[i] = ld_stream_u4(blk + 16 + 64 * h + 16 * i);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) nib[i] = make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-                const int jl = 4 * h + 2 * a;   // sub-blocks jl (low nibbles), jl + 1 (high)
-                uint32_t sc0, sc1, mdummy;
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, jl, sc0, mdummy);
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, jl + 1, sc1, mdummy);
+        const int sw = r & 7;
+        for (int b = 0; b < nb; ++b) {
+            const int rs = b % kRawSlots, ruse = b / kRawSlots;
+            if (!warp_wait(&bar.raw_full[rs], ruse & 1, &abort_s, p.status)) break;
+            const uint8_t *raw = sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes;
+            const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
+            bool ok = true;
+            for (int i = 0; i < 4; ++i) {
+                const int q = 4 * b + i;
+                const int slot = q % kStages, round = q / kStages;
+                if (round > 0 && !(ok = warp_wait(&bar.st_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
+                const uint4 n0v = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
+                const uint4 n1v = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
+                uint32_t sc0, sc1, md;
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
                 const float scl = DEBUG ? 1.0f : (float)sc0;
                 const float sch = DEBUG ? 1.0f : (float)sc1;
                 const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
                 const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
-                const uint32_t wv[8] = {nib[2 * a].x,     nib[2 * a].y,     nib[2 * a].z,     nib[2 * a].w,
-                                        nib[2 * a + 1].x, nib[2 * a + 1].y, nib[2 * a + 1].z, nib[2 * a + 1].w};
-                uint8_t *atom = sm + Smem::b_atom(slot, a) + (size_t)r * 128;
+                const uint32_t wv[8] = {n0v.x, n0v.y, n0v.z, n0v.w, n1v.x, n1v.y, n1v.z, n1v.w};
+                uint8_t *atom = sm + Smem::b_atom(slot) + (size_t)r * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint4 lo, hi;
@@ -289,51 +311,53 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                     nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
                     nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
                     nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
-                    *reinterpret_cast<uint4 *>(atom + ((c ^ (r & 7)) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(atom + (((c + 4) ^ (r & 7)) << 4)) = hi;
+                    *reinterpret_cast<uint4 *>(atom + ((c ^ sw) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(atom + (((c + 4) ^ sw) << 4)) = hi;
                 }
-            }
-            if (h == 0) {
-                const int mi = b & 1, use = b >> 1;
-                // mins as the B operand of the per-super-block min MMA
-                if (use > 0 && !warp_wait(&bar.min_empty[mi], (use & 1) ^ 1, &abort_s, p.status)) break;
-                uint32_t mn[8], scd;
+                if (i == 0) {
+                    const int mi = b & 1, use = b >> 1;
+                    // mins as the B operand of the min MMA; d, dmin for the epilogue
+                    if (use > 0 && !(ok = warp_wait(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status)))
+                        break;
+                    uint32_t mn[8], scd;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, mn[j]);
-                uint4 m0;
-                m0.x = h2_bits(__floats2half2_rn((float)mn[0], (float)mn[1]));
-                m0.y = h2_bits(__floats2half2_rn((float)mn[2], (float)mn[3]));
-                m0.z = h2_bits(__floats2half2_rn((float)mn[4], (float)mn[5]));
-                m0.w = h2_bits(__floats2half2_rn((float)mn[6], (float)mn[7]));
-                uint8_t *bm = sm + Smem::bmin(mi) + (size_t)r * 32;
-                const int sw = (r >> 2) & 1;
-                *reinterpret_cast<uint4 *>(bm + ((0 ^ sw) << 4)) = m0;
-                *reinterpret_cast<uint4 *>(bm + ((1 ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
-                // d, dmin for the epilogue
-                if (use > 0 && !warp_wait(&bar.dd_free[mi], (use - 1) & 1, &abort_s, p.status)) break;
-                const float2 dd = valid ? __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x))
-                                        : make_float2(0.0f, 0.0f);
-                reinterpret_cast<float2 *>(sm + Smem::dd(mi))[r] = dd;
+                    for (int j = 0; j < 8; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, mn[j]);
+                    uint4 m0;
+                    m0.x = h2_bits(__floats2half2_rn((float)mn[0], (float)mn[1]));
+                    m0.y = h2_bits(__floats2half2_rn((float)mn[2], (float)mn[3]));
+                    m0.z = h2_bits(__floats2half2_rn((float)mn[4], (float)mn[5]));
+                    m0.w = h2_bits(__floats2half2_rn((float)mn[6], (float)mn[7]));
+                    uint8_t *bmr = sm + Smem::bmin(mi) + (size_t)r * 32;
+                    const int s32 = (r >> 2) & 1;
+                    *reinterpret_cast<uint4 *>(bmr + ((0 ^ s32) << 4)) = m0;
+                    *reinterpret_cast<uint4 *>(bmr + ((1 ^ s32) << 4)) = make_uint4(0, 0, 0, 0);
+                    if (use > 0 && !(ok = warp_wait(&bar.dd_free[mi], (use - 1) & 1, &abort_s, p.status))) break;
+                    reinterpret_cast<float2 *>(sm + Smem::dd(mi))[r] =
+                        __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bar.bmin_full[mi]);
+                        mbar_arrive(&bar.dd_full[mi]);
+                    }
+                }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bar.bmin_full[mi]);
-                    mbar_arrive(&bar.dd_full[mi]);
-                }
+                if (lane == 0) mbar_arrive(&bar.b_full[slot]);
             }
-            fence_async_smem();
+            if (!ok) break;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.b_full[slot]);
+            if (lane == 0) mbar_arrive(&bar.raw_empty[rs]);
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int e = warp - kEpiWarp0;
-        const int cg = e >> 2;                    // column group: columns 64cg .. 64cg+63
+        const int e_w = warp - kEpiWarp0;
+        const int cg = e_w >> 2;                  // column group: columns 64cg .. 64cg+63
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int tl = 32 * quarter + lane;       // token within the tile
         const int tok = t0 + tl;
         const bool tvalid = tok < p.B;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(kEpiCols * cg);
         const int nsub = nb * 8;
         float inner[kEpiCols];
 #pragma unroll
@@ -346,12 +370,9 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             if (tvalid && !DEBUG && b + 1 < nb)
                 d8next = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * (b + 1)));
             for (int j = 0; j < 8; ++j) {
-                const int s = 8 * b + j;
-                const int buf = s & 1, use = s >> 1;
-                if (!warp_wait(&bar.mma_done[buf], use & 1, &abort_s, p.status)) {
-                    ok = false;
-                    break;
-                }
+                const int e = 9 * b + j;
+                const int buf = e % kRing, use = e / kRing;
+                if (!(ok = warp_wait(&bar.ring_full[buf], use & 1, &abort_s, p.status))) break;
                 tc_fence_after();
                 const uint32_t w2 = (j < 4) ? ((j < 2) ? d8raw.x : d8raw.y) : ((j < 6) ? d8raw.z : d8raw.w);
                 const uint16_t hb = (j & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xFFFFu);
@@ -359,7 +380,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
 #pragma unroll
                 for (int chunk = 0; chunk < kEpiCols / 32; ++chunk) {
                     uint32_t r[32];
-                    tmem_ld32(lane_base + (buf ? kColD1 : kColD0) + kEpiCols * cg + 32 * chunk, r);
+                    tmem_ld32(lane_base + 128u * (uint32_t)buf + 32 * chunk, r);
                     tmem_wait_ld();
                     if (DEBUG) {
                         if (tvalid) {
@@ -367,33 +388,37 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                             for (int c = 0; c < 32; ++c) {
                                 const int n = n0 + kEpiCols * cg + 32 * chunk + c;
                                 if (n < p.N)
-                                    p.isums[((size_t)tok * p.N + n) * nsub + s] = (int32_t)__uint_as_float(r[c]);
+                                    p.isums[((size_t)tok * p.N + n) * nsub + 8 * b + j] =
+                                        (int32_t)__uint_as_float(r[c]);
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            inner[32 * chunk + c] = fmaf(d8, __uint_as_float(r[c]), inner[32 * chunk + c]);
+                        for (int c = 0; c < 32; c += 2)
+                            ffma2(inner[32 * chunk + c], inner[32 * chunk + c + 1], __uint_as_float(r[c]),
+                                  __uint_as_float(r[c + 1]), d8);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.epi_done[buf]);
+                if (lane == 0) mbar_arrive(&bar.ring_empty[buf]);
             }
             if (!ok) break;
             d8raw = d8next;
-            // super-block end: acc = acc + d_b * inner - dmin_b * minsum
-            const int mi = b & 1, use = b >> 1;
-            if (!warp_wait(bar.min_done, b & 1, &abort_s, p.status)) break;
-            if (!warp_wait(&bar.dd_full[mi], use & 1, &abort_s, p.status)) break;
+            // super-block end: acc += d_b * inner - dmin_b * minsum
+            const int e = 9 * b + 8;
+            const int buf = e % kRing, use = e / kRing;
+            const int mi = b & 1, muse = b >> 1;
+            if (!(ok = warp_wait(&bar.ring_full[buf], use & 1, &abort_s, p.status))) break;
+            if (!(ok = warp_wait(&bar.dd_full[mi], muse & 1, &abort_s, p.status))) break;
             tc_fence_after();
             if (!DEBUG) {
                 const float2 *dd = reinterpret_cast<const float2 *>(sm + Smem::dd(mi)) + kEpiCols * cg;
 #pragma unroll
                 for (int q16 = 0; q16 < kEpiCols / 16; ++q16) {
                     uint32_t mr[16], ar[16];
-                    tmem_ld16(lane_base + kColMin + kEpiCols * cg + 16 * q16, mr);
-                    if (b > 0) tmem_ld16(lane_base + kColAcc + kEpiCols * cg + 16 * q16, ar);
+                    tmem_ld16(lane_base + 128u * (uint32_t)buf + 16 * q16, mr);
+                    if (b > 0) tmem_ld16(lane_base + kColAcc + 16 * q16, ar);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -403,7 +428,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                         acc = fmaf(-v.y, __uint_as_float(mr[c]), acc);
                         ar[c] = __float_as_uint(acc);
                     }
-                    tmem_st16(lane_base + kColAcc + kEpiCols * cg + 16 * q16, ar);
+                    tmem_st16(lane_base + kColAcc + 16 * q16, ar);
                 }
                 tmem_wait_st();
 #pragma unroll
@@ -412,7 +437,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(bar.min_free);
+                mbar_arrive(&bar.ring_empty[buf]);
                 mbar_arrive(&bar.dd_free[mi]);
             }
         }
@@ -420,7 +445,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             uint32_t ar[16];
 #pragma unroll
             for (int q16 = 0; q16 < kEpiCols / 16; ++q16) {
-                tmem_ld16(lane_base + kColAcc + kEpiCols * cg + 16 * q16, ar);
+                tmem_ld16(lane_base + kColAcc + 16 * q16, ar);
                 tmem_wait_ld();
                 if (tvalid) {
                     float *yrow = p.y + (size_t)tok * p.N;
@@ -480,19 +505,19 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D fp16 tensor [rows][cols] (row stride = cols*2 bytes), box box_cols x box_rows
-cudaError_t make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                      uint32_t box_rows, CUtensorMapSwizzle sw)
+// 2-D tensor [rows][cols] of `esize`-byte elements, row stride = cols*esize
+// bytes, box box_cols x box_rows; out-of-range elements read as zero
+cudaError_t make_tmap(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *base, uint64_t cols,
+                      uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * esize};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -507,18 +532,22 @@ cudaError_t launch_wide(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     q8_to_f16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(a.qs, a16, n16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    CUtensorMap ta, ts;
-    if ((e = make_tmap(&ta, a16, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    CUtensorMap ta, ts, tw;
+    const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if ((e = make_tmap(&ta, f16, 2, a16, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
-    if ((e = make_tmap(&ts, a.s, (uint64_t)K / 32, (uint64_t)B, 16, BM, CU_TENSOR_MAP_SWIZZLE_32B)) != cudaSuccess)
+    if ((e = make_tmap(&ts, f16, 2, a.s, (uint64_t)K / 32, (uint64_t)B, 16, BM, CU_TENSOR_MAP_SWIZZLE_32B)) !=
+        cudaSuccess)
+        return e;
+    // weights as bytes [N][K/256*144]: one box = one super-block of 128 rows
+    if ((e = make_tmap(&tw, u8, 1, W, (uint64_t)(K / 256) * kQ4KBlockBytes, (uint64_t)N, kQ4KBlockBytes, BN,
+                       CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
     GemmParams p{};
-    p.W = static_cast<const uint8_t *>(W);
     p.N = N;
     p.K = K;
     p.B = B;
     p.nb = K / 256;
-    p.rowbytes = (uint32_t)p.nb * kQ4KBlockBytes;
     p.t_tiles = (B + BM - 1) / BM;
     p.d8 = reinterpret_cast<const __half *>(a.d);
     p.y = y;
@@ -534,7 +563,7 @@ cudaError_t launch_wide(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
         g_attr_bytes[dev][DEBUG] = smem;
     }
     const long long grid = (long long)p.t_tiles * ((N + BN - 1) / BN);
-    q4k_gemm_wide_kernel<DEBUG><<<(unsigned)grid, kThreads, smem, st>>>(ta, ts, p);
+    q4k_gemm_wide_kernel<DEBUG><<<(unsigned)grid, kThreads, smem, st>>>(ta, ts, tw, p);
     return cudaGetLastError();
 }
 
