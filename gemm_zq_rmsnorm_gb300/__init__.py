@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_AL
 EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
            "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
-           "zq_device_status")
+           "zq_device_status", "zq_q4k_gemm_noalloc")
 
 
 class ZQError(RuntimeError):
@@ -65,6 +65,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_version": ([], i),
         "zq_debug_q4k_isums": ([P, i, i, _Q8, i, P, i, P, sz, P], i),
         "zq_device_status": ([P, i], i),
+        "zq_q4k_gemm_noalloc": ([P, i, i, _Q8, i, P, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +174,17 @@ def q4k_gemm(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.zq_q4k_gemm(_ptr(W), N, K, a._c(), B, _ptr(y), _ptr(workspace), wbytes,
                            _stream(stream)))
+    return y
+
+
+def q4k_gemm_noalloc(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
+                     y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """zq_q4k_gemm with the library's built-in scratch (no workspace; see zq.h)."""
+    lib = load()
+    B = a.B if B is None else B
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=a.qs.device)
+    _check(lib.zq_q4k_gemm_noalloc(_ptr(W), N, K, a._c(), B, _ptr(y), _stream(stream)))
     return y
 
 

@@ -232,6 +232,27 @@ int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *w
     return launched(launch_gemm_tc_wide(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (prefill)");
 }
 
+int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream)
+{
+    int st = check_q4k(W, N, K, "zq_q4k_gemm_noalloc");
+    if (st) return st;
+    if ((st = check_q8(a, "zq_q4k_gemm_noalloc"))) return st;
+    if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_q4k_gemm_noalloc: B = %d must be in [1, 65536]", B);
+    if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemm_noalloc: null y");
+    if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm_noalloc: y must be 16-byte aligned");
+    const size_t need = gemm_tc_workspace_bytes(N, K, B);
+    if (need > noalloc_scratch_bytes())
+        return fail(ZQ_ERR_WORKSPACE,
+                    "zq_q4k_gemm_noalloc: B*K = %lld needs %zu bytes of scratch, more than the built-in %zu "
+                    "(B*K <= %zu); use zq_q4k_gemm with a workspace",
+                    (long long)B * K, need, noalloc_scratch_bytes(), noalloc_scratch_bytes() / 2);
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B == 1) return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, s), "zq_q4k_gemm_noalloc (B=1)");
+    return launched(launch_gemm_noalloc(W, N, K, a, B, y, s), "zq_q4k_gemm_noalloc");
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

@@ -27,6 +27,8 @@ cudaError_t launch_gemm_tc_narrow(const void *W, int N, int K, zq_q8_1 a, int B,
                                   cudaStream_t st);
 size_t gemm_tc_workspace_bytes(int N, int K, int B);
 bool gemv_stream_supported(int K);
+size_t noalloc_scratch_bytes();
+cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
                                float *y2, unsigned int *status, cudaStream_t st);
 

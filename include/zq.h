@@ -141,6 +141,32 @@ ZQ_API int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_
 ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * zq_q4k_gemm for callers that cannot provide device memory.  (No counterpart
+ * on the pages this library follows: it is an interface for integration.)
+ * Some callers cannot allocate or pass scratch memory when they call: work
+ * recorded while a CUDA graph is being captured, engines that hand out device
+ * memory only from a fixed arena set up at start-up, plugins run by a host
+ * framework that offers them no allocator.  This entry point computes exactly
+ * what zq_q4k_gemm computes (same kernels, same results) but takes its scratch
+ * from a fixed device array inside the library instead of a workspace
+ * argument, and never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - Limit: 2*B*K bytes of scratch must fit in the array (20 MiB), i.e.
+ *     B*K <= 10485760 (for example B = 512 with K up to 20480); larger shapes
+ *     return ZQ_ERR_WORKSPACE without launching.  B = 1 needs no scratch.
+ *   - Every GPU that loads the library holds the 20 MiB array until the
+ *     process exits.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the previous call's contents
+ *     (each call overwrites what it reads).  Calls whose kernels overlap on the
+ *     GPU -- on different streams, or from several host threads without
+ *     ordering -- race on it: order them on one stream.
+ */
+ZQ_API int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
+                               void *stream);
+
 /* Bytes of device workspace zq_q4k_gemm needs for this shape (0 if none). */
 ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
 
