@@ -289,10 +289,12 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
         else:
             zq.q4k_gemm(w1, N, K, a, wl.B, y1, wl.ws)
 
-    R = max(wl.R, -(-3 * L2_BYTES // (N * K * 144 // 256 * (2 if paired and wl.B == 1 else 1))))
-    R = min(R, wl.R)
-    graphs = [capture(torch, lambda r=r: one(r), stream) for r in range(R)]
-    ms = time_graphs(torch, graphs, max(steps * 4, 20), warmup, stream)
+    # one graph holds several launches (rotating weight copies), so the timing
+    # is the kernel's device time, not the host's per-replay overhead
+    per_graph = 4 * wl.R
+    g = capture(torch, lambda: [one(i % wl.R) for i in range(per_graph)], stream)
+    reps = max(3, steps // 4)
+    ms = time_graphs(torch, [g], reps, max(1, warmup // 2), stream) / per_graph
     units = 2 if (paired and wl.B == 1) else 1
     if wl.B == 1:
         alg = proj_bytes(K, N, 1) * units - (K * (1 + 4 / 32) if units == 2 else 0)

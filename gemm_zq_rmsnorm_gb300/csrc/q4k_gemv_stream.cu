@@ -13,14 +13,15 @@
 // bulk copies of contiguous weight tiles (R whole rows, or a piece of one
 // long row; rows are contiguous, so a tile is one copy) into a ring of large
 // shared-memory stages, completing on mbarriers.  Sixteen consumer warps
-// decode each 144-byte super-block from shared memory -- four lanes per
-// block, lane p taking the 32 nibble bytes of sub-blocks 2p (low nibbles) and
+// decode the 144-byte super-blocks from shared memory in groups of four
+// lanes -- lane p takes the 32 nibble bytes of sub-blocks 2p (low nibbles) and
 // 2p+1 (high nibbles) -- and form the two 32-wide integer sums with dp4a
-// against the Q8_1 activation row staged once per CTA.  Each lane applies
-// d*sc*d8*I - dmin*m*s8 in fp32, the four lanes of a block add up, and after
-// the stage the blocks of each row are summed in a fixed order into y.  The
-// paired kernel is the same launch over the rows of both matrices, sharing the
-// staged activations.
+// against the Q8_1 activation row staged once per CTA.  A group walks a
+// strided segment of one row (up to four blocks), applies
+// d*sc*d8*I - dmin*m*s8 in fp32 and accumulates in registers; after the stage
+// the segments of each row are summed in a fixed order into y.  The paired
+// kernel is the same launch over the rows of both matrices, sharing the staged
+// activations.
 #include "zq_async.cuh"
 #include "zq_internal.cuh"
 
@@ -33,7 +34,8 @@ constexpr int kThreads = kConsumers + 32;
 constexpr int kStages = 3;
 constexpr int kStageMax = 64 * 1024;
 constexpr int kMaxBlk = kStageMax / kQ4KBlockBytes;   // 455 blocks per stage
-constexpr int kTasksPerStep = 8 * kConsumerWarps;      // blocks per warp-step
+constexpr int kGroups = 8 * kConsumerWarps;            // four-lane task groups per CTA
+constexpr int kSeg = 4;                                // max blocks per task
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxK = 32768;                           // activation staged in smem
 
@@ -47,7 +49,6 @@ struct StreamParams {
     int CB;               // blocks per piece
     int groups_per_mat;
     int total_groups;
-    uint32_t nb_magic;    // ceil(2^32 / nb) for nb >= 2: task / nb = umulhi(task, nb_magic), task < 2^16
     uint32_t stage_alloc; // bytes reserved per stage (multiple of 128)
     const int8_t *qs;
     const __half *d;
@@ -64,14 +65,13 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + 
 __host__ __device__ constexpr size_t act_bytes(int K) { return (size_t)K / 64 * 80; }
 
 struct SmemLayout {
-    size_t ring, act_qs, act_d, act_s, contrib, bars, total;
+    size_t ring, act_qs, act_ds, contrib, bars, total;
     __host__ __device__ SmemLayout(int K, uint32_t stage_alloc)
     {
         ring = 0;
         act_qs = ring + (size_t)kStages * stage_alloc;
-        act_d = align_up(act_qs + act_bytes(K), 16);
-        act_s = align_up(act_d + (size_t)K / 16, 16);
-        contrib = align_up(act_s + (size_t)K / 16, 16);
+        act_ds = align_up(act_qs + act_bytes(K), 16);     // uint2 per sub-block pair: d8 pair, s8 pair
+        contrib = align_up(act_ds + (size_t)K / 64 * 8, 16);
         bars = align_up(contrib + (size_t)kStages * kMaxBlk * 4, 8);
         total = bars + 2 * kStages * 8;
     }
@@ -103,7 +103,7 @@ __device__ __forceinline__ void q4k_pair_scales(const uint4 &hdr, int p, uint32_
 // Contribution of this lane's pair of sub-blocks (2p, 2p+1; all 64 weights)
 // of one super-block b of a row to y.
 __device__ __forceinline__ float block_part(const uint8_t *blk, int p, int b, const uint8_t *aq,
-                                            const uint32_t *ad2, const uint32_t *as2)
+                                            const uint2 *ads)
 {
     const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);
@@ -137,9 +137,9 @@ __device__ __forceinline__ float block_part(const uint8_t *blk, int p, int b, co
     const int J0 = (int)(sc & 0xFFu) * I0;
     const int J1 = (int)(sc >> 8) * (I1 >> 4);
     const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));  // d, dmin
-    const uint32_t pair = (uint32_t)(4 * b + p);
-    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ad2[pair]));
-    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&as2[pair]));
+    const uint2 ds = ads[4 * b + p];
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.y));
     const float main = fmaf(d8.y, (float)J1, d8.x * (float)J0);
     const float mins = fmaf((float)(mn >> 8), s8.y, (float)(mn & 0xFFu) * s8.x);
     return fmaf(dd.x, main, -dd.y * mins);
@@ -151,8 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
     const SmemLayout L(p.K, p.stage_alloc);
     uint8_t *ring = smem + L.ring;
     uint8_t *aq = smem + L.act_qs;
-    uint32_t *ad2 = reinterpret_cast<uint32_t *>(smem + L.act_d);
-    uint32_t *as2 = reinterpret_cast<uint32_t *>(smem + L.act_s);
+    uint2 *ads = reinterpret_cast<uint2 *>(smem + L.act_ds);
     float *contrib = reinterpret_cast<float *>(smem + L.contrib);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kStages;
@@ -206,16 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
             *reinterpret_cast<uint4 *>(aq + 80 * (c >> 2) + 16 * (c & 3)) = __ldg(gq + c);
         const uint32_t *gd = reinterpret_cast<const uint32_t *>(p.d);
         const uint32_t *gs = reinterpret_cast<const uint32_t *>(p.s);
-        for (int c = tid; c < p.K / 64; c += kConsumers) {
-            ad2[c] = __ldg(gd + c);
-            as2[c] = __ldg(gs + c);
-        }
+        for (int c = tid; c < p.K / 64; c += kConsumers) ads[c] = make_uint2(__ldg(gd + c), __ldg(gs + c));
     }
     named_bar(1, kConsumers);
 
-    const int grp = lane >> 2;          // block within the warp's step (8 per step)
-    const int pp = lane & 3;            // sub-block pair 2pp, 2pp+1
-    const unsigned gmask = 0xFu << (4 * grp);
+    // Work of a stage: each row's blocks are split into nseg strided segments
+    // (segment s takes blocks s, s + nseg, ...); a task is one (row, segment)
+    // and runs on one group of four lanes, which accumulates in registers.
+    // Neighbouring groups take neighbouring segments, i.e. neighbouring blocks,
+    // so their shared-memory reads fall in different bank groups.
+    const int G = warp * 8 + (lane >> 2);   // task group, 128 per CTA
+    const int pp = lane & 3;                // sub-block pair 2pp, 2pp+1
+    const unsigned gmask = 0xFu << (4 * (lane >> 2));
     uint32_t it = 0;
     for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
         const int mat = g / p.groups_per_mat;
@@ -234,35 +235,27 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
             if (!ok) abort_s = 1;
             const uint8_t *stage = ring + (size_t)slot * p.stage_alloc;
             float *cb = contrib + slot * kMaxBlk;
-            const int nblk = (p.P == 1) ? rows * p.nb : min(p.CB, p.nb - pc * p.CB);
+            // blocks per row in this stage and where they start in the row
+            const int rowblk = (p.P == 1) ? p.nb : min(p.CB, p.nb - pc * p.CB);
             const int bbase = pc * p.CB;
+            const int nrows = (p.P == 1) ? rows : 1;
+            const int nseg = (rowblk + kSeg - 1) / kSeg;
+            const int ntask = nrows * nseg;
             if (ok) {
-                // two independent blocks per lane per iteration
-                for (int t0 = warp * 8 + grp; t0 < nblk; t0 += 2 * kTasksPerStep) {
-                    const int t1 = t0 + kTasksPerStep;
-                    const bool has1 = t1 < nblk;
-                    int b0, b1;
-                    if (p.P == 1) {
-                        // nb == 1 has no 32-bit magic (it would be 2^32)
-                        const int r0 = p.nb == 1 ? t0 : (int)__umulhi((uint32_t)t0, p.nb_magic);
-                        const int r1 = p.nb == 1 ? t1 : (int)__umulhi((uint32_t)t1, p.nb_magic);
-                        b0 = t0 - r0 * p.nb;
-                        b1 = t1 - r1 * p.nb;
-                    } else {
-                        b0 = bbase + t0;
-                        b1 = bbase + t1;
+                for (int t = G; t < ntask; t += kGroups) {
+                    const int r = t / nseg;
+                    const int sg = t - r * nseg;
+                    const uint8_t *rowp = stage + (size_t)r * rowblk * kQ4KBlockBytes;
+                    float c = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kSeg; ++i) {
+                        const int lb = sg + i * nseg;   // block within this stage's row
+                        if (lb < rowblk)
+                            c += block_part(rowp + (size_t)lb * kQ4KBlockBytes, pp, bbase + lb, aq, ads);
                     }
-                    float c0 = block_part(stage + (size_t)t0 * kQ4KBlockBytes, pp, b0, aq, ad2, as2);
-                    float c1 = has1 ? block_part(stage + (size_t)t1 * kQ4KBlockBytes, pp, b1, aq, ad2, as2)
-                                    : 0.0f;
-                    c0 += __shfl_xor_sync(gmask, c0, 1);
-                    c1 += __shfl_xor_sync(gmask, c1, 1);
-                    c0 += __shfl_xor_sync(gmask, c0, 2);
-                    c1 += __shfl_xor_sync(gmask, c1, 2);
-                    if (pp == 0) {
-                        cb[t0] = c0;
-                        if (has1) cb[t1] = c1;
-                    }
+                    c += __shfl_xor_sync(gmask, c, 1);
+                    c += __shfl_xor_sync(gmask, c, 2);
+                    if (pp == 0) cb[t] = c;
                 }
             }
             named_bar(1, kConsumers);
@@ -270,15 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
             if (tid == 0) mbar_arrive(&empty[slot]);
             if (p.P == 1) {
                 for (int r = warp; r < rows; r += kConsumerWarps) {
-                    float v = 0.0f;
-                    for (int q = lane; q < p.nb; q += 32) v += cb[r * p.nb + q];
+                    float v = lane < nseg ? cb[r * nseg + lane] : 0.0f;
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                     if (lane == 0) yv[row0 + r] = v;
                 }
             } else if (warp == 0) {
                 float v = 0.0f;
-                for (int q = lane; q < nblk; q += 32) v += cb[q];
+                for (int q = lane; q < nseg; q += 32) v += cb[q];
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
                 row_acc += v;
@@ -328,7 +320,6 @@ cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q
         p.P = (p.nb + p.CB - 1) / p.CB;
         p.stage_alloc = (uint32_t)align_up((size_t)p.CB * kQ4KBlockBytes, 128);
     }
-    p.nb_magic = p.nb >= 2 ? (uint32_t)((0x100000000ull + (uint64_t)p.nb - 1) / (uint64_t)p.nb) : 0u;
     p.groups_per_mat = (N + p.R - 1) / p.R;
     p.total_groups = p.groups_per_mat * nmat;
     p.qs = a.qs;

@@ -4,40 +4,157 @@
 // activation packing share one wide per-token kernel, saving a second read of
 // the activations and a launch.
 //
-// One CTA of 256 threads per token.  Thread t owns the 32-element blocks
-// b = t, t+256, t+512, ... of its token, which is exactly the slot layout of
-// the fixed summation order of the library's definition (per-block fused
-// multiply-add chain, per-slot sum over b = t mod 256, pairwise tree over the
-// 256 slots).  Every floating-point step is an explicitly rounded IEEE fp32
-// operation (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so the
-// codes and scales are reproducible bit for bit on any conforming
-// implementation of the same definition.
+// The sum of squares follows the library's fixed order: per 32-element block
+// a fused multiply-add chain over its squares in index order (p_b); 256 slots,
+// slot t the sum of p_b over b = t (mod 256) in increasing b; a pairwise tree
+// over the slots.  Every floating-point step is an explicitly rounded IEEE
+// fp32 operation (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so
+// codes and scales are reproducible bit for bit.
+//
+// One CTA per token with one thread per 32-element block (up to 1024
+// threads): every block's fma chain runs in parallel, the partials go through
+// shared memory in block order, the block stays in registers between the two
+// passes, and only the 256-slot sums and the tree are serial.  Rows of up to
+// 2048 blocks (K <= 65536) give a thread two blocks; wider rows use a 256-thread
+// kernel in which thread t owns the blocks of slot t.
 //
 // HBM roofline: reads B*K*4 bytes of x (+ K*4 of gamma, cached), writes
-// B*K*(1 + 4/32) bytes.  The kernel is tiny next to the projections that
-// consume its output.
+// B*K*(1 + 4/32) bytes.  At B = 1 the kernel is latency-bound.
 #include "zq_internal.cuh"
 
 namespace zq {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxBlocks = 2048;   // K <= 65536 on this path
 
-__global__ void __launch_bounds__(kThreads)
-rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma,
-                    int K, float eps, int8_t *__restrict__ qs,
-                    __half *__restrict__ dq, __half *__restrict__ sq)
+// Quantise one 32-value block (already normalised) to Q8_1 and store it.
+__device__ __forceinline__ void pack_block(const float (&xh)[32], int8_t *qdst, __half *dq, __half *sq)
 {
-    __shared__ float slot_s[kThreads];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xh[i]));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    int sum = 0;
+    uint32_t packed[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float q = roundf(__fmul_rn(xh[4 * v + c], id));
+            q = fminf(fmaxf(q, -127.0f), 127.0f);
+            const int qi = (int)q;
+            sum += qi;
+            word |= ((uint32_t)(qi & 0xFF)) << (8 * c);
+        }
+        packed[v] = word;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(qdst);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    *dq = __float2half_rn(d);
+    *sq = __float2half_rn(__fmul_rn(d, (float)sum));
+}
+
+__global__ void __launch_bounds__(kMaxThreads)
+rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma, int K, float eps,
+                    int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq)
+{
+    __shared__ float part_s[kMaxBlocks];   // p_b, in block order
+    __shared__ float slot_s[256];
     __shared__ float r_s;
 
     const int t = threadIdx.x;
+    const int nthr = blockDim.x;
     const int nblk = K >> 5;
     const float *xt = x + (size_t)blockIdx.x * K;
+    const bool one = nblk <= nthr;   // one block per thread: keep it in registers
 
-    // pass 1: slot t = sum over its blocks of the per-block fma chain
+    // pass 1: p_b for every block
+    float xr[32];
+    for (int b = t; b < nblk; b += nthr) {
+        const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float4 f = __ldg(p + v);
+            xr[4 * v + 0] = f.x;
+            xr[4 * v + 1] = f.y;
+            xr[4 * v + 2] = f.z;
+            xr[4 * v + 3] = f.w;
+        }
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part = __fmaf_rn(xr[i], xr[i], part);
+        part_s[b] = part;
+    }
+    __syncthreads();
+    // slot t: blocks t, t + 256, ... added in increasing b, from +0
+    if (t < 256) {
+        float slot = 0.0f;
+        for (int b = t; b < nblk; b += 256) slot = __fadd_rn(slot, part_s[b]);
+        slot_s[t] = slot;
+    }
+    __syncthreads();
+    // pairwise tree, off = 128 .. 32 through shared memory, 16 .. 1 in a warp
+#pragma unroll
+    for (int off = 128; off >= 32; off >>= 1) {
+        if (t < off) slot_s[t] = __fadd_rn(slot_s[t], slot_s[t + off]);
+        __syncthreads();
+    }
+    if (t < 32) {
+        float v = slot_s[t];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+        if (t == 0) {
+            const float mean = __fdiv_rn(v, (float)K);
+            r_s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        }
+    }
+    __syncthreads();
+    const float r = r_s;
+
+    // pass 2: normalise and pack each block
+    for (int b = t; b < nblk; b += nthr) {
+        if (!one) {
+            const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 f = __ldg(p + v);
+                xr[4 * v + 0] = f.x;
+                xr[4 * v + 1] = f.y;
+                xr[4 * v + 2] = f.z;
+                xr[4 * v + 3] = f.w;
+            }
+        }
+        const float4 *g = reinterpret_cast<const float4 *>(gamma + 32 * b);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {   // normalise in place
+            const float4 w = __ldg(g + v);
+            xr[4 * v + 0] = __fmul_rn(__fmul_rn(xr[4 * v + 0], r), w.x);
+            xr[4 * v + 1] = __fmul_rn(__fmul_rn(xr[4 * v + 1], r), w.y);
+            xr[4 * v + 2] = __fmul_rn(__fmul_rn(xr[4 * v + 2], r), w.z);
+            xr[4 * v + 3] = __fmul_rn(__fmul_rn(xr[4 * v + 3], r), w.w);
+        }
+        const size_t o = (size_t)blockIdx.x * nblk + b;
+        pack_block(xr, qs + (size_t)blockIdx.x * K + 32 * b, dq + o, sq + o);
+    }
+}
+
+// Rows wider than kMaxBlocks blocks: one CTA of 256 threads per token, thread
+// t owning the blocks t, t+256, ... (its slot), re-reading x in pass 2.
+__global__ void __launch_bounds__(256)
+rmsnorm_q8_1_wide_kernel(const float *__restrict__ x, const float *__restrict__ gamma, int K, float eps,
+                         int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq)
+{
+    __shared__ float slot_s[256];
+    __shared__ float r_s;
+    const int t = threadIdx.x;
+    const int nblk = K >> 5;
+    const float *xt = x + (size_t)blockIdx.x * K;
     float slot = 0.0f;
-    for (int b = t; b < nblk; b += kThreads) {
+    for (int b = t; b < nblk; b += 256) {
         const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
         float part = 0.0f;
 #pragma unroll
@@ -52,7 +169,6 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
     }
     slot_s[t] = slot;
     __syncthreads();
-    // pairwise tree, off = 128 .. 32 through shared memory
 #pragma unroll
     for (int off = 128; off >= 32; off >>= 1) {
         if (t < off) slot_s[t] = __fadd_rn(slot_s[t], slot_s[t + off]);
@@ -60,7 +176,6 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
     }
     if (t < 32) {
         float v = slot_s[t];
-        // off = 16 .. 1 within the first warp: lane l < off adds lane l + off
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
         if (t == 0) {
@@ -70,13 +185,10 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
     }
     __syncthreads();
     const float r = r_s;
-
-    // pass 2: normalise and pack each owned block
-    for (int b = t; b < nblk; b += kThreads) {
+    for (int b = t; b < nblk; b += 256) {
         const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
         const float4 *g = reinterpret_cast<const float4 *>(gamma + 32 * b);
         float xh[32];
-        float amax = 0.0f;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             const float4 f = __ldg(p + v);
@@ -86,42 +198,26 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
             xh[4 * v + 2] = __fmul_rn(__fmul_rn(f.z, r), w.z);
             xh[4 * v + 3] = __fmul_rn(__fmul_rn(f.w, r), w.w);
         }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xh[i]));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-        int sum = 0;
-        uint32_t packed[8];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float q = roundf(__fmul_rn(xh[4 * v + c], id));
-                q = fminf(fmaxf(q, -127.0f), 127.0f);
-                const int qi = (int)q;
-                sum += qi;
-                word |= ((uint32_t)(qi & 0xFF)) << (8 * c);
-            }
-            packed[v] = word;
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(qs + (size_t)blockIdx.x * K + 32 * b);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
         const size_t o = (size_t)blockIdx.x * nblk + b;
-        dq[o] = __float2half_rn(d);
-        sq[o] = __float2half_rn(__fmul_rn(d, (float)sum));
+        pack_block(xh, qs + (size_t)blockIdx.x * K + 32 * b, dq + o, sq + o);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K,
-                                float eps, zq_q8_1 out, cudaStream_t st)
+cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float eps, zq_q8_1 out,
+                                cudaStream_t st)
 {
-    rmsnorm_q8_1_kernel<<<B, kThreads, 0, st>>>(
-        x, gamma, K, eps, out.qs, reinterpret_cast<__half *>(out.d),
-        reinterpret_cast<__half *>(out.s));
+    const int nblk = K / 32;
+    __half *dq = reinterpret_cast<__half *>(out.d);
+    __half *sq = reinterpret_cast<__half *>(out.s);
+    if (nblk <= kMaxBlocks) {
+        int threads = nblk < kMaxThreads ? (nblk + 31) / 32 * 32 : kMaxThreads;
+        if (threads < 256) threads = 256;   // the slot tree needs 256 threads
+        rmsnorm_q8_1_kernel<<<B, threads, 0, st>>>(x, gamma, K, eps, out.qs, dq, sq);
+    } else {
+        rmsnorm_q8_1_wide_kernel<<<B, 256, 0, st>>>(x, gamma, K, eps, out.qs, dq, sq);
+    }
     return cudaGetLastError();
 }
 

@@ -95,6 +95,10 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return p;
 }
 
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy / MMA) accesses of the same memory.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Named barrier over `threads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t threads)
 {
