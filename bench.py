@@ -39,6 +39,22 @@ METRIC = "Q4_K GEMV HBM GB/s (B=1) & GEMM int8 TOPS (B=512), % of GB300 roofline
 L2_BYTES = 129 * 1024 * 1024
 
 
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu capture (profiles/traffic.json),
+    or None when the kernel source changed since the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["sha256_16"]:
+        return None
+    return int(rec["dram_bytes"])
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -417,7 +433,8 @@ def main():
             "roofline": {"bound": "hbm", "kernel": f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}",
                          "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
-                         "traffic": None, "kernel_ms": round(dms, 5)},
+                         "traffic": recorded_traffic(f"q4k_gemv_stream_pair_{dK}x{dN}") if dp else None,
+                         "kernel_ms": round(dms, 5)},
             "gpu_launches": wl_dec.launches_per_step() * args.steps,
             "clocks": clk.summary(),
         })
@@ -453,7 +470,8 @@ def main():
                                 "frac": round(ach / pk["bf16_tflops"], 4),
                                 "peak_source": pk["source"] + " bf16 dense burst (fp16 operands run at the bf16 rate; "
                                                "int8 tcgen05 is not available on sm_103a)",
-                                "traffic": None, "kernel_ms": round(dms, 5)},
+                                "traffic": recorded_traffic(f"q4k_gemm_wide_{B}x{dK}x{dN}"),
+                                "kernel_ms": round(dms, 5)},
                    "gpu_launches": wl.launches_per_step() * max(3, args.steps // 5), "clocks": clk.summary()}
             sub.append(rec)
             del wl
