@@ -22,10 +22,13 @@
 // zeros) in TMEM, and the epilogue folds acc += d_b*inner - dmin_b*minsum into
 // an fp32 accumulator kept in TMEM.
 //
-// Warp roles (14 warps): 0 TMA producer (fp16 activation tiles, s8 tiles),
-// 1 MMA issuer + TMEM owner, 2-5 weight converters (Q4_K bytes -> sc*q fp16
-// in the 128-byte-swizzled K-major layout, mins, d/dmin), 6-13 epilogue
-// (2 column groups of 64 x 4 lane quarters).  Every wait is bounded.
+// Warp roles (20 warps): 0 TMA producer (fp16 activation tiles in a
+// six-stage ring, s8 tiles, raw Q4_K tiles two super-blocks ahead), 1 MMA
+// issuer + TMEM owner, 2-3 weight converters (Q4_K bytes -> sc*q fp16 in the
+// 128-byte-swizzled K-major layout, two rows per thread, three-stage ring;
+// mins; d/dmin), 4-19 epilogue (4 column groups of 32 x 4 lane quarters),
+// which hand each TMEM buffer back right after reading it.  Every wait is
+// bounded.
 #include <cuda.h>
 
 #include "zq_internal.cuh"
@@ -36,44 +39,45 @@ namespace {
 
 constexpr int BM = 128;               // tokens per tile (TMEM lanes)
 constexpr int BN = 128;               // weight rows per tile (TMEM columns)
-constexpr int kStages = 4;            // operand stages of K = 64 (two sub-blocks)
+constexpr int kAStages = 6;           // activation operand stages of K = 64 (two sub-blocks)
+constexpr int kBStages = 3;           // converted weight operand stages of K = 64
 constexpr int kAtomBytes = 128 * 128; // 128 rows x 64 fp16 (128 B), 128-byte swizzle
-constexpr int kStageBytes = 2 * kAtomBytes;  // A atom + B atom
-constexpr int kRawSlots = 4;          // raw Q4_K tiles in flight (super-blocks)
+constexpr int kRawSlots = 3;          // raw Q4_K tiles in flight (super-blocks)
 constexpr int kRawBytes = BN * kQ4KBlockBytes;  // 128 rows x 144 B
 constexpr int kMinBytes = 128 * 32;   // 128 rows x 16 fp16, 32-byte swizzle
 constexpr int kRing = 3;              // TMEM result buffers (sub-block or min products)
-constexpr int kWarps = 14;
+constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
-constexpr int kConvWarp0 = 2, kConvWarps = 4;
-constexpr int kEpiWarp0 = 6, kEpiWarps = 8;
-constexpr int kEpiCols = BN / (kEpiWarps / 4);   // 64 columns per epilogue thread
+constexpr int kConvWarp0 = 2, kConvWarps = 2;   // each converter thread owns two weight rows
+constexpr int kEpiWarp0 = 4, kEpiWarps = 16;
+constexpr int kEpiCols = BN / (kEpiWarps / 4);   // 32 columns per epilogue thread
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColAcc = 384;     // ring buffers at 0, 128, 256
 
 struct Smem {
     // offsets from the 1024-aligned base
-    static constexpr size_t raw(int i) { return (size_t)i * kRawBytes; }
-    static constexpr size_t stage(int s) { return raw(kRawSlots) + (size_t)s * kStageBytes; }
-    static constexpr size_t a_atom(int s) { return stage(s); }
-    static constexpr size_t b_atom(int s) { return stage(s) + kAtomBytes; }
-    static constexpr size_t amin(int i) { return stage(kStages) + (size_t)i * 2 * kMinBytes; }
+    static constexpr size_t a_atom(int s) { return (size_t)s * kAtomBytes; }
+    static constexpr size_t b_atom(int s) { return a_atom(kAStages) + (size_t)s * kAtomBytes; }
+    static constexpr size_t raw(int i) { return b_atom(kBStages) + (size_t)i * kRawBytes; }
+    static constexpr size_t amin(int i) { return raw(kRawSlots) + (size_t)i * 2 * kMinBytes; }
     static constexpr size_t bmin(int i) { return amin(i) + kMinBytes; }
     static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }
     static constexpr size_t bars() { return dd(2); }
-    static constexpr int kNumBars = 5 * kStages + 3 * 2 + 2 * kRing + 2 * 2;
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawSlots + 3 * 2 + 2 * kRing + 2 * 2;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }  // + alignment slack
 };
-static_assert(kRawSlots == kStages, "barrier block layout assumes equal counts");
 static_assert(Smem::total() <= 227 * 1024, "shared memory budget");
+static_assert(kRawBytes % 1024 == 0, "raw slots keep the operand atoms 1024-byte aligned");
 
 struct Bars {
-    uint64_t *a_full, *b_full, *st_empty, *raw_full, *raw_empty;  // [kStages]
-    uint64_t *amin_full, *bmin_full, *min_empty;                  // [2]
-    uint64_t *ring_full, *ring_empty;                             // [kRing]
-    uint64_t *dd_full, *dd_free;                                  // [2]
+    uint64_t *a_full, *a_empty;                   // [kAStages]
+    uint64_t *b_full, *b_empty;                   // [kBStages]
+    uint64_t *raw_full, *raw_empty;               // [kRawSlots]
+    uint64_t *amin_full, *bmin_full, *min_empty;  // [2]
+    uint64_t *ring_full, *ring_empty;             // [kRing]
+    uint64_t *dd_full, *dd_free;                  // [2]
 };
 
 struct GemmParams {
@@ -138,7 +142,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 template <bool DEBUG>
-__global__ void __maxnreg__(128)
+__global__ void __maxnreg__(96)
 q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_s,
                      const __grid_constant__ CUtensorMap tmap_w, const GemmParams p)
 {
@@ -149,16 +153,17 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
     Bars bar;
     bar.a_full = bm;
-    bar.b_full = bm + kStages;
-    bar.st_empty = bm + 2 * kStages;
-    bar.raw_full = bm + 3 * kStages;
-    bar.raw_empty = bm + 4 * kStages;
-    bar.amin_full = bm + 5 * kStages;
+    bar.a_empty = bar.a_full + kAStages;
+    bar.b_full = bar.a_empty + kAStages;
+    bar.b_empty = bar.b_full + kBStages;
+    bar.raw_full = bar.b_empty + kBStages;
+    bar.raw_empty = bar.raw_full + kRawSlots;
+    bar.amin_full = bar.raw_empty + kRawSlots;
     bar.bmin_full = bar.amin_full + 2;
-    bar.min_empty = bar.amin_full + 4;
-    bar.ring_full = bar.amin_full + 6;
+    bar.min_empty = bar.bmin_full + 2;
+    bar.ring_full = bar.min_empty + 2;
     bar.ring_empty = bar.ring_full + kRing;
-    bar.dd_full = bar.ring_full + 2 * kRing;
+    bar.dd_full = bar.ring_empty + kRing;
     bar.dd_free = bar.dd_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
@@ -169,12 +174,24 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     const int t0 = t_tile * BM;
     const int n0 = n_tile * BN;
     const int nb = p.nb;
+    const int nq = 4 * nb;   // operand stages (K = 64 each)
+    // Each CTA walks the super-blocks in its own rotated order, so the CTAs
+    // that share an activation tile (and those that share a weight tile) do not
+    // all request the same L2 lines at the same time.  The fp32 sums are
+    // order-free; the integer sub-block sums are unaffected.
+    const int rot = (n_tile + 5 * t_tile) % nb;
+    auto sb = [&](int b) { return b + rot < nb ? b + rot : b + rot - nb; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kAStages; ++s) {
             mbar_init(&bar.a_full[s], 1);
+            mbar_init(&bar.a_empty[s], 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
             mbar_init(&bar.b_full[s], kConvWarps);
-            mbar_init(&bar.st_empty[s], 1);
+            mbar_init(&bar.b_empty[s], 1);
+        }
+        for (int s = 0; s < kRawSlots; ++s) {
             mbar_init(&bar.raw_full[s], 1);
             mbar_init(&bar.raw_empty[s], kConvWarps);
         }
@@ -205,30 +222,32 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             prefetch_tmap(&tmap_s);
             prefetch_tmap(&tmap_w);
             bool ok = true;
+            // raw weight tiles run kRawSlots - 1 super-blocks ahead of the
+            // activation tiles; activation stage q = 4b + i
+            int next_raw = 0;
             auto load_raw = [&](int bb) -> bool {
                 const int rs = bb % kRawSlots, use = bb / kRawSlots;
                 if (use > 0 && !wait_ok(&bar.raw_empty[rs], (use - 1) & 1, &abort_s, p.status)) return false;
                 mbar_arrive_expect_tx(&bar.raw_full[rs], kRawBytes);
-                tma_load_2d(sm + Smem::raw(rs), &tmap_w, kQ4KBlockBytes * bb, n0, &bar.raw_full[rs]);
+                tma_load_2d(sm + Smem::raw(rs), &tmap_w, kQ4KBlockBytes * sb(bb), n0, &bar.raw_full[rs]);
                 return true;
             };
-            for (int bb = 0; bb < nb && bb < kRawSlots - 1 && ok; ++bb) ok = load_raw(bb);
-            for (int b = 0; b < nb && ok; ++b) {
-                if (b + kRawSlots - 1 < nb && !(ok = load_raw(b + kRawSlots - 1))) break;
-                for (int i = 0; i < 4; ++i) {
-                    const int q = 4 * b + i;
-                    const int slot = q % kStages, round = q / kStages;
-                    if (round > 0 && !(ok = wait_ok(&bar.st_empty[slot], (round - 1) & 1, &abort_s, p.status)))
-                        break;
-                    mbar_arrive_expect_tx(&bar.a_full[slot], kAtomBytes);
-                    tma_load_2d(sm + Smem::a_atom(slot), &tmap_a, 256 * b + 64 * i, t0, &bar.a_full[slot]);
-                    if (i == 0) {
-                        const int mi = b & 1, use = b >> 1;
-                        if (use > 0 && !(ok = wait_ok(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status)))
-                            break;
-                        mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
-                        tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * b, t0, &bar.amin_full[mi]);
-                    }
+            for (; next_raw < nb && next_raw < kRawSlots - 1 && ok; ++next_raw) ok = load_raw(next_raw);
+            for (int q = 0; q < nq && ok; ++q) {
+                const int b = q >> 2, i = q & 3;
+                if (i == 0 && next_raw < nb) {
+                    if (!(ok = load_raw(next_raw))) break;
+                    ++next_raw;
+                }
+                const int slot = q % kAStages, round = q / kAStages;
+                if (round > 0 && !(ok = wait_ok(&bar.a_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
+                mbar_arrive_expect_tx(&bar.a_full[slot], kAtomBytes);
+                tma_load_2d(sm + Smem::a_atom(slot), &tmap_a, 256 * sb(b) + 64 * i, t0, &bar.a_full[slot]);
+                if (i == 0) {
+                    const int mi = b & 1, use = b >> 1;
+                    if (use > 0 && !(ok = wait_ok(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
+                    mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
+                    tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * sb(b), t0, &bar.amin_full[mi]);
                 }
             }
         }
@@ -237,103 +256,116 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
         if (lane == 0) {
             const uint32_t base = smem_u32(sm);
             bool ok = true;
-            for (int b = 0; b < nb && ok; ++b) {
-                for (int i = 0; i < 4 && ok; ++i) {
-                    const int q = 4 * b + i;
-                    const int slot = q % kStages, round = q / kStages;
-                    ok = wait_ok(&bar.a_full[slot], round & 1, &abort_s, p.status) &&
-                         wait_ok(&bar.b_full[slot], round & 1, &abort_s, p.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t a_at = base + (uint32_t)Smem::a_atom(slot);
-                    const uint32_t b_at = base + (uint32_t)Smem::b_atom(slot);
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int e = 9 * b + 2 * i + jj;
-                        const int buf = e % kRing, use = e / kRing;
-                        if (use > 0 && !(ok = wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status)))
-                            break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            const uint32_t off = (uint32_t)(jj * 64 + kk * 32);
-                            mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(a_at + off, 16, 1024, kLayoutSw128),
-                                    smem_desc(b_at + off, 16, 1024, kLayoutSw128), kIdesc, (uint32_t)kk);
-                        }
-                        mma_commit(&bar.ring_full[buf]);
-                    }
-                    if (ok) mma_commit(&bar.st_empty[slot]);
-                }
-                if (!ok) break;
-                // the super-block's min product: sum_j s8[t][bj] * m_j[n]
-                const int e = 9 * b + 8;
-                const int buf = e % kRing, use = e / kRing;
-                const int mi = b & 1, muse = b >> 1;
-                ok = wait_ok(&bar.amin_full[mi], muse & 1, &abort_s, p.status) &&
-                     wait_ok(&bar.bmin_full[mi], muse & 1, &abort_s, p.status) &&
-                     (use == 0 || wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status));
+            for (int q = 0; q < nq && ok; ++q) {
+                const int b = q >> 2, i = q & 3;
+                const int as = q % kAStages, bs = q % kBStages;
+                ok = wait_ok(&bar.a_full[as], (q / kAStages) & 1, &abort_s, p.status) &&
+                     wait_ok(&bar.b_full[bs], (q / kBStages) & 1, &abort_s, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(base + (uint32_t)Smem::amin(mi), 16, 256, kLayoutSw32),
-                        smem_desc(base + (uint32_t)Smem::bmin(mi), 16, 256, kLayoutSw32), kIdesc, 0u);
-                mma_commit(&bar.ring_full[buf]);
-                mma_commit(&bar.min_empty[mi]);
+                const uint32_t a_at = base + (uint32_t)Smem::a_atom(as);
+                const uint32_t b_at = base + (uint32_t)Smem::b_atom(bs);
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int e = 9 * b + 2 * i + jj;
+                    const int buf = e % kRing, use = e / kRing;
+                    if (use > 0 && !(ok = wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t off = (uint32_t)(jj * 64 + kk * 32);
+                        mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(a_at + off, 16, 1024, kLayoutSw128),
+                                smem_desc(b_at + off, 16, 1024, kLayoutSw128), kIdesc, (uint32_t)kk);
+                    }
+                    mma_commit(&bar.ring_full[buf]);
+                }
+                if (!ok) break;
+                mma_commit(&bar.a_empty[as]);
+                mma_commit(&bar.b_empty[bs]);
+                if (i == 3) {
+                    // the super-block's min product: sum_j s8[t][bj] * m_j[n]
+                    const int e = 9 * b + 8;
+                    const int buf = e % kRing, use = e / kRing;
+                    const int mi = b & 1, muse = b >> 1;
+                    ok = wait_ok(&bar.amin_full[mi], muse & 1, &abort_s, p.status) &&
+                         wait_ok(&bar.bmin_full[mi], muse & 1, &abort_s, p.status) &&
+                         (use == 0 || wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_f16(tmem + 128u * (uint32_t)buf,
+                            smem_desc(base + (uint32_t)Smem::amin(mi), 16, 256, kLayoutSw32),
+                            smem_desc(base + (uint32_t)Smem::bmin(mi), 16, 256, kLayoutSw32), kIdesc, 0u);
+                    mma_commit(&bar.ring_full[buf]);
+                    mma_commit(&bar.min_empty[mi]);
+                }
             }
         }
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------- converters
-        const int r = (warp - kConvWarp0) * 32 + lane;   // row within the tile
-        const int sw = r & 7;
+        // thread r converts weight rows r and r + 64 of the tile
+        const int r0 = (warp - kConvWarp0) * 32 + lane;
         for (int b = 0; b < nb; ++b) {
             const int rs = b % kRawSlots, ruse = b / kRawSlots;
             if (!warp_wait(&bar.raw_full[rs], ruse & 1, &abort_s, p.status)) break;
-            const uint8_t *raw = sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes;
-            const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
+            const uint8_t *rawbase = sm + Smem::raw(rs);
+            const uint4 hdr0 = *reinterpret_cast<const uint4 *>(rawbase + (size_t)r0 * kQ4KBlockBytes);
+            const uint4 hdr1 = *reinterpret_cast<const uint4 *>(rawbase + (size_t)(r0 + 64) * kQ4KBlockBytes);
             bool ok = true;
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 4 && ok; ++i) {
                 const int q = 4 * b + i;
-                const int slot = q % kStages, round = q / kStages;
-                if (round > 0 && !(ok = warp_wait(&bar.st_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
-                const uint4 n0v = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
-                const uint4 n1v = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
-                uint32_t sc0, sc1, md;
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
-                const float scl = DEBUG ? 1.0f : (float)sc0;
-                const float sch = DEBUG ? 1.0f : (float)sc1;
-                const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
-                const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
-                const uint32_t wv[8] = {n0v.x, n0v.y, n0v.z, n0v.w, n1v.x, n1v.y, n1v.z, n1v.w};
-                uint8_t *atom = sm + Smem::b_atom(slot) + (size_t)r * 128;
+                const int bs = q % kBStages, round = q / kBStages;
+                if (round > 0 && !(ok = warp_wait(&bar.b_empty[bs], (round - 1) & 1, &abort_s, p.status))) break;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 lo, hi;
-                    nib4_to_h2<false>(wv[2 * c], s_lo, o_lo, lo.x, lo.y);
-                    nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
-                    nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
-                    nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
-                    *reinterpret_cast<uint4 *>(atom + ((c ^ sw) << 4)) = lo;
-                    *reinterpret_cast<uint4 *>(atom + (((c + 4) ^ sw) << 4)) = hi;
+                for (int h = 0; h < 2; ++h) {
+                    const int r = r0 + 64 * h;
+                    const uint4 &hdr = h ? hdr1 : hdr0;
+                    const uint8_t *raw = rawbase + (size_t)r * kQ4KBlockBytes;
+                    const uint4 n0v = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
+                    const uint4 n1v = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
+                    uint32_t sc0, sc1, md;
+                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
+                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
+                    const float scl = DEBUG ? 1.0f : (float)sc0;
+                    const float sch = DEBUG ? 1.0f : (float)sc1;
+                    const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
+                    const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
+                    const uint32_t wv[8] = {n0v.x, n0v.y, n0v.z, n0v.w, n1v.x, n1v.y, n1v.z, n1v.w};
+                    uint8_t *atom = sm + Smem::b_atom(bs) + (size_t)r * 128;
+                    const int sw = r & 7;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 lo, hi;
+                        nib4_to_h2<false>(wv[2 * c], s_lo, o_lo, lo.x, lo.y);
+                        nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
+                        nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
+                        nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
+                        *reinterpret_cast<uint4 *>(atom + ((c ^ sw) << 4)) = lo;
+                        *reinterpret_cast<uint4 *>(atom + (((c + 4) ^ sw) << 4)) = hi;
+                    }
                 }
                 if (i == 0) {
                     const int mi = b & 1, use = b >> 1;
                     // mins as the B operand of the min MMA; d, dmin for the epilogue
-                    if (use > 0 && !(ok = warp_wait(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status)))
-                        break;
-                    uint32_t mn[8], scd;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, mn[j]);
-                    uint4 m0;
-                    m0.x = h2_bits(__floats2half2_rn((float)mn[0], (float)mn[1]));
-                    m0.y = h2_bits(__floats2half2_rn((float)mn[2], (float)mn[3]));
-                    m0.z = h2_bits(__floats2half2_rn((float)mn[4], (float)mn[5]));
-                    m0.w = h2_bits(__floats2half2_rn((float)mn[6], (float)mn[7]));
-                    uint8_t *bmr = sm + Smem::bmin(mi) + (size_t)r * 32;
-                    const int s32 = (r >> 2) & 1;
-                    *reinterpret_cast<uint4 *>(bmr + ((0 ^ s32) << 4)) = m0;
-                    *reinterpret_cast<uint4 *>(bmr + ((1 ^ s32) << 4)) = make_uint4(0, 0, 0, 0);
+                    if (use > 0 && !(ok = warp_wait(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
                     if (use > 0 && !(ok = warp_wait(&bar.dd_free[mi], (use - 1) & 1, &abort_s, p.status))) break;
-                    reinterpret_cast<float2 *>(sm + Smem::dd(mi))[r] =
-                        __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = r0 + 64 * h;
+                        const uint4 &hdr = h ? hdr1 : hdr0;
+                        uint32_t mn[8], scd;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, mn[j]);
+                        uint4 m0;
+                        m0.x = h2_bits(__floats2half2_rn((float)mn[0], (float)mn[1]));
+                        m0.y = h2_bits(__floats2half2_rn((float)mn[2], (float)mn[3]));
+                        m0.z = h2_bits(__floats2half2_rn((float)mn[4], (float)mn[5]));
+                        m0.w = h2_bits(__floats2half2_rn((float)mn[6], (float)mn[7]));
+                        uint8_t *bmr = sm + Smem::bmin(mi) + (size_t)r * 32;
+                        const int s32 = (r >> 2) & 1;
+                        *reinterpret_cast<uint4 *>(bmr + ((0 ^ s32) << 4)) = m0;
+                        *reinterpret_cast<uint4 *>(bmr + ((1 ^ s32) << 4)) = make_uint4(0, 0, 0, 0);
+                        reinterpret_cast<float2 *>(sm + Smem::dd(mi))[r] =
+                            __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+                    }
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -343,7 +375,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.b_full[slot]);
+                if (lane == 0) mbar_arrive(&bar.b_full[bs]);
             }
             if (!ok) break;
             __syncwarp();
@@ -352,7 +384,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     } else {
         // ---------------------------------------------------- epilogue
         const int e_w = warp - kEpiWarp0;
-        const int cg = e_w >> 2;                  // column group: columns 64cg .. 64cg+63
+        const int cg = e_w >> 2;                  // column group: columns 32cg .. 32cg+31
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
         const int tl = 32 * quarter + lane;       // token within the tile
         const int tok = t0 + tl;
@@ -363,45 +395,41 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
 #pragma unroll
         for (int c = 0; c < kEpiCols; ++c) inner[c] = 0.0f;
         uint4 d8raw = make_uint4(0, 0, 0, 0);
-        if (tvalid && !DEBUG) d8raw = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub));
+        if (tvalid && !DEBUG) d8raw = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(0)));
         bool ok = true;
         for (int b = 0; b < nb && ok; ++b) {
             uint4 d8next = make_uint4(0, 0, 0, 0);
             if (tvalid && !DEBUG && b + 1 < nb)
-                d8next = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * (b + 1)));
+                d8next = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(b + 1)));
             for (int j = 0; j < 8; ++j) {
                 const int e = 9 * b + j;
                 const int buf = e % kRing, use = e / kRing;
                 if (!(ok = warp_wait(&bar.ring_full[buf], use & 1, &abort_s, p.status))) break;
                 tc_fence_after();
-                const uint32_t w2 = (j < 4) ? ((j < 2) ? d8raw.x : d8raw.y) : ((j < 6) ? d8raw.z : d8raw.w);
-                const uint16_t hb = (j & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xFFFFu);
-                const float d8 = __half2float(__ushort_as_half(hb));
-#pragma unroll
-                for (int chunk = 0; chunk < kEpiCols / 32; ++chunk) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_base + 128u * (uint32_t)buf + 32 * chunk, r);
-                    tmem_wait_ld();
-                    if (DEBUG) {
-                        if (tvalid) {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) {
-                                const int n = n0 + kEpiCols * cg + 32 * chunk + c;
-                                if (n < p.N)
-                                    p.isums[((size_t)tok * p.N + n) * nsub + 8 * b + j] =
-                                        (int32_t)__uint_as_float(r[c]);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 2)
-                            ffma2(inner[32 * chunk + c], inner[32 * chunk + c + 1], __uint_as_float(r[c]),
-                                  __uint_as_float(r[c + 1]), d8);
-                    }
-                }
+                uint32_t r[32];
+                tmem_ld32(lane_base + 128u * (uint32_t)buf, r);
+                tmem_wait_ld();
+                // hand the buffer back before the arithmetic
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.ring_empty[buf]);
+                if (DEBUG) {
+                    if (tvalid) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int n = n0 + kEpiCols * cg + c;
+                            if (n < p.N)
+                                p.isums[((size_t)tok * p.N + n) * nsub + 8 * sb(b) + j] = (int32_t)__uint_as_float(r[c]);
+                        }
+                    }
+                } else {
+                    const uint32_t w2 = (j < 4) ? ((j < 2) ? d8raw.x : d8raw.y) : ((j < 6) ? d8raw.z : d8raw.w);
+                    const uint16_t hb = (j & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xFFFFu);
+                    const float d8 = __half2float(__ushort_as_half(hb));
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2)
+                        ffma2(inner[c], inner[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), d8);
+                }
             }
             if (!ok) break;
             d8raw = d8next;
