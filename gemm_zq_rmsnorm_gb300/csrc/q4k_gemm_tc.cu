@@ -15,20 +15,23 @@
 // (<= 945, exact in binary16).  Every product and every partial sum of a
 // sub-block is an integer below 2^22, so the fp32 tensor-core accumulator
 // holds sc_j * I exactly.  Per sub-block the MMA (M = 128 tokens, N = 128
-// weight rows, K = 32 as two K = 16 steps) writes one of two TMEM buffers;
-// epilogue warps read it back and accumulate inner += d8 * D in registers
-// (d8 is a per-lane scalar: TMEM lanes are tokens).  Once per super-block a
-// second MMA forms sum_j s8[t][bj] * m_j[n] (K = 16: eight mins and eight
-// zeros) in TMEM, and the epilogue folds acc += d_b*inner - dmin_b*minsum into
-// an fp32 accumulator kept in TMEM.
+// weight rows, K = 32 as two K = 16 steps) writes one of four TMEM buffers
+// (all 512 columns); epilogue warps read it back and fold it into an fp32
+// accumulator held in registers, acc += d_b * (d8 * D) (d8 is a per-lane
+// scalar: TMEM lanes are tokens; d_b a per-column one).  Once per super-block
+// a second MMA forms sum_j s8[t][bj] * m_j[n] (K = 16: eight mins and eight
+// zeros) in a buffer of the same ring, and the epilogue subtracts
+// dmin_b * minsum.
 //
 // Warp roles (20 warps): 0 TMA producer (fp16 activation tiles in a
 // six-stage ring, s8 tiles, raw Q4_K tiles two super-blocks ahead), 1 MMA
 // issuer + TMEM owner, 2-3 weight converters (Q4_K bytes -> sc*q fp16 in the
 // 128-byte-swizzled K-major layout, two rows per thread, three-stage ring;
 // mins; d/dmin), 4-19 epilogue (4 column groups of 32 x 4 lane quarters),
-// which hand each TMEM buffer back right after reading it.  Every wait is
-// bounded.
+// which hand each TMEM buffer back right after reading it.  The issuer keeps
+// its loop to descriptor additions and counter updates: one thread feeds the
+// tensor pipe, so its instruction count per MMA bounds the kernel.  Every
+// wait is bounded.
 #include <cuda.h>
 
 #include "zq_internal.cuh"
@@ -45,7 +48,7 @@ constexpr int kAtomBytes = 128 * 128; // 128 rows x 64 fp16 (128 B), 128-byte sw
 constexpr int kRawSlots = 3;          // raw Q4_K tiles in flight (super-blocks)
 constexpr int kRawBytes = BN * kQ4KBlockBytes;  // 128 rows x 144 B
 constexpr int kMinBytes = 128 * 32;   // 128 rows x 16 fp16, 32-byte swizzle
-constexpr int kRing = 3;              // TMEM result buffers (sub-block or min products)
+constexpr int kRing = 4;              // TMEM result buffers (sub-block or min products)
 constexpr int kWarps = 20;
 constexpr int kThreads = kWarps * 32;
 constexpr int kConvWarp0 = 2, kConvWarps = 2;   // each converter thread owns two weight rows
@@ -53,7 +56,8 @@ constexpr int kEpiWarp0 = 4, kEpiWarps = 16;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);   // 32 columns per epilogue thread
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc = 384;     // ring buffers at 0, 128, 256
+static_assert(kRing * BN == (int)kTmemCols, "the result ring fills tensor memory");
+static_assert((kRing & (kRing - 1)) == 0, "ring index by mask");
 
 struct Smem {
     // offsets from the 1024-aligned base
@@ -62,7 +66,7 @@ struct Smem {
     static constexpr size_t raw(int i) { return b_atom(kBStages) + (size_t)i * kRawBytes; }
     static constexpr size_t amin(int i) { return raw(kRawSlots) + (size_t)i * 2 * kMinBytes; }
     static constexpr size_t bmin(int i) { return amin(i) + kMinBytes; }
-    static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }
+    static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }  // d[BN] then dmin[BN]
     static constexpr size_t bars() { return dd(2); }
     static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawSlots + 3 * 2 + 2 * kRing + 2 * 2;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
@@ -70,6 +74,7 @@ struct Smem {
 };
 static_assert(Smem::total() <= 227 * 1024, "shared memory budget");
 static_assert(kRawBytes % 1024 == 0, "raw slots keep the operand atoms 1024-byte aligned");
+static_assert(Smem::total() < (1u << 18), "descriptor start addresses stay inside their 14-bit field");
 
 struct Bars {
     uint64_t *a_full, *a_empty;                   // [kAStages]
@@ -106,19 +111,18 @@ __device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 of
     o1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h1), scale, off));
 }
 
-// (c0, c1) += (a0, a1) * (b, b), one packed fp32x2 FMA
-__device__ __forceinline__ void ffma2(float &c0, float &c1, float a0, float a1, float b)
+// (c0, c1) += (d0, d1) * ((a0, a1) * (s, s)): two packed fp32x2 operations
+__device__ __forceinline__ void scale_acc2(float &c0, float &c1, float a0, float a1, float s, float d0, float d1)
 {
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%0, %1};\n\t"
-        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+    asm("{\n\t.reg .b64 ra, rs, rd, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\tmov.b64 rd, {%5, %6};\n\tmov.b64 rc, {%0, %1};\n\t"
+        "mul.rn.f32x2 ra, ra, rs;\n\tfma.rn.f32x2 rc, rd, ra, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
         : "+f"(c0), "+f"(c1)
-        : "f"(a0), "f"(a1), "f"(b));
+        : "f"(a0), "f"(a1), "f"(s), "f"(d0), "f"(d1));
 }
 
 // bounded wait that also gives up at once when another role already failed
-__device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                        unsigned int *status)
+__device__ __noinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *status)
 {
     if (*abort_flag) return false;
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
@@ -130,14 +134,21 @@ __device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile
     return false;
 }
 
+// one probe inline, the bounded loop only when the phase is not complete yet
+__device__ __forceinline__ bool wait_fast(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status)
+{
+    return mbar_try_wait(bar, parity) || wait_ok(bar, parity, abort_flag, status);
+}
+
 // one lane polls, then every lane acquires the completed phase itself
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                          unsigned int *status)
 {
     bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_ok(bar, parity, abort_flag, status);
+    if ((threadIdx.x & 31) == 0) ok = wait_fast(bar, parity, abort_flag, status);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) ok = wait_ok(bar, parity, abort_flag, status);
+    if (ok) ok = wait_fast(bar, parity, abort_flag, status);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -227,7 +238,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             int next_raw = 0;
             auto load_raw = [&](int bb) -> bool {
                 const int rs = bb % kRawSlots, use = bb / kRawSlots;
-                if (use > 0 && !wait_ok(&bar.raw_empty[rs], (use - 1) & 1, &abort_s, p.status)) return false;
+                if (use > 0 && !wait_fast(&bar.raw_empty[rs], (use - 1) & 1, &abort_s, p.status)) return false;
                 mbar_arrive_expect_tx(&bar.raw_full[rs], kRawBytes);
                 tma_load_2d(sm + Smem::raw(rs), &tmap_w, kQ4KBlockBytes * sb(bb), n0, &bar.raw_full[rs]);
                 return true;
@@ -240,12 +251,12 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                     ++next_raw;
                 }
                 const int slot = q % kAStages, round = q / kAStages;
-                if (round > 0 && !(ok = wait_ok(&bar.a_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
+                if (round > 0 && !(ok = wait_fast(&bar.a_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
                 mbar_arrive_expect_tx(&bar.a_full[slot], kAtomBytes);
                 tma_load_2d(sm + Smem::a_atom(slot), &tmap_a, 256 * sb(b) + 64 * i, t0, &bar.a_full[slot]);
                 if (i == 0) {
                     const int mi = b & 1, use = b >> 1;
-                    if (use > 0 && !(ok = wait_ok(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
+                    if (use > 0 && !(ok = wait_fast(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
                     mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
                     tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * sb(b), t0, &bar.amin_full[mi]);
                 }
@@ -255,48 +266,56 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
         // ---------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t base = smem_u32(sm);
+            // descriptors of stage 0 / min slot 0; every other operand tile is
+            // reached by adding its byte offset / 16 to the start-address field
+            const uint64_t a_desc0 = smem_desc(base + (uint32_t)Smem::a_atom(0), 16, 1024, kLayoutSw128);
+            const uint64_t b_desc0 = smem_desc(base + (uint32_t)Smem::b_atom(0), 16, 1024, kLayoutSw128);
+            const uint64_t amin_desc0 = smem_desc(base + (uint32_t)Smem::amin(0), 16, 256, kLayoutSw32);
+            const uint64_t bmin_desc0 = smem_desc(base + (uint32_t)Smem::bmin(0), 16, 256, kLayoutSw32);
+            constexpr uint32_t kAtom16 = kAtomBytes >> 4, kMinSlot16 = (2 * kMinBytes) >> 4;
+            int as = 0, bs = 0;
+            uint32_t aph = 0, bph = 0, e = 0;   // e: ring entries issued so far
             bool ok = true;
-            for (int q = 0; q < nq && ok; ++q) {
-                const int b = q >> 2, i = q & 3;
-                const int as = q % kAStages, bs = q % kBStages;
-                ok = wait_ok(&bar.a_full[as], (q / kAStages) & 1, &abort_s, p.status) &&
-                     wait_ok(&bar.b_full[bs], (q / kBStages) & 1, &abort_s, p.status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t a_at = base + (uint32_t)Smem::a_atom(as);
-                const uint32_t b_at = base + (uint32_t)Smem::b_atom(bs);
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int e = 9 * b + 2 * i + jj;
-                    const int buf = e % kRing, use = e / kRing;
-                    if (use > 0 && !(ok = wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status))) break;
-                    tc_fence_after();
+            for (int b = 0; b < nb && ok; ++b) {
+                for (int i = 0; i < 4; ++i) {
+                    if (!(ok = wait_fast(&bar.a_full[as], aph, &abort_s, p.status) &&
+                               wait_fast(&bar.b_full[bs], bph, &abort_s, p.status)))
+                        break;
+                    const uint64_t ad = a_desc0 + (uint64_t)(as * kAtom16);
+                    const uint64_t bd = b_desc0 + (uint64_t)(bs * kAtom16);
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t off = (uint32_t)(jj * 64 + kk * 32);
-                        mma_f16(tmem + 128u * (uint32_t)buf, smem_desc(a_at + off, 16, 1024, kLayoutSw128),
-                                smem_desc(b_at + off, 16, 1024, kLayoutSw128), kIdesc, (uint32_t)kk);
+                    for (int jj = 0; jj < 2; ++jj, ++e) {
+                        const uint32_t buf = e & (kRing - 1);
+                        if (e >= (uint32_t)kRing &&
+                            !(ok = wait_fast(&bar.ring_empty[buf], ((e / kRing) - 1) & 1, &abort_s, p.status)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem + (uint32_t)BN * buf;
+                        mma_f16(d_tmem, ad + (uint64_t)(jj * 4), bd + (uint64_t)(jj * 4), kIdesc, 0u);
+                        mma_f16(d_tmem, ad + (uint64_t)(jj * 4 + 2), bd + (uint64_t)(jj * 4 + 2), kIdesc, 1u);
+                        mma_commit(&bar.ring_full[buf]);
                     }
-                    mma_commit(&bar.ring_full[buf]);
+                    if (!ok) break;
+                    mma_commit(&bar.a_empty[as]);
+                    mma_commit(&bar.b_empty[bs]);
+                    if (++as == kAStages) { as = 0; aph ^= 1u; }
+                    if (++bs == kBStages) { bs = 0; bph ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(&bar.a_empty[as]);
-                mma_commit(&bar.b_empty[bs]);
-                if (i == 3) {
-                    // the super-block's min product: sum_j s8[t][bj] * m_j[n]
-                    const int e = 9 * b + 8;
-                    const int buf = e % kRing, use = e / kRing;
-                    const int mi = b & 1, muse = b >> 1;
-                    ok = wait_ok(&bar.amin_full[mi], muse & 1, &abort_s, p.status) &&
-                         wait_ok(&bar.bmin_full[mi], muse & 1, &abort_s, p.status) &&
-                         (use == 0 || wait_ok(&bar.ring_empty[buf], (use - 1) & 1, &abort_s, p.status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    mma_f16(tmem + 128u * (uint32_t)buf,
-                            smem_desc(base + (uint32_t)Smem::amin(mi), 16, 256, kLayoutSw32),
-                            smem_desc(base + (uint32_t)Smem::bmin(mi), 16, 256, kLayoutSw32), kIdesc, 0u);
-                    mma_commit(&bar.ring_full[buf]);
-                    mma_commit(&bar.min_empty[mi]);
-                }
+                // the super-block's min product: sum_j s8[t][bj] * m_j[n]
+                const int mi = b & 1;
+                const uint32_t mpar = (uint32_t)(b >> 1) & 1u, buf = e & (kRing - 1);
+                if (!(ok = wait_fast(&bar.amin_full[mi], mpar, &abort_s, p.status) &&
+                           wait_fast(&bar.bmin_full[mi], mpar, &abort_s, p.status) &&
+                           (e < (uint32_t)kRing ||
+                            wait_fast(&bar.ring_empty[buf], ((e / kRing) - 1) & 1, &abort_s, p.status))))
+                    break;
+                tc_fence_after();
+                mma_f16(tmem + (uint32_t)BN * buf, amin_desc0 + (uint64_t)(mi * kMinSlot16),
+                        bmin_desc0 + (uint64_t)(mi * kMinSlot16), kIdesc, 0u);
+                mma_commit(&bar.ring_full[buf]);
+                mma_commit(&bar.min_empty[mi]);
+                ++e;
             }
         }
     } else if (warp < kEpiWarp0) {
@@ -347,6 +366,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                     // mins as the B operand of the min MMA; d, dmin for the epilogue
                     if (use > 0 && !(ok = warp_wait(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
                     if (use > 0 && !(ok = warp_wait(&bar.dd_free[mi], (use - 1) & 1, &abort_s, p.status))) break;
+                    float *ddp = reinterpret_cast<float *>(sm + Smem::dd(mi));
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int r = r0 + 64 * h;
@@ -363,8 +383,9 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                         const int s32 = (r >> 2) & 1;
                         *reinterpret_cast<uint4 *>(bmr + ((0 ^ s32) << 4)) = m0;
                         *reinterpret_cast<uint4 *>(bmr + ((1 ^ s32) << 4)) = make_uint4(0, 0, 0, 0);
-                        reinterpret_cast<float2 *>(sm + Smem::dd(mi))[r] =
-                            __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+                        const float2 dm = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+                        ddp[r] = dm.x;
+                        ddp[BN + r] = dm.y;
                     }
                     fence_async_smem();
                     __syncwarp();
@@ -391,30 +412,33 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
         const bool tvalid = tok < p.B;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(kEpiCols * cg);
         const int nsub = nb * 8;
-        float inner[kEpiCols];
+        float acc[kEpiCols];
 #pragma unroll
-        for (int c = 0; c < kEpiCols; ++c) inner[c] = 0.0f;
+        for (int c = 0; c < kEpiCols; ++c) acc[c] = 0.0f;
         uint4 d8raw = make_uint4(0, 0, 0, 0);
         if (tvalid && !DEBUG) d8raw = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(0)));
         bool ok = true;
+        uint32_t e = 0;   // ring entries consumed so far
         for (int b = 0; b < nb && ok; ++b) {
+            const int mi = b & 1, muse = b >> 1;
             uint4 d8next = make_uint4(0, 0, 0, 0);
             if (tvalid && !DEBUG && b + 1 < nb)
                 d8next = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(b + 1)));
-            for (int j = 0; j < 8; ++j) {
-                const int e = 9 * b + j;
-                const int buf = e % kRing, use = e / kRing;
-                if (!(ok = warp_wait(&bar.ring_full[buf], use & 1, &abort_s, p.status))) break;
+            if (!(ok = warp_wait(&bar.dd_full[mi], muse & 1, &abort_s, p.status))) break;
+            const float *dcol = reinterpret_cast<const float *>(sm + Smem::dd(mi)) + kEpiCols * cg;
+            for (int j = 0; j < 9; ++j, ++e) {   // j = 8: the min product
+                const uint32_t buf = e & (kRing - 1);
+                if (!(ok = warp_wait(&bar.ring_full[buf], (e / kRing) & 1, &abort_s, p.status))) break;
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld32(lane_base + 128u * (uint32_t)buf, r);
+                tmem_ld32(lane_base + (uint32_t)BN * buf, r);
                 tmem_wait_ld();
                 // hand the buffer back before the arithmetic
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.ring_empty[buf]);
                 if (DEBUG) {
-                    if (tvalid) {
+                    if (tvalid && j < 8) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
                             const int n = n0 + kEpiCols * cg + c;
@@ -422,67 +446,45 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                                 p.isums[((size_t)tok * p.N + n) * nsub + 8 * sb(b) + j] = (int32_t)__uint_as_float(r[c]);
                         }
                     }
-                } else {
+                } else if (j < 8) {
                     const uint32_t w2 = (j < 4) ? ((j < 2) ? d8raw.x : d8raw.y) : ((j < 6) ? d8raw.z : d8raw.w);
                     const uint16_t hb = (j & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xFFFFu);
                     const float d8 = __half2float(__ushort_as_half(hb));
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2)
-                        ffma2(inner[c], inner[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), d8);
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 dv = *reinterpret_cast<const float4 *>(dcol + c);
+                        scale_acc2(acc[c], acc[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), d8, dv.x, dv.y);
+                        scale_acc2(acc[c + 2], acc[c + 3], __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), d8,
+                                   dv.z, dv.w);
+                    }
+                } else {
+                    // super-block end: acc -= dmin_b * minsum
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 mv = *reinterpret_cast<const float4 *>(dcol + BN + c);
+                        acc[c] = fmaf(-mv.x, __uint_as_float(r[c]), acc[c]);
+                        acc[c + 1] = fmaf(-mv.y, __uint_as_float(r[c + 1]), acc[c + 1]);
+                        acc[c + 2] = fmaf(-mv.z, __uint_as_float(r[c + 2]), acc[c + 2]);
+                        acc[c + 3] = fmaf(-mv.w, __uint_as_float(r[c + 3]), acc[c + 3]);
+                    }
                 }
             }
             if (!ok) break;
             d8raw = d8next;
-            // super-block end: acc += d_b * inner - dmin_b * minsum
-            const int e = 9 * b + 8;
-            const int buf = e % kRing, use = e / kRing;
-            const int mi = b & 1, muse = b >> 1;
-            if (!(ok = warp_wait(&bar.ring_full[buf], use & 1, &abort_s, p.status))) break;
-            if (!(ok = warp_wait(&bar.dd_full[mi], muse & 1, &abort_s, p.status))) break;
-            tc_fence_after();
-            if (!DEBUG) {
-                const float2 *dd = reinterpret_cast<const float2 *>(sm + Smem::dd(mi)) + kEpiCols * cg;
-#pragma unroll
-                for (int q16 = 0; q16 < kEpiCols / 16; ++q16) {
-                    uint32_t mr[16], ar[16];
-                    tmem_ld16(lane_base + 128u * (uint32_t)buf + 16 * q16, mr);
-                    if (b > 0) tmem_ld16(lane_base + kColAcc + 16 * q16, ar);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float2 v = dd[16 * q16 + c];
-                        float acc = b > 0 ? __uint_as_float(ar[c]) : 0.0f;
-                        acc = fmaf(v.x, inner[16 * q16 + c], acc);
-                        acc = fmaf(-v.y, __uint_as_float(mr[c]), acc);
-                        ar[c] = __float_as_uint(acc);
-                    }
-                    tmem_st16(lane_base + kColAcc + 16 * q16, ar);
-                }
-                tmem_wait_st();
-#pragma unroll
-                for (int c = 0; c < kEpiCols; ++c) inner[c] = 0.0f;
-            }
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar.ring_empty[buf]);
-                mbar_arrive(&bar.dd_free[mi]);
-            }
+            if (lane == 0) mbar_arrive(&bar.dd_free[mi]);
         }
-        if (ok && !abort_s && !DEBUG) {
-            uint32_t ar[16];
+        if (ok && !abort_s && !DEBUG && tvalid) {
+            float *yrow = p.y + (size_t)tok * p.N + n0 + kEpiCols * cg;
+            const int ncols = min(kEpiCols, p.N - (n0 + kEpiCols * cg));
+            if (ncols == kEpiCols && (p.N & 3) == 0) {
 #pragma unroll
-            for (int q16 = 0; q16 < kEpiCols / 16; ++q16) {
-                tmem_ld16(lane_base + kColAcc + 16 * q16, ar);
-                tmem_wait_ld();
-                if (tvalid) {
-                    float *yrow = p.y + (size_t)tok * p.N;
+                for (int c = 0; c < kEpiCols; c += 4)
+                    *reinterpret_cast<float4 *>(yrow + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+            } else {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int n = n0 + kEpiCols * cg + 16 * q16 + c;
-                        if (n < p.N) yrow[n] = __uint_as_float(ar[c]);
-                    }
-                }
+                for (int c = 0; c < kEpiCols; ++c)
+                    if (c < ncols) yrow[c] = acc[c];
             }
         }
     }
