@@ -1,7 +1,8 @@
 // q4k_gemm_noalloc.cu -- zq_q4k_gemm without a caller-supplied workspace.
 //
-// The batched projection needs scratch device memory (an fp16 copy of the
-// activation codes that the tensor cores read).  zq_q4k_gemm takes it from the
+// The batched projection needs scratch device memory (the binary16 hi/lo
+// split of the activations that the tensor cores read, and a per-token
+// scale).  zq_q4k_gemm takes it from the
 // caller.  Some callers cannot hand out or obtain device memory at the point of
 // the call: code that runs while a CUDA graph is being captured (where
 // allocating would break the capture), engines that own every byte of device
@@ -17,8 +18,9 @@
 namespace zq {
 namespace {
 
-// Bytes of the shared scratch: B * K fp16 activation codes, B * K <= 10 Mi.
-constexpr size_t kNoAllocScratchBytes = 20u << 20;
+// Bytes of the shared scratch: 4 * B * K (hi and lo halves) plus 4 * B (the
+// token scales) for B * K <= 10 Mi and B <= 65536.
+constexpr size_t kNoAllocScratchBytes = (40u << 20) + (256u << 10);
 
 // One array per device that loads the library; it lives until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -56,8 +58,7 @@ cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, f
     void *ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
     if (e != cudaSuccess) return e;
-    if (B <= 16) return launch_gemm_tc_narrow(W, N, K, a, B, y, nullptr, ws, st);
-    return launch_gemm_tc_wide(W, N, K, a, B, y, nullptr, ws, st);
+    return launch_gemm_tc(W, N, K, a, B, y, ws, st);
 }
 
 }  // namespace zq

@@ -2,73 +2,77 @@
 // cores (B >= 2 tokens).
 //
 // MIInfer README, "Current phase": token-batched chunk projections for
-// prefill, a raw int8 GEMM as the speed bound of the native Q4_K path, and
-// tensor-core prefill; ZINC docs "ROCm backend", "Build and verify": matrix-
-// core prefill tiles that consume the Q4 weights directly.
+// prefill and tensor-core prefill; ZINC docs "ROCm backend", "Build and
+// verify": matrix-core prefill tiles that consume the Q4 weights directly.
 //
-// The contraction is exact in integers per 32-weight sub-block, as the
-// projection's definition requires:
-//   y[t][n] = sum_b d_b[n] * ( sum_j d8[t][bj] * sc_j[n] * I[t][n][bj] )
-//           - sum_b dmin_b[n] * ( sum_j m_j[n] * s8[t][bj] ).
-// sm_103a has no int8 tcgen05 MMA, so both operands are fed as fp16 holding
-// small integers exactly: A = activation codes q8 (|q8| <= 127), B = sc_j*q4
-// (<= 945, exact in binary16).  Every product and every partial sum of a
-// sub-block is an integer below 2^22, so the fp32 tensor-core accumulator
-// holds sc_j * I exactly.  Per sub-block the MMA (M = 128 tokens, N = 128
-// weight rows, K = 32 as two K = 16 steps) writes one of four TMEM buffers
-// (all 512 columns); epilogue warps read it back and fold it into an fp32
-// accumulator held in registers, acc += d_b * (d8 * D) (d8 is a per-lane
-// scalar: TMEM lanes are tokens; d_b a per-column one).  Once per super-block
-// a second MMA forms sum_j s8[t][bj] * m_j[n] (K = 16: eight mins and eight
-// zeros) in a buffer of the same ring, and the epilogue subtracts
-// dmin_b * minsum.
+// The projection is
+//   y[t][n] = sum_b d_b[n] * sum_{k in b} x'[t][k] * w[n][k]
+//           - sum_b dmin_b[n] * sum_j m_j[n] * s8[t][bj],
+// with x'[t][k] = q8[t][k] * d8[t][k/32] (the Q8_1 value) and w = sc_j * q4,
+// an integer up to 945.  sm_103a has no int8 tcgen05 MMA, and scaling 32-wide
+// integer partial sums by d8 one sub-block at a time makes the epilogue, not
+// the tensor cores, the bound.  Instead every x' (18 significant bits, exact in
+// fp32) is split into two binary16 numbers, hi = fp16(x') and lo = fp16(x' - hi)
+// (at most 7 significant bits, exact), and each K = 16 step issues two MMAs,
+// hi * w and lo * w, into one fp32 accumulator.  Every product is exact; the
+// only rounding is the fp32 accumulation over the 256 weights of a
+// super-block.  Tokens whose codes would overflow binary16 are scaled by a
+// power of two first (undone exactly in the epilogue).  So one TMEM
+// accumulator per super-block replaces eight per-sub-block ones: the epilogue
+// folds it in with acc += d_b * X once per super-block, and a small MMA per
+// super-block forms the min term sum_j s8[t][bj] * m_j[n] (s8 a binary16
+// value, m_j <= 63: exact products) that it subtracts as dmin_b * Mn.
 //
-// Warp roles (20 warps): 0 TMA producer (fp16 activation tiles in a
-// six-stage ring, s8 tiles, raw Q4_K tiles two super-blocks ahead), 1 MMA
-// issuer + TMEM owner, 2-3 weight converters (Q4_K bytes -> sc*q fp16 in the
-// 128-byte-swizzled K-major layout, two rows per thread, three-stage ring;
-// mins; d/dmin), 4-19 epilogue (4 column groups of 32 x 4 lane quarters),
-// which hand each TMEM buffer back right after reading it.  The issuer keeps
-// its loop to descriptor additions and counter updates: one thread feeds the
-// tensor pipe, so its instruction count per MMA bounds the kernel.  Every
-// wait is bounded.
+// Tile: M = 128 tokens (TMEM lanes) x N = 128 weight rows (TMEM columns).
+// TMEM (512 columns) holds two super-blocks in flight, each an X and an Mn
+// buffer.  Warp roles (26 warps): 0 TMA producer (hi/lo activation tiles and
+// s8 tiles, raw Q4_K tiles two super-blocks ahead), 1 MMA issuer + TMEM owner,
+// 2-9 weight converters (Q4_K bytes -> sc*q fp16 in the 128-byte-swizzled
+// K-major layout, half a row per thread; mins; d/dmin), 10-25 epilogue (4
+// column groups of 32 x 4 lane quarters) holding the fp32 accumulator in
+// registers.
+// Every wait is bounded.
 #include <cuda.h>
 
 #include "zq_internal.cuh"
 #include "zq_tc.cuh"
+#include "zq_tc_common.cuh"
 
 namespace zq {
 namespace {
 
 constexpr int BM = 128;               // tokens per tile (TMEM lanes)
 constexpr int BN = 128;               // weight rows per tile (TMEM columns)
-constexpr int kAStages = 6;           // activation operand stages of K = 64 (two sub-blocks)
-constexpr int kBStages = 3;           // converted weight operand stages of K = 64
+constexpr int kStages = 3;            // operand stages of K = 64 (two sub-blocks)
 constexpr int kAtomBytes = 128 * 128; // 128 rows x 64 fp16 (128 B), 128-byte swizzle
+constexpr int kAStageBytes = 2 * kAtomBytes;    // hi atom, lo atom
 constexpr int kRawSlots = 3;          // raw Q4_K tiles in flight (super-blocks)
 constexpr int kRawBytes = BN * kQ4KBlockBytes;  // 128 rows x 144 B
 constexpr int kMinBytes = 128 * 32;   // 128 rows x 16 fp16, 32-byte swizzle
-constexpr int kRing = 4;              // TMEM result buffers (sub-block or min products)
-constexpr int kWarps = 20;
+constexpr int kWarps = 26;
 constexpr int kThreads = kWarps * 32;
-constexpr int kConvWarp0 = 2, kConvWarps = 2;   // each converter thread owns two weight rows
-constexpr int kEpiWarp0 = 4, kEpiWarps = 16;
+constexpr int kConvWarp0 = 2, kConvWarps = 8;   // a converter thread owns half of one weight row
+constexpr int kEpiWarp0 = 10, kEpiWarps = 16;
 constexpr int kEpiCols = BN / (kEpiWarps / 4);   // 32 columns per epilogue thread
+// registers: warps are spread over the SM's four sub-partitions, at most
+// ceil(26 / 4) = 7 on one, and a sub-partition holds 16384 registers
+constexpr int kMaxRegs = 72;
+static_assert(((kWarps + 3) / 4) * 32 * kMaxRegs <= 16384, "register file of one sub-partition");
+static_assert(kConvWarps * 32 == 2 * BN, "two converter threads per weight row");
+static_assert(kEpiWarp0 % 4 == 2, "epilogue lane quarters follow warp % 4");
 constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
-constexpr uint32_t kTmemCols = 512;
-static_assert(kRing * BN == (int)kTmemCols, "the result ring fills tensor memory");
-static_assert((kRing & (kRing - 1)) == 0, "ring index by mask");
+constexpr uint32_t kTmemCols = 512;   // [X0 | Mn0 | X1 | Mn1], 128 columns each
 
 struct Smem {
     // offsets from the 1024-aligned base
-    static constexpr size_t a_atom(int s) { return (size_t)s * kAtomBytes; }
-    static constexpr size_t b_atom(int s) { return a_atom(kAStages) + (size_t)s * kAtomBytes; }
-    static constexpr size_t raw(int i) { return b_atom(kBStages) + (size_t)i * kRawBytes; }
+    static constexpr size_t a_stage(int s) { return (size_t)s * kAStageBytes; }  // hi, then lo
+    static constexpr size_t b_atom(int s) { return a_stage(kStages) + (size_t)s * kAtomBytes; }
+    static constexpr size_t raw(int i) { return b_atom(kStages) + (size_t)i * kRawBytes; }
     static constexpr size_t amin(int i) { return raw(kRawSlots) + (size_t)i * 2 * kMinBytes; }
     static constexpr size_t bmin(int i) { return amin(i) + kMinBytes; }
-    static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }  // d[BN] then dmin[BN]
+    static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }  // d[BN], then -dmin[BN]
     static constexpr size_t bars() { return dd(2); }
-    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawSlots + 3 * 2 + 2 * kRing + 2 * 2;
+    static constexpr int kNumBars = 3 * kStages + 2 * kRawSlots + 3 * 2 + 2 * 4 + 2 * 2;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }  // + alignment slack
 };
@@ -77,85 +81,35 @@ static_assert(kRawBytes % 1024 == 0, "raw slots keep the operand atoms 1024-byte
 static_assert(Smem::total() < (1u << 18), "descriptor start addresses stay inside their 14-bit field");
 
 struct Bars {
-    uint64_t *a_full, *a_empty;                   // [kAStages]
-    uint64_t *b_full, *b_empty;                   // [kBStages]
+    uint64_t *a_full, *b_full, *ab_empty;         // [kStages]
     uint64_t *raw_full, *raw_empty;               // [kRawSlots]
     uint64_t *amin_full, *bmin_full, *min_empty;  // [2]
-    uint64_t *ring_full, *ring_empty;             // [kRing]
+    uint64_t *ring_full, *ring_empty;             // [4]: X0, Mn0, X1, Mn1
     uint64_t *dd_full, *dd_free;                  // [2]
 };
 
 struct GemmParams {
     int N, K, B, nb;
     int t_tiles;
-    const __half *d8;   // Q8_1 scales [B][K/32]
-    float *y;           // [B][N]
-    int32_t *isums;     // debug export [B][N][K/32] (or null)
+    const float *tscale;   // [B] power of two that undoes the code scaling
+    float *y;              // [B][N]
     unsigned int *status;
 };
 
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-// Four fp16 sc*q values (two half2) from four nibbles at bytes 0..3 of w,
-// low (HIGH = false) or high nibble, in natural order.  (1024 + q) * sc - 1024 * sc
-// and (1024 + 16 q) * sc/16 - 64 * sc are exact in one fused rounding.
-template <bool HIGH>
-__device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 off, uint32_t &o0, uint32_t &o1)
+// (c0, c1) += (a0, a1) * (b0, b1)
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float b0, float b1)
 {
-    const uint32_t p0 = __byte_perm(w, 0, 0x4140);  // [b0, 0, b1, 0]
-    const uint32_t p1 = __byte_perm(w, 0, 0x4342);  // [b2, 0, b3, 0]
-    const uint32_t m = HIGH ? 0x00F000F0u : 0x000F000Fu;
-    const uint32_t h0 = (p0 & m) | 0x64006400u;
-    const uint32_t h1 = (p1 & m) | 0x64006400u;
-    o0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h0), scale, off));
-    o1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h1), scale, off));
-}
-
-// (c0, c1) += (d0, d1) * ((a0, a1) * (s, s)): two packed fp32x2 operations
-__device__ __forceinline__ void scale_acc2(float &c0, float &c1, float a0, float a1, float s, float d0, float d1)
-{
-    asm("{\n\t.reg .b64 ra, rs, rd, rc;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\tmov.b64 rd, {%5, %6};\n\tmov.b64 rc, {%0, %1};\n\t"
-        "mul.rn.f32x2 ra, ra, rs;\n\tfma.rn.f32x2 rc, rd, ra, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
         : "+f"(c0), "+f"(c1)
-        : "f"(a0), "f"(a1), "f"(s), "f"(d0), "f"(d1));
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// bounded wait that also gives up at once when another role already failed
-__device__ __noinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag, unsigned int *status)
-{
-    if (*abort_flag) return false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 1023u) == 1023u && *abort_flag) return false;
-    }
-    flag_timeout(status);
-    *abort_flag = 1;
-    return false;
-}
-
-// one probe inline, the bounded loop only when the phase is not complete yet
-__device__ __forceinline__ bool wait_fast(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *status)
-{
-    return mbar_try_wait(bar, parity) || wait_ok(bar, parity, abort_flag, status);
-}
-
-// one lane polls, then every lane acquires the completed phase itself
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         unsigned int *status)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_fast(bar, parity, abort_flag, status);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) ok = wait_fast(bar, parity, abort_flag, status);
-    return __all_sync(0xffffffffu, ok);
-}
-
-template <bool DEBUG>
-__global__ void __maxnreg__(96)
-q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_s,
-                     const __grid_constant__ CUtensorMap tmap_w, const GemmParams p)
+__global__ void __maxnreg__(kMaxRegs)
+q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
+                   const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_w,
+                   const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -164,17 +118,16 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
     Bars bar;
     bar.a_full = bm;
-    bar.a_empty = bar.a_full + kAStages;
-    bar.b_full = bar.a_empty + kAStages;
-    bar.b_empty = bar.b_full + kBStages;
-    bar.raw_full = bar.b_empty + kBStages;
+    bar.b_full = bar.a_full + kStages;
+    bar.ab_empty = bar.b_full + kStages;
+    bar.raw_full = bar.ab_empty + kStages;
     bar.raw_empty = bar.raw_full + kRawSlots;
     bar.amin_full = bar.raw_empty + kRawSlots;
     bar.bmin_full = bar.amin_full + 2;
     bar.min_empty = bar.bmin_full + 2;
     bar.ring_full = bar.min_empty + 2;
-    bar.ring_empty = bar.ring_full + kRing;
-    bar.dd_full = bar.ring_empty + kRing;
+    bar.ring_empty = bar.ring_full + 4;
+    bar.dd_full = bar.ring_empty + 4;
     bar.dd_free = bar.dd_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
@@ -188,19 +141,15 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     const int nq = 4 * nb;   // operand stages (K = 64 each)
     // Each CTA walks the super-blocks in its own rotated order, so the CTAs
     // that share an activation tile (and those that share a weight tile) do not
-    // all request the same L2 lines at the same time.  The fp32 sums are
-    // order-free; the integer sub-block sums are unaffected.
+    // all request the same L2 lines at the same time.
     const int rot = (n_tile + 5 * t_tile) % nb;
     auto sb = [&](int b) { return b + rot < nb ? b + rot : b + rot - nb; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kAStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar.a_full[s], 1);
-            mbar_init(&bar.a_empty[s], 1);
-        }
-        for (int s = 0; s < kBStages; ++s) {
             mbar_init(&bar.b_full[s], kConvWarps);
-            mbar_init(&bar.b_empty[s], 1);
+            mbar_init(&bar.ab_empty[s], 1);
         }
         for (int s = 0; s < kRawSlots; ++s) {
             mbar_init(&bar.raw_full[s], 1);
@@ -213,7 +162,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             mbar_init(&bar.dd_full[i], kConvWarps);
             mbar_init(&bar.dd_free[i], kEpiWarps);
         }
-        for (int i = 0; i < kRing; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&bar.ring_full[i], 1);
             mbar_init(&bar.ring_empty[i], kEpiWarps);
         }
@@ -229,12 +178,13 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tmap_a);
+            prefetch_tmap(&tmap_hi);
+            prefetch_tmap(&tmap_lo);
             prefetch_tmap(&tmap_s);
             prefetch_tmap(&tmap_w);
             bool ok = true;
             // raw weight tiles run kRawSlots - 1 super-blocks ahead of the
-            // activation tiles; activation stage q = 4b + i
+            // activation tiles; stage q = 4b + i
             int next_raw = 0;
             auto load_raw = [&](int bb) -> bool {
                 const int rs = bb % kRawSlots, use = bb / kRawSlots;
@@ -250,10 +200,12 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                     if (!(ok = load_raw(next_raw))) break;
                     ++next_raw;
                 }
-                const int slot = q % kAStages, round = q / kAStages;
-                if (round > 0 && !(ok = wait_fast(&bar.a_empty[slot], (round - 1) & 1, &abort_s, p.status))) break;
-                mbar_arrive_expect_tx(&bar.a_full[slot], kAtomBytes);
-                tma_load_2d(sm + Smem::a_atom(slot), &tmap_a, 256 * sb(b) + 64 * i, t0, &bar.a_full[slot]);
+                const int s = q % kStages, round = q / kStages;
+                if (round > 0 && !(ok = wait_fast(&bar.ab_empty[s], (round - 1) & 1, &abort_s, p.status))) break;
+                const int kx = 256 * sb(b) + 64 * i;
+                mbar_arrive_expect_tx(&bar.a_full[s], kAStageBytes);
+                tma_load_2d(sm + Smem::a_stage(s), &tmap_hi, kx, t0, &bar.a_full[s]);
+                tma_load_2d(sm + Smem::a_stage(s) + kAtomBytes, &tmap_lo, kx, t0, &bar.a_full[s]);
                 if (i == 0) {
                     const int mi = b & 1, use = b >> 1;
                     if (use > 0 && !(ok = wait_fast(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
@@ -268,109 +220,97 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
             const uint32_t base = smem_u32(sm);
             // descriptors of stage 0 / min slot 0; every other operand tile is
             // reached by adding its byte offset / 16 to the start-address field
-            const uint64_t a_desc0 = smem_desc(base + (uint32_t)Smem::a_atom(0), 16, 1024, kLayoutSw128);
+            const uint64_t a_desc0 = smem_desc(base + (uint32_t)Smem::a_stage(0), 16, 1024, kLayoutSw128);
             const uint64_t b_desc0 = smem_desc(base + (uint32_t)Smem::b_atom(0), 16, 1024, kLayoutSw128);
             const uint64_t amin_desc0 = smem_desc(base + (uint32_t)Smem::amin(0), 16, 256, kLayoutSw32);
             const uint64_t bmin_desc0 = smem_desc(base + (uint32_t)Smem::bmin(0), 16, 256, kLayoutSw32);
             constexpr uint32_t kAtom16 = kAtomBytes >> 4, kMinSlot16 = (2 * kMinBytes) >> 4;
-            int as = 0, bs = 0;
-            uint32_t aph = 0, bph = 0, e = 0;   // e: ring entries issued so far
+            int s = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (int b = 0; b < nb && ok; ++b) {
+                const int mi = b & 1;
+                const uint32_t use = (uint32_t)(b >> 1);   // earlier super-blocks on these buffers
+                const uint32_t xbuf = 2u * (uint32_t)mi, mbuf = xbuf + 1u;
+                const uint32_t x_tmem = tmem + (uint32_t)BN * xbuf;
+                if (use > 0 && !(ok = wait_fast(&bar.ring_empty[xbuf], (use - 1) & 1, &abort_s, p.status))) break;
+                tc_fence_after();
                 for (int i = 0; i < 4; ++i) {
-                    if (!(ok = wait_fast(&bar.a_full[as], aph, &abort_s, p.status) &&
-                               wait_fast(&bar.b_full[bs], bph, &abort_s, p.status)))
+                    if (!(ok = wait_fast(&bar.a_full[s], ph, &abort_s, p.status) &&
+                               wait_fast(&bar.b_full[s], ph, &abort_s, p.status)))
                         break;
-                    const uint64_t ad = a_desc0 + (uint64_t)(as * kAtom16);
-                    const uint64_t bd = b_desc0 + (uint64_t)(bs * kAtom16);
+                    tc_fence_after();
+                    const uint64_t ahi = a_desc0 + (uint64_t)(2 * s * kAtom16);
+                    const uint64_t alo = ahi + (uint64_t)kAtom16;
+                    const uint64_t bd = b_desc0 + (uint64_t)(s * kAtom16);
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj, ++e) {
-                        const uint32_t buf = e & (kRing - 1);
-                        if (e >= (uint32_t)kRing &&
-                            !(ok = wait_fast(&bar.ring_empty[buf], ((e / kRing) - 1) & 1, &abort_s, p.status)))
-                            break;
-                        tc_fence_after();
-                        const uint32_t d_tmem = tmem + (uint32_t)BN * buf;
-                        mma_f16(d_tmem, ad + (uint64_t)(jj * 4), bd + (uint64_t)(jj * 4), kIdesc, 0u);
-                        mma_f16(d_tmem, ad + (uint64_t)(jj * 4 + 2), bd + (uint64_t)(jj * 4 + 2), kIdesc, 1u);
-                        mma_commit(&bar.ring_full[buf]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_f16(x_tmem, ahi + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc,
+                                (i | kk) != 0 ? 1u : 0u);
+                        mma_f16(x_tmem, alo + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, 1u);
                     }
-                    if (!ok) break;
-                    mma_commit(&bar.a_empty[as]);
-                    mma_commit(&bar.b_empty[bs]);
-                    if (++as == kAStages) { as = 0; aph ^= 1u; }
-                    if (++bs == kBStages) { bs = 0; bph ^= 1u; }
+                    mma_commit(&bar.ab_empty[s]);
+                    if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
+                mma_commit(&bar.ring_full[xbuf]);
                 // the super-block's min product: sum_j s8[t][bj] * m_j[n]
-                const int mi = b & 1;
-                const uint32_t mpar = (uint32_t)(b >> 1) & 1u, buf = e & (kRing - 1);
-                if (!(ok = wait_fast(&bar.amin_full[mi], mpar, &abort_s, p.status) &&
-                           wait_fast(&bar.bmin_full[mi], mpar, &abort_s, p.status) &&
-                           (e < (uint32_t)kRing ||
-                            wait_fast(&bar.ring_empty[buf], ((e / kRing) - 1) & 1, &abort_s, p.status))))
+                if (!(ok = wait_fast(&bar.amin_full[mi], use & 1, &abort_s, p.status) &&
+                           wait_fast(&bar.bmin_full[mi], use & 1, &abort_s, p.status) &&
+                           (use == 0 || wait_fast(&bar.ring_empty[mbuf], (use - 1) & 1, &abort_s, p.status))))
                     break;
                 tc_fence_after();
-                mma_f16(tmem + (uint32_t)BN * buf, amin_desc0 + (uint64_t)(mi * kMinSlot16),
+                mma_f16(tmem + (uint32_t)BN * mbuf, amin_desc0 + (uint64_t)(mi * kMinSlot16),
                         bmin_desc0 + (uint64_t)(mi * kMinSlot16), kIdesc, 0u);
-                mma_commit(&bar.ring_full[buf]);
+                mma_commit(&bar.ring_full[mbuf]);
                 mma_commit(&bar.min_empty[mi]);
-                ++e;
             }
         }
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------- converters
-        // thread r converts weight rows r and r + 64 of the tile
-        const int r0 = (warp - kConvWarp0) * 32 + lane;
+        // thread (r, h) converts bytes 16h .. 16h+15 of weight row r's 32-byte
+        // nibble group: weights 16h.. of the stage's first sub-block (low
+        // nibbles) and of its second (high nibbles); h = 0 also writes the
+        // row's mins and d / -dmin once per super-block
+        const int ct = (warp - kConvWarp0) * 32 + lane;
+        const int r = ct & (BN - 1), h = ct >> 7;
+        const int sw = r & 7;
         for (int b = 0; b < nb; ++b) {
             const int rs = b % kRawSlots, ruse = b / kRawSlots;
             if (!warp_wait(&bar.raw_full[rs], ruse & 1, &abort_s, p.status)) break;
-            const uint8_t *rawbase = sm + Smem::raw(rs);
-            const uint4 hdr0 = *reinterpret_cast<const uint4 *>(rawbase + (size_t)r0 * kQ4KBlockBytes);
-            const uint4 hdr1 = *reinterpret_cast<const uint4 *>(rawbase + (size_t)(r0 + 64) * kQ4KBlockBytes);
+            const uint8_t *raw = sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes;
+            const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
             bool ok = true;
             for (int i = 0; i < 4 && ok; ++i) {
                 const int q = 4 * b + i;
-                const int bs = q % kBStages, round = q / kBStages;
-                if (round > 0 && !(ok = warp_wait(&bar.b_empty[bs], (round - 1) & 1, &abort_s, p.status))) break;
+                const int s = q % kStages, round = q / kStages;
+                if (round > 0 && !(ok = warp_wait(&bar.ab_empty[s], (round - 1) & 1, &abort_s, p.status))) break;
+                const uint4 nv = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i + 16 * h);
+                uint32_t sc0, sc1, md;
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
+                const float scl = (float)sc0, sch = (float)sc1;
+                const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
+                const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
+                const uint32_t wv[4] = {nv.x, nv.y, nv.z, nv.w};
+                uint8_t *atom = sm + Smem::b_atom(s) + (size_t)r * 128;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = r0 + 64 * h;
-                    const uint4 &hdr = h ? hdr1 : hdr0;
-                    const uint8_t *raw = rawbase + (size_t)r * kQ4KBlockBytes;
-                    const uint4 n0v = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
-                    const uint4 n1v = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
-                    uint32_t sc0, sc1, md;
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
-                    const float scl = DEBUG ? 1.0f : (float)sc0;
-                    const float sch = DEBUG ? 1.0f : (float)sc1;
-                    const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
-                    const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
-                    const uint32_t wv[8] = {n0v.x, n0v.y, n0v.z, n0v.w, n1v.x, n1v.y, n1v.z, n1v.w};
-                    uint8_t *atom = sm + Smem::b_atom(bs) + (size_t)r * 128;
-                    const int sw = r & 7;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 lo, hi;
-                        nib4_to_h2<false>(wv[2 * c], s_lo, o_lo, lo.x, lo.y);
-                        nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
-                        nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
-                        nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
-                        *reinterpret_cast<uint4 *>(atom + ((c ^ sw) << 4)) = lo;
-                        *reinterpret_cast<uint4 *>(atom + (((c + 4) ^ sw) << 4)) = hi;
-                    }
+                for (int c = 0; c < 2; ++c) {
+                    uint4 lo, hi;
+                    nib4_to_h2<false>(wv[2 * c], s_lo, o_lo, lo.x, lo.y);
+                    nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
+                    nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
+                    nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
+                    const int cl = 2 * h + c;   // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4 *>(atom + ((cl ^ sw) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(atom + (((cl + 4) ^ sw) << 4)) = hi;
                 }
                 if (i == 0) {
                     const int mi = b & 1, use = b >> 1;
-                    // mins as the B operand of the min MMA; d, dmin for the epilogue
+                    // mins as the B operand of the min MMA; d, -dmin for the epilogue
                     if (use > 0 && !(ok = warp_wait(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
                     if (use > 0 && !(ok = warp_wait(&bar.dd_free[mi], (use - 1) & 1, &abort_s, p.status))) break;
-                    float *ddp = reinterpret_cast<float *>(sm + Smem::dd(mi));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = r0 + 64 * h;
-                        const uint4 &hdr = h ? hdr1 : hdr0;
+                    if (h == 0) {
                         uint32_t mn[8], scd;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, mn[j]);
@@ -384,8 +324,9 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                         *reinterpret_cast<uint4 *>(bmr + ((0 ^ s32) << 4)) = m0;
                         *reinterpret_cast<uint4 *>(bmr + ((1 ^ s32) << 4)) = make_uint4(0, 0, 0, 0);
                         const float2 dm = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+                        float *ddp = reinterpret_cast<float *>(sm + Smem::dd(mi));
                         ddp[r] = dm.x;
-                        ddp[BN + r] = dm.y;
+                        ddp[BN + r] = -dm.y;
                     }
                     fence_async_smem();
                     __syncwarp();
@@ -396,7 +337,7 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.b_full[bs]);
+                if (lane == 0) mbar_arrive(&bar.b_full[s]);
             }
             if (!ok) break;
             __syncwarp();
@@ -405,86 +346,79 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     } else {
         // ---------------------------------------------------- epilogue
         const int e_w = warp - kEpiWarp0;
-        const int cg = e_w >> 2;                  // column group: columns 32cg .. 32cg+31
+        const int cg = e_w >> 2;                  // column group: columns 64cg .. 64cg+63
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
-        const int tl = 32 * quarter + lane;       // token within the tile
-        const int tok = t0 + tl;
+        const int tok = t0 + 32 * quarter + lane;
         const bool tvalid = tok < p.B;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(kEpiCols * cg);
-        const int nsub = nb * 8;
+        // X carries the codes' scale 2^-k; scale the min term the same way and
+        // undo both at the store
+        const float tsc = tvalid ? p.tscale[tok] : 1.0f;
+        const float itsc = 1.0f / tsc;   // exact: tsc is a power of two
         float acc[kEpiCols];
 #pragma unroll
         for (int c = 0; c < kEpiCols; ++c) acc[c] = 0.0f;
-        uint4 d8raw = make_uint4(0, 0, 0, 0);
-        if (tvalid && !DEBUG) d8raw = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(0)));
         bool ok = true;
-        uint32_t e = 0;   // ring entries consumed so far
         for (int b = 0; b < nb && ok; ++b) {
-            const int mi = b & 1, muse = b >> 1;
-            uint4 d8next = make_uint4(0, 0, 0, 0);
-            if (tvalid && !DEBUG && b + 1 < nb)
-                d8next = __ldg(reinterpret_cast<const uint4 *>(p.d8 + (size_t)tok * nsub + 8 * sb(b + 1)));
-            if (!(ok = warp_wait(&bar.dd_full[mi], muse & 1, &abort_s, p.status))) break;
+            const int mi = b & 1;
+            const uint32_t use = (uint32_t)(b >> 1);
+            const uint32_t xbuf = 2u * (uint32_t)mi, mbuf = xbuf + 1u;
+            if (!(ok = warp_wait(&bar.dd_full[mi], use & 1, &abort_s, p.status))) break;
             const float *dcol = reinterpret_cast<const float *>(sm + Smem::dd(mi)) + kEpiCols * cg;
-            for (int j = 0; j < 9; ++j, ++e) {   // j = 8: the min product
-                const uint32_t buf = e & (kRing - 1);
-                if (!(ok = warp_wait(&bar.ring_full[buf], (e / kRing) & 1, &abort_s, p.status))) break;
-                tc_fence_after();
-                uint32_t r[32];
-                tmem_ld32(lane_base + (uint32_t)BN * buf, r);
+            uint32_t r[16];
+            // acc += d_b * X, 16 columns at a time
+            if (!(ok = warp_wait(&bar.ring_full[xbuf], use & 1, &abort_s, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < kEpiCols / 16; ++q) {
+                tmem_ld16(lane_base + (uint32_t)BN * xbuf + 16u * q, r);
                 tmem_wait_ld();
-                // hand the buffer back before the arithmetic
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.ring_empty[buf]);
-                if (DEBUG) {
-                    if (tvalid && j < 8) {
+                if (q == kEpiCols / 16 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.ring_empty[xbuf]);
+                }
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int n = n0 + kEpiCols * cg + c;
-                            if (n < p.N)
-                                p.isums[((size_t)tok * p.N + n) * nsub + 8 * sb(b) + j] = (int32_t)__uint_as_float(r[c]);
-                        }
-                    }
-                } else if (j < 8) {
-                    const uint32_t w2 = (j < 4) ? ((j < 2) ? d8raw.x : d8raw.y) : ((j < 6) ? d8raw.z : d8raw.w);
-                    const uint16_t hb = (j & 1) ? (uint16_t)(w2 >> 16) : (uint16_t)(w2 & 0xFFFFu);
-                    const float d8 = __half2float(__ushort_as_half(hb));
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 dv = *reinterpret_cast<const float4 *>(dcol + c);
-                        scale_acc2(acc[c], acc[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), d8, dv.x, dv.y);
-                        scale_acc2(acc[c + 2], acc[c + 3], __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), d8,
-                                   dv.z, dv.w);
-                    }
-                } else {
-                    // super-block end: acc -= dmin_b * minsum
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 mv = *reinterpret_cast<const float4 *>(dcol + BN + c);
-                        acc[c] = fmaf(-mv.x, __uint_as_float(r[c]), acc[c]);
-                        acc[c + 1] = fmaf(-mv.y, __uint_as_float(r[c + 1]), acc[c + 1]);
-                        acc[c + 2] = fmaf(-mv.z, __uint_as_float(r[c + 2]), acc[c + 2]);
-                        acc[c + 3] = fmaf(-mv.w, __uint_as_float(r[c + 3]), acc[c + 3]);
-                    }
+                for (int c = 0; c < 16; c += 2) {
+                    const float2 dv = *reinterpret_cast<const float2 *>(dcol + 16 * q + c);
+                    fma2(acc[16 * q + c], acc[16 * q + c + 1], dv.x, dv.y, __uint_as_float(r[c]),
+                         __uint_as_float(r[c + 1]));
                 }
             }
-            if (!ok) break;
-            d8raw = d8next;
+            // acc -= dmin_b * Mn * 2^-k
+            if (!(ok = warp_wait(&bar.ring_full[mbuf], use & 1, &abort_s, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < kEpiCols / 16; ++q) {
+                tmem_ld16(lane_base + (uint32_t)BN * mbuf + 16u * q, r);
+                tmem_wait_ld();
+                if (q == kEpiCols / 16 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar.ring_empty[mbuf]);
+                }
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    const float2 mv = *reinterpret_cast<const float2 *>(dcol + BN + 16 * q + c);
+                    fma2(acc[16 * q + c], acc[16 * q + c + 1], mv.x * itsc, mv.y * itsc, __uint_as_float(r[c]),
+                         __uint_as_float(r[c + 1]));
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.dd_free[mi]);
         }
-        if (ok && !abort_s && !DEBUG && tvalid) {
+        if (ok && !abort_s && tvalid) {
             float *yrow = p.y + (size_t)tok * p.N + n0 + kEpiCols * cg;
             const int ncols = min(kEpiCols, p.N - (n0 + kEpiCols * cg));
             if (ncols == kEpiCols && (p.N & 3) == 0) {
 #pragma unroll
                 for (int c = 0; c < kEpiCols; c += 4)
-                    *reinterpret_cast<float4 *>(yrow + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                    *reinterpret_cast<float4 *>(yrow + c) =
+                        make_float4(acc[c] * tsc, acc[c + 1] * tsc, acc[c + 2] * tsc, acc[c + 3] * tsc);
             } else {
 #pragma unroll
                 for (int c = 0; c < kEpiCols; ++c)
-                    if (c < ncols) yrow[c] = acc[c];
+                    if (c < ncols) yrow[c] = acc[c] * tsc;
             }
         }
     }
@@ -494,6 +428,59 @@ q4k_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_co
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// One CTA per token: x' = q8 * d8 split into binary16 hi + lo.  The token's
+// codes are scaled by 2^-k, k >= 0 the least that keeps 127 * max d8 within
+// binary16 range, and tscale[t] = 2^k.
+constexpr int kSplitThreads = 256;
+
+__global__ void __launch_bounds__(kSplitThreads)
+q8_split_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d8, int K, __half *__restrict__ hi,
+                __half *__restrict__ lo, float *__restrict__ tscale)
+{
+    __shared__ float red[kSplitThreads / 32];
+    const int t = blockIdx.x;
+    const int nblk = K >> 5;
+    const __half *dt = d8 + (size_t)t * nblk;
+    float m = 0.0f;
+    for (int j = threadIdx.x; j < nblk; j += kSplitThreads) m = fmaxf(m, fabsf(__half2float(dt[j])));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kSplitThreads / 32; ++w) m = fmaxf(m, red[w]);
+    int k = 0;
+    const float bound = 127.0f * m;   // >= every |x'| of the token
+    if (bound > 65504.0f) frexpf(bound / 65504.0f, &k);   // bound / 65504 <= 2^k
+    const float down = ldexpf(1.0f, -k);
+    if (threadIdx.x == 0) tscale[t] = ldexpf(1.0f, k);
+    const int8_t *qt = qs + (size_t)t * K;
+    for (int g = threadIdx.x; g < (K >> 4); g += kSplitThreads) {
+        const int4 v = __ldg(reinterpret_cast<const int4 *>(qt) + g);
+        const float dv = __half2float(dt[g >> 1]) * down;
+        const int w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t oh[8], ol[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int x = w[i >> 1];
+            float a[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) a[h] = (float)(int8_t)((x >> (16 * (i & 1) + 8 * h)) & 0xFF) * dv;
+            const __half2 vh = __floats2half2_rn(a[0], a[1]);
+            const float2 back = __half22float2(vh);
+            oh[i] = h2_bits(vh);
+            ol[i] = h2_bits(__floats2half2_rn(a[0] - back.x, a[1] - back.y));
+        }
+        uint4 *dh = reinterpret_cast<uint4 *>(hi + (size_t)t * K) + 2 * g;
+        uint4 *dl = reinterpret_cast<uint4 *>(lo + (size_t)t * K) + 2 * g;
+        dh[0] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+        dh[1] = make_uint4(oh[4], oh[5], oh[6], oh[7]);
+        dl[0] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+        dl[1] = make_uint4(ol[4], ol[5], ol[6], ol[7]);
     }
 }
 
@@ -516,7 +503,6 @@ __global__ void q8_to_f16_kernel(const int8_t *__restrict__ qs, __half *__restri
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -535,10 +521,15 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D tensor [rows][cols] of `esize`-byte elements, row stride = cols*esize
-// bytes, box box_cols x box_rows; out-of-range elements read as zero
-cudaError_t make_tmap(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *base, uint64_t cols,
-                      uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
+size_t g_attr_bytes[64];
+
+// workspace layout: hi [B][K] fp16 | lo [B][K] fp16 | tscale [B] fp32
+size_t split_bytes(int K, int B) { return (size_t)B * K * sizeof(__half); }
+
+}  // namespace
+
+cudaError_t make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *base, uint64_t cols,
+                         uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -551,27 +542,41 @@ cudaError_t make_tmap(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, co
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t g_attr_bytes[64][2];
-
-template <bool DEBUG>
-cudaError_t launch_wide(const void *W, int N, int K, zq_q8_1 a, int B, float *y, int32_t *isums, void *ws,
-                        cudaStream_t st)
+cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream_t st)
 {
-    __half *a16 = static_cast<__half *>(ws);
-    const size_t n16 = (size_t)B * K / 16;
-    q8_to_f16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(a.qs, a16, n16);
+    const size_t n16 = n / 16;
+    if (n16 == 0) return cudaSuccess;
+    q8_to_f16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(qs, out, n16);
+    return cudaGetLastError();
+}
+
+size_t gemm_tc_workspace_bytes(int N, int K, int B)
+{
+    (void)N;
+    if (B <= 1) return 0;
+    return 2 * split_bytes(K, B) + (((size_t)B * sizeof(float) + 255) & ~(size_t)255);
+}
+
+cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, cudaStream_t st)
+{
+    __half *hi = static_cast<__half *>(ws);
+    __half *lo = reinterpret_cast<__half *>(static_cast<uint8_t *>(ws) + split_bytes(K, B));
+    float *tscale = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + 2 * split_bytes(K, B));
+    q8_split_kernel<<<B, kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d), K, hi, lo, tscale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    CUtensorMap ta, ts, tw;
+    CUtensorMap th, tl, ts, tw;
     const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    if ((e = make_tmap(&ta, f16, 2, a16, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    if ((e = make_tmap_2d(&th, f16, 2, hi, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
         return e;
-    if ((e = make_tmap(&ts, f16, 2, a.s, (uint64_t)K / 32, (uint64_t)B, 16, BM, CU_TENSOR_MAP_SWIZZLE_32B)) !=
+    if ((e = make_tmap_2d(&tl, f16, 2, lo, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if ((e = make_tmap_2d(&ts, f16, 2, a.s, (uint64_t)K / 32, (uint64_t)B, 16, BM, CU_TENSOR_MAP_SWIZZLE_32B)) !=
         cudaSuccess)
         return e;
     // weights as bytes [N][K/256*144]: one box = one super-block of 128 rows
-    if ((e = make_tmap(&tw, u8, 1, W, (uint64_t)(K / 256) * kQ4KBlockBytes, (uint64_t)N, kQ4KBlockBytes, BN,
-                       CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+    if ((e = make_tmap_2d(&tw, u8, 1, W, (uint64_t)(K / 256) * kQ4KBlockBytes, (uint64_t)N, kQ4KBlockBytes, BN,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
         return e;
     GemmParams p{};
     p.N = N;
@@ -579,46 +584,21 @@ cudaError_t launch_wide(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     p.B = B;
     p.nb = K / 256;
     p.t_tiles = (B + BM - 1) / BM;
-    p.d8 = reinterpret_cast<const __half *>(a.d);
+    p.tscale = tscale;
     p.y = y;
-    p.isums = isums;
     p.status = device_status_word();
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const size_t smem = Smem::total();
-    if (g_attr_bytes[dev][DEBUG] < smem) {
-        e = cudaFuncSetAttribute(q4k_gemm_wide_kernel<DEBUG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (g_attr_bytes[dev] < smem) {
+        e = cudaFuncSetAttribute(q4k_gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        g_attr_bytes[dev][DEBUG] = smem;
+        g_attr_bytes[dev] = smem;
     }
     const long long grid = (long long)p.t_tiles * ((N + BN - 1) / BN);
-    q4k_gemm_wide_kernel<DEBUG><<<(unsigned)grid, kThreads, smem, st>>>(ta, ts, tw, p);
+    q4k_gemm_tc_kernel<<<(unsigned)grid, kThreads, smem, st>>>(th, tl, ts, tw, p);
     return cudaGetLastError();
-}
-
-}  // namespace
-
-size_t gemm_tc_workspace_bytes(int N, int K, int B)
-{
-    (void)N;
-    if (B <= 1) return 0;
-    return (size_t)B * K * sizeof(__half);
-}
-
-cudaError_t launch_gemm_tc_wide(const void *W, int N, int K, zq_q8_1 a, int B, float *y, int32_t *isums, void *ws,
-                                cudaStream_t st)
-{
-    if (isums) return launch_wide<true>(W, N, K, a, B, nullptr, isums, ws, st);
-    return launch_wide<false>(W, N, K, a, B, y, nullptr, ws, st);
-}
-
-cudaError_t launch_gemm_tc_narrow(const void *W, int N, int K, zq_q8_1 a, int B, float *y, int32_t *isums,
-                                  void *ws, cudaStream_t st)
-{
-    // chunk sizes run on the same tensor-core kernel: one 128-token tile whose
-    // rows beyond B are zero-filled by the TMA and never stored
-    return launch_gemm_tc_wide(W, N, K, a, B, y, isums, ws, st);
 }
 
 }  // namespace zq

@@ -228,8 +228,8 @@ int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *w
     if ((st = check_device(&dev))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (B == 1) return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, s), "zq_q4k_gemm (B=1)");
-    if (B <= 16) return launched(launch_gemm_tc_narrow(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (chunk)");
-    return launched(launch_gemm_tc_wide(W, N, K, a, B, y, nullptr, workspace, s), "zq_q4k_gemm (prefill)");
+    return launched(launch_gemm_tc(W, N, K, a, B, y, workspace, s),
+                    B <= 16 ? "zq_q4k_gemm (chunk)" : "zq_q4k_gemm (prefill)");
 }
 
 int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream)
@@ -244,8 +244,8 @@ int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     if (need > noalloc_scratch_bytes())
         return fail(ZQ_ERR_WORKSPACE,
                     "zq_q4k_gemm_noalloc: B*K = %lld needs %zu bytes of scratch, more than the built-in %zu "
-                    "(B*K <= %zu); use zq_q4k_gemm with a workspace",
-                    (long long)B * K, need, noalloc_scratch_bytes(), noalloc_scratch_bytes() / 2);
+                    "(B*K <= 10485760); use zq_q4k_gemm with a workspace",
+                    (long long)B * K, need, noalloc_scratch_bytes());
     int dev;
     if ((st = check_device(&dev))) return st;
     cudaStream_t s = (cudaStream_t)stream;
@@ -286,8 +286,8 @@ int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B, int32_t *i
     if ((st = check_device(&dev))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (path == 0) return launched(launch_gemv(W, nullptr, N, K, a, B, nullptr, nullptr, isums, s), "isums (dp4a)");
-    if (path == 1) return launched(launch_gemm_tc_wide(W, N, K, a, B, nullptr, isums, workspace, s), "isums (prefill)");
-    return launched(launch_gemm_tc_narrow(W, N, K, a, B, nullptr, isums, workspace, s), "isums (chunk)");
+    return launched(launch_isums_tc(W, N, K, a, B, isums, workspace, s),
+                    path == 1 ? "isums (tensor cores, prefill sizes)" : "isums (tensor cores, chunk sizes)");
 }
 
 }  // extern "C"

@@ -19,13 +19,11 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
 cudaError_t launch_gemv(const void *W, const void *W2, int N, int K, zq_q8_1 a,
                         int B, float *y, float *y2, int32_t *isums,
                         cudaStream_t st);
-cudaError_t launch_gemm_tc_wide(const void *W, int N, int K, zq_q8_1 a, int B,
-                                float *y, int32_t *isums, void *ws,
-                                cudaStream_t st);
-cudaError_t launch_gemm_tc_narrow(const void *W, int N, int K, zq_q8_1 a, int B,
-                                  float *y, int32_t *isums, void *ws,
-                                  cudaStream_t st);
+cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
+                           void *ws, cudaStream_t st);
 size_t gemm_tc_workspace_bytes(int N, int K, int B);
+cudaError_t launch_isums_tc(const void *W, int N, int K, zq_q8_1 a, int B,
+                            int32_t *isums, void *ws, cudaStream_t st);
 bool gemv_stream_supported(int K);
 size_t noalloc_scratch_bytes();
 cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);

@@ -1,0 +1,73 @@
+// zq_tc_common.cuh -- pieces shared by the two tcgen05 kernels (the batched
+// projection and the integer sub-block export): Q4_K nibble -> fp16
+// conversion, bounded mbarrier waits that stop every role once one has failed,
+// and the host-side tensor-map and activation-code helpers.
+#pragma once
+
+#include <cuda.h>
+
+#include "zq_internal.cuh"
+#include "zq_tc.cuh"
+
+namespace zq {
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// Four fp16 values scale*q (two half2) from the four nibbles at bytes 0..3 of
+// w, low (HIGH = false) or high nibble, in natural order.  The nibble is placed
+// in the mantissa of 1024 (low) or 1024 + 16 q (high), so with scale = s,
+// off = -1024 s (low) or scale = s/16, off = -64 s (high) one fused fp16
+// operation gives s*q; exact while s*q fits in 11 bits.
+template <bool HIGH>
+__device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 off, uint32_t &o0, uint32_t &o1)
+{
+    const uint32_t p0 = __byte_perm(w, 0, 0x4140);  // [b0, 0, b1, 0]
+    const uint32_t p1 = __byte_perm(w, 0, 0x4342);  // [b2, 0, b3, 0]
+    const uint32_t m = HIGH ? 0x00F000F0u : 0x000F000Fu;
+    const uint32_t h0 = (p0 & m) | 0x64006400u;
+    const uint32_t h1 = (p1 & m) | 0x64006400u;
+    o0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h0), scale, off));
+    o1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&h1), scale, off));
+}
+
+// Bounded wait that also gives up at once when another role already failed.
+static __device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                            unsigned int *status)
+{
+    if (*abort_flag) return false;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 1023u) == 1023u && *abort_flag) return false;
+    }
+    flag_timeout(status);
+    *abort_flag = 1;
+    return false;
+}
+
+// One probe inline; the bounded loop only when the phase is not complete yet.
+__device__ __forceinline__ bool wait_fast(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status)
+{
+    return mbar_try_wait(bar, parity) || wait_ok(bar, parity, abort_flag, status);
+}
+
+// One lane polls, then every lane acquires the completed phase itself.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned int *status)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_fast(bar, parity, abort_flag, status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok) ok = wait_fast(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// 2-D tensor [rows][cols] of `esize`-byte elements, row stride cols * esize
+// bytes, box box_cols x box_rows; elements outside the tensor read as zero.
+cudaError_t make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *base, uint64_t cols,
+                         uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
+// q8 activation codes -> fp16 (exact), n codes, n a multiple of 16.
+cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream_t st);
+
+}  // namespace zq

@@ -130,12 +130,17 @@ ZQ_API int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_
  * token-batched chunk projections and tensor-core/int8 GEMM prefill).
  *   W : Q4_K N x K;  a : Q8_1 of B tokens;  y : fp32 [B][N].
  *   workspace / workspace_bytes : caller-owned device scratch of at least
- *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0).
- *     It holds the fp16 copy of the activation codes the tensor cores read;
- *     its contents on entry do not matter and are not preserved.
- * B = 1 runs the decode mat-vec.  2 <= B <= 16 runs the chunk path (tensor
- * cores, weights unpacked once per tile and shared by the tokens); B >= 17
- * runs the prefill path (tensor cores, 128-token tiles).
+ *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0;
+ *     4*B*K + 4*B rounded up to 256 otherwise).  It holds the activations the
+ *     tensor cores read, each Q8_1 value q8*d8 split into two binary16
+ *     numbers, and a per-token scale; its contents on entry do not matter and
+ *     are not preserved.
+ * B = 1 runs the decode mat-vec.  B >= 2 runs the tensor cores on tiles of
+ * 128 tokens x 128 weight rows (2 <= B <= 16: the chunk sizes, one partly
+ * filled token tile whose weights are unpacked once and shared).  There every
+ * product of an activation part and a weight code sc*q4 is exact and the
+ * products are summed in fp32 per 256-weight super-block, then scaled by
+ * d_b (and the min term by dmin_b) in fp32.
  * Shapes: 1 <= B <= 65536, N >= 1, K % 256 == 0, K >= 256.
  */
 ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
@@ -151,10 +156,11 @@ ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
  * what zq_q4k_gemm computes (same kernels, same results) but takes its scratch
  * from a fixed device array inside the library instead of a workspace
  * argument, and never calls cudaMalloc, cudaFree or any allocating routine.
- *   - Limit: 2*B*K bytes of scratch must fit in the array (20 MiB), i.e.
- *     B*K <= 10485760 (for example B = 512 with K up to 20480); larger shapes
- *     return ZQ_ERR_WORKSPACE without launching.  B = 1 needs no scratch.
- *   - Every GPU that loads the library holds the 20 MiB array until the
+ *   - Limit: the workspace of zq_q4k_gemm (4*B*K + 4*B bytes) must fit in the
+ *     array (40 MiB + 256 KiB), i.e. B*K <= 10485760 (for example B = 512
+ *     with K up to 20480); larger shapes return ZQ_ERR_WORKSPACE without
+ *     launching.  B = 1 needs no scratch.
+ *   - Every GPU that loads the library holds the 40 MiB array until the
  *     process exits.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
@@ -191,10 +197,11 @@ ZQ_API int zq_version(void);
 /*
  * Test hook: exact sub-block integer sums I[t][n][K/32] (int32, device
  * memory) computed by the kernels' own inner products.  path = 0: the packed
- * dot4 (dp4a) inner product of the mat-vec kernels, any B; path = 1: the
- * tensor-core prefill kernel (B >= 17), read back from its accumulators;
- * path = 2: the tensor-core chunk kernel (2 <= B <= 16).  For paths 1 and 2
- * the workspace rules of zq_q4k_gemm apply.
+ * dot4 (dp4a) inner product of the mat-vec kernels, any B; paths 1 (B >= 17)
+ * and 2 (2 <= B <= 16): tcgen05 MMAs on the projection's tile layout, fp16
+ * operands holding q8 and q4 exactly, one K = 32 accumulator per sub-block
+ * read back from tensor memory.  For paths 1 and 2 the workspace rules of
+ * zq_q4k_gemm apply.
  */
 ZQ_API int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B,
                        int32_t *isums, int path, void *workspace,

@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_entry_point(B, K, N):
 
 def test_noalloc_rejects_oversized_shape_without_launch():
     lib = zq.load()
-    B, K, N = 1024, 16384, 256                  # 2*B*K = 32 MiB > 20 MiB
+    B, K, N = 1024, 16384, 256                  # B*K = 16 Mi > 10 Mi
     qs = torch.zeros((B, K), dtype=torch.int8, device="cuda")
     d = torch.zeros((B, K // 32), dtype=torch.float16, device="cuda")
     s = torch.zeros((B, K // 32), dtype=torch.float16, device="cuda")
