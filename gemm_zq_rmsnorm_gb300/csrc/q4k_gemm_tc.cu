@@ -72,7 +72,7 @@ struct Smem {
     static constexpr size_t bmin(int i) { return amin(i) + kMinBytes; }
     static constexpr size_t dd(int i) { return amin(2) + (size_t)i * BN * 8; }  // d[BN], then -dmin[BN]
     static constexpr size_t bars() { return dd(2); }
-    static constexpr int kNumBars = 3 * kStages + 2 * kRawSlots + 3 * 2 + 2 * 4 + 2 * 2;
+    static constexpr int kNumBars = 2 * kStages + 2 * kRawSlots + 2 * 2 + 2 * 4 + 2 * 2;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }  // + alignment slack
 };
@@ -81,9 +81,12 @@ static_assert(kRawBytes % 1024 == 0, "raw slots keep the operand atoms 1024-byte
 static_assert(Smem::total() < (1u << 18), "descriptor start addresses stay inside their 14-bit field");
 
 struct Bars {
-    uint64_t *a_full, *b_full, *ab_empty;         // [kStages]
+    // full[s]: the TMA's activation bytes and every converter warp's weights
+    // of stage s have landed (one wait for the issuer); empty[s]: the MMAs
+    // reading stage s have completed
+    uint64_t *full, *empty;                       // [kStages]
     uint64_t *raw_full, *raw_empty;               // [kRawSlots]
-    uint64_t *amin_full, *bmin_full, *min_empty;  // [2]
+    uint64_t *min_full, *min_empty;               // [2]: s8 tile (TMA) and mins (converters)
     uint64_t *ring_full, *ring_empty;             // [4]: X0, Mn0, X1, Mn1
     uint64_t *dd_full, *dd_free;                  // [2]
 };
@@ -117,14 +120,12 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
 
     uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
     Bars bar;
-    bar.a_full = bm;
-    bar.b_full = bar.a_full + kStages;
-    bar.ab_empty = bar.b_full + kStages;
-    bar.raw_full = bar.ab_empty + kStages;
+    bar.full = bm;
+    bar.empty = bar.full + kStages;
+    bar.raw_full = bar.empty + kStages;
     bar.raw_empty = bar.raw_full + kRawSlots;
-    bar.amin_full = bar.raw_empty + kRawSlots;
-    bar.bmin_full = bar.amin_full + 2;
-    bar.min_empty = bar.bmin_full + 2;
+    bar.min_full = bar.raw_empty + kRawSlots;
+    bar.min_empty = bar.min_full + 2;
     bar.ring_full = bar.min_empty + 2;
     bar.ring_empty = bar.ring_full + 4;
     bar.dd_full = bar.ring_empty + 4;
@@ -147,17 +148,15 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar.a_full[s], 1);
-            mbar_init(&bar.b_full[s], kConvWarps);
-            mbar_init(&bar.ab_empty[s], 1);
+            mbar_init(&bar.full[s], 1 + kConvWarps);
+            mbar_init(&bar.empty[s], 1);
         }
         for (int s = 0; s < kRawSlots; ++s) {
             mbar_init(&bar.raw_full[s], 1);
             mbar_init(&bar.raw_empty[s], kConvWarps);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar.amin_full[i], 1);
-            mbar_init(&bar.bmin_full[i], kConvWarps);
+            mbar_init(&bar.min_full[i], 1 + kConvWarps);
             mbar_init(&bar.min_empty[i], 1);
             mbar_init(&bar.dd_full[i], kConvWarps);
             mbar_init(&bar.dd_free[i], kEpiWarps);
@@ -201,16 +200,16 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
                     ++next_raw;
                 }
                 const int s = q % kStages, round = q / kStages;
-                if (round > 0 && !(ok = wait_fast(&bar.ab_empty[s], (round - 1) & 1, &abort_s, p.status))) break;
+                if (round > 0 && !(ok = wait_fast(&bar.empty[s], (round - 1) & 1, &abort_s, p.status))) break;
                 const int kx = 256 * sb(b) + 64 * i;
-                mbar_arrive_expect_tx(&bar.a_full[s], kAStageBytes);
-                tma_load_2d(sm + Smem::a_stage(s), &tmap_hi, kx, t0, &bar.a_full[s]);
-                tma_load_2d(sm + Smem::a_stage(s) + kAtomBytes, &tmap_lo, kx, t0, &bar.a_full[s]);
+                mbar_arrive_expect_tx(&bar.full[s], kAStageBytes);
+                tma_load_2d(sm + Smem::a_stage(s), &tmap_hi, kx, t0, &bar.full[s]);
+                tma_load_2d(sm + Smem::a_stage(s) + kAtomBytes, &tmap_lo, kx, t0, &bar.full[s]);
                 if (i == 0) {
                     const int mi = b & 1, use = b >> 1;
                     if (use > 0 && !(ok = wait_fast(&bar.min_empty[mi], (use - 1) & 1, &abort_s, p.status))) break;
-                    mbar_arrive_expect_tx(&bar.amin_full[mi], kMinBytes);
-                    tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * sb(b), t0, &bar.amin_full[mi]);
+                    mbar_arrive_expect_tx(&bar.min_full[mi], kMinBytes);
+                    tma_load_2d(sm + Smem::amin(mi), &tmap_s, 8 * sb(b), t0, &bar.min_full[mi]);
                 }
             }
         }
@@ -236,9 +235,7 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
                 if (use > 0 && !(ok = wait_fast(&bar.ring_empty[xbuf], (use - 1) & 1, &abort_s, p.status))) break;
                 tc_fence_after();
                 for (int i = 0; i < 4; ++i) {
-                    if (!(ok = wait_fast(&bar.a_full[s], ph, &abort_s, p.status) &&
-                               wait_fast(&bar.b_full[s], ph, &abort_s, p.status)))
-                        break;
+                    if (!(ok = wait_fast(&bar.full[s], ph, &abort_s, p.status))) break;
                     tc_fence_after();
                     const uint64_t ahi = a_desc0 + (uint64_t)(2 * s * kAtom16);
                     const uint64_t alo = ahi + (uint64_t)kAtom16;
@@ -249,14 +246,13 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
                                 (i | kk) != 0 ? 1u : 0u);
                         mma_f16(x_tmem, alo + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), kIdesc, 1u);
                     }
-                    mma_commit(&bar.ab_empty[s]);
+                    mma_commit(&bar.empty[s]);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit(&bar.ring_full[xbuf]);
                 // the super-block's min product: sum_j s8[t][bj] * m_j[n]
-                if (!(ok = wait_fast(&bar.amin_full[mi], use & 1, &abort_s, p.status) &&
-                           wait_fast(&bar.bmin_full[mi], use & 1, &abort_s, p.status) &&
+                if (!(ok = wait_fast(&bar.min_full[mi], use & 1, &abort_s, p.status) &&
                            (use == 0 || wait_fast(&bar.ring_empty[mbuf], (use - 1) & 1, &abort_s, p.status))))
                     break;
                 tc_fence_after();
@@ -284,7 +280,7 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
             for (int i = 0; i < 4 && ok; ++i) {
                 const int q = 4 * b + i;
                 const int s = q % kStages, round = q / kStages;
-                if (round > 0 && !(ok = warp_wait(&bar.ab_empty[s], (round - 1) & 1, &abort_s, p.status))) break;
+                if (round > 0 && !(ok = warp_wait(&bar.empty[s], (round - 1) & 1, &abort_s, p.status))) break;
                 const uint4 nv = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i + 16 * h);
                 uint32_t sc0, sc1, md;
                 q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
@@ -331,13 +327,13 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&bar.bmin_full[mi]);
+                        mbar_arrive(&bar.min_full[mi]);
                         mbar_arrive(&bar.dd_full[mi]);
                     }
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.b_full[s]);
+                if (lane == 0) mbar_arrive(&bar.full[s]);
             }
             if (!ok) break;
             __syncwarp();

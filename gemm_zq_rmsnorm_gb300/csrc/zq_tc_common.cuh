@@ -31,7 +31,7 @@ __device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 of
 }
 
 // Bounded wait that also gives up at once when another role already failed.
-static __device__ __forceinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+static __device__ __noinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                             unsigned int *status)
 {
     if (*abort_flag) return false;
