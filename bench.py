@@ -470,7 +470,7 @@ def main():
                                 "frac": round(ach / pk["bf16_tflops"], 4),
                                 "peak_source": pk["source"] + " bf16 dense burst (fp16 operands run at the bf16 rate; "
                                                "int8 tcgen05 is not available on sm_103a)",
-                                "traffic": recorded_traffic(f"q4k_gemm_wide_{B}x{dK}x{dN}"),
+                                "traffic": recorded_traffic(f"q4k_gemm_tc_{B}x{dK}x{dN}"),
                                 "kernel_ms": round(dms, 5)},
                    "gpu_launches": wl.launches_per_step() * max(3, args.steps // 5), "clocks": clk.summary()}
             sub.append(rec)
