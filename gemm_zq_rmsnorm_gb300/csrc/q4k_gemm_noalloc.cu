@@ -58,7 +58,8 @@ cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, f
     void *ws = nullptr;
     cudaError_t e = scratch_for_current_device(&ws);
     if (e != cudaSuccess) return e;
-    return launch_gemm_tc(W, N, K, a, B, y, ws, st);
+    // one K range per tile: the fixed array holds no split-K partial sums
+    return launch_gemm_tc(W, N, K, a, B, y, ws, false, st);
 }
 
 }  // namespace zq

@@ -94,8 +94,9 @@ struct Bars {
 struct GemmParams {
     int N, K, B, nb;
     int t_tiles;
+    int splits;            // K ranges (split-K); CTA = (split, token tile, weight tile)
     const float *tscale;   // [B] power of two that undoes the code scaling
-    float *y;              // [B][N]
+    float *y;              // [B][N], or [splits][B][N] partial sums when splits > 1
     unsigned int *status;
 };
 
@@ -134,17 +135,21 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int t_tile = blockIdx.x % p.t_tiles;
-    const int n_tile = blockIdx.x / p.t_tiles;
+    const int split = blockIdx.x % p.splits;
+    const int tile = blockIdx.x / p.splits;
+    const int t_tile = tile % p.t_tiles;
+    const int n_tile = tile / p.t_tiles;
     const int t0 = t_tile * BM;
     const int n0 = n_tile * BN;
-    const int nb = p.nb;
+    // this CTA's super-blocks: [b_begin, b_begin + nb) of the row
+    const int b_begin = (int)((long long)split * p.nb / p.splits);
+    const int nb = (int)((long long)(split + 1) * p.nb / p.splits) - b_begin;
     const int nq = 4 * nb;   // operand stages (K = 64 each)
-    // Each CTA walks the super-blocks in its own rotated order, so the CTAs
+    // Each CTA walks its super-blocks in its own rotated order, so the CTAs
     // that share an activation tile (and those that share a weight tile) do not
     // all request the same L2 lines at the same time.
     const int rot = (n_tile + 5 * t_tile) % nb;
-    auto sb = [&](int b) { return b + rot < nb ? b + rot : b + rot - nb; };
+    auto sb = [&](int b) { return b_begin + (b + rot < nb ? b + rot : b + rot - nb); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -404,7 +409,8 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
             if (lane == 0) mbar_arrive(&bar.dd_free[mi]);
         }
         if (ok && !abort_s && tvalid) {
-            float *yrow = p.y + (size_t)tok * p.N + n0 + kEpiCols * cg;
+            const int sp_now = (int)(blockIdx.x % (unsigned)p.splits);
+            float *yrow = p.y + ((size_t)sp_now * p.B + tok) * p.N + n0 + kEpiCols * cg;
             const int ncols = min(kEpiCols, p.N - (n0 + kEpiCols * cg));
             if (ncols == kEpiCols && (p.N & 3) == 0) {
 #pragma unroll
@@ -499,6 +505,22 @@ __global__ void q8_to_f16_kernel(const int8_t *__restrict__ qs, __half *__restri
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// y = sum over the splits of the partial products, in split order
+__global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int splits, size_t n4, float4 *__restrict__ y)
+{
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 a = __ldg(part + i);
+    for (int s = 1; s < splits; ++s) {
+        const float4 b = __ldg(part + (size_t)s * n4 + i);
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+    }
+    y[i] = a;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -519,8 +541,35 @@ EncodeTiledFn encode_fn()
 
 size_t g_attr_bytes[64];
 
-// workspace layout: hi [B][K] fp16 | lo [B][K] fp16 | tscale [B] fp32
+// workspace layout: hi [B][K] fp16 | lo [B][K] fp16 | tscale [B] fp32 |
+// partial sums [splits][B][N] fp32 (when splits > 1)
 size_t split_bytes(int K, int B) { return (size_t)B * K * sizeof(__half); }
+size_t tscale_bytes(int B) { return ((size_t)B * sizeof(float) + 255) & ~(size_t)255; }
+
+// Split-K count: tiles that fill the SMs unevenly waste whole waves (a
+// 512 x 5120 output is 160 tiles for 152 SMs: two waves, the second almost
+// empty).  Model the time of `s` splits as waves * (super-blocks per split +
+// a fixed per-CTA cost) plus the partial-sum traffic, and take the smallest
+// s within 3 % of the best, keeping >= 2 super-blocks per split.
+int choose_splits(int B, int N, int K, int sms)
+{
+    const long long tiles = (long long)((B + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int nb = K / 256;
+    const int smax = nb / 2 < 8 ? nb / 2 : 8;
+    double cost[9];
+    double best = 1e300;
+    for (int sp = 1; sp <= (smax > 1 ? smax : 1); ++sp) {
+        const long long ctas = tiles * sp;
+        const double waves = (double)((ctas + sms - 1) / sms);
+        double c = waves * ((double)nb / sp + 1.5);
+        if (sp > 1) c += (double)(sp + 1) * B * N * 4.0 / 1.85e7;   // partials, in super-block times
+        cost[sp] = c;
+        if (c < best) best = c;
+    }
+    for (int sp = 1; sp <= (smax > 1 ? smax : 1); ++sp)
+        if (cost[sp] <= best * 1.03) return sp;
+    return 1;
+}
 
 }  // namespace
 
@@ -546,18 +595,22 @@ cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream
     return cudaGetLastError();
 }
 
-size_t gemm_tc_workspace_bytes(int N, int K, int B)
+size_t gemm_tc_workspace_bytes(int N, int K, int B, bool allow_split)
 {
-    (void)N;
     if (B <= 1) return 0;
-    return 2 * split_bytes(K, B) + (((size_t)B * sizeof(float) + 255) & ~(size_t)255);
+    const int sp = allow_split ? choose_splits(B, N, K, num_sms()) : 1;
+    return 2 * split_bytes(K, B) + tscale_bytes(B) + (sp > 1 ? (size_t)sp * B * N * sizeof(float) : 0);
 }
 
-cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, cudaStream_t st)
+cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, bool allow_split,
+                           cudaStream_t st)
 {
-    __half *hi = static_cast<__half *>(ws);
-    __half *lo = reinterpret_cast<__half *>(static_cast<uint8_t *>(ws) + split_bytes(K, B));
-    float *tscale = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + 2 * split_bytes(K, B));
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    __half *hi = reinterpret_cast<__half *>(w8);
+    __half *lo = reinterpret_cast<__half *>(w8 + split_bytes(K, B));
+    float *tscale = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B));
+    const int splits = allow_split ? choose_splits(B, N, K, num_sms()) : 1;
+    float *part = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B));
     q8_split_kernel<<<B, kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d), K, hi, lo, tscale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -580,8 +633,9 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
     p.B = B;
     p.nb = K / 256;
     p.t_tiles = (B + BM - 1) / BM;
+    p.splits = splits;
     p.tscale = tscale;
-    p.y = y;
+    p.y = splits > 1 ? part : y;
     p.status = device_status_word();
     int dev = 0;
     cudaGetDevice(&dev);
@@ -592,8 +646,13 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
         if (e != cudaSuccess) return e;
         g_attr_bytes[dev] = smem;
     }
-    const long long grid = (long long)p.t_tiles * ((N + BN - 1) / BN);
+    const long long grid = (long long)p.t_tiles * ((N + BN - 1) / BN) * splits;
     q4k_gemm_tc_kernel<<<(unsigned)grid, kThreads, smem, st>>>(th, tl, ts, tw, p);
+    if (splits == 1) return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t n4 = (size_t)B * N / 4;
+    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
+                                                                          splits, n4, reinterpret_cast<float4 *>(y));
     return cudaGetLastError();
 }
 

@@ -113,11 +113,24 @@ cudaError_t launch_gemv_dispatch(const void *W, const void *W2, int N, int K, zq
     return launch_gemv(W, W2, N, K, a, 1, y, y2, nullptr, st);
 }
 
+// SM count of the current device, read once per device; launch shapes and
+// workspace sizes derive from it, so the workspace query and the call agree.
 int num_sms()
 {
     int dev = 0;
-    cudaGetDevice(&dev);
-    return (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0) ? g_sms[dev] : 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 148;
+    }
+    if (g_sms[dev] <= 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            return 148;
+        }
+        g_sms[dev] = v;
+    }
+    return g_sms[dev];
 }
 
 }  // namespace zq
@@ -228,7 +241,7 @@ int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *w
     if ((st = check_device(&dev))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (B == 1) return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, s), "zq_q4k_gemm (B=1)");
-    return launched(launch_gemm_tc(W, N, K, a, B, y, workspace, s),
+    return launched(launch_gemm_tc(W, N, K, a, B, y, workspace, true, s),
                     B <= 16 ? "zq_q4k_gemm (chunk)" : "zq_q4k_gemm (prefill)");
 }
 
@@ -240,7 +253,7 @@ int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_q4k_gemm_noalloc: B = %d must be in [1, 65536]", B);
     if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemm_noalloc: null y");
     if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm_noalloc: y must be 16-byte aligned");
-    const size_t need = gemm_tc_workspace_bytes(N, K, B);
+    const size_t need = gemm_tc_workspace_bytes(N, K, B, false);
     if (need > noalloc_scratch_bytes())
         return fail(ZQ_ERR_WORKSPACE,
                     "zq_q4k_gemm_noalloc: B*K = %lld needs %zu bytes of scratch, more than the built-in %zu "

@@ -19,9 +19,10 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
 cudaError_t launch_gemv(const void *W, const void *W2, int N, int K, zq_q8_1 a,
                         int B, float *y, float *y2, int32_t *isums,
                         cudaStream_t st);
+// allow_split = false keeps one K range per tile (no partial-sum buffer).
 cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
-                           void *ws, cudaStream_t st);
-size_t gemm_tc_workspace_bytes(int N, int K, int B);
+                           void *ws, bool allow_split, cudaStream_t st);
+size_t gemm_tc_workspace_bytes(int N, int K, int B, bool allow_split = true);
 cudaError_t launch_isums_tc(const void *W, int N, int K, zq_q8_1 a, int B,
                             int32_t *isums, void *ws, cudaStream_t st);
 bool gemv_stream_supported(int K);
