@@ -106,11 +106,15 @@ class LayerWorkload:
     """One decoder layer's projections at batch B with R rotating weight copies."""
 
     def __init__(self, name, shapes, B, seed=0, min_rotation_bytes=3 * L2_BYTES, layers=1,
-                 extra=None):
+                 extra=None, fused=None):
         import torch
         import gemm_zq_rmsnorm_gb300 as zq
         self.zq, self.torch = zq, torch
         self.name, self.B = name, B
+        # B = 1: one launch per layer input normalises it and runs every
+        # projection that reads it (zq_rmsnorm_q4k_gemv); otherwise
+        # RMSNorm+Q8_1 first, then one call per projection
+        self.fused = (B == 1) if fused is None else fused
         dev = "cuda"
         self.extra = list(extra or [])
         self.shapes = shapes + self.extra
@@ -174,8 +178,45 @@ class LayerWorkload:
             if paired:
                 zq.q4k_gemm(w2, N, K, a, self.B, y2, self.ws, stream=stream)
 
+    def fused_groups(self, r, layer=0):
+        """(input key, K, [W], [N], [y]) per fused launch: the matrices of one
+        layer that read the same input, at most four per launch."""
+        layers_w, extra_w = self.W[r]
+        out = []
+        for k, K in self.inputs_K:
+            mats = []
+            for (pname, KK, N, paired) in self.layer_shapes:
+                if self.key_of[pname] != k:
+                    continue
+                w1, w2 = layers_w[layer][pname]
+                y1, y2 = self.y[pname]
+                mats.append((w1, N, y1[0]))
+                if paired:
+                    mats.append((w2, N, y2[0]))
+            for i in range(0, len(mats), 4):
+                c = mats[i:i + 4]
+                out.append((k, K, [m[0] for m in c], [m[1] for m in c], [m[2] for m in c]))
+        return out
+
+    def _run_fused(self, r, stream):
+        zq = self.zq
+        for li in range(self.layers):
+            for (k, K, Ws, Ns, ys) in self.fused_groups(r, li):
+                zq.rmsnorm_q4k_gemv(self.x[k][0], self.g[k], inputs.EPS, Ws, Ns, ys, stream=stream)
+        layers_w, extra_w = self.W[r]
+        for (pname, K, N, paired) in self.extra:
+            w1, w2 = extra_w[pname]
+            k = self.key_of[pname]
+            y1, y2 = self.y[pname]
+            Ws, Ns, ys = [w1], [N], [y1[0]]
+            if paired:
+                Ws, Ns, ys = Ws + [w2], Ns + [N], ys + [y2[0]]
+            zq.rmsnorm_q4k_gemv(self.x[k][0], self.g[k], inputs.EPS, Ws, Ns, ys, stream=stream)
+
     # one pass of the path
     def run(self, r=0, stream=None):
+        if self.fused:
+            return self._run_fused(r, stream)
         for k, K in self.inputs_K:
             self.zq.rmsnorm_q8_1(self.x[k], self.g[k], inputs.EPS, out=self.a[k], stream=stream)
         layers_w, extra_w = self.W[r]
@@ -188,6 +229,8 @@ class LayerWorkload:
             self._proj(pname, K, N, paired, w1, w2, stream)
 
     def launches_per_step(self):
+        if self.fused:
+            return len(self.fused_groups(0)) * self.layers + len(self.extra)
         n = len(self.inputs_K)
         for (pname, K, N, paired) in self.layer_shapes * self.layers + self.extra:
             calls = 1 if (self.B == 1 or not paired) else 2
@@ -297,7 +340,11 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
     def one(r):
         w1, w2 = wl.weights(r, pname)
         y1, y2 = wl.y[pname]
-        if wl.B == 1:
+        if wl.fused:
+            k = wl.key_of[pname]
+            Ws, Ns, ys = ([w1, w2], [N, N], [y1[0], y2[0]]) if paired else ([w1], [N], [y1[0]])
+            zq.rmsnorm_q4k_gemv(wl.x[k][0], wl.g[k], inputs.EPS, Ws, Ns, ys)
+        elif wl.B == 1:
             if paired:
                 zq.q4k_gemv_pair(w1, w2, N, K, a, y1, y2)
             else:
@@ -312,7 +359,10 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
     reps = max(3, steps // 4)
     ms = time_graphs(torch, [g], reps, max(1, warmup // 2), stream) / per_graph
     units = 2 if (paired and wl.B == 1) else 1
-    if wl.B == 1:
+    if wl.fused:
+        # weights once, x and gamma (the kernel normalises and packs x itself), y
+        alg = units * N * K * 144 // 256 + 2 * K * 4 + units * N * 4
+    elif wl.B == 1:
         alg = proj_bytes(K, N, 1) * units - (K * (1 + 4 / 32) if units == 2 else 0)
     else:
         alg = 2 * wl.B * N * K
@@ -369,6 +419,8 @@ def main():
                     choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-path", default="fused", choices=["fused", "two-step"],
+                    help="B = 1 step: fused RMSNorm+mat-vec launches, or RMSNorm+Q8_1 then per-projection calls")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference" or os.environ.get("ZQ_BENCH_DEBUG"), "W >= 3"
 
@@ -405,13 +457,14 @@ def main():
         return float(t.item())
 
     wl_dec = None
+    fz = args.decode_path == "fused"
     if args.workload in ("headline", "decode-27b"):
-        wl_dec = LayerWorkload("decode-27b-layer", inputs.LAYER_27B, 1)
+        wl_dec = LayerWorkload("decode-27b-layer", inputs.LAYER_27B, 1, fused=fz)
     elif args.workload == "decode-small":
         wl_dec = LayerWorkload("decode-small-28L+lm_head", inputs.SMALL_DECODE[:-1], 1, layers=28,
-                               extra=[inputs.SMALL_DECODE[-1]])
+                               extra=[inputs.SMALL_DECODE[-1]], fused=fz)
     elif args.workload == "tiny":
-        wl_dec = LayerWorkload("tiny-1024x1024", inputs.TINY, 1, min_rotation_bytes=3 * L2_BYTES)
+        wl_dec = LayerWorkload("tiny-1024x1024", inputs.TINY, 1, min_rotation_bytes=3 * L2_BYTES, fused=fz)
 
     out = dict(result)
     if wl_dec is not None:
@@ -428,12 +481,17 @@ def main():
             "config": {"workload": wl_dec.name, "B": 1, "hidden": wl_dec.inputs_K[0][1],
                        "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl_dec.shapes],
                        "layers": wl_dec.layers, "weight_copies_rotated": wl_dec.R,
+                       "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
+                                       if wl_dec.fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
                        "l2": f"inputs larger than L2: {wl_dec.R} rotating weight copies of the step",
                        "algorithmic_bytes_per_step": int(wl_dec.algo_bytes())},
-            "roofline": {"bound": "hbm", "kernel": f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}",
+            "roofline": {"bound": "hbm",
+                         "kernel": (f"rmsnorm_q4k_gemv {dK}->{dN}{' x2 (gate+up)' if dp else ''}" if wl_dec.fused
+                                    else f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}"),
                          "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
-                         "traffic": recorded_traffic(f"q4k_gemv_stream_pair_{dK}x{dN}") if dp else None,
+                         "traffic": (recorded_traffic(f"{'fused_' if wl_dec.fused else ''}q4k_gemv_stream_pair_{dK}x{dN}")
+                                     if dp else None),
                          "kernel_ms": round(dms, 5)},
             "gpu_launches": wl_dec.launches_per_step() * args.steps,
             "clocks": clk.summary(),

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_AL
 EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
            "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
-           "zq_device_status", "zq_q4k_gemm_noalloc")
+           "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv")
 
 
 class ZQError(RuntimeError):
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_debug_q4k_isums": ([P, i, i, _Q8, i, P, i, P, sz, P], i),
         "zq_device_status": ([P, i], i),
         "zq_q4k_gemm_noalloc": ([P, i, i, _Q8, i, P, P], i),
+        "zq_q4k_gemv_multi": ([i, P, P, i, _Q8, P, P], i),
+        "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -135,6 +137,44 @@ def rmsnorm_q8_1(x: torch.Tensor, gamma: torch.Tensor, eps: float, out: Q8_1 | N
         out = empty_q8_1(B, K, x.device)
     _check(lib.zq_rmsnorm_q8_1(_ptr(x), _ptr(gamma), B, K, float(eps), out._c(), _stream(stream)))
     return out
+
+
+def _job_arrays(Ws, Ns, ys):
+    n = len(Ws)
+    if not (len(Ns) == n and len(ys) == n):
+        raise ValueError("W, N and y lists must have the same length")
+    W_arr = (ctypes.c_void_p * max(n, 1))(*[w.data_ptr() for w in Ws])
+    N_arr = (ctypes.c_int * max(n, 1))(*[int(v) for v in Ns])
+    y_arr = (ctypes.c_void_p * max(n, 1))(*[y.data_ptr() for y in ys])
+    return n, W_arr, N_arr, y_arr
+
+
+def q4k_gemv_multi(Ws, Ns, K: int, a: Q8_1, ys=None, stream=None):
+    """y[m] = W[m] a for up to four matrices sharing one Q8_1 input (see
+    zq_q4k_gemv_multi); returns the list of outputs."""
+    lib = load()
+    if ys is None:
+        ys = [torch.empty(int(n), dtype=torch.float32, device=a.qs.device) for n in Ns]
+    n, W_arr, N_arr, y_arr = _job_arrays(Ws, Ns, ys)
+    _check(lib.zq_q4k_gemv_multi(n, ctypes.cast(W_arr, ctypes.c_void_p), ctypes.cast(N_arr, ctypes.c_void_p), K,
+                                 a._c(), ctypes.cast(y_arr, ctypes.c_void_p), _stream(stream)))
+    return ys
+
+
+def rmsnorm_q4k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, Ws, Ns, ys=None,
+                     q8_out: Q8_1 | None = None, stream=None):
+    """RMSNorm + Q8_1 of one token x fp32 [K] (or [1][K]) fused with the
+    mat-vecs of up to four matrices (see zq_rmsnorm_q4k_gemv)."""
+    lib = load()
+    K = x.shape[-1]
+    if ys is None:
+        ys = [torch.empty(int(n), dtype=torch.float32, device=x.device) for n in Ns]
+    n, W_arr, N_arr, y_arr = _job_arrays(Ws, Ns, ys)
+    q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
+    _check(lib.zq_rmsnorm_q4k_gemv(_ptr(x), _ptr(gamma), float(eps), K, n, ctypes.cast(W_arr, ctypes.c_void_p),
+                                   ctypes.cast(N_arr, ctypes.c_void_p), ctypes.cast(y_arr, ctypes.c_void_p), q8,
+                                   _stream(stream)))
+    return ys
 
 
 def q4k_gemv(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor | None = None,

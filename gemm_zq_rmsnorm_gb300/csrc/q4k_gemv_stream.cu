@@ -21,9 +21,17 @@
 // d*sc*d8*I - dmin*m*s8 in fp32 and accumulates in registers; after the stage
 // the segments of each row are summed in a fixed order into y.  The paired
 // kernel is the same launch over the rows of both matrices, sharing the staged
-// activations.
+// activations.  Up to four matrices that read the same input (q/k/v, gate/up)
+// share one launch the same way.
+//
+// With x and gamma instead of Q8_1 codes the consumers first compute RMSNorm
+// and the Q8_1 packing of x themselves, in the canonical order of the
+// RMSNorm+Q8_1 kernel (same bytes), straight into the shared-memory staging,
+// while the producer already streams weights: the normalised input never
+// goes through HBM and the separate launch disappears.
 #include "zq_async.cuh"
 #include "zq_internal.cuh"
+#include "zq_q8_1_pack.cuh"
 
 namespace zq {
 namespace {
@@ -38,23 +46,40 @@ constexpr int kGroups = 8 * kConsumerWarps;            // four-lane task groups 
 constexpr int kSeg = 4;                                // max blocks per task
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxK = 32768;                           // activation staged in smem
+constexpr int kMaxMats = kGemvMaxMats;
 
 struct StreamParams {
-    const uint8_t *W[2];
-    float *y[2];
-    int N, K, nb;
+    const uint8_t *W[kMaxMats];
+    float *y[kMaxMats];
+    int N[kMaxMats];
+    int gstart[kMaxMats + 1];   // first row group of each matrix; gstart[nmat] = total
+    int nmat;
+    int K, nb;
     uint32_t rowbytes;
     int R;                // rows per group
     int P;                // pieces per group (> 1 only when R == 1)
     int CB;               // blocks per piece
-    int groups_per_mat;
     int total_groups;
     uint32_t stage_alloc; // bytes reserved per stage (multiple of 128)
+    // input: Q8_1 planes, or (x, gamma, eps) normalised in the kernel
     const int8_t *qs;
     const __half *d;
     const __half *s;
+    const float *x;
+    const float *gamma;
+    float eps;
+    zq_q8_1 q8out;        // fused input only: codes also written here by CTA 0 (qs may be null)
     unsigned int *status;
 };
+
+// matrix of row group g
+__device__ __forceinline__ int group_mat(const StreamParams &p, int g)
+{
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxMats; ++i) m += (i < p.nmat && g >= p.gstart[i]) ? 1 : 0;
+    return m;
+}
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -63,6 +88,8 @@ __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + 
 // quarter-warp (two consecutive super-blocks x four pairs) then start in
 // eight different 16-byte bank groups.
 __host__ __device__ constexpr size_t act_bytes(int K) { return (size_t)K / 64 * 80; }
+
+static_assert(kStages * kMaxBlk >= kMaxK / 32 + 257, "RMSNorm scratch fits in the contribution area");
 
 struct SmemLayout {
     size_t ring, act_qs, act_ds, contrib, bars, total;
@@ -168,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
         }
         abort_s = 0;
         fence_mbar_init();
+        pdl_launch_dependents();
     }
     __syncthreads();
 
@@ -177,17 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
             const uint64_t policy = l2_evict_first_policy();
             uint32_t it = 0;
             for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
-                const int mat = g / p.groups_per_mat;
-                const int row0 = (g % p.groups_per_mat) * p.R;
-                const int rows = min(p.R, p.N - row0);
+                const int mat = group_mat(p, g);
+                const int row0 = (g - p.gstart[mat]) * p.R;
+                const int rows = min(p.R, p.N[mat] - row0);
                 for (int pc = 0; pc < p.P; ++pc, ++it) {
                     const uint32_t slot = it % kStages, round = it / kStages;
                     if (round > 0 && !mbar_wait(&empty[slot], (round & 1) ^ 1, p.status)) return;
                     const uint32_t bytes = (p.P == 1)
                                                ? (uint32_t)rows * p.rowbytes
                                                : (uint32_t)min(p.CB, p.nb - pc * p.CB) * kQ4KBlockBytes;
-                    const uint8_t *src = (mat ? p.W[1] : p.W[0]) + (size_t)row0 * p.rowbytes +
-                                         (size_t)pc * p.CB * kQ4KBlockBytes;
+                    const uint8_t *src = p.W[mat] + (size_t)row0 * p.rowbytes + (size_t)pc * p.CB * kQ4KBlockBytes;
                     mbar_arrive_expect_tx(&full[slot], bytes);
                     bulk_g2s_hint(ring + (size_t)slot * p.stage_alloc, src, bytes, &full[slot], policy);
                 }
@@ -197,15 +224,136 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
     }
 
     // ---------------------------------------------------------- consumers
-    // stage the activation row: codes with the 80-byte group stride, scales
-    // and sums as they are (pairs of binary16 per 32-bit word)
-    {
+    // The producer streams weights (written by no kernel) from the start; the
+    // activations may come from the previous kernel on the stream, and y may
+    // still be read by it: wait for that kernel before touching either.
+    pdl_wait();
+    if (p.x == nullptr) {
+        // stage the activation row: codes with the 80-byte group stride,
+        // scales and sums as they are (pairs of binary16 per 32-bit word)
         const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs);
         for (int c = tid; c < p.K / 16; c += kConsumers)
             *reinterpret_cast<uint4 *>(aq + 80 * (c >> 2) + 16 * (c & 3)) = __ldg(gq + c);
         const uint32_t *gd = reinterpret_cast<const uint32_t *>(p.d);
         const uint32_t *gs = reinterpret_cast<const uint32_t *>(p.s);
         for (int c = tid; c < p.K / 64; c += kConsumers) ads[c] = make_uint2(__ldg(gd + c), __ldg(gs + c));
+    } else {
+        // RMSNorm + Q8_1 of x in the canonical order (per-block fma chains,
+        // 256 slots in increasing block order, pairwise tree), packed into
+        // the staging; scratch in the (still unused) contribution area.
+        // Eight lanes share a 32-value block, each holding four consecutive
+        // values, so every load instruction of a warp reads 512 contiguous
+        // bytes; the block's fma chain runs through the eight lanes in order
+        // (shuffles), and amax and the code sum are exact group reductions.
+        const int nblk = p.K >> 5;
+        float *part = contrib;                // [nblk]
+        float *slot = contrib + kMaxK / 32;   // [256] and r
+        const int grp = tid >> 3, sub = tid & 7;
+        constexpr int kGroupsPerPass = kConsumers / 8;   // 64 blocks per pass
+        constexpr int kUnroll = 9;                       // passes with loads in flight together (K <= 18432: one)
+        for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
+            float4 xv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;   // CTA-uniform
+                const int b = base + kGroupsPerPass * u + grp;
+                xv[u] = b < nblk ? __ldg(reinterpret_cast<const float4 *>(p.x + 32 * b) + sub)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                float pr = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (sub == j) {
+                        pr = __fmaf_rn(xv[u].x, xv[u].x, pr);
+                        pr = __fmaf_rn(xv[u].y, xv[u].y, pr);
+                        pr = __fmaf_rn(xv[u].z, xv[u].z, pr);
+                        pr = __fmaf_rn(xv[u].w, xv[u].w, pr);
+                    }
+                    pr = __shfl_sync(0xffffffffu, pr, (lane & ~7) | j);
+                }
+                const int b = base + kGroupsPerPass * u + grp;
+                if (sub == 0 && b < nblk) part[b] = pr;
+            }
+        }
+        named_bar(1, kConsumers);
+        if (tid < 256) {
+            float v = 0.0f;
+            for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
+            slot[tid] = v;
+        }
+        named_bar(1, kConsumers);
+#pragma unroll
+        for (int off = 128; off >= 32; off >>= 1) {
+            if (tid < off) slot[tid] = __fadd_rn(slot[tid], slot[tid + off]);
+            named_bar(1, kConsumers);
+        }
+        if (tid < 32) {
+            float v = slot[tid];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+            if (tid == 0) slot[256] = rms_scale(v, p.K, p.eps);
+        }
+        named_bar(1, kConsumers);
+        const float r = slot[256];
+        __half *ads16 = reinterpret_cast<__half *>(ads);
+        const bool out = blockIdx.x == 0 && p.q8out.qs != nullptr;
+        for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
+            float4 xv[kUnroll], gv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                const int b = base + kGroupsPerPass * u + grp;
+                const bool in = b < nblk;
+                xv[u] = in ? __ldg(reinterpret_cast<const float4 *>(p.x + 32 * b) + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
+                gv[u] = in ? __ldg(reinterpret_cast<const float4 *>(p.gamma + 32 * b) + sub)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                const int b = base + kGroupsPerPass * u + grp;
+                float xh[4];
+                xh[0] = __fmul_rn(__fmul_rn(xv[u].x, r), gv[u].x);
+                xh[1] = __fmul_rn(__fmul_rn(xv[u].y, r), gv[u].y);
+                xh[2] = __fmul_rn(__fmul_rn(xv[u].z, r), gv[u].z);
+                xh[3] = __fmul_rn(__fmul_rn(xv[u].w, r), gv[u].w);
+                float amax = fmaxf(fmaxf(fabsf(xh[0]), fabsf(xh[1])), fmaxf(fabsf(xh[2]), fabsf(xh[3])));
+#pragma unroll
+                for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+                const float d = __fdiv_rn(amax, 127.0f);
+                const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+                uint32_t word = 0;
+                int qsum = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float q = roundf(__fmul_rn(xh[c], id));
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    const int qi = (int)q;
+                    qsum += qi;
+                    word |= ((uint32_t)(qi & 0xFF)) << (8 * c);
+                }
+#pragma unroll
+                for (int m = 1; m < 8; m <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, m);
+                if (b < nblk) {
+                    *reinterpret_cast<uint32_t *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 4 * sub) = word;
+                    const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
+                    if (sub == 0) {
+                        ads16[4 * (b >> 1) + (b & 1)] = dh;
+                        ads16[4 * (b >> 1) + 2 + (b & 1)] = sh;
+                    }
+                    if (out) {
+                        reinterpret_cast<uint32_t *>(p.q8out.qs + 32 * b)[sub] = word;
+                        if (sub == 0) {
+                            reinterpret_cast<__half *>(p.q8out.d)[b] = dh;
+                            reinterpret_cast<__half *>(p.q8out.s)[b] = sh;
+                        }
+                    }
+                }
+            }
+        }
     }
     named_bar(1, kConsumers);
 
@@ -219,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
     const unsigned gmask = 0xFu << (4 * (lane >> 2));
     uint32_t it = 0;
     for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
-        const int mat = g / p.groups_per_mat;
-        const int row0 = (g % p.groups_per_mat) * p.R;
-        const int rows = min(p.R, p.N - row0);
-        float *yv = mat ? p.y[1] : p.y[0];
+        const int mat = group_mat(p, g);
+        const int row0 = (g - p.gstart[mat]) * p.R;
+        const int rows = min(p.R, p.N[mat] - row0);
+        float *yv = p.y[mat];
         float row_acc = 0.0f;
         for (int pc = 0; pc < p.P; ++pc, ++it) {
             const uint32_t slot = it % kStages, round = it / kStages;
@@ -282,50 +430,49 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
 
 size_t g_attr_bytes[64];
 
-}  // namespace
-
-bool gemv_stream_supported(int K) { return K <= kMaxK; }
-
-cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
-                               float *y2, unsigned int *status, cudaStream_t st)
+// shared launch set-up of both input kinds
+cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, cudaStream_t st)
 {
-    StreamParams p{};
-    p.W[0] = static_cast<const uint8_t *>(W);
-    p.W[1] = static_cast<const uint8_t *>(W2);
-    p.y[0] = y;
-    p.y[1] = y2;
-    p.N = N;
+    p.nmat = job.nmat;
+    long long totalN = 0;
+    for (int m = 0; m < job.nmat; ++m) {
+        p.W[m] = static_cast<const uint8_t *>(job.W[m]);
+        p.y[m] = job.y[m];
+        p.N[m] = job.N[m];
+        totalN += job.N[m];
+    }
     p.K = K;
     p.nb = K / 256;
     p.rowbytes = (uint32_t)p.nb * kQ4KBlockBytes;
-    const int nmat = W2 ? 2 : 1;
     const int sms = num_sms();
     // stage size: as large as shared memory allows (<= 64 KB), but small
     // enough that every CTA gets >= 3 stages of work
     const size_t fixed = SmemLayout(K, 0).total;
     size_t cap = (kSmemLimit - fixed) / kStages / 128 * 128;
     cap = cap > (size_t)kStageMax ? (size_t)kStageMax : cap;
-    const double total = (double)nmat * N * p.rowbytes;
+    const double total = (double)totalN * p.rowbytes;
     size_t target = (size_t)(total / sms / 3);
     target = target < 4096 ? 4096 : (target > cap ? cap : target);
-    if (p.rowbytes <= target) {
-        p.R = (int)(target / p.rowbytes);
+    // A row is split into pieces only when it does not fit in a stage at all,
+    // so a row's summation order depends on K alone, not on which other
+    // matrices share the launch.
+    if (p.rowbytes <= cap) {
+        p.R = p.rowbytes <= target ? (int)(target / p.rowbytes) : 1;
         p.P = 1;
         p.CB = p.nb;
         p.stage_alloc = (uint32_t)align_up((size_t)p.R * p.rowbytes, 128);
     } else {
         p.R = 1;
-        p.CB = (int)(target / kQ4KBlockBytes);
+        p.CB = (int)(cap / kQ4KBlockBytes);
         if (p.CB < 1) p.CB = 1;
         p.P = (p.nb + p.CB - 1) / p.CB;
         p.stage_alloc = (uint32_t)align_up((size_t)p.CB * kQ4KBlockBytes, 128);
     }
-    p.groups_per_mat = (N + p.R - 1) / p.R;
-    p.total_groups = p.groups_per_mat * nmat;
-    p.qs = a.qs;
-    p.d = reinterpret_cast<const __half *>(a.d);
-    p.s = reinterpret_cast<const __half *>(a.s);
-    p.status = status;
+    p.gstart[0] = 0;
+    for (int m = 0; m < kMaxMats; ++m)
+        p.gstart[m + 1] = p.gstart[m] + (m < job.nmat ? (job.N[m] + p.R - 1) / p.R : 0);
+    p.total_groups = p.gstart[job.nmat];
+    p.status = device_status_word();
     const SmemLayout L(K, p.stage_alloc);
     int dev = 0;
     cudaGetDevice(&dev);
@@ -337,8 +484,31 @@ cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q
         g_attr_bytes[dev] = L.total;
     }
     const int grid = p.total_groups < sms ? p.total_groups : sms;
-    q4k_gemv_stream_kernel<<<grid, kThreads, L.total, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(q4k_gemv_stream_kernel, dim3(grid), dim3(kThreads), L.total, st, p);
+}
+
+}  // namespace
+
+bool gemv_stream_supported(int K) { return K <= kMaxK; }
+
+cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_t st)
+{
+    StreamParams p{};
+    p.qs = a.qs;
+    p.d = reinterpret_cast<const __half *>(a.d);
+    p.s = reinterpret_cast<const __half *>(a.s);
+    return launch_stream(p, job, K, st);
+}
+
+cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
+                                     const zq_q8_1 *q8out, cudaStream_t st)
+{
+    StreamParams p{};
+    p.x = x;
+    p.gamma = gamma;
+    p.eps = eps;
+    if (q8out) p.q8out = *q8out;
+    return launch_stream(p, job, K, st);
 }
 
 }  // namespace zq

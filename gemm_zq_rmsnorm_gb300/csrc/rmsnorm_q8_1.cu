@@ -20,7 +20,9 @@
 //
 // HBM roofline: reads B*K*4 bytes of x (+ K*4 of gamma, cached), writes
 // B*K*(1 + 4/32) bytes.  At B = 1 the kernel is latency-bound.
+#include "zq_async.cuh"
 #include "zq_internal.cuh"
+#include "zq_q8_1_pack.cuh"
 
 namespace zq {
 namespace {
@@ -31,31 +33,12 @@ constexpr int kMaxBlocks = 2048;   // K <= 65536 on this path
 // Quantise one 32-value block (already normalised) to Q8_1 and store it.
 __device__ __forceinline__ void pack_block(const float (&xh)[32], int8_t *qdst, __half *dq, __half *sq)
 {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xh[i]));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-    int sum = 0;
-    uint32_t packed[8];
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float q = roundf(__fmul_rn(xh[4 * v + c], id));
-            q = fminf(fmaxf(q, -127.0f), 127.0f);
-            const int qi = (int)q;
-            sum += qi;
-            word |= ((uint32_t)(qi & 0xFF)) << (8 * c);
-        }
-        packed[v] = word;
-    }
+    const Q8Block o = q8_1_pack(xh);
     uint4 *dst = reinterpret_cast<uint4 *>(qdst);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    *dq = __float2half_rn(d);
-    *sq = __float2half_rn(__fmul_rn(d, (float)sum));
+    dst[0] = o.q0;
+    dst[1] = o.q1;
+    *dq = o.d;
+    *sq = o.s;
 }
 
 __global__ void __launch_bounds__(kMaxThreads)
@@ -71,6 +54,8 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
     const int nblk = K >> 5;
     const float *xt = x + (size_t)blockIdx.x * K;
     const bool one = nblk <= nthr;   // one block per thread: keep it in registers
+    pdl_wait();                  // x may come from the previous kernel; Q8_1 may still be read by it
+    pdl_launch_dependents();
 
     // pass 1: p_b for every block
     float xr[32];
@@ -153,6 +138,8 @@ rmsnorm_q8_1_wide_kernel(const float *__restrict__ x, const float *__restrict__ 
     const int t = threadIdx.x;
     const int nblk = K >> 5;
     const float *xt = x + (size_t)blockIdx.x * K;
+    pdl_wait();
+    pdl_launch_dependents();
     float slot = 0.0f;
     for (int b = t; b < nblk; b += 256) {
         const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
@@ -214,11 +201,9 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     if (nblk <= kMaxBlocks) {
         int threads = nblk < kMaxThreads ? (nblk + 31) / 32 * 32 : kMaxThreads;
         if (threads < 256) threads = 256;   // the slot tree needs 256 threads
-        rmsnorm_q8_1_kernel<<<B, threads, 0, st>>>(x, gamma, K, eps, out.qs, dq, sq);
-    } else {
-        rmsnorm_q8_1_wide_kernel<<<B, 256, 0, st>>>(x, gamma, K, eps, out.qs, dq, sq);
+        return launch_pdl(rmsnorm_q8_1_kernel, dim3(B), dim3(threads), 0, st, x, gamma, K, eps, out.qs, dq, sq);
     }
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_q8_1_wide_kernel, dim3(B), dim3(256), 0, st, x, gamma, K, eps, out.qs, dq, sq);
 }
 
 }  // namespace zq

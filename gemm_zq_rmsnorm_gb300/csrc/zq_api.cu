@@ -109,7 +109,19 @@ unsigned int *device_status_word()
 cudaError_t launch_gemv_dispatch(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
                                  float *y2, cudaStream_t st)
 {
-    if (gemv_stream_supported(K)) return launch_gemv_stream(W, W2, N, K, a, y, y2, device_status_word(), st);
+    if (gemv_stream_supported(K)) {
+        GemvJob job{};
+        job.nmat = W2 ? 2 : 1;
+        job.W[0] = W;
+        job.N[0] = N;
+        job.y[0] = y;
+        if (W2) {
+            job.W[1] = W2;
+            job.N[1] = N;
+            job.y[1] = y2;
+        }
+        return launch_gemv_stream(job, K, a, st);
+    }
     return launch_gemv(W, W2, N, K, a, 1, y, y2, nullptr, st);
 }
 
@@ -214,6 +226,71 @@ int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_1 a, fl
     if ((st = check_device(&dev))) return st;
     return launched(launch_gemv_dispatch(Wg, Wu, N, K, a, y_gate, y_up, (cudaStream_t)stream),
                     "zq_q4k_gemv_pair launch");
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the multi-matrix decode entry points; fills the job.
+int check_job(const char *name, int nmat, const void *const *W, const int *N, int K, float *const *y, GemvJob &job)
+{
+    if (nmat < 1 || nmat > kGemvMaxMats)
+        return fail(ZQ_ERR_ARG, "%s: nmat = %d must be in [1, %d]", name, nmat, kGemvMaxMats);
+    if (!W || !N || !y) return fail(ZQ_ERR_ARG, "%s: null W, N or y array", name);
+    job = GemvJob{};
+    job.nmat = nmat;
+    for (int m = 0; m < nmat; ++m) {
+        int st = check_q4k(W[m], N[m], K, name);
+        if (st) return st;
+        if (!y[m]) return fail(ZQ_ERR_ARG, "%s: null y[%d]", name, m);
+        if (!aligned16(y[m])) return fail(ZQ_ERR_ALIGN, "%s: y[%d] must be 16-byte aligned", name, m);
+        job.W[m] = W[m];
+        job.N[m] = N[m];
+        job.y[m] = y[m];
+    }
+    return ZQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int zq_q4k_gemv_multi(int nmat, const void *const *W, const int *N, int K, zq_q8_1 a, float *const *y,
+                      void *stream)
+{
+    GemvJob job;
+    int st = check_job("zq_q4k_gemv_multi", nmat, W, N, K, y, job);
+    if (st) return st;
+    if ((st = check_q8(a, "zq_q4k_gemv_multi"))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gemv_stream_supported(K)) return launched(launch_gemv_stream(job, K, a, s), "zq_q4k_gemv_multi launch");
+    for (int m = 0; m < nmat; ++m) {   // wide rows: one direct-load launch per matrix
+        cudaError_t e = launch_gemv(job.W[m], nullptr, job.N[m], K, a, 1, job.y[m], nullptr, nullptr, s);
+        if (e != cudaSuccess) return launched(e, "zq_q4k_gemv_multi launch");
+    }
+    return ZQ_OK;
+}
+
+int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, int nmat, const void *const *W,
+                        const int *N, float *const *y, const zq_q8_1 *q8_out, void *stream)
+{
+    if (!x || !gamma) return fail(ZQ_ERR_ARG, "zq_rmsnorm_q4k_gemv: null x or gamma");
+    if (!aligned16(x) || !aligned16(gamma))
+        return fail(ZQ_ERR_ALIGN, "zq_rmsnorm_q4k_gemv: x and gamma must be 16-byte aligned");
+    if (!(eps >= 0.0f) || eps != eps) return fail(ZQ_ERR_ARG, "zq_rmsnorm_q4k_gemv: eps must be >= 0");
+    GemvJob job;
+    int st = check_job("zq_rmsnorm_q4k_gemv", nmat, W, N, K, y, job);
+    if (st) return st;
+    if (!gemv_stream_supported(K))
+        return fail(ZQ_ERR_SHAPE, "zq_rmsnorm_q4k_gemv: K = %d above the in-kernel normalisation limit 32768", K);
+    if (q8_out && (st = check_q8(*q8_out, "zq_rmsnorm_q4k_gemv (q8_out)"))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, q8_out, (cudaStream_t)stream),
+                    "zq_rmsnorm_q4k_gemv launch");
 }
 
 size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B)

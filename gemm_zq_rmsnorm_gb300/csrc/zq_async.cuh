@@ -105,6 +105,12 @@ __device__ __forceinline__ void named_bar(uint32_t id, uint32_t threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrive at a named barrier without waiting for it.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -28,8 +28,43 @@ cudaError_t launch_isums_tc(const void *W, int N, int K, zq_q8_1 a, int B,
 bool gemv_stream_supported(int K);
 size_t noalloc_scratch_bytes();
 cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
-cudaError_t launch_gemv_stream(const void *W, const void *W2, int N, int K, zq_q8_1 a, float *y,
-                               float *y2, unsigned int *status, cudaStream_t st);
+// Decode mat-vec job: up to kGemvMaxMats Q4_K matrices (N[m] x K) that read
+// the same input vector.
+constexpr int kGemvMaxMats = 4;
+struct GemvJob {
+    int nmat;
+    const void *W[kGemvMaxMats];
+    int N[kGemvMaxMats];
+    float *y[kGemvMaxMats];
+};
+// input: Q8_1 codes of one token
+cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_t st);
+// input: x and gamma; RMSNorm + Q8_1 computed in the kernel (q8out, when
+// non-null, receives the codes)
+cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
+                                     const zq_q8_1 *q8out, cudaStream_t st);
+
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous kernel on the stream is still running.  Every kernel launched this
+// way executes griddepcontrol.wait before it reads anything an earlier kernel
+// may write and before it writes anything; only reads of data no kernel of
+// the library writes (weights) and on-chip set-up may come first.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 // Device-side error word of the current device (bit 0: a bounded wait in a
 // pipelined kernel expired).  Valid after the first successful device check.

@@ -126,6 +126,37 @@ ZQ_API int zq_q4k_gemv_pair(const void *Wg, const void *Wu, int N, int K, zq_q8_
                      float *y_gate, float *y_up, void *stream);
 
 /*
+ * Decode mat-vec of up to four matrices that read the same Q8_1 input, in one
+ * launch (ZINC docs "ROCm backend": Q8 activations packed once and reused by
+ * the Q4_K projections that follow; MIInfer README, "Status": shared
+ * activation staging).  The q/k/v projections of a layer are the intended use.
+ *   nmat : 1..4;  W[m] : Q4_K N[m] x K (16-byte aligned);  y[m] : fp32 [N[m]]
+ *   (16-byte aligned);  W, N, y are host arrays of nmat entries.
+ * Each y[m] equals zq_q4k_gemv(W[m], N[m], K, a, y[m]) bit for bit.  Shapes as
+ * zq_q4k_gemv; K > 32768 runs one launch per matrix.
+ */
+ZQ_API int zq_q4k_gemv_multi(int nmat, const void *const *W, const int *N, int K, zq_q8_1 a,
+                             float *const *y, void *stream);
+
+/*
+ * Fused decode step: RMSNorm and Q8_1 packing of one token x (as
+ * zq_rmsnorm_q8_1 with B = 1), then y[m] = W[m] (Q8_1 of x) for up to four
+ * matrices, in one launch (ZINC docs "ROCm backend", "Build and verify":
+ * normalisation and Q8 packing fused ahead of the Q4 projections).  Every
+ * thread block computes the codes itself in shared memory in the canonical
+ * order, so they are byte for byte those of zq_rmsnorm_q8_1 and each y[m]
+ * equals zq_q4k_gemv on them bit for bit.  The normalised input never goes
+ * through device memory unless q8_out (optional, may be NULL; planes of one
+ * token) asks for it.
+ *   x, gamma : fp32 [K], 16-byte aligned;  eps >= 0;
+ *   nmat, W, N, y : as zq_q4k_gemv_multi.
+ * Shapes: K % 256 == 0, 256 <= K <= 32768 (larger K: ZQ_ERR_SHAPE).
+ */
+ZQ_API int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, int nmat,
+                               const void *const *W, const int *N, float *const *y,
+                               const zq_q8_1 *q8_out, void *stream);
+
+/*
  * Batched projection of B tokens (MIInfer README, "Current phase":
  * token-batched chunk projections and tensor-core/int8 GEMM prefill).
  *   W : Q4_K N x K;  a : Q8_1 of B tokens;  y : fp32 [B][N].

@@ -106,3 +106,41 @@ def test_binding_raises_without_device():
         pytest.skip("a GPU is present")
     with pytest.raises(Exception):
         zq.rmsnorm_q8_1(torch.zeros(1, 64), torch.ones(64), 1e-6)
+
+
+def _arr(ctype, vals):
+    return (ctype * max(len(vals), 1))(*vals)
+
+
+@pytest.mark.parametrize("nmat,Ws,Ns,ys,K,status", [
+    (0, [A16], [10], [A16], 1024, -1),                 # no matrix
+    (5, [A16] * 5, [10] * 5, [A16] * 5, 1024, -1),     # more than four
+    (2, [A16, None], [10, 10], [A16, A16], 1024, -1),  # null second matrix
+    (2, [A16, A16], [10, 0], [A16, A16], 1024, -2),    # N = 0
+    (1, [A16], [10], [A16], 1000, -2),                 # K % 256
+    (2, [A16, A16], [10, 10], [A16, A8], 1024, -3),    # misaligned y
+])
+def test_gemv_multi_rejects(lib, nmat, Ws, Ns, ys, K, status):
+    W = _arr(ctypes.c_void_p, Ws)
+    N = _arr(ctypes.c_int, Ns)
+    y = _arr(ctypes.c_void_p, ys)
+    assert lib.zq_q4k_gemv_multi(nmat, ctypes.cast(W, ctypes.c_void_p), ctypes.cast(N, ctypes.c_void_p), K, q8(),
+                                 ctypes.cast(y, ctypes.c_void_p), None) == status
+    assert lib.zq_last_error()
+
+
+@pytest.mark.parametrize("x,eps,K,nmat,status", [
+    (None, 1e-6, 1024, 1, -1),      # null x
+    (A8, 1e-6, 1024, 1, -3),        # misaligned x
+    (A16, -1.0, 1024, 1, -1),       # negative eps
+    (A16, 1e-6, 1024, 0, -1),       # no matrix
+    (A16, 1e-6, 33024, 1, -2),      # K above the in-kernel normalisation limit
+])
+def test_rmsnorm_gemv_rejects(lib, x, eps, K, nmat, status):
+    W = _arr(ctypes.c_void_p, [A16])
+    N = _arr(ctypes.c_int, [10])
+    y = _arr(ctypes.c_void_p, [A16])
+    assert lib.zq_rmsnorm_q4k_gemv(x, A16, eps, K, nmat, ctypes.cast(W, ctypes.c_void_p),
+                                   ctypes.cast(N, ctypes.c_void_p), ctypes.cast(y, ctypes.c_void_p), None,
+                                   None) == status
+    assert lib.zq_last_error()
