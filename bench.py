@@ -234,7 +234,13 @@ class LayerWorkload:
         n = len(self.inputs_K)
         for (pname, K, N, paired) in self.layer_shapes * self.layers + self.extra:
             calls = 1 if (self.B == 1 or not paired) else 2
-            per = 1 if self.B == 1 else (2 if self.zq.gemm_workspace_bytes(N, K, self.B) else 1)
+            if self.B == 1:
+                per = 1
+            else:
+                # q8 split + GEMM, + the split-K reduction when the workspace
+                # holds partial sums beyond the hi/lo activations and scales
+                base = 4 * self.B * K + (4 * self.B + 255) // 256 * 256
+                per = 2 + (1 if self.zq.gemm_workspace_bytes(N, K, self.B) > base else 0)
             n += calls * per
         return n
 
