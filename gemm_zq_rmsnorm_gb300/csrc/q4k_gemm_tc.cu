@@ -541,6 +541,8 @@ EncodeTiledFn encode_fn()
 
 size_t g_attr_bytes[64];
 
+}  // namespace
+
 // workspace layout: hi [B][K] fp16 | lo [B][K] fp16 | tscale [B] fp32 |
 // partial sums [splits][B][N] fp32 (when splits > 1)
 size_t split_bytes(int K, int B) { return (size_t)B * K * sizeof(__half); }
@@ -553,6 +555,8 @@ size_t tscale_bytes(int B) { return ((size_t)B * sizeof(float) + 255) & ~(size_t
 // s within 3 % of the best, keeping >= 2 super-blocks per split.
 int choose_splits(int B, int N, int K, int sms)
 {
+    // both tensor-core kernels tile the weight rows by 128; the batched one
+    // also tiles the tokens by 128, the small-batch one takes all B <= 16
     const long long tiles = (long long)((B + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int nb = K / 256;
     const int smax = nb / 2 < 8 ? nb / 2 : 8;
@@ -571,7 +575,19 @@ int choose_splits(int B, int N, int K, int sms)
     return 1;
 }
 
-}  // namespace
+cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, cudaStream_t st)
+{
+    q8_split_kernel<<<B, kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d), K, hi, lo, tscale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st)
+{
+    const size_t n4 = n / 4;
+    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
+                                                                          splits, n4, reinterpret_cast<float4 *>(y));
+    return cudaGetLastError();
+}
 
 cudaError_t make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize, const void *base, uint64_t cols,
                          uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
@@ -611,9 +627,11 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
     float *tscale = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B));
     const int splits = allow_split ? choose_splits(B, N, K, num_sms()) : 1;
     float *part = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B));
-    q8_split_kernel<<<B, kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d), K, hi, lo, tscale);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_q8_split(a, K, B, hi, lo, tscale, st);
     if (e != cudaSuccess) return e;
+    if (B <= kSmallMaxB)
+        return launch_gemm_small(W, N, K, B, hi, lo, reinterpret_cast<const __half *>(a.s), tscale,
+                                 splits > 1 ? part : y, y, splits, st);
     CUtensorMap th, tl, ts, tw;
     const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16, u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if ((e = make_tmap_2d(&th, f16, 2, hi, (uint64_t)K, (uint64_t)B, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
@@ -650,10 +668,7 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
     q4k_gemm_tc_kernel<<<(unsigned)grid, kThreads, smem, st>>>(th, tl, ts, tw, p);
     if (splits == 1) return cudaGetLastError();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t n4 = (size_t)B * N / 4;
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
-                                                                          splits, n4, reinterpret_cast<float4 *>(y));
-    return cudaGetLastError();
+    return launch_splitk_reduce(part, splits, (size_t)B * N, y, st);
 }
 
 }  // namespace zq

@@ -1,15 +1,15 @@
 // zq_async.cuh -- thin inline-PTX wrappers for the asynchronous machinery of
 // sm_100-class GPUs used by the streaming and tensor-core kernels: mbarriers,
 // bulk (TMA) copies, named barriers, programmatic dependent launch.
-// Every wait is bounded: after kSpinLimit polls it gives up and reports it,
-// so a broken pipeline returns an error instead of hanging the GPU.
+// Every wait is bounded: after kWaitLimitNs (by the global timer) it gives up
+// and reports it, so a broken pipeline returns an error instead of hanging the
+// GPU.
 #pragma once
 
 #include <stdint.h>
 
 namespace zq {
 
-constexpr uint32_t kSpinLimit = 1u << 24;
 
 // device-wide error word: bit 0 = a bounded wait expired
 __device__ __forceinline__ void flag_timeout(unsigned int *status)
@@ -56,12 +56,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Same test, letting the thread sleep until the phase completes or about
+// `ns` nanoseconds pass: a waiting warp then takes no issue slots from the
+// warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every wait gives up after this long (sleeping polls of kSleepNs each).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kSleepNs = 20000;
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and raises the status flag) if it did not complete in time.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    do {
+        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    } while (global_ns() - t0 < kWaitLimitNs);
     flag_timeout(status);
     return false;
 }

@@ -31,14 +31,17 @@ __device__ __forceinline__ void nib4_to_h2(uint32_t w, __half2 scale, __half2 of
 }
 
 // Bounded wait that also gives up at once when another role already failed.
+// It sleeps between polls (woken by the phase's completion), so waiting
+// warps leave the issue slots to the converters and the issuer.
 static __device__ __noinline__ bool wait_ok(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                             unsigned int *status)
 {
     if (*abort_flag) return false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 1023u) == 1023u && *abort_flag) return false;
-    }
+    const uint64_t t0 = global_ns();
+    do {
+        if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+        if (*abort_flag) return false;
+    } while (global_ns() - t0 < kWaitLimitNs);
     flag_timeout(status);
     *abort_flag = 1;
     return false;
@@ -69,5 +72,25 @@ cudaError_t make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize,
 
 // q8 activation codes -> fp16 (exact), n codes, n a multiple of 16.
 cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream_t st);
+
+// ---- shared by the two projection kernels (q4k_gemm_tc.cu) ---------------
+// Workspace: hi [B][K] binary16 | lo [B][K] binary16 | token scales [B] fp32
+// (padded to 256 B) | split-K partial sums [splits][B][N] fp32.
+size_t split_bytes(int K, int B);
+size_t tscale_bytes(int B);
+// x' = q8 * d8 of every token split into exact binary16 hi + lo, with a
+// per-token power-of-two scale that keeps the codes in binary16 range.
+cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, cudaStream_t st);
+// y[i] = sum over splits of part[s][i] (in split order), n a multiple of 4.
+cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st);
+// split-K count for an output of B x N tiled by 128 x 128
+int choose_splits(int B, int N, int K, int sms);
+
+// ---- small-batch projection (q4k_gemm_small.cu), 2 <= B <= kSmallMaxB ----
+constexpr int kSmallMaxB = 16;
+// out = y (splits == 1) or the partial-sum area; y receives the result.
+cudaError_t launch_gemm_small(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
+                              const __half *s8, const float *tscale, float *out, float *y, int splits,
+                              cudaStream_t st);
 
 }  // namespace zq
