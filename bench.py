@@ -375,6 +375,56 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
     return ms, alg, (K, N, paired)
 
 
+def dequant_then_gemm(torch, wl, steps, warmup, stream):
+    """The dequantise-then-GEMM design measured beside the library's own
+    prefill: every projection's Q4_K weights dequantised to binary16 by
+    zq_q4k_dequant_f16, the Q8_1 activations to binary16 q8*d8, then a dense
+    cuBLAS fp16 GEMM (torch.matmul).  A comparison only: the library's path
+    keeps the weights in Q4_K."""
+    zq = wl.zq
+    B = wl.B
+    maxNK = max(N * K for (_, K, N, _) in wl.shapes)
+    wbuf = torch.empty(maxNK, dtype=torch.float16, device="cuda")
+    x16 = {}
+
+    def act(k):
+        a = wl.a[k]
+        return (a.qs.float() * a.d.float().repeat_interleave(32, dim=1)).half()
+
+    def step(r, only=None):
+        for k, K in wl.inputs_K:
+            zq.rmsnorm_q8_1(wl.x[k], wl.g[k], inputs.EPS, out=wl.a[k])
+            x16[k] = act(k)
+        layers_w, _ = wl.W[r]
+        for (pname, K, N, paired) in wl.layer_shapes:
+            if only and pname != only:
+                continue
+            for w in layers_w[0][pname]:
+                if w is None:
+                    continue
+                wd = zq.q4k_dequant_f16(w, N, K, out=wbuf[:N * K].view(N, K))
+                torch.matmul(x16[wl.key_of[pname]], wd.t())
+
+    graphs = [capture(torch, lambda r=r: step(r), stream) for r in range(wl.R)]
+    ms = time_graphs(torch, graphs, steps, warmup, stream)
+    # the gate projection alone: dequantisation, then the GEMM
+    (_, K, N, _) = [sh for sh in wl.shapes if sh[0] == "gate_up"][0]
+    w1 = wl.weights(0, "gate_up")[0]
+    xg = act(wl.key_of["gate_up"])
+    wd = wbuf[:N * K].view(N, K)
+    gd = capture(torch, lambda: [zq.q4k_dequant_f16(wl.weights(i % wl.R, "gate_up")[0], N, K, out=wd)
+                                 for i in range(4)], stream)
+    gm = capture(torch, lambda: [torch.matmul(xg, wd.t()) for _ in range(4)], stream)
+    d_ms = time_graphs(torch, [gd], max(3, steps // 4), 2, stream) / 4
+    m_ms = time_graphs(torch, [gm], max(3, steps // 4), 2, stream) / 4
+    del wbuf
+    return {"design": "dequantise-then-GEMM: zq_q4k_dequant_f16 + cuBLAS fp16 GEMM (torch.matmul), comparison only",
+            "ms_per_step": round(ms, 4), "value": round(wl.algo_ops() / (ms * 1e-3) / 1e12, 2), "unit": "TOPS",
+            "gate_dequant_ms": round(d_ms, 5), "gate_gemm_ms": round(m_ms, 5),
+            "note": "binary16 weights and activations: products are rounded, unlike the library's exact hi/lo "
+                    "products; the dequantised copy is 3.6x the Q4_K bytes"}
+
+
 _ORACLE_CACHE = {}
 
 
@@ -425,6 +475,8 @@ def main():
                     choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compare-dequant", action="store_true",
+                    help="also time the dequantise-then-GEMM design (cuBLAS) on the 512-token layer")
     ap.add_argument("--decode-path", default="fused", choices=["fused", "two-step"],
                     help="B = 1 step: fused RMSNorm+mat-vec launches, or RMSNorm+Q8_1 then per-projection calls")
     args = ap.parse_args()
@@ -537,6 +589,8 @@ def main():
                                 "traffic": recorded_traffic(f"q4k_gemm_tc_{B}x{dK}x{dN}"),
                                 "kernel_ms": round(dms, 5)},
                    "gpu_launches": wl.launches_per_step() * max(3, args.steps // 5), "clocks": clk.summary()}
+            if B == inputs.PREFILL_B and args.compare_dequant:
+                rec["dequant_then_gemm"] = dequant_then_gemm(torch, wl, max(3, args.steps // 5), args.warmup, stream)
             sub.append(rec)
             del wl
             torch.cuda.empty_cache()
@@ -545,6 +599,8 @@ def main():
             out.update({"value": r0["value"], "unit": "TOPS", "ms_per_step": r0["ms_per_step"], "dtype": "u8",
                         "config": {"workload": r0["workload"], "B": r0["B"]}, "roofline": r0["roofline"],
                         "gpu_launches": r0["gpu_launches"], "clocks": r0["clocks"]})
+            if "dequant_then_gemm" in r0:
+                out["dequant_then_gemm"] = r0["dequant_then_gemm"]
             if len(sub) > 1:
                 out["more"] = sub[1:]
         else:

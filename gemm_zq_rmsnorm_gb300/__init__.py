@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_AL
 EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
            "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
-           "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv")
+           "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
+           "zq_q4k_dequant_f16")
 
 
 class ZQError(RuntimeError):
@@ -67,6 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_device_status": ([P, i], i),
         "zq_q4k_gemm_noalloc": ([P, i, i, _Q8, i, P, P], i),
         "zq_q4k_gemv_multi": ([i, P, P, i, _Q8, P, P], i),
+        "zq_q4k_dequant_f16": ([P, i, i, P, P], i),
         "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P], i),
     }
     for name, (args, res) in sig.items():
@@ -175,6 +177,15 @@ def rmsnorm_q4k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, Ws, Ns, y
                                    ctypes.cast(N_arr, ctypes.c_void_p), ctypes.cast(y_arr, ctypes.c_void_p), q8,
                                    _stream(stream)))
     return ys
+
+
+def q4k_dequant_f16(W: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Q4_K N x K -> binary16 [N][K] (see zq_q4k_dequant_f16)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float16, device=W.device)
+    _check(lib.zq_q4k_dequant_f16(_ptr(W), N, K, _ptr(out), _stream(stream)))
+    return out
 
 
 def q4k_gemv(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor | None = None,

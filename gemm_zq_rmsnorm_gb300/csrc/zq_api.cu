@@ -343,6 +343,17 @@ int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     return launched(launch_gemm_noalloc(W, N, K, a, B, y, s), "zq_q4k_gemm_noalloc");
 }
 
+int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream)
+{
+    int st = check_q4k(W, N, K, "zq_q4k_dequant_f16");
+    if (st) return st;
+    if (!out) return fail(ZQ_ERR_ARG, "zq_q4k_dequant_f16: null out");
+    if (!aligned16(out)) return fail(ZQ_ERR_ALIGN, "zq_q4k_dequant_f16: out must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_q4k_dequant_f16(W, N, K, out, (cudaStream_t)stream), "zq_q4k_dequant_f16 launch");
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

@@ -27,6 +27,7 @@ cudaError_t launch_isums_tc(const void *W, int N, int K, zq_q8_1 a, int B,
                             int32_t *isums, void *ws, cudaStream_t st);
 bool gemv_stream_supported(int K);
 size_t noalloc_scratch_bytes();
+cudaError_t launch_q4k_dequant_f16(const void *W, int N, int K, void *out, cudaStream_t st);
 cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 // Decode mat-vec job: up to kGemvMaxMats Q4_K matrices (N[m] x K) that read
 // the same input vector.

@@ -204,6 +204,17 @@ ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
 ZQ_API int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
                                void *stream);
 
+/*
+ * Q4_K weights dequantised to binary16, for a dequantise-then-GEMM prefill
+ * (MIInfer README, "Current phase": 16-bit dequantised weights ahead of a
+ * dense GEMM).  The library's own projections do not use it; it lets that
+ * design be measured beside them.
+ *   W : Q4_K N x K;  out : binary16 [N][K] (device, 16-byte aligned, 2*N*K bytes).
+ * Per weight, in fp32: a = d*sc, b = dmin*m (exact), w = a*q - b (one
+ * rounding), then w rounded to binary16 (nearest even).
+ */
+ZQ_API int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream);
+
 /* Bytes of device workspace zq_q4k_gemm needs for this shape (0 if none). */
 ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
 

@@ -60,6 +60,8 @@ def _load():
         lib.zqo_q4k_unpack.restype = None
         lib.zqo_q4k_dequant.argtypes = [P, i, i, P]
         lib.zqo_q4k_dequant.restype = None
+        lib.zqo_q4k_dequant_f16.argtypes = [P, i, i, P]
+        lib.zqo_q4k_dequant_f16.restype = None
         lib.zqo_q4k_isums.argtypes = [P, i, i, P, i, P]
         lib.zqo_q4k_isums.restype = None
         lib.zqo_q4k_matmul_rows.argtypes = [P, i, i, P, P, P, i, P, i, P, P]
@@ -125,6 +127,16 @@ def q4k_dequant(W: np.ndarray, N: int, K: int) -> np.ndarray:
     assert W.size == N * (K // 256) * 144
     w = np.zeros((N, K), np.float64)
     _load().zqo_q4k_dequant(_p(W), N, K, _p(w))
+    return w
+
+
+def q4k_dequant_f16(W: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Binary16 bit patterns [N][K] of the weights, via fp32 a*q - b (see
+    zqo_q4k_dequant_f16)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    assert W.size == N * (K // 256) * 144
+    w = np.zeros((N, K), np.uint16)
+    _load().zqo_q4k_dequant_f16(_p(W), N, K, _p(w))
     return w
 
 

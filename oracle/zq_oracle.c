@@ -210,6 +210,29 @@ void zqo_q4k_dequant(const uint8_t *W, int N, int K, double *w)
         }
 }
 
+/* Binary16 dequantised weights, the input of a dequantise-then-GEMM prefill
+ * (MIInfer README, "Current phase": Q4_K dequantised to 16-bit weights ahead
+ * of a dense GEMM).  In fp32: a = d*sc and b = dmin*m (both exact), then
+ * w = a*q - b (a*q exact, one rounding), then w rounded to binary16. */
+void zqo_q4k_dequant_f16(const uint8_t *W, int N, int K, uint16_t *w16)
+{
+    int nb = K / 256;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b) {
+            float d, dmin;
+            uint8_t sc[8], m[8], q[256];
+            zqo_q4k_unpack(W + ((size_t)n * nb + b) * 144, &d, &dmin, sc, m, q);
+            for (int j = 0; j < 8; ++j) {
+                float a = d * (float)sc[j];
+                float bm = dmin * (float)m[j];
+                for (int i = 0; i < 32; ++i) {
+                    float w = a * (float)q[32 * j + i] - bm;
+                    w16[(size_t)n * K + 256 * b + 32 * j + i] = zqo_f32_to_f16(w);
+                }
+            }
+        }
+}
+
 /* ------------------------------------------------------------------------
  * Sub-block integer dot sums I[t][n][b*8+j] = sum_i q4 * q8 over the 32
  * weights of sub-block j of super-block b (MIInfer README, "Status": the

@@ -276,3 +276,38 @@ def test_row_subset_matches_full():
     rows = [8, 0, 4]
     ys, Ss = oracle.q4k_matmul(W, N, K, qs, d, s, rows=rows)
     assert np.array_equal(ys, y[:, rows]) and np.array_equal(Ss, S[:, rows])
+
+
+def test_dequant_f16_matches_numpy_float32_steps():
+    """Binary16 weights: numpy's own IEEE float32 steps (a = d*sc, b = dmin*m,
+    a*q - b) and its float16 rounding, from the generator's fields (not the
+    oracle's unpacking)."""
+    N, K = 3, 512
+    f = inputs.q4k_fields(21, N, K)
+    W = inputs.pack_q4k(f)
+    got = oracle.q4k_dequant_f16(W, N, K)
+    d = f.d.view(np.float16).astype(np.float32)      # [N][nb]
+    dm = f.dmin.view(np.float16).astype(np.float32)
+    nb = K // 256
+    want = np.zeros((N, K), np.uint16)
+    for n in range(N):
+        for b in range(nb):
+            for j in range(8):
+                a = np.float32(d[n, b] * np.float32(f.sc[n, b, j]))
+                bm = np.float32(dm[n, b] * np.float32(f.m[n, b, j]))
+                q = f.q[n, b, j].astype(np.float32)
+                w = (a * q - bm).astype(np.float32)
+                want[n, 256 * b + 32 * j:256 * b + 32 * j + 32] = w.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_dequant_f16_within_half_ulp_of_fp64():
+    """|w16 - w| <= half a binary16 ulp of w plus the fp32 rounding, against
+    the fp64 dequantisation, on random and extreme fields."""
+    N, K = 64, 1024
+    W = inputs.q4k_weights(22, N, K)
+    w64 = oracle.q4k_dequant(W, N, K)
+    w16 = oracle.q4k_dequant_f16(W, N, K).view(np.float16).astype(np.float64)
+    a = np.abs(w64)
+    ulp16 = np.where(a < 2.0 ** -14, 2.0 ** -24, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 10))
+    assert np.all(np.abs(w16 - w64) <= 0.5 * ulp16 + a * 2.0 ** -24 + 1e-30)
