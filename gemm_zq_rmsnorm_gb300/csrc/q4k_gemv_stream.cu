@@ -394,13 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
                     const int r = t / nseg;
                     const int sg = t - r * nseg;
                     const uint8_t *rowp = stage + (size_t)r * rowblk * kQ4KBlockBytes;
-                    float c = 0.0f;
+                    // all of the segment's blocks are read unconditionally (a
+                    // block past the row end re-reads the first one and is
+                    // dropped), so their shared-memory loads can all be in
+                    // flight together; the sum keeps the segment order
+                    float part[kSeg];
 #pragma unroll
                     for (int i = 0; i < kSeg; ++i) {
-                        const int lb = sg + i * nseg;   // block within this stage's row
-                        if (lb < rowblk)
-                            c += block_part(rowp + (size_t)lb * kQ4KBlockBytes, pp, bbase + lb, aq, ads);
+                        const int lb0 = sg + i * nseg;   // block within this stage's row
+                        const int lb = lb0 < rowblk ? lb0 : sg;
+                        part[i] = block_part(rowp + (size_t)lb * kQ4KBlockBytes, pp, bbase + lb, aq, ads);
                     }
+                    float c = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kSeg; ++i)
+                        if (sg + i * nseg < rowblk) c += part[i];
                     c += __shfl_xor_sync(gmask, c, 1);
                     c += __shfl_xor_sync(gmask, c, 2);
                     if (pp == 0) cb[t] = c;
