@@ -241,38 +241,43 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
         // RMSNorm + Q8_1 of x in the canonical order (per-block fma chains,
         // 256 slots in increasing block order, pairwise tree), packed into
         // the staging; scratch in the (still unused) contribution area.
-        // Eight lanes share a 32-value block, each holding four consecutive
-        // values, so every load instruction of a warp reads 512 contiguous
-        // bytes; the block's fma chain runs through the eight lanes in order
-        // (shuffles), and amax and the code sum are exact group reductions.
+        // Four lanes share a 32-value block, each holding eight consecutive
+        // values, so every load instruction of a warp reads 1 KB of
+        // consecutive bytes; the block's fma chain runs through the four lanes
+        // in order (shuffles), and amax and the code sum are exact group
+        // reductions.
         const int nblk = p.K >> 5;
         float *part = contrib;                // [nblk]
         float *slot = contrib + kMaxK / 32;   // [256] and r
-        const int grp = tid >> 3, sub = tid & 7;
-        constexpr int kGroupsPerPass = kConsumers / 8;   // 64 blocks per pass
-        constexpr int kUnroll = 9;                       // passes with loads in flight together (K <= 18432: one)
+        const int grp = tid >> 2, sub = tid & 3;
+        constexpr int kGroupsPerPass = kConsumers / 4;   // 128 blocks per pass
+        constexpr int kUnroll = 3;                       // passes with loads in flight together
         for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
-            float4 xv[kUnroll];
+            float4 xv[kUnroll][2];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (base + kGroupsPerPass * u >= nblk) break;   // CTA-uniform
                 const int b = base + kGroupsPerPass * u + grp;
-                xv[u] = b < nblk ? __ldg(reinterpret_cast<const float4 *>(p.x + 32 * b) + sub)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                xv[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (base + kGroupsPerPass * u >= nblk) break;
                 float pr = 0.0f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     if (sub == j) {
-                        pr = __fmaf_rn(xv[u].x, xv[u].x, pr);
-                        pr = __fmaf_rn(xv[u].y, xv[u].y, pr);
-                        pr = __fmaf_rn(xv[u].z, xv[u].z, pr);
-                        pr = __fmaf_rn(xv[u].w, xv[u].w, pr);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            pr = __fmaf_rn(xv[u][h].x, xv[u][h].x, pr);
+                            pr = __fmaf_rn(xv[u][h].y, xv[u][h].y, pr);
+                            pr = __fmaf_rn(xv[u][h].z, xv[u][h].z, pr);
+                            pr = __fmaf_rn(xv[u][h].w, xv[u][h].w, pr);
+                        }
                     }
-                    pr = __shfl_sync(0xffffffffu, pr, (lane & ~7) | j);
+                    pr = __shfl_sync(0xffffffffu, pr, (lane & ~3) | j);
                 }
                 const int b = base + kGroupsPerPass * u + grp;
                 if (sub == 0 && b < nblk) part[b] = pr;
@@ -301,51 +306,61 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
         __half *ads16 = reinterpret_cast<__half *>(ads);
         const bool out = blockIdx.x == 0 && p.q8out.qs != nullptr;
         for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
-            float4 xv[kUnroll], gv[kUnroll];
+            float4 xv[kUnroll][2], gv[kUnroll][2];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (base + kGroupsPerPass * u >= nblk) break;
                 const int b = base + kGroupsPerPass * u + grp;
                 const bool in = b < nblk;
-                xv[u] = in ? __ldg(reinterpret_cast<const float4 *>(p.x + 32 * b) + sub) : make_float4(0.f, 0.f, 0.f, 0.f);
-                gv[u] = in ? __ldg(reinterpret_cast<const float4 *>(p.gamma + 32 * b) + sub)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    xv[u][h] = in ? __ldg(px + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    gv[u][h] = in ? __ldg(pg + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 if (base + kGroupsPerPass * u >= nblk) break;
                 const int b = base + kGroupsPerPass * u + grp;
-                float xh[4];
-                xh[0] = __fmul_rn(__fmul_rn(xv[u].x, r), gv[u].x);
-                xh[1] = __fmul_rn(__fmul_rn(xv[u].y, r), gv[u].y);
-                xh[2] = __fmul_rn(__fmul_rn(xv[u].z, r), gv[u].z);
-                xh[3] = __fmul_rn(__fmul_rn(xv[u].w, r), gv[u].w);
-                float amax = fmaxf(fmaxf(fabsf(xh[0]), fabsf(xh[1])), fmaxf(fabsf(xh[2]), fabsf(xh[3])));
+                float xh[8];
 #pragma unroll
-                for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+                for (int h = 0; h < 2; ++h) {
+                    xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[u][h].x, r), gv[u][h].x);
+                    xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[u][h].y, r), gv[u][h].y);
+                    xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[u][h].z, r), gv[u][h].z);
+                    xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[u][h].w, r), gv[u][h].w);
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(xh[c]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                 const float d = __fdiv_rn(amax, 127.0f);
                 const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-                uint32_t word = 0;
+                uint32_t word[2] = {0u, 0u};
                 int qsum = 0;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     float q = roundf(__fmul_rn(xh[c], id));
                     q = fminf(fmaxf(q, -127.0f), 127.0f);
                     const int qi = (int)q;
                     qsum += qi;
-                    word |= ((uint32_t)(qi & 0xFF)) << (8 * c);
+                    word[c >> 2] |= ((uint32_t)(qi & 0xFF)) << (8 * (c & 3));
                 }
-#pragma unroll
-                for (int m = 1; m < 8; m <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, m);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
                 if (b < nblk) {
-                    *reinterpret_cast<uint32_t *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 4 * sub) = word;
+                    *reinterpret_cast<uint2 *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 8 * sub) =
+                        make_uint2(word[0], word[1]);
                     const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
                     if (sub == 0) {
                         ads16[4 * (b >> 1) + (b & 1)] = dh;
                         ads16[4 * (b >> 1) + 2 + (b & 1)] = sh;
                     }
                     if (out) {
-                        reinterpret_cast<uint32_t *>(p.q8out.qs + 32 * b)[sub] = word;
+                        reinterpret_cast<uint2 *>(p.q8out.qs + 32 * b)[sub] = make_uint2(word[0], word[1]);
                         if (sub == 0) {
                             reinterpret_cast<__half *>(p.q8out.d)[b] = dh;
                             reinterpret_cast<__half *>(p.q8out.s)[b] = sh;
