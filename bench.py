@@ -115,6 +115,7 @@ class LayerWorkload:
         # projection that reads it (zq_rmsnorm_q4k_gemv); otherwise
         # RMSNorm+Q8_1 first, then one call per projection
         self.fused = (B == 1) if fused is None else fused
+        self.prefetch = True
         dev = "cuda"
         self.extra = list(extra or [])
         self.shapes = shapes + self.extra
@@ -198,20 +199,32 @@ class LayerWorkload:
                 out.append((k, K, [m[0] for m in c], [m[1] for m in c], [m[2] for m in c]))
         return out
 
-    def _run_fused(self, r, stream):
-        zq = self.zq
+    def _fused_calls(self, r):
+        calls = []
         for li in range(self.layers):
-            for (k, K, Ws, Ns, ys) in self.fused_groups(r, li):
-                zq.rmsnorm_q4k_gemv(self.x[k][0], self.g[k], inputs.EPS, Ws, Ns, ys, stream=stream)
+            calls += self.fused_groups(r, li)
         layers_w, extra_w = self.W[r]
         for (pname, K, N, paired) in self.extra:
             w1, w2 = extra_w[pname]
-            k = self.key_of[pname]
             y1, y2 = self.y[pname]
             Ws, Ns, ys = [w1], [N], [y1[0]]
             if paired:
                 Ws, Ns, ys = Ws + [w2], Ns + [N], ys + [y2[0]]
-            zq.rmsnorm_q4k_gemv(self.x[k][0], self.g[k], inputs.EPS, Ws, Ns, ys, stream=stream)
+            calls.append((self.key_of[pname], K, Ws, Ns, ys))
+        return calls
+
+    # bytes of the next launch's first matrix that a fused launch pulls into L2
+    PREFETCH_MAX = 32 << 20
+
+    def _run_fused(self, r, stream):
+        zq = self.zq
+        calls = self._fused_calls(r)
+        after = self._fused_calls((r + 1) % self.R)[0]   # the next step starts on the next copy
+        for i, (k, K, Ws, Ns, ys) in enumerate(calls):
+            nxt = calls[i + 1] if i + 1 < len(calls) else after
+            pf = nxt[2][0] if self.prefetch else None
+            zq.rmsnorm_q4k_gemv(self.x[k][0], self.g[k], inputs.EPS, Ws, Ns, ys, stream=stream, l2_prefetch=pf,
+                                l2_prefetch_bytes=min(pf.numel(), self.PREFETCH_MAX) if pf is not None else 0)
 
     # one pass of the path
     def run(self, r=0, stream=None):

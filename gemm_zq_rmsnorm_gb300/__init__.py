@@ -69,7 +69,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_q4k_gemm_noalloc": ([P, i, i, _Q8, i, P, P], i),
         "zq_q4k_gemv_multi": ([i, P, P, i, _Q8, P, P], i),
         "zq_q4k_dequant_f16": ([P, i, i, P, P], i),
-        "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P], i),
+        "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -164,9 +164,11 @@ def q4k_gemv_multi(Ws, Ns, K: int, a: Q8_1, ys=None, stream=None):
 
 
 def rmsnorm_q4k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, Ws, Ns, ys=None,
-                     q8_out: Q8_1 | None = None, stream=None):
+                     q8_out: Q8_1 | None = None, stream=None, l2_prefetch: torch.Tensor | None = None,
+                     l2_prefetch_bytes: int = 0):
     """RMSNorm + Q8_1 of one token x fp32 [K] (or [1][K]) fused with the
-    mat-vecs of up to four matrices (see zq_rmsnorm_q4k_gemv)."""
+    mat-vecs of up to four matrices (see zq_rmsnorm_q4k_gemv); l2_prefetch
+    optionally names the bytes the next launch will read."""
     lib = load()
     K = x.shape[-1]
     if ys is None:
@@ -175,7 +177,8 @@ def rmsnorm_q4k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, Ws, Ns, y
     q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
     _check(lib.zq_rmsnorm_q4k_gemv(_ptr(x), _ptr(gamma), float(eps), K, n, ctypes.cast(W_arr, ctypes.c_void_p),
                                    ctypes.cast(N_arr, ctypes.c_void_p), ctypes.cast(y_arr, ctypes.c_void_p), q8,
-                                   _stream(stream)))
+                                   _ptr(l2_prefetch),
+                                   int(l2_prefetch_bytes if l2_prefetch is not None else 0), _stream(stream)))
     return ys
 
 

@@ -69,6 +69,8 @@ struct StreamParams {
     const float *gamma;
     float eps;
     zq_q8_1 q8out;        // fused input only: codes also written here by CTA 0 (qs may be null)
+    const uint8_t *pf;    // bytes for the next launch to pull into L2 once this one's are requested
+    size_t pf_bytes;
     unsigned int *status;
 };
 
@@ -218,6 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
                     mbar_arrive_expect_tx(&full[slot], bytes);
                     bulk_g2s_hint(ring + (size_t)slot * p.stage_alloc, src, bytes, &full[slot], policy);
                 }
+            }
+            // every weight byte of this CTA is requested: while the consumers
+            // finish, warm L2 with this CTA's share of the bytes the next
+            // launch will stream
+            if (p.pf != nullptr) {
+                const size_t share = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+                const size_t b0 = (size_t)blockIdx.x * share;
+                const size_t b1 = min(b0 + share, p.pf_bytes & ~(size_t)15);
+                for (size_t o = b0; o < b1; o += 65536)
+                    bulk_prefetch_l2(p.pf + o, (uint32_t)min((size_t)65536, b1 - o));
             }
         }
         return;
@@ -524,13 +536,15 @@ cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_
 }
 
 cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
-                                     const zq_q8_1 *q8out, cudaStream_t st)
+                                     const zq_q8_1 *q8out, const void *pf, size_t pf_bytes, cudaStream_t st)
 {
     StreamParams p{};
     p.x = x;
     p.gamma = gamma;
     p.eps = eps;
     if (q8out) p.q8out = *q8out;
+    p.pf = static_cast<const uint8_t *>(pf);
+    p.pf_bytes = pf_bytes;
     return launch_stream(p, job, K, st);
 }
 

@@ -275,7 +275,8 @@ int zq_q4k_gemv_multi(int nmat, const void *const *W, const int *N, int K, zq_q8
 }
 
 int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, int nmat, const void *const *W,
-                        const int *N, float *const *y, const zq_q8_1 *q8_out, void *stream)
+                        const int *N, float *const *y, const zq_q8_1 *q8_out, const void *l2_prefetch,
+                        size_t l2_prefetch_bytes, void *stream)
 {
     if (!x || !gamma) return fail(ZQ_ERR_ARG, "zq_rmsnorm_q4k_gemv: null x or gamma");
     if (!aligned16(x) || !aligned16(gamma))
@@ -287,9 +288,12 @@ int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, in
     if (!gemv_stream_supported(K))
         return fail(ZQ_ERR_SHAPE, "zq_rmsnorm_q4k_gemv: K = %d above the in-kernel normalisation limit 32768", K);
     if (q8_out && (st = check_q8(*q8_out, "zq_rmsnorm_q4k_gemv (q8_out)"))) return st;
+    if (l2_prefetch && !aligned16(l2_prefetch))
+        return fail(ZQ_ERR_ALIGN, "zq_rmsnorm_q4k_gemv: l2_prefetch must be 16-byte aligned");
     int dev;
     if ((st = check_device(&dev))) return st;
-    return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, q8_out, (cudaStream_t)stream),
+    return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, q8_out, l2_prefetch,
+                                             l2_prefetch ? l2_prefetch_bytes : 0, (cudaStream_t)stream),
                     "zq_rmsnorm_q4k_gemv launch");
 }
 

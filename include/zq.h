@@ -149,12 +149,18 @@ ZQ_API int zq_q4k_gemv_multi(int nmat, const void *const *W, const int *N, int K
  * through device memory unless q8_out (optional, may be NULL; planes of one
  * token) asks for it.
  *   x, gamma : fp32 [K], 16-byte aligned;  eps >= 0;
- *   nmat, W, N, y : as zq_q4k_gemv_multi.
+ *   nmat, W, N, y : as zq_q4k_gemv_multi;
+ *   l2_prefetch, l2_prefetch_bytes : optional (NULL / 0): device bytes the
+ *     caller's next launch will read (the next projection's weights); once
+ *     its own weights are requested, the kernel pulls them into L2 so that the
+ *     next launch starts on L2 hits.  16-byte aligned; a hint, never read by
+ *     this call's arithmetic.
  * Shapes: K % 256 == 0, 256 <= K <= 32768 (larger K: ZQ_ERR_SHAPE).
  */
 ZQ_API int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, int nmat,
                                const void *const *W, const int *N, float *const *y,
-                               const zq_q8_1 *q8_out, void *stream);
+                               const zq_q8_1 *q8_out, const void *l2_prefetch,
+                               size_t l2_prefetch_bytes, void *stream);
 
 /*
  * Batched projection of B tokens (MIInfer README, "Current phase":

@@ -142,5 +142,5 @@ def test_rmsnorm_gemv_rejects(lib, x, eps, K, nmat, status):
     y = _arr(ctypes.c_void_p, [A16])
     assert lib.zq_rmsnorm_q4k_gemv(x, A16, eps, K, nmat, ctypes.cast(W, ctypes.c_void_p),
                                    ctypes.cast(N, ctypes.c_void_p), ctypes.cast(y, ctypes.c_void_p), None,
-                                   None) == status
+                                   None, 0, None) == status
     assert lib.zq_last_error()
