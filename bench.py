@@ -388,6 +388,37 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
     return ms, alg, (K, N, paired)
 
 
+def silu_down(torch, wl, steps, warmup, stream):
+    """The FFN down projection fed by SiLU(gate) * up of the layer's gate/up
+    outputs: Q8_1 packing inside the mat-vec launch (zq_silu_q4k_gemv) against
+    a separate packing launch (zq_silu_mul_q8_1) followed by zq_q4k_gemv.
+    Per-launch device times over graphs of back-to-back calls, rotating
+    weight copies."""
+    zq = wl.zq
+    (_, K, N, _) = [sh for sh in wl.shapes if sh[0] == "down"][0]
+    yg, yu = wl.y["gate_up"]
+    g, u = yg[0], yu[0]
+    y = wl.y["down"][0]
+    a = zq.empty_q8_1(1, K)
+    per = 4 * wl.R
+
+    def fused():
+        for i in range(per):
+            zq.silu_q4k_gemv(g, u, [wl.weights(i % wl.R, "down")[0]], [N], [y[0]])
+
+    def two_step():
+        for i in range(per):
+            zq.silu_mul_q8_1(yg, yu, out=a)
+            zq.q4k_gemv(wl.weights(i % wl.R, "down")[0], N, K, a, y[0])
+
+    reps = max(3, steps // 4)
+    tf = time_graphs(torch, [capture(torch, fused, stream)], reps, max(1, warmup // 2), stream) / per
+    tt = time_graphs(torch, [capture(torch, two_step, stream)], reps, max(1, warmup // 2), stream) / per
+    return {"projection": f"down {K}->{N} fed by silu(gate)*up", "fused_us": round(tf * 1e3, 2),
+            "two_step_us": round(tt * 1e3, 2), "fused_gain": round(tt / tf, 3),
+            "fused_gbs": round(N * K * 144 / 256 / (tf * 1e-3) / 1e9, 1)}
+
+
 def dequant_then_gemm(torch, wl, steps, warmup, stream):
     """The dequantise-then-GEMM design measured beside the library's own
     prefill: every projection's Q4_K weights dequantised to binary16 by
@@ -567,6 +598,8 @@ def main():
             "gpu_launches": wl_dec.launches_per_step() * args.steps,
             "clocks": clk.summary(),
         })
+        if any(sh[0] == "down" for sh in wl_dec.shapes) and any(sh[0] == "gate_up" for sh in wl_dec.shapes):
+            out["silu_down"] = silu_down(torch, wl_dec, args.steps, args.warmup, stream)
         if not args.no_e2e:
             out["e2e"] = e2e(torch, wl_dec, args.steps, args.warmup)
         if rank == 0 and not args.no_cpu_baseline:

@@ -27,7 +27,7 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
            "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
            "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
-           "zq_q4k_dequant_f16")
+           "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv")
 
 
 class ZQError(RuntimeError):
@@ -69,6 +69,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_q4k_gemm_noalloc": ([P, i, i, _Q8, i, P, P], i),
         "zq_q4k_gemv_multi": ([i, P, P, i, _Q8, P, P], i),
         "zq_q4k_dequant_f16": ([P, i, i, P, P], i),
+        "zq_silu_mul_q8_1": ([P, P, i, i, _Q8, P], i),
+        "zq_silu_q4k_gemv": ([P, P, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
         "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
     }
     for name, (args, res) in sig.items():
@@ -189,6 +191,33 @@ def q4k_dequant_f16(W: torch.Tensor, N: int, K: int, out: torch.Tensor | None = 
         out = torch.empty((N, K), dtype=torch.float16, device=W.device)
     _check(lib.zq_q4k_dequant_f16(_ptr(W), N, K, _ptr(out), _stream(stream)))
     return out
+
+
+def silu_mul_q8_1(gate: torch.Tensor, up: torch.Tensor, out: Q8_1 | None = None, stream=None) -> Q8_1:
+    """Q8_1 of silu(gate) * up, fp32 [B][K] each (see zq_silu_mul_q8_1)."""
+    lib = load()
+    B, K = gate.shape
+    if out is None:
+        out = empty_q8_1(B, K, gate.device)
+    _check(lib.zq_silu_mul_q8_1(_ptr(gate), _ptr(up), B, K, out._c(), _stream(stream)))
+    return out
+
+
+def silu_q4k_gemv(gate: torch.Tensor, up: torch.Tensor, Ws, Ns, ys=None, q8_out: Q8_1 | None = None,
+                  stream=None, l2_prefetch: torch.Tensor | None = None, l2_prefetch_bytes: int = 0):
+    """Q8_1 of silu(gate) * up for one token (fp32 [K] each) fused with the
+    mat-vecs of up to four matrices (see zq_silu_q4k_gemv)."""
+    lib = load()
+    K = gate.shape[-1]
+    if ys is None:
+        ys = [torch.empty(int(n), dtype=torch.float32, device=gate.device) for n in Ns]
+    n, W_arr, N_arr, y_arr = _job_arrays(Ws, Ns, ys)
+    q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
+    _check(lib.zq_silu_q4k_gemv(_ptr(gate), _ptr(up), K, n, ctypes.cast(W_arr, ctypes.c_void_p),
+                                ctypes.cast(N_arr, ctypes.c_void_p), ctypes.cast(y_arr, ctypes.c_void_p), q8,
+                                _ptr(l2_prefetch), int(l2_prefetch_bytes if l2_prefetch is not None else 0),
+                                _stream(stream)))
+    return ys
 
 
 def q4k_gemv(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor | None = None,

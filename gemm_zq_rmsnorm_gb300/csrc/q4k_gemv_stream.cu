@@ -68,6 +68,7 @@ struct StreamParams {
     const float *x;
     const float *gamma;
     float eps;
+    int silu;             // x, gamma are gate and up: the input is silu(gate) * up, no normalisation
     zq_q8_1 q8out;        // fused input only: codes also written here by CTA 0 (qs may be null)
     const uint8_t *pf;    // bytes for the next launch to pull into L2 once this one's are requested
     size_t pf_bytes;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
         const int grp = tid >> 2, sub = tid & 3;
         constexpr int kGroupsPerPass = kConsumers / 4;   // 128 blocks per pass
         constexpr int kUnroll = 3;                       // passes with loads in flight together
-        for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
+        for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
             float4 xv[kUnroll][2];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
@@ -295,26 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
                 if (sub == 0 && b < nblk) part[b] = pr;
             }
         }
-        named_bar(1, kConsumers);
-        if (tid < 256) {
-            float v = 0.0f;
-            for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
-            slot[tid] = v;
-        }
-        named_bar(1, kConsumers);
-#pragma unroll
-        for (int off = 128; off >= 32; off >>= 1) {
-            if (tid < off) slot[tid] = __fadd_rn(slot[tid], slot[tid + off]);
+        float r = 1.0f;
+        if (!p.silu) {
             named_bar(1, kConsumers);
-        }
-        if (tid < 32) {
-            float v = slot[tid];
+            if (tid < 256) {
+                float v = 0.0f;
+                for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
+                slot[tid] = v;
+            }
+            named_bar(1, kConsumers);
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
-            if (tid == 0) slot[256] = rms_scale(v, p.K, p.eps);
+            for (int off = 128; off >= 32; off >>= 1) {
+                if (tid < off) slot[tid] = __fadd_rn(slot[tid], slot[tid + off]);
+                named_bar(1, kConsumers);
+            }
+            if (tid < 32) {
+                float v = slot[tid];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+                if (tid == 0) slot[256] = rms_scale(v, p.K, p.eps);
+            }
+            named_bar(1, kConsumers);
+            r = slot[256];
         }
-        named_bar(1, kConsumers);
-        const float r = slot[256];
         __half *ads16 = reinterpret_cast<__half *>(ads);
         const bool out = blockIdx.x == 0 && p.q8out.qs != nullptr;
         for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
@@ -339,10 +343,17 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_stream_kernel(const Stre
                 float xh[8];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[u][h].x, r), gv[u][h].x);
-                    xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[u][h].y, r), gv[u][h].y);
-                    xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[u][h].z, r), gv[u][h].z);
-                    xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[u][h].w, r), gv[u][h].w);
+                    if (p.silu) {
+                        xh[4 * h + 0] = silu_mul(xv[u][h].x, gv[u][h].x);
+                        xh[4 * h + 1] = silu_mul(xv[u][h].y, gv[u][h].y);
+                        xh[4 * h + 2] = silu_mul(xv[u][h].z, gv[u][h].z);
+                        xh[4 * h + 3] = silu_mul(xv[u][h].w, gv[u][h].w);
+                    } else {
+                        xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[u][h].x, r), gv[u][h].x);
+                        xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[u][h].y, r), gv[u][h].y);
+                        xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[u][h].z, r), gv[u][h].z);
+                        xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[u][h].w, r), gv[u][h].w);
+                    }
                 }
                 float amax = 0.0f;
 #pragma unroll
@@ -536,12 +547,14 @@ cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_
 }
 
 cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
-                                     const zq_q8_1 *q8out, const void *pf, size_t pf_bytes, cudaStream_t st)
+                                     bool silu, const zq_q8_1 *q8out, const void *pf, size_t pf_bytes,
+                                     cudaStream_t st)
 {
     StreamParams p{};
     p.x = x;
     p.gamma = gamma;
     p.eps = eps;
+    p.silu = silu ? 1 : 0;
     if (q8out) p.q8out = *q8out;
     p.pf = static_cast<const uint8_t *>(pf);
     p.pf_bytes = pf_bytes;

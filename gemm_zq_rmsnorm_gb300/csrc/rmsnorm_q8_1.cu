@@ -190,7 +190,41 @@ rmsnorm_q8_1_wide_kernel(const float *__restrict__ x, const float *__restrict__ 
     }
 }
 
+// h = silu(g) * u packed to Q8_1: one thread per 32-value block
+__global__ void __launch_bounds__(256)
+silu_mul_q8_1_kernel(const float *__restrict__ g, const float *__restrict__ u, int K, int8_t *__restrict__ qs,
+                     __half *__restrict__ dq, __half *__restrict__ sq)
+{
+    pdl_wait();   // g and u may come from the previous kernel; the codes may still be read by it
+    pdl_launch_dependents();
+    const int nblk = K >> 5;
+    const int b = blockIdx.y * blockDim.x + threadIdx.x;
+    if (b >= nblk) return;
+    const size_t off = (size_t)blockIdx.x * K + 32 * (size_t)b;
+    const float4 *pg = reinterpret_cast<const float4 *>(g + off);
+    const float4 *pu = reinterpret_cast<const float4 *>(u + off);
+    float h[32];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const float4 a = __ldg(pg + v), c = __ldg(pu + v);
+        h[4 * v + 0] = silu_mul(a.x, c.x);
+        h[4 * v + 1] = silu_mul(a.y, c.y);
+        h[4 * v + 2] = silu_mul(a.z, c.z);
+        h[4 * v + 3] = silu_mul(a.w, c.w);
+    }
+    const size_t o = (size_t)blockIdx.x * nblk + b;
+    pack_block(h, qs + off, dq + o, sq + o);
+}
+
 }  // namespace
+
+cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, zq_q8_1 out, cudaStream_t st)
+{
+    const int nblk = K / 32;
+    const dim3 grid((unsigned)B, (unsigned)((nblk + 255) / 256));
+    return launch_pdl(silu_mul_q8_1_kernel, grid, dim3(256), 0, st, g, u, K, out.qs,
+                      reinterpret_cast<__half *>(out.d), reinterpret_cast<__half *>(out.s));
+}
 
 cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float eps, zq_q8_1 out,
                                 cudaStream_t st)

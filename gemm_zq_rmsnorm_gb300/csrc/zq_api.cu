@@ -292,7 +292,7 @@ int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, in
         return fail(ZQ_ERR_ALIGN, "zq_rmsnorm_q4k_gemv: l2_prefetch must be 16-byte aligned");
     int dev;
     if ((st = check_device(&dev))) return st;
-    return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, q8_out, l2_prefetch,
+    return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, false, q8_out, l2_prefetch,
                                              l2_prefetch ? l2_prefetch_bytes : 0, (cudaStream_t)stream),
                     "zq_rmsnorm_q4k_gemv launch");
 }
@@ -345,6 +345,43 @@ int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     cudaStream_t s = (cudaStream_t)stream;
     if (B == 1) return launched(launch_gemv_dispatch(W, nullptr, N, K, a, y, nullptr, s), "zq_q4k_gemm_noalloc (B=1)");
     return launched(launch_gemm_noalloc(W, N, K, a, B, y, s), "zq_q4k_gemm_noalloc");
+}
+
+int zq_silu_mul_q8_1(const float *gate, const float *up, int B, int K, zq_q8_1 out, void *stream)
+{
+    if (!gate || !up) return fail(ZQ_ERR_ARG, "zq_silu_mul_q8_1: null gate or up");
+    if (!aligned16(gate) || !aligned16(up))
+        return fail(ZQ_ERR_ALIGN, "zq_silu_mul_q8_1: gate and up must be 16-byte aligned");
+    if (B < 1 || B > 65535) return fail(ZQ_ERR_SHAPE, "zq_silu_mul_q8_1: B = %d out of range", B);
+    if (K < 32 || K % 32 != 0 || K > (1 << 22))
+        return fail(ZQ_ERR_SHAPE, "zq_silu_mul_q8_1: K = %d must be a multiple of 32 in [32, 2^22]", K);
+    int st = check_q8(out, "zq_silu_mul_q8_1");
+    if (st) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_silu_mul_q8_1(gate, up, B, K, out, (cudaStream_t)stream), "zq_silu_mul_q8_1 launch");
+}
+
+int zq_silu_q4k_gemv(const float *gate, const float *up, int K, int nmat, const void *const *W, const int *N,
+                     float *const *y, const zq_q8_1 *q8_out, const void *l2_prefetch, size_t l2_prefetch_bytes,
+                     void *stream)
+{
+    if (!gate || !up) return fail(ZQ_ERR_ARG, "zq_silu_q4k_gemv: null gate or up");
+    if (!aligned16(gate) || !aligned16(up))
+        return fail(ZQ_ERR_ALIGN, "zq_silu_q4k_gemv: gate and up must be 16-byte aligned");
+    GemvJob job;
+    int st = check_job("zq_silu_q4k_gemv", nmat, W, N, K, y, job);
+    if (st) return st;
+    if (!gemv_stream_supported(K))
+        return fail(ZQ_ERR_SHAPE, "zq_silu_q4k_gemv: K = %d above the in-kernel packing limit 32768", K);
+    if (q8_out && (st = check_q8(*q8_out, "zq_silu_q4k_gemv (q8_out)"))) return st;
+    if (l2_prefetch && !aligned16(l2_prefetch))
+        return fail(ZQ_ERR_ALIGN, "zq_silu_q4k_gemv: l2_prefetch must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_gemv_stream_fused(job, K, gate, up, 0.0f, true, q8_out, l2_prefetch,
+                                             l2_prefetch ? l2_prefetch_bytes : 0, (cudaStream_t)stream),
+                    "zq_silu_q4k_gemv launch");
 }
 
 int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream)

@@ -40,11 +40,13 @@ struct GemvJob {
 };
 // input: Q8_1 codes of one token
 cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_t st);
-// input: x and gamma; RMSNorm + Q8_1 computed in the kernel (q8out, when
-// non-null, receives the codes); pf/pf_bytes: optional range pulled into L2
-// for the next launch
+// input: x and gamma, RMSNorm + Q8_1 computed in the kernel; or (silu) gate
+// and up, Q8_1 of silu(gate) * up.  q8out, when non-null, receives the codes;
+// pf/pf_bytes: optional range pulled into L2 for the next launch.
 cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
-                                     const zq_q8_1 *q8out, const void *pf, size_t pf_bytes, cudaStream_t st);
+                                     bool silu, const zq_q8_1 *q8out, const void *pf, size_t pf_bytes,
+                                     cudaStream_t st);
+cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, zq_q8_1 out, cudaStream_t st);
 
 // Launch with programmatic dependent launch: the kernel may start while the
 // previous kernel on the stream is still running.  Every kernel launched this

@@ -89,4 +89,34 @@ __device__ __forceinline__ void block_normalise(const float *xb, const float *gb
     }
 }
 
+// SiLU(gate) * up in the library's fp32 steps (every implementation that
+// follows them gets the same value, hence the same Q8_1 codes; MIInfer
+// README, "Current phase": SiLU(gate)*up feeding the down projection):
+//   exp32(a): a clamped to [-86, 88]; k = rint(a * log2 e);
+//     r = fma(-k, ln2_hi, a); r = fma(-k, ln2_lo, r)  (ln 2 split in two, the
+//     high part exact in 16 bits); p = Horner sum of r^n/n!, n <= 7, with fma;
+//     result p * 2^k (exact);
+//   silu(g) = g / (1 + exp32(-g));  h = silu(g) * u.
+__device__ __forceinline__ float exp32(float a)
+{
+    a = fminf(fmaxf(a, -86.0f), 88.0f);
+    const float kf = rintf(__fmul_rn(a, 0x1.715476p+0f));
+    float r = __fmaf_rn(-kf, 0x1.62e4p-1f, a);
+    r = __fmaf_rn(-kf, 0x1.7f7d1cp-20f, r);
+    float p = 0x1.a01a02p-13f;
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)kf + 127) << 23));
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp32(-g))), u);
+}
+
 }  // namespace zq

@@ -211,6 +211,33 @@ ZQ_API int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, fl
                                void *stream);
 
 /*
+ * SiLU(gate) * up packed to Q8_1: the input of the FFN down projection
+ * (MIInfer README, "Current phase": a fused SiLU(gate)*up epilogue feeding the
+ * down projection).  h = silu(gate) * up with silu(g) = g / (1 + exp(-g)); the
+ * pages fix no precision, so every step is one IEEE fp32 operation of this
+ * library's definition -- exp(a) for a clamped to [-86, 88] as rint-based
+ * range reduction with ln 2 in two parts, a degree-7 Taylor polynomial of
+ * e^r in fma Horner form with coefficients 1/n! rounded to fp32, and an exact
+ * power-of-two scaling -- and h is packed exactly as zq_rmsnorm_q8_1 packs xh.
+ *   gate, up : fp32 [B][K] (16-byte aligned);  out : Q8_1 planes of B x K.
+ * Shapes: B >= 1, K % 32 == 0.
+ */
+ZQ_API int zq_silu_mul_q8_1(const float *gate, const float *up, int B, int K, zq_q8_1 out,
+                            void *stream);
+
+/*
+ * Fused down-projection step: the Q8_1 of silu(gate) * up (as
+ * zq_silu_mul_q8_1 with B = 1, byte for byte) computed inside the mat-vec
+ * kernel, then y[m] = W[m] h for up to four matrices, in one launch.
+ *   gate, up : fp32 [K];  nmat, W, N, y, q8_out, l2_prefetch : as
+ *   zq_rmsnorm_q4k_gemv.  Shapes: K % 256 == 0, 256 <= K <= 32768.
+ */
+ZQ_API int zq_silu_q4k_gemv(const float *gate, const float *up, int K, int nmat,
+                            const void *const *W, const int *N, float *const *y,
+                            const zq_q8_1 *q8_out, const void *l2_prefetch,
+                            size_t l2_prefetch_bytes, void *stream);
+
+/*
  * Q4_K weights dequantised to binary16, for a dequantise-then-GEMM prefill
  * (MIInfer README, "Current phase": 16-bit dequantised weights ahead of a
  * dense GEMM).  The library's own projections do not use it; it lets that

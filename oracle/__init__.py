@@ -62,6 +62,12 @@ def _load():
         lib.zqo_q4k_dequant.restype = None
         lib.zqo_q4k_dequant_f16.argtypes = [P, i, i, P]
         lib.zqo_q4k_dequant_f16.restype = None
+        lib.zqo_exp32.argtypes = [f]
+        lib.zqo_exp32.restype = f
+        lib.zqo_silu32.argtypes = [f]
+        lib.zqo_silu32.restype = f
+        lib.zqo_silu_mul_q8_1.argtypes = [P, P, i, i, P, P, P]
+        lib.zqo_silu_mul_q8_1.restype = None
         lib.zqo_q4k_isums.argtypes = [P, i, i, P, i, P]
         lib.zqo_q4k_isums.restype = None
         lib.zqo_q4k_matmul_rows.argtypes = [P, i, i, P, P, P, i, P, i, P, P]
@@ -106,6 +112,31 @@ def rmsnorm_q8_1(x: np.ndarray, gamma: np.ndarray, eps: float):
     d = np.zeros((B, K // 32), np.uint16)
     s = np.zeros((B, K // 32), np.uint16)
     _load().zqo_rmsnorm_q8_1(_p(x), _p(g), B, K, eps, _p(qs), _p(d), _p(s))
+    return qs, d, s
+
+
+def exp32(a) -> np.ndarray:
+    """The library's fp32 exponential (range reduction + degree-7 polynomial)."""
+    lib = _load()
+    return np.array([lib.zqo_exp32(float(v)) for v in np.asarray(a, np.float32).ravel()], np.float32)
+
+
+def silu32(g) -> np.ndarray:
+    """silu(g) = g / (1 + exp32(-g)), fp32 steps."""
+    lib = _load()
+    return np.array([lib.zqo_silu32(float(v)) for v in np.asarray(g, np.float32).ravel()], np.float32)
+
+
+def silu_mul_q8_1(g: np.ndarray, u: np.ndarray):
+    """Q8_1 of silu(g) * u (fp32 [B][K] each) -> (qs, d bits, s bits)."""
+    g = np.ascontiguousarray(np.atleast_2d(g), dtype=np.float32)
+    u = np.ascontiguousarray(np.atleast_2d(u), dtype=np.float32)
+    B, K = g.shape
+    assert u.shape == g.shape and K % 32 == 0
+    qs = np.zeros((B, K), np.int8)
+    d = np.zeros((B, K // 32), np.uint16)
+    s = np.zeros((B, K // 32), np.uint16)
+    _load().zqo_silu_mul_q8_1(_p(g), _p(u), B, K, _p(qs), _p(d), _p(s))
     return qs, d, s
 
 

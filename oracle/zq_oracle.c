@@ -167,6 +167,86 @@ void zqo_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float ep
 }
 
 /* ------------------------------------------------------------------------
+ * SiLU(gate) * up packed to Q8_1: the input of the FFN down projection
+ * (MIInfer README, "Current phase": a fused SiLU(gate)*up epilogue ahead of
+ * the down projection).  The pages fix no precision.  This library defines
+ * every step as one IEEE fp32 operation, so that any implementation that
+ * follows the steps produces the same codes:
+ *   e = exp32(-g);  silu = g / (1 + e);  h = silu * up;  Q8_1 of h as above.
+ * exp32(a): a clamped to [-86, 88];  k = rint(a * LOG2E);
+ *   r = fma(-k, LN2_HI, a);  r = fma(-k, LN2_LO, r)   (Cody-Waite split of
+ *   ln 2: LN2_HI holds its leading 16 bits, so k * LN2_HI is exact);
+ *   p = sum_{n<=7} r^n / n! in Horner form with fma, coefficients rounded to
+ *   fp32 (|r| <= 0.347: the truncation is below 2^-27 relative);
+ *   result = p * 2^k, an exact scaling for k in [-124, 127].
+ * ---------------------------------------------------------------------- */
+static float zqo_pow2i(int k) /* 2^k for -126 <= k <= 127, exactly */
+{
+    uint32_t bits = (uint32_t)(k + 127) << 23;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+float zqo_exp32(float a)
+{
+    /* fp32 roundings of log2(e), of ln 2 split in two, and of 1/n! */
+    const float LOG2E = 0x1.715476p+0f;
+    const float LN2_HI = 0x1.62e4p-1f;
+    const float LN2_LO = 0x1.7f7d1cp-20f;
+    a = fminf(fmaxf(a, -86.0f), 88.0f);
+    float kf = rintf(a * LOG2E);
+    float r = fmaf(-kf, LN2_HI, a);
+    r = fmaf(-kf, LN2_LO, r);
+    float p = 0x1.a01a02p-13f;        /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);  /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);   /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);   /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);   /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    return p * zqo_pow2i((int)kf);
+}
+
+float zqo_silu32(float g)
+{
+    float e = zqo_exp32(-g);
+    return g / (1.0f + e);
+}
+
+/* h[t][k] = silu(g[t][k]) * u[t][k], packed to Q8_1 like zqo_rmsnorm_q8_1. */
+void zqo_silu_mul_q8_1(const float *g, const float *u, int B, int K, int8_t *qs, uint16_t *d16,
+                       uint16_t *s16)
+{
+    for (int t = 0; t < B; ++t) {
+        for (int b = 0; b < K / 32; ++b) {
+            float h[32];
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                size_t k = (size_t)t * K + 32 * b + i;
+                float v = zqo_silu32(g[k]) * u[k];
+                h[i] = v;
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            float d = amax / 127.0f;
+            float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+            int sum = 0;
+            for (int i = 0; i < 32; ++i) {
+                float q = roundf(h[i] * id); /* half away from zero */
+                if (q > 127.0f) q = 127.0f;
+                if (q < -127.0f) q = -127.0f;
+                qs[(size_t)t * K + 32 * b + i] = (int8_t)q;
+                sum += (int)q;
+            }
+            float s = d * (float)sum;
+            d16[(size_t)t * (K / 32) + b] = zqo_f32_to_f16(d);
+            s16[(size_t)t * (K / 32) + b] = zqo_f32_to_f16(s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------
  * Q4_K super-block decode (MIInfer README, "Status": Q4_K metadata staging
  * decodes the packed 6-bit scales/mins; the layout is the one stated at the
  * top of this file).

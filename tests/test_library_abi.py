@@ -144,3 +144,10 @@ def test_rmsnorm_gemv_rejects(lib, x, eps, K, nmat, status):
                                    ctypes.cast(N, ctypes.c_void_p), ctypes.cast(y, ctypes.c_void_p), None,
                                    None, 0, None) == status
     assert lib.zq_last_error()
+
+
+@pytest.mark.parametrize("g,u,B,K,status", [
+    (None, A16, 1, 64, -1), (A8, A16, 1, 64, -3), (A16, A16, 0, 64, -2), (A16, A16, 1, 48, -2)])
+def test_silu_mul_rejects(lib, g, u, B, K, status):
+    assert lib.zq_silu_mul_q8_1(g, u, B, K, q8(), None) == status
+    assert lib.zq_last_error()

@@ -311,3 +311,45 @@ def test_dequant_f16_within_half_ulp_of_fp64():
     a = np.abs(w64)
     ulp16 = np.where(a < 2.0 ** -14, 2.0 ** -24, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 10))
     assert np.all(np.abs(w16 - w64) <= 0.5 * ulp16 + a * 2.0 ** -24 + 1e-30)
+
+
+# ---------------------------------------------------------------- SiLU * up
+def test_exp32_within_two_ulp_of_fp64():
+    """exp32 against numpy's fp64 exponential on a dense grid of the clamped
+    range, and exactly 1 at 0."""
+    a = np.concatenate([np.linspace(-86, 88, 200001), np.linspace(-1, 1, 20001)]).astype(np.float32)
+    e = oracle.exp32(a).astype(np.float64)
+    ref = np.exp(a.astype(np.float64))
+    assert np.all(np.abs(e - ref) <= 2.0 ** -22 * ref)
+    assert oracle.exp32([0.0])[0] == 1.0
+
+
+def test_silu32_identities():
+    """silu(0) = 0; silu(g) - silu(-g) = g (the two logistic factors sum to
+    one); silu(g) -> g for large g and -> 0 for very negative g; within a
+    few ulp of the fp64 formula."""
+    g = np.linspace(-20, 20, 40001).astype(np.float32)
+    s = oracle.silu32(g).astype(np.float64)
+    sn = oracle.silu32(-g).astype(np.float64)
+    gd = g.astype(np.float64)
+    assert oracle.silu32([0.0])[0] == 0.0
+    assert np.all(np.abs((s - sn) - gd) <= 1e-6 * np.maximum(np.abs(gd), 1e-30) + 1e-7)
+    ref = gd / (1.0 + np.exp(-gd))
+    assert np.all(np.abs(s - ref) <= 2.0 ** -21 * np.abs(ref) + 1e-30)
+    big = oracle.silu32([30.0, 80.0, -80.0])
+    assert big[0] == np.float32(30.0) and big[1] == np.float32(80.0) and abs(big[2]) < 1e-30
+
+
+def test_silu_mul_q8_1_zero_up_and_single_spike():
+    """up = 0 gives all-zero codes and scales; a single non-zero product in a
+    block packs to code 127 with d = |h| / 127."""
+    K = 64
+    g = np.linspace(-3, 3, K, dtype=np.float32)[None]
+    qs, d, s = oracle.silu_mul_q8_1(g, np.zeros((1, K), np.float32))
+    assert not qs.any() and not d.any() and not s.any()
+    u = np.zeros((1, K), np.float32)
+    u[0, 40] = 2.0
+    qs, d, s = oracle.silu_mul_q8_1(g, u)
+    h = oracle.silu32([g[0, 40]])[0] * np.float32(2.0)
+    assert qs[0, 40] == (127 if h > 0 else -127) and np.count_nonzero(qs) == 1
+    assert d[0, 1] == oracle.f32_to_f16_bits([np.float32(abs(h)) / np.float32(127.0)])[0]
