@@ -519,6 +519,8 @@ def main():
                     choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-l2-prefetch", action="store_true",
+                    help="fused decode launches do not pull the next launch's weights into L2")
     ap.add_argument("--compare-dequant", action="store_true",
                     help="also time the dequantise-then-GEMM design (cuBLAS) on the 512-token layer")
     ap.add_argument("--decode-path", default="fused", choices=["fused", "two-step"],
@@ -570,6 +572,7 @@ def main():
 
     out = dict(result)
     if wl_dec is not None:
+        wl_dec.prefetch = not args.no_l2_prefetch
         barrier()
         with Clocks(local_rank) as clk:
             ms, _ = bench_workload(torch, wl_dec, args.steps, args.warmup, stream)
@@ -584,6 +587,7 @@ def main():
                        "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl_dec.shapes],
                        "layers": wl_dec.layers, "weight_copies_rotated": wl_dec.R,
                        "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
+                                       + ("; each launch pulls the next one's weights into L2" if wl_dec.prefetch else "")
                                        if wl_dec.fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
                        "l2": f"inputs larger than L2: {wl_dec.R} rotating weight copies of the step",
                        "algorithmic_bytes_per_step": int(wl_dec.algo_bytes())},
