@@ -161,6 +161,118 @@ def q4k_weights(seed: int, N: int, K: int, *, tag_offset: int = 0) -> np.ndarray
 
 
 # --------------------------------------------------------------------------
+# Q5_K and Q6_K weights (the other k-quant blocks of Q4_K_M checkpoints)
+# --------------------------------------------------------------------------
+TAG_QH, TAG_Q6, TAG_Q6SC, TAG_Q6D = 15, 16, 17, 18
+
+
+@dataclasses.dataclass
+class Q5KFields:
+    """Unpacked fields of an N x K Q5_K matrix: as Q4_K, with 5-bit quants."""
+    d: np.ndarray      # uint16 binary16 bits [N, nb]
+    dmin: np.ndarray   # uint16 binary16 bits [N, nb]
+    sc: np.ndarray     # uint8 [N, nb, 8], 0..63
+    m: np.ndarray      # uint8 [N, nb, 8], 0..63
+    q: np.ndarray      # uint8 [N, nb, 8, 32], 0..31
+
+
+def q5k_fields(seed: int, N: int, K: int, *, tag_offset: int = 0) -> Q5KFields:
+    """Scales, mins and d/dmin drawn as for Q4_K; quants U{0..31} (the low
+    four bits from the Q4_K nibble stream, the fifth from a stream of its own)."""
+    f4 = q4k_fields(seed, N, K, tag_offset=tag_offset)
+    nblk = N * (K // 256)
+    raw = bits(seed, TAG_QH + tag_offset, nblk * 4)            # 64 high bits per uint64
+    shifts = np.arange(64, dtype=np.uint64)
+    hb = ((raw[:, None] >> shifts[None, :]) & np.uint64(1)).astype(np.uint8)
+    q = f4.q | (hb.reshape(f4.q.shape) << 4)
+    return Q5KFields(d=f4.d, dmin=f4.dmin, sc=f4.sc, m=f4.m, q=q)
+
+
+def pack_q5k(f: Q5KFields) -> np.ndarray:
+    """Encode fields into the 176-byte block layout; returns uint8 [N, nb*176].
+
+    bytes 0..15 as Q4_K (d, dmin, the twelve scale/min bytes);
+    bytes 16..47 qh: bit j of byte 16+i = bit 4 of q[j][i];
+    bytes 48..175: byte 48 + 32*p + i = (q[2p][i] & 15) | (q[2p+1][i] & 15) << 4.
+    """
+    N, nb = f.d.shape
+    assert f.q.max() < 32
+    low = pack_q4k(Q4KFields(d=f.d, dmin=f.dmin, sc=f.sc, m=f.m, q=f.q & 15)).reshape(N, nb, 144)
+    out = np.zeros((N, nb, 176), np.uint8)
+    out[:, :, 0:16] = low[:, :, 0:16]
+    hb = (f.q >> 4).astype(np.uint16)                           # [N, nb, 8, 32]
+    qh = np.zeros((N, nb, 32), np.uint16)
+    for j in range(8):
+        qh |= hb[:, :, j, :] << j
+    out[:, :, 16:48] = qh.astype(np.uint8)
+    out[:, :, 48:176] = low[:, :, 16:144]
+    return out.reshape(N, nb * 176)
+
+
+def q5k_weights(seed: int, N: int, K: int, *, tag_offset: int = 0) -> np.ndarray:
+    return pack_q5k(q5k_fields(seed, N, K, tag_offset=tag_offset))
+
+
+@dataclasses.dataclass
+class Q6KFields:
+    """Unpacked fields of an N x K Q6_K matrix (16 sub-blocks of 16 weights)."""
+    d: np.ndarray      # uint16 binary16 bits [N, nb]
+    sc: np.ndarray     # int8 [N, nb, 16], -128..127
+    q: np.ndarray      # uint8 [N, nb, 16, 16], 0..63 (weight value d*sc*(q-32))
+
+
+def q6k_fields(seed: int, N: int, K: int, *, tag_offset: int = 0) -> Q6KFields:
+    """Quants U{0..63}, scales U{-128..127} (the full int8 range), d =
+    binary16(U(1e-5, 1e-4)) so that |d*sc*(q-32)| stays below 0.41 like the
+    Q4_K weights."""
+    assert K % 256 == 0 and K > 0 and N > 0
+    nb = K // 256
+    nblk = N * nb
+    raw = bits(seed, TAG_Q6 + tag_offset, nblk * 32)            # 8 six-bit quants per uint64
+    shifts = np.arange(8, dtype=np.uint64) * np.uint64(6)
+    q = ((raw[:, None] >> shifts[None, :]) & np.uint64(63)).astype(np.uint8).reshape(N, nb, 16, 16)
+    sc = (uniform_int(seed, TAG_Q6SC + tag_offset, nblk * 16, 0, 255) - 128).astype(np.int8).reshape(N, nb, 16)
+    dv = 1e-5 + 9e-5 * uniform01(seed, TAG_Q6D + tag_offset, nblk)
+    d = dv.astype(np.float16).view(np.uint16).reshape(N, nb)
+    return Q6KFields(d=d, sc=sc, q=q)
+
+
+def pack_q6k(f: Q6KFields) -> np.ndarray:
+    """Encode fields into the 210-byte block layout; returns uint8 [N, nb*210].
+
+    Weight k (0..255) of a block has half h = k // 128, and within the half
+    quarter c = (k % 128) // 32 and position i = k % 32:
+      low four bits of q in byte 64*h + 32*(c % 2) + i (bytes 0..127), low
+        nibble for c < 2, high nibble for c >= 2;
+      top two bits of q in bits 2c, 2c+1 of byte 128 + 32*h + i (bytes 128..191);
+    bytes 192..207: the 16 int8 scales, sc[s] for weights 16s..16s+15;
+    bytes 208..209: d (little-endian binary16).
+    """
+    N, nb = f.d.shape
+    assert f.q.max() < 64
+    q = f.q.reshape(N, nb, 2, 4, 32).astype(np.uint16)          # [.., h, c, i]
+    out = np.zeros((N, nb, 210), np.uint8)
+    lo = q & 15
+    ql = np.zeros((N, nb, 2, 2, 32), np.uint16)                 # [.., h, c % 2, i]
+    ql[:, :, :, 0, :] = lo[:, :, :, 0, :] | (lo[:, :, :, 2, :] << 4)
+    ql[:, :, :, 1, :] = lo[:, :, :, 1, :] | (lo[:, :, :, 3, :] << 4)
+    out[:, :, 0:128] = ql.reshape(N, nb, 128).astype(np.uint8)
+    hi = q >> 4
+    qh = np.zeros((N, nb, 2, 32), np.uint16)
+    for c in range(4):
+        qh |= hi[:, :, :, c, :] << (2 * c)
+    out[:, :, 128:192] = qh.reshape(N, nb, 64).astype(np.uint8)
+    out[:, :, 192:208] = f.sc.view(np.uint8)
+    out[:, :, 208] = (f.d & 0xFF).astype(np.uint8)
+    out[:, :, 209] = (f.d >> 8).astype(np.uint8)
+    return out.reshape(N, nb * 210)
+
+
+def q6k_weights(seed: int, N: int, K: int, *, tag_offset: int = 0) -> np.ndarray:
+    return pack_q6k(q6k_fields(seed, N, K, tag_offset=tag_offset))
+
+
+# --------------------------------------------------------------------------
 # named workloads (shapes of the pages' models; every input synthetic)
 # --------------------------------------------------------------------------
 EPS = 1e-6

@@ -72,6 +72,18 @@ def _load():
         lib.zqo_q4k_isums.restype = None
         lib.zqo_q4k_matmul_rows.argtypes = [P, i, i, P, P, P, i, P, i, P, P]
         lib.zqo_q4k_matmul_rows.restype = None
+        lib.zqo_q5k_unpack.argtypes = [P, P, P, P, P, P]
+        lib.zqo_q5k_unpack.restype = None
+        lib.zqo_q6k_unpack.argtypes = [P, P, P, P]
+        lib.zqo_q6k_unpack.restype = None
+        lib.zqo_q5k_dequant.argtypes = [P, i, i, P]
+        lib.zqo_q5k_dequant.restype = None
+        lib.zqo_q6k_dequant.argtypes = [P, i, i, P]
+        lib.zqo_q6k_dequant.restype = None
+        lib.zqo_q5k_matmul_rows.argtypes = [P, i, i, P, P, P, i, P, i, P, P]
+        lib.zqo_q5k_matmul_rows.restype = None
+        lib.zqo_q6k_matmul_rows.argtypes = [P, i, i, P, P, i, P, i, P, P]
+        lib.zqo_q6k_matmul_rows.restype = None
         _lib = lib
     return _lib
 
@@ -203,4 +215,70 @@ def q4k_matmul(W, N, K, qs, d, s, rows=None, want_scale=True):
         _p(W), N, K, _p(qs), _p(d), _p(s), B,
         _p(rows_arr) if rows_arr is not None else None, R, _p(y),
         _p(S) if S is not None else None)
+    return (y, S) if want_scale else y
+
+
+# ---------------------------------------------------------------- Q5_K, Q6_K
+BLOCK_BYTES = {"q4k": 144, "q5k": 176, "q6k": 210}
+
+
+def q5k_unpack(block: np.ndarray):
+    """One 176-byte Q5_K super-block -> (d, dmin, sc[8], m[8], q[256] 0..31)."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8)
+    assert blk.size == 176
+    d = ctypes.c_float()
+    dmin = ctypes.c_float()
+    sc = np.zeros(8, np.uint8)
+    m = np.zeros(8, np.uint8)
+    q = np.zeros(256, np.uint8)
+    _load().zqo_q5k_unpack(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(m), _p(q))
+    return np.float32(d.value), np.float32(dmin.value), sc, m, q
+
+
+def q6k_unpack(block: np.ndarray):
+    """One 210-byte Q6_K super-block -> (d, sc[16] int8, q[256] 0..63)."""
+    blk = np.ascontiguousarray(block, dtype=np.uint8)
+    assert blk.size == 210
+    d = ctypes.c_float()
+    sc = np.zeros(16, np.int8)
+    q = np.zeros(256, np.uint8)
+    _load().zqo_q6k_unpack(_p(blk), ctypes.byref(d), _p(sc), _p(q))
+    return np.float32(d.value), sc, q
+
+
+def kq_dequant(fmt: str, W: np.ndarray, N: int, K: int) -> np.ndarray:
+    """fp64 weights [N][K] of a Q5_K ("q5k") or Q6_K ("q6k") matrix."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    assert W.size == N * (K // 256) * BLOCK_BYTES[fmt]
+    w = np.zeros((N, K), np.float64)
+    fn = {"q5k": _load().zqo_q5k_dequant, "q6k": _load().zqo_q6k_dequant}[fmt]
+    fn(_p(W), N, K, _p(w))
+    return w
+
+
+def kq_matmul(fmt, W, N, K, qs, d, s, rows=None, want_scale=True):
+    """q4k_matmul for a matrix of format fmt ("q4k", "q5k" or "q6k")."""
+    if fmt == "q4k":
+        return q4k_matmul(W, N, K, qs, d, s, rows=rows, want_scale=want_scale)
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    assert W.size == N * (K // 256) * BLOCK_BYTES[fmt]
+    qs = np.ascontiguousarray(np.atleast_2d(qs), dtype=np.int8)
+    d = np.ascontiguousarray(np.atleast_2d(d), dtype=np.uint16)
+    s = np.ascontiguousarray(np.atleast_2d(s), dtype=np.uint16)
+    B = qs.shape[0]
+    assert qs.shape[1] == K and d.shape == (B, K // 32) and s.shape == (B, K // 32)
+    if rows is None:
+        R, rows_arr = N, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32)
+        R = rows_arr.size
+        assert rows_arr.min() >= 0 and rows_arr.max() < N
+    y = np.zeros((B, R), np.float32)
+    S = np.zeros((B, R), np.float64) if want_scale else None
+    rp = _p(rows_arr) if rows_arr is not None else None
+    Sp = _p(S) if S is not None else None
+    if fmt == "q5k":
+        _load().zqo_q5k_matmul_rows(_p(W), N, K, _p(qs), _p(d), _p(s), B, rp, R, _p(y), Sp)
+    else:
+        _load().zqo_q6k_matmul_rows(_p(W), N, K, _p(qs), _p(d), B, rp, R, _p(y), Sp)
     return (y, S) if want_scale else y

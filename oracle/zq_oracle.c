@@ -387,4 +387,160 @@ void zqo_q4k_matmul(const uint8_t *W, int N, int K, const int8_t *qs,
     zqo_q4k_matmul_rows(W, N, K, qs, d16, s16, B, NULL, N, y, S);
 }
 
+/* ------------------------------------------------------------------------
+ * Q5_K and Q6_K: the other k-quant blocks of a Q4_K_M checkpoint (MIInfer
+ * README, "Status": Q5_K x Q8_1 MMVQ-style recurrent output projection,
+ * Q5_K scale/min hoisting and paired nibbles; MMVQ-style Q6_K x Q8_1 LM
+ * head; ZINC docs "ROCm backend": packed Q8 activations feed the hot Q4_K,
+ * Q5_K and Q6_K projections).  As for Q4_K, the pages name the formats but
+ * print no byte layout; the layouts below are the readings used throughout:
+ *
+ *   Q5_K super-block (256 weights, 176 bytes):
+ *     bytes 0..15   d, dmin and the twelve scale/min bytes, exactly as Q4_K;
+ *     bytes 16..47  qh: bit j of byte 16+i is bit 4 of weight i of
+ *                   sub-block j;
+ *     bytes 48..175 the low four bits of the quants, placed as the Q4_K
+ *                   nibbles (byte 48 + 32*(j/2) + i, low nibble for even j).
+ *     w = d*sc[j]*q - dmin*m[j], q in 0..31.
+ *
+ *   Q6_K super-block (256 weights, 210 bytes; sixteen sub-blocks of 16):
+ *     weight k: h = k/128, c = (k%128)/32, i = k%32;
+ *     bytes 0..127   low four bits of q in byte 64h + 32(c%2) + i, low
+ *                    nibble for c < 2, high nibble for c >= 2;
+ *     bytes 128..191 top two bits of q in bits 2c, 2c+1 of byte 128 + 32h + i;
+ *     bytes 192..207 sixteen int8 scales, sc[s] for weights 16s..16s+15;
+ *     bytes 208..209 d (binary16).
+ *     w = d*sc[k/16]*(q - 32), q in 0..63.
+ *
+ *   Output, per token t and row n, with exact integer sub-block sums:
+ *     Q5_K: as Q4_K, y = sum_b sum_j d*sc_j*d8*I_j - dmin*m_j*s8,
+ *           I_j = sum over the 32 weights of q5*q8;
+ *     Q6_K: y = sum_b sum_s d*sc_s*d8_{t,k/32}*I_s,
+ *           I_s = sum over the 16 weights of (q6 - 32)*q8;
+ *   the float part accumulated in fp64.  S[t][r] = sum_k |w*xq| as for Q4_K.
+ * ---------------------------------------------------------------------- */
+void zqo_q5k_unpack(const uint8_t *blk, float *d, float *dmin,
+                    uint8_t sc[8], uint8_t m[8], uint8_t q[256])
+{
+    /* bytes 0..15 and the low bits share the Q4_K reading; rebuild a Q4_K
+     * block from them and add the fifth bit */
+    uint8_t q4[144];
+    memcpy(q4, blk, 16);
+    memcpy(q4 + 16, blk + 48, 128);
+    zqo_q4k_unpack(q4, d, dmin, sc, m, q);
+    const uint8_t *QH = blk + 16;
+    for (int j = 0; j < 8; ++j)
+        for (int i = 0; i < 32; ++i)
+            q[32 * j + i] = (uint8_t)(q[32 * j + i] | (((QH[i] >> j) & 1) << 4));
+}
+
+void zqo_q6k_unpack(const uint8_t *blk, float *d, int8_t sc[16], uint8_t q[256])
+{
+    for (int k = 0; k < 256; ++k) {
+        int h = k / 128, c = (k % 128) / 32, i = k % 32;
+        uint8_t lb = blk[64 * h + 32 * (c % 2) + i];
+        uint8_t low = (c < 2) ? (lb & 15) : (lb >> 4);
+        uint8_t top = (blk[128 + 32 * h + i] >> (2 * c)) & 3;
+        q[k] = (uint8_t)(low | (top << 4));
+    }
+    for (int s = 0; s < 16; ++s) sc[s] = (int8_t)blk[192 + s];
+    *d = zqo_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8)));
+}
+
+void zqo_q5k_dequant(const uint8_t *W, int N, int K, double *w)
+{
+    int nb = K / 256;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b) {
+            float d, dmin;
+            uint8_t sc[8], m[8], q[256];
+            zqo_q5k_unpack(W + ((size_t)n * nb + b) * 176, &d, &dmin, sc, m, q);
+            for (int k = 0; k < 256; ++k)
+                w[(size_t)n * K + 256 * b + k] = (double)d * sc[k / 32] * q[k] - (double)dmin * m[k / 32];
+        }
+}
+
+void zqo_q6k_dequant(const uint8_t *W, int N, int K, double *w)
+{
+    int nb = K / 256;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b) {
+            float d;
+            int8_t sc[16];
+            uint8_t q[256];
+            zqo_q6k_unpack(W + ((size_t)n * nb + b) * 210, &d, sc, q);
+            for (int k = 0; k < 256; ++k)
+                w[(size_t)n * K + 256 * b + k] = (double)d * sc[k / 16] * ((int)q[k] - 32);
+        }
+}
+
+/* Projection of a Q5_K matrix, rows and outputs as zqo_q4k_matmul_rows. */
+void zqo_q5k_matmul_rows(const uint8_t *W, int N, int K, const int8_t *qs,
+                         const uint16_t *d16, const uint16_t *s16, int B,
+                         const int32_t *rows, int R, float *y, double *S)
+{
+    int nb = K / 256;
+    for (int t = 0; t < B; ++t)
+        for (int r = 0; r < R; ++r) {
+            int n = rows ? rows[r] : r;
+            double acc = 0.0, abs_acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                float d, dmin;
+                uint8_t sc[8], m[8], q[256];
+                zqo_q5k_unpack(W + ((size_t)n * nb + b) * 176, &d, &dmin, sc, m, q);
+                for (int j = 0; j < 8; ++j) {
+                    const int8_t *a = qs + (size_t)t * K + 256 * b + 32 * j;
+                    double d8 = zqo_f16_to_f32(d16[(size_t)t * (K / 32) + 8 * b + j]);
+                    double s8 = zqo_f16_to_f32(s16[(size_t)t * (K / 32) + 8 * b + j]);
+                    int64_t isum = 0;
+                    for (int i = 0; i < 32; ++i) isum += (int64_t)q[32 * j + i] * a[i];
+                    acc += (double)d * sc[j] * d8 * (double)isum - (double)dmin * m[j] * s8;
+                    if (S) {
+                        for (int i = 0; i < 32; ++i) {
+                            double w = (double)d * sc[j] * q[32 * j + i] - (double)dmin * m[j];
+                            abs_acc += fabs(w * (d8 * a[i]));
+                        }
+                    }
+                }
+            }
+            y[(size_t)t * R + r] = (float)acc;
+            if (S) S[(size_t)t * R + r] = abs_acc;
+        }
+}
+
+/* Projection of a Q6_K matrix; s16 is not used (the Q6_K offset is inside
+ * the integer sums). */
+void zqo_q6k_matmul_rows(const uint8_t *W, int N, int K, const int8_t *qs,
+                         const uint16_t *d16, int B,
+                         const int32_t *rows, int R, float *y, double *S)
+{
+    int nb = K / 256;
+    for (int t = 0; t < B; ++t)
+        for (int r = 0; r < R; ++r) {
+            int n = rows ? rows[r] : r;
+            double acc = 0.0, abs_acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                float d;
+                int8_t sc[16];
+                uint8_t q[256];
+                zqo_q6k_unpack(W + ((size_t)n * nb + b) * 210, &d, sc, q);
+                for (int sb = 0; sb < 16; ++sb) {
+                    const int8_t *a = qs + (size_t)t * K + 256 * b + 16 * sb;
+                    double d8 = zqo_f16_to_f32(d16[(size_t)t * (K / 32) + 8 * b + sb / 2]);
+                    int64_t isum = 0;
+                    for (int i = 0; i < 16; ++i) isum += (int64_t)((int)q[16 * sb + i] - 32) * a[i];
+                    acc += (double)d * sc[sb] * d8 * (double)isum;
+                    if (S) {
+                        for (int i = 0; i < 16; ++i) {
+                            double w = (double)d * sc[sb] * ((int)q[16 * sb + i] - 32);
+                            abs_acc += fabs(w * (d8 * a[i]));
+                        }
+                    }
+                }
+            }
+            y[(size_t)t * R + r] = (float)acc;
+            if (S) S[(size_t)t * R + r] = abs_acc;
+        }
+}
+
 int zqo_version(void) { return 1; }
