@@ -27,7 +27,9 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_gemm_workspace_bytes", "zq_q4k_bytes", "zq_q8_1_bytes",
            "zq_status_string", "zq_last_error", "zq_version", "zq_debug_q4k_isums",
            "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
-           "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv")
+           "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
+           "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
+           "zq_q5k_bytes", "zq_q6k_bytes")
 
 
 class ZQError(RuntimeError):
@@ -72,6 +74,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_silu_mul_q8_1": ([P, P, i, i, _Q8, P], i),
         "zq_silu_q4k_gemv": ([P, P, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
         "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
+        "zq_q5k_gemm": ([P, i, i, _Q8, i, P, P], i),
+        "zq_q6k_gemm": ([P, i, i, _Q8, i, P, P], i),
+        "zq_q5k_gemv": ([P, i, i, _Q8, P, P], i),
+        "zq_q6k_gemv": ([P, i, i, _Q8, P, P], i),
+        "zq_rmsnorm_q6k_gemv": ([P, P, f, i, P, i, P, ctypes.POINTER(_Q8), P], i),
+        "zq_q5k_bytes": ([i, i], sz),
+        "zq_q6k_bytes": ([i, i], sz),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -268,6 +277,42 @@ def q4k_gemm_noalloc(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = N
     if y is None:
         y = torch.empty((B, N), dtype=torch.float32, device=a.qs.device)
     _check(lib.zq_q4k_gemm_noalloc(_ptr(W), N, K, a._c(), B, _ptr(y), _stream(stream)))
+    return y
+
+
+def kq_bytes(fmt: str, N: int, K: int) -> int:
+    """Storage bytes of an N x K matrix of format "q4k", "q5k" or "q6k"."""
+    fn = {"q4k": load().zq_q4k_bytes, "q5k": load().zq_q5k_bytes, "q6k": load().zq_q6k_bytes}[fmt]
+    return int(fn(N, K))
+
+
+def kq_gemm(fmt: str, W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
+            y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [B][N] for a Q5_K ("q5k") or Q6_K ("q6k") matrix and 1 <= B <= 16
+    tokens (see zq_q5k_gemm / zq_q6k_gemm; B = 1 goes through *_gemv)."""
+    lib = load()
+    B = a.B if B is None else B
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=a.qs.device)
+    if B == 1:
+        fn = {"q5k": lib.zq_q5k_gemv, "q6k": lib.zq_q6k_gemv}[fmt]
+        _check(fn(_ptr(W), N, K, a._c(), _ptr(y), _stream(stream)))
+    else:
+        fn = {"q5k": lib.zq_q5k_gemm, "q6k": lib.zq_q6k_gemm}[fmt]
+        _check(fn(_ptr(W), N, K, a._c(), B, _ptr(y), _stream(stream)))
+    return y
+
+
+def rmsnorm_q6k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, W: torch.Tensor, N: int,
+                     y: torch.Tensor | None = None, q8_out: Q8_1 | None = None, stream=None) -> torch.Tensor:
+    """RMSNorm + Q8_1 of one token x fp32 [K] fused with a Q6_K mat-vec (the LM
+    head after the final norm; see zq_rmsnorm_q6k_gemv)."""
+    lib = load()
+    K = x.shape[-1]
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
+    _check(lib.zq_rmsnorm_q6k_gemv(_ptr(x), _ptr(gamma), float(eps), K, _ptr(W), N, _ptr(y), q8, _stream(stream)))
     return y
 
 

@@ -1,0 +1,810 @@
+// kq_gemv_stream.cuh -- decode mat-vec of k-quant weights (Q4_K, Q5_K, Q6_K)
+// against Q8_1 activations, with the weights streamed through shared memory
+// by bulk (TMA) copies.  Instantiated per weight format (and token count) in
+// q4k_gemv_stream.cu and kq_gemv_q56k.cu.
+//
+// MIInfer README, "Status": Q4_K x Q8_1 MMVQ-style projections (FFN down,
+// shared gate/up; Q4_K metadata staging; packed int8 dot4; activations reused
+// from on-chip memory), the Q5_K x Q8_1 MMVQ-style recurrent output
+// projection (scale/min hoisting, paired nibbles) and the MMVQ-style Q6_K x
+// Q8_1 LM head.  ZINC docs "ROCm backend", "Build and verify": paired Q4
+// projections; packed Q8 activations for the hot Q4_K, Q5_K and Q6_K
+// projections.
+//
+// The mat-vec is bound by HBM bandwidth: every weight byte is read exactly
+// once.  To keep enough bytes in flight independently of register pressure,
+// one persistent CTA per SM runs a producer warp that issues 1-D bulk copies
+// of contiguous weight tiles (R whole rows, or a piece of one long row; rows
+// are contiguous, so a tile is one copy) into a ring of large shared-memory
+// stages, completing on mbarriers.  Sixteen consumer warps decode the
+// super-blocks from shared memory in groups of four lanes -- lane p takes the
+// 64 weights of Q8_1 blocks 2p and 2p+1 of the super-block -- and form the
+// integer sub-block sums with dp4a against the Q8_1 activation rows staged
+// once per CTA.  A group walks a strided segment of one row (up to four
+// blocks), applies the scales in fp32 and accumulates in registers; after the
+// stage the segments of each row are summed in a fixed order into y.  Up to
+// four matrices that read the same input (q/k/v, gate/up) share one launch.
+//
+// Q6_K blocks are 210 bytes, so rows and blocks are only 2-byte aligned.  The
+// producer copies each tile from the 16-byte boundary below it (the bytes of
+// the last tile past the last 16-byte boundary of the matrix, if any, with
+// plain loads), and the consumers read the blocks with aligned 32-bit loads
+// and byte permutes.
+//
+// With x and gamma instead of Q8_1 codes (one token) the consumers first
+// compute RMSNorm and the Q8_1 packing of x themselves, in the canonical order
+// of the RMSNorm+Q8_1 kernel (same bytes), straight into the shared-memory
+// staging, while the producer already streams weights: the normalised input
+// never goes through HBM and the separate launch disappears.
+//
+// With NT > 1 the CTA stages NT tokens and every decoded weight is used for
+// all of them (Q5_K and Q6_K small-batch projections).
+#pragma once
+
+#include <type_traits>
+
+#include "zq_async.cuh"
+#include "zq_internal.cuh"
+#include "zq_q8_1_pack.cuh"
+
+namespace zq {
+namespace stream {
+
+enum : int { kFmtQ4K = 4, kFmtQ5K = 5, kFmtQ6K = 6 };
+template <int FMT> struct Fmt;
+template <> struct Fmt<kFmtQ4K> { static constexpr int kBytes = 144; };
+template <> struct Fmt<kFmtQ5K> { static constexpr int kBytes = 176; };
+template <> struct Fmt<kFmtQ6K> { static constexpr int kBytes = 210; };
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 3;
+constexpr int kStageMax = 64 * 1024;
+constexpr int kMaxBlk = kStageMax / 144;               // 455: blocks (>= tasks) per stage, any format
+constexpr int kGroups = 8 * kConsumerWarps;            // four-lane task groups per CTA
+constexpr int kSeg = 4;                                // max blocks per task
+constexpr int kSmemLimit = 227 * 1024 - 1024;        // dynamic bytes: the static part pads to 1 KB
+constexpr int kMaxK = 32768;                           // one row of segments per warp in the reduction
+constexpr int kMaxMats = kGemvMaxMats;
+
+struct StreamParams {
+    const uint8_t *W[kMaxMats];
+    float *y[kMaxMats];
+    int N[kMaxMats];
+    int gstart[kMaxMats + 1];   // first row group of each matrix; gstart[nmat] = total
+    int nmat;
+    int K, nb;
+    int ntok;             // tokens of this launch (<= NT); token t's y row is y[m] + t * N[m]
+    uint32_t rowbytes;
+    int R;                // rows per group
+    int P;                // pieces per group (> 1 only when R == 1)
+    int CB;               // blocks per piece
+    int total_groups;
+    uint32_t stage_alloc; // bytes reserved per stage (multiple of 128)
+    // input: Q8_1 planes, or (x, gamma, eps) normalised in the kernel
+    const int8_t *qs;
+    const __half *d;
+    const __half *s;
+    const float *x;
+    const float *gamma;
+    float eps;
+    int silu;             // x, gamma are gate and up: the input is silu(gate) * up, no normalisation
+    zq_q8_1 q8out;        // fused input only: codes also written here by CTA 0 (qs may be null)
+    const uint8_t *pf;    // bytes for the next launch to pull into L2 once this one's are requested
+    size_t pf_bytes;
+    unsigned int *status;
+};
+
+// matrix of row group g
+__device__ __forceinline__ int group_mat(const StreamParams &p, int g)
+{
+    int m = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxMats; ++i) m += (i < p.nmat && g >= p.gstart[i]) ? 1 : 0;
+    return m;
+}
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Activation codes are stored with 16 bytes of padding after every 64: the
+// 64-byte group g (Q8_1 block pair) starts at 80*g.  The eight lanes of a
+// quarter-warp (two consecutive super-blocks x four pairs) then start in
+// eight different 16-byte bank groups.
+__host__ __device__ constexpr size_t act_bytes(int K) { return (size_t)K / 64 * 80; }
+// d8 pair and s8 pair (binary16) per Q8_1 block pair
+__host__ __device__ constexpr size_t ads_bytes(int K) { return (size_t)K / 64 * 8; }
+
+static_assert(kStages * kMaxBlk >= kMaxK / 32 + 257, "RMSNorm scratch fits in the contribution area");
+
+struct SmemLayout {
+    size_t ring, act_qs, act_ds, contrib, bars, total;
+    __host__ __device__ SmemLayout(int K, uint32_t stage_alloc, int nt)
+    {
+        ring = 0;
+        act_qs = ring + (size_t)kStages * stage_alloc;
+        act_ds = align_up(act_qs + (size_t)nt * act_bytes(K), 16);
+        contrib = align_up(act_ds + (size_t)nt * ads_bytes(K), 16);
+        bars = align_up(contrib + (size_t)nt * kStages * kMaxBlk * 4, 8);
+        total = bars + 2 * kStages * 8;
+    }
+};
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Scales and mins of sub-blocks 2p and 2p+1 of a Q4_K / Q5_K header, packed
+// as bytes 0 and 1 of the returned words (branch-free; p = 0..3).
+__device__ __forceinline__ void pair_scales(const uint4 &hdr, int p, uint32_t &sc, uint32_t &mn)
+{
+    const uint32_t j = (uint32_t)(2 * p) & 3u;            // byte index within a 4-byte word
+    const uint32_t sel = j | ((j + 1) << 4);                // bytes j, j+1 -> bytes 0, 1
+    const uint32_t s0 = __byte_perm(hdr.y, 0, sel);         // S[j], S[j+1]
+    const uint32_t s1 = __byte_perm(hdr.z, 0, sel);         // S[4+j], S[5+j]
+    const uint32_t s2 = __byte_perm(hdr.w, 0, sel);         // S[8+j], S[9+j]
+    const uint32_t lo_sc = s0 & 0x3F3Fu, lo_mn = s1 & 0x3F3Fu;
+    const uint32_t hi_sc = (s2 & 0x0F0Fu) | ((s0 >> 2) & 0x3030u);
+    const uint32_t hi_mn = ((s2 >> 4) & 0x0F0Fu) | ((s1 >> 2) & 0x3030u);
+    sc = p < 2 ? lo_sc : hi_sc;
+    mn = p < 2 ? lo_mn : hi_mn;
+}
+
+// Q4_K: contribution of this lane's pair of sub-blocks (2p, 2p+1; all 64
+// weights) of one super-block b of a row to y.
+__device__ __forceinline__ float q4k_block_part(const uint8_t *blk, int p, int b, const uint8_t *aq,
+                                                const uint2 *ads)
+{
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * p);
+    const uint8_t *ap = aq + 80 * (4 * b + p);
+    const uint4 a00 = *reinterpret_cast<const uint4 *>(ap);
+    const uint4 a01 = *reinterpret_cast<const uint4 *>(ap + 16);
+    const uint4 a10 = *reinterpret_cast<const uint4 *>(ap + 32);
+    const uint4 a11 = *reinterpret_cast<const uint4 *>(ap + 48);
+    constexpr uint32_t LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+    int I0 = 0, I1 = 0;
+    I0 = dp4a_us(q0.x & LO, a00.x, I0);
+    I1 = dp4a_us(q0.x & HI, a10.x, I1);  // high nibbles in place: 16x the true products
+    I0 = dp4a_us(q0.y & LO, a00.y, I0);
+    I1 = dp4a_us(q0.y & HI, a10.y, I1);
+    I0 = dp4a_us(q0.z & LO, a00.z, I0);
+    I1 = dp4a_us(q0.z & HI, a10.z, I1);
+    I0 = dp4a_us(q0.w & LO, a00.w, I0);
+    I1 = dp4a_us(q0.w & HI, a10.w, I1);
+    I0 = dp4a_us(q1.x & LO, a01.x, I0);
+    I1 = dp4a_us(q1.x & HI, a11.x, I1);
+    I0 = dp4a_us(q1.y & LO, a01.y, I0);
+    I1 = dp4a_us(q1.y & HI, a11.y, I1);
+    I0 = dp4a_us(q1.z & LO, a01.z, I0);
+    I1 = dp4a_us(q1.z & HI, a11.z, I1);
+    I0 = dp4a_us(q1.w & LO, a01.w, I0);
+    I1 = dp4a_us(q1.w & HI, a11.w, I1);
+    uint32_t sc, mn;
+    pair_scales(hdr, p, sc, mn);
+    // exact integer scaling: |sc*I| <= 63*60960 < 2^22; I1 carries the factor 16
+    const int J0 = (int)(sc & 0xFFu) * I0;
+    const int J1 = (int)(sc >> 8) * (I1 >> 4);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));  // d, dmin
+    const uint2 ds = ads[4 * b + p];
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.y));
+    const float main = fmaf(d8.y, (float)J1, d8.x * (float)J0);
+    const float mins = fmaf((float)(mn >> 8), s8.y, (float)(mn & 0xFFu) * s8.x);
+    return fmaf(dd.x, main, -dd.y * mins);
+}
+
+// ---- Q5_K: lane p decodes the 5-bit quants of sub-blocks 2p and 2p+1 ----
+struct Q5Lane {
+    uint32_t q0[8], q1[8];   // quants 0..31, four per word, sub-blocks 2p and 2p+1
+    uint32_t sc, mn;         // scales / mins of the two sub-blocks (bytes 0, 1)
+    float d, dmin;
+};
+
+__device__ __forceinline__ void q5k_decode(const uint8_t *blk, int p, Q5Lane &w)
+{
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + 16);
+    const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + 32);
+    const uint4 l0 = *reinterpret_cast<const uint4 *>(blk + 48 + 32 * p);
+    const uint4 l1 = *reinterpret_cast<const uint4 *>(blk + 64 + 32 * p);
+    const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    // bit 2p (2p+1) of every qh byte becomes bit 4 of the quant
+    const int s0 = 2 * p, s1 = 2 * p + 1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t b0 = s0 <= 4 ? qh[k] << (4 - s0) : qh[k] >> (s0 - 4);
+        const uint32_t b1 = s1 <= 4 ? qh[k] << (4 - s1) : qh[k] >> (s1 - 4);
+        w.q0[k] = (ql[k] & 0x0F0F0F0Fu) | (b0 & 0x10101010u);
+        w.q1[k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (b1 & 0x10101010u);
+    }
+    pair_scales(hdr, p, w.sc, w.mn);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+    w.d = dd.x;
+    w.dmin = dd.y;
+}
+
+// a[0..1]: the 32 codes of Q8_1 block 2p, a[2..3]: block 2p+1; ds = d8 pair,
+// s8 pair (binary16).
+__device__ __forceinline__ float q5k_dot(const Q5Lane &w, const uint4 (&a)[4], uint2 ds)
+{
+    int I0 = 0, I1 = 0;
+    I0 = dp4a_us(w.q0[0], a[0].x, I0);
+    I0 = dp4a_us(w.q0[1], a[0].y, I0);
+    I0 = dp4a_us(w.q0[2], a[0].z, I0);
+    I0 = dp4a_us(w.q0[3], a[0].w, I0);
+    I0 = dp4a_us(w.q0[4], a[1].x, I0);
+    I0 = dp4a_us(w.q0[5], a[1].y, I0);
+    I0 = dp4a_us(w.q0[6], a[1].z, I0);
+    I0 = dp4a_us(w.q0[7], a[1].w, I0);
+    I1 = dp4a_us(w.q1[0], a[2].x, I1);
+    I1 = dp4a_us(w.q1[1], a[2].y, I1);
+    I1 = dp4a_us(w.q1[2], a[2].z, I1);
+    I1 = dp4a_us(w.q1[3], a[2].w, I1);
+    I1 = dp4a_us(w.q1[4], a[3].x, I1);
+    I1 = dp4a_us(w.q1[5], a[3].y, I1);
+    I1 = dp4a_us(w.q1[6], a[3].z, I1);
+    I1 = dp4a_us(w.q1[7], a[3].w, I1);
+    // exact: |sc*I| <= 63*31*127*32 < 2^23
+    const int J0 = (int)(w.sc & 0xFFu) * I0;
+    const int J1 = (int)(w.sc >> 8) * I1;
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.y));
+    const float main = fmaf(d8.y, (float)J1, d8.x * (float)J0);
+    const float mins = fmaf((float)(w.mn >> 8), s8.y, (float)(w.mn & 0xFFu) * s8.x);
+    return fmaf(w.d, main, -w.dmin * mins);
+}
+
+// ---- Q6_K: lane p decodes weights 64p..64p+63 (four 16-weight sub-blocks) ----
+struct Q6Lane {
+    uint32_t q[16];   // q - 32 as signed bytes, four per word; words 4u..4u+3 = sub-block 4p+u
+    uint32_t sc4;     // the four int8 scales of sub-blocks 4p..4p+3
+    float d;
+};
+
+// 32-bit word at byte offset o of a 2-byte-aligned block: aligned loads and a
+// byte permute (sel = 0x3210 when the block is 4-byte aligned, else 0x5432).
+__device__ __forceinline__ uint32_t ld_w32(const uint8_t *base4, int o, uint32_t sel)
+{
+    const uint32_t lo = *reinterpret_cast<const uint32_t *>(base4 + o);
+    const uint32_t hi = *reinterpret_cast<const uint32_t *>(base4 + o + 4);
+    return __byte_perm(lo, hi, sel);
+}
+
+__device__ __forceinline__ void q6k_decode(const uint8_t *blk, int p, Q6Lane &w)
+{
+    const int h = p >> 1, odd = p & 1;
+    const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(blk) & 2u;
+    const uint8_t *base4 = blk - mis;
+    const uint32_t sel = mis ? 0x5432u : 0x3210u;
+    // low bits: bytes 64h .. 64h+63 (quarter 2*odd in the first 32, quarter
+    // 2*odd+1 in the next 32), low nibble for p even, high nibble for p odd
+    uint32_t raw[17];
+#pragma unroll
+    for (int k = 0; k < 17; ++k) raw[k] = *reinterpret_cast<const uint32_t *>(base4 + 64 * h + 4 * k);
+    uint32_t rh[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) rh[k] = *reinterpret_cast<const uint32_t *>(base4 + 128 + 32 * h + 4 * k);
+    const int nsh = 4 * odd;          // nibble
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t qh = __byte_perm(rh[k], rh[k + 1], sel);
+        const uint32_t la = __byte_perm(raw[k], raw[k + 1], sel);
+        const uint32_t lb = __byte_perm(raw[k + 8], raw[k + 9], sel);
+        // top-bit pairs of quarters 2*odd (bits 4*odd..) and 2*odd+1 (bits
+        // 4*odd+2..) of every qh byte, moved to bits 4..5
+        const uint32_t ta = odd ? qh : qh << 4;
+        const uint32_t tb = odd ? qh >> 2 : qh << 2;
+        const uint32_t qa = ((la >> nsh) & 0x0F0F0F0Fu) | (ta & 0x30303030u);
+        const uint32_t qb = ((lb >> nsh) & 0x0F0F0F0Fu) | (tb & 0x30303030u);
+        // q - 32 as a signed byte: q >= 32 -> q & 31; q < 32 -> (q & 31) | 0xE0
+        w.q[k] = (qa & 0x1F1F1F1Fu) | ((~qa & 0x20202020u) * 7u);
+        w.q[8 + k] = (qb & 0x1F1F1F1Fu) | ((~qb & 0x20202020u) * 7u);
+    }
+    w.sc4 = ld_w32(base4, 192 + 4 * p, sel);
+    w.d = __half2float(*reinterpret_cast<const __half *>(blk + 208));
+}
+
+__device__ __forceinline__ int sext8(uint32_t v, int byte) { return (int)(int8_t)(uint8_t)(v >> (8 * byte)); }
+
+// a[0..1]: codes of Q8_1 block 2p (sub-blocks 4p, 4p+1), a[2..3]: block 2p+1
+// (sub-blocks 4p+2, 4p+3); ds.x = d8 pair (binary16).
+__device__ __forceinline__ float q6k_dot(const Q6Lane &w, const uint4 (&a)[4], uint2 ds)
+{
+    int I[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        int s = 0;
+        s = dp4a_ss(w.q[4 * u + 0], a[u].x, s);
+        s = dp4a_ss(w.q[4 * u + 1], a[u].y, s);
+        s = dp4a_ss(w.q[4 * u + 2], a[u].z, s);
+        s = dp4a_ss(w.q[4 * u + 3], a[u].w, s);
+        I[u] = s;
+    }
+    // exact: |sc*I| <= 128*16*32*127 and the sum of two stays below 2^24
+    const int J0 = sext8(w.sc4, 0) * I[0] + sext8(w.sc4, 1) * I[1];
+    const int J1 = sext8(w.sc4, 2) * I[2] + sext8(w.sc4, 3) * I[3];
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
+    return w.d * fmaf(d8.y, (float)J1, d8.x * (float)J0);
+}
+
+template <int FMT, int NT>
+__global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const StreamParams p)
+{
+    constexpr int kBytes = Fmt<FMT>::kBytes;
+    constexpr bool kAligned = (kBytes % 16) == 0;
+    static_assert(FMT != kFmtQ4K || NT == 1, "Q4_K small batches run on the tensor-core kernel");
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const SmemLayout L(p.K, p.stage_alloc, NT);
+    uint8_t *ring = smem + L.ring;
+    uint8_t *aq = smem + L.act_qs;
+    uint2 *ads = reinterpret_cast<uint2 *>(smem + L.act_ds);
+    float *contrib = reinterpret_cast<float *>(smem + L.contrib);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kStages;
+    __shared__ volatile int abort_s;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const size_t tq = act_bytes(p.K);          // staging stride of one token's codes
+    const int tds = p.K / 64;                  // and of its d8/s8 pairs (uint2 units)
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        abort_s = 0;
+        fence_mbar_init();
+        pdl_launch_dependents();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first_policy();
+            uint32_t it = 0;
+            for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
+                const int mat = group_mat(p, g);
+                const int row0 = (g - p.gstart[mat]) * p.R;
+                const int rows = min(p.R, p.N[mat] - row0);
+                for (int pc = 0; pc < p.P; ++pc, ++it) {
+                    const uint32_t slot = it % kStages, round = it / kStages;
+                    if (round > 0 && !mbar_wait(&empty[slot], (round & 1) ^ 1, p.status)) return;
+                    const size_t bytes = (p.P == 1) ? (size_t)rows * p.rowbytes
+                                                    : (size_t)min(p.CB, p.nb - pc * p.CB) * kBytes;
+                    const size_t start = (size_t)row0 * p.rowbytes + (size_t)pc * p.CB * kBytes;
+                    uint8_t *dst = ring + (size_t)slot * p.stage_alloc;
+                    if (kAligned) {
+                        mbar_arrive_expect_tx(&full[slot], (uint32_t)bytes);
+                        bulk_g2s_hint(dst, p.W[mat] + start, (uint32_t)bytes, &full[slot], policy);
+                    } else {
+                        // copy from the 16-byte boundary below the tile; bytes past
+                        // the matrix's last 16-byte boundary go by plain loads
+                        const size_t end = start + bytes;
+                        const size_t total = (size_t)p.N[mat] * p.rowbytes;
+                        const size_t lo = start & ~(size_t)15;
+                        const size_t hi = min((end + 15) & ~(size_t)15, total & ~(size_t)15);
+                        for (size_t o = hi; o < end; ++o) dst[o - lo] = __ldg(p.W[mat] + o);
+                        if (end > hi) fence_async_smem();
+                        mbar_arrive_expect_tx(&full[slot], (uint32_t)(hi - lo));
+                        bulk_g2s_hint(dst, p.W[mat] + lo, (uint32_t)(hi - lo), &full[slot], policy);
+                    }
+                }
+            }
+            // every weight byte of this CTA is requested: while the consumers
+            // finish, warm L2 with this CTA's share of the bytes the next
+            // launch will stream
+            if (p.pf != nullptr) {
+                const size_t share = ((p.pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(size_t)15;
+                const size_t b0 = (size_t)blockIdx.x * share;
+                const size_t b1 = min(b0 + share, p.pf_bytes & ~(size_t)15);
+                for (size_t o = b0; o < b1; o += 65536)
+                    bulk_prefetch_l2(p.pf + o, (uint32_t)min((size_t)65536, b1 - o));
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    // The producer streams weights (written by no kernel) from the start; the
+    // activations may come from the previous kernel on the stream, and y may
+    // still be read by it: wait for that kernel before touching either.
+    pdl_wait();
+    if (p.x == nullptr) {
+        // stage the activation rows: codes with the 80-byte group stride,
+        // scales and sums as they are (pairs of binary16 per 32-bit word)
+        for (int t = 0; t < p.ntok; ++t) {
+            const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs + (size_t)t * p.K);
+            uint8_t *aqt = aq + t * tq;
+            for (int c = tid; c < p.K / 16; c += kConsumers)
+                *reinterpret_cast<uint4 *>(aqt + 80 * (c >> 2) + 16 * (c & 3)) = __ldg(gq + c);
+            const uint32_t *gd = reinterpret_cast<const uint32_t *>(p.d + (size_t)t * (p.K / 32));
+            const uint32_t *gs = reinterpret_cast<const uint32_t *>(p.s + (size_t)t * (p.K / 32));
+            for (int c = tid; c < p.K / 64; c += kConsumers)
+                ads[t * tds + c] = make_uint2(__ldg(gd + c), __ldg(gs + c));
+        }
+    } else {
+        // RMSNorm + Q8_1 of x in the canonical order (per-block fma chains,
+        // 256 slots in increasing block order, pairwise tree), packed into
+        // the staging; scratch in the (still unused) contribution area.
+        // Four lanes share a 32-value block, each holding eight consecutive
+        // values, so every load instruction of a warp reads 1 KB of
+        // consecutive bytes; the block's fma chain runs through the four lanes
+        // in order (shuffles), and amax and the code sum are exact group
+        // reductions.  (One token: the host launches this form with NT = 1.)
+        const int nblk = p.K >> 5;
+        float *part = contrib;                // [nblk]
+        float *slot = contrib + kMaxK / 32;   // [256] and r
+        const int grp = tid >> 2, sub = tid & 3;
+        constexpr int kGroupsPerPass = kConsumers / 4;   // 128 blocks per pass
+        constexpr int kUnroll = 3;                       // passes with loads in flight together
+        for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
+            float4 xv[kUnroll][2];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;   // CTA-uniform
+                const int b = base + kGroupsPerPass * u + grp;
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                xv[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                float pr = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (sub == j) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            pr = __fmaf_rn(xv[u][h].x, xv[u][h].x, pr);
+                            pr = __fmaf_rn(xv[u][h].y, xv[u][h].y, pr);
+                            pr = __fmaf_rn(xv[u][h].z, xv[u][h].z, pr);
+                            pr = __fmaf_rn(xv[u][h].w, xv[u][h].w, pr);
+                        }
+                    }
+                    pr = __shfl_sync(0xffffffffu, pr, (lane & ~3) | j);
+                }
+                const int b = base + kGroupsPerPass * u + grp;
+                if (sub == 0 && b < nblk) part[b] = pr;
+            }
+        }
+        float r = 1.0f;
+        if (!p.silu) {
+            named_bar(1, kConsumers);
+            if (tid < 256) {
+                float v = 0.0f;
+                for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
+                slot[tid] = v;
+            }
+            named_bar(1, kConsumers);
+#pragma unroll
+            for (int off = 128; off >= 32; off >>= 1) {
+                if (tid < off) slot[tid] = __fadd_rn(slot[tid], slot[tid + off]);
+                named_bar(1, kConsumers);
+            }
+            if (tid < 32) {
+                float v = slot[tid];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+                if (tid == 0) slot[256] = rms_scale(v, p.K, p.eps);
+            }
+            named_bar(1, kConsumers);
+            r = slot[256];
+        }
+        __half *ads16 = reinterpret_cast<__half *>(ads);
+        const bool out = blockIdx.x == 0 && p.q8out.qs != nullptr;
+        for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
+            float4 xv[kUnroll][2], gv[kUnroll][2];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                const int b = base + kGroupsPerPass * u + grp;
+                const bool in = b < nblk;
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    xv[u][h] = in ? __ldg(px + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    gv[u][h] = in ? __ldg(pg + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (base + kGroupsPerPass * u >= nblk) break;
+                const int b = base + kGroupsPerPass * u + grp;
+                float xh[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (p.silu) {
+                        xh[4 * h + 0] = silu_mul(xv[u][h].x, gv[u][h].x);
+                        xh[4 * h + 1] = silu_mul(xv[u][h].y, gv[u][h].y);
+                        xh[4 * h + 2] = silu_mul(xv[u][h].z, gv[u][h].z);
+                        xh[4 * h + 3] = silu_mul(xv[u][h].w, gv[u][h].w);
+                    } else {
+                        xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[u][h].x, r), gv[u][h].x);
+                        xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[u][h].y, r), gv[u][h].y);
+                        xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[u][h].z, r), gv[u][h].z);
+                        xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[u][h].w, r), gv[u][h].w);
+                    }
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(xh[c]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const float d = __fdiv_rn(amax, 127.0f);
+                const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+                uint32_t word[2] = {0u, 0u};
+                int qsum = 0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float q = roundf(__fmul_rn(xh[c], id));
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    const int qi = (int)q;
+                    qsum += qi;
+                    word[c >> 2] |= ((uint32_t)(qi & 0xFF)) << (8 * (c & 3));
+                }
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+                if (b < nblk) {
+                    *reinterpret_cast<uint2 *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 8 * sub) =
+                        make_uint2(word[0], word[1]);
+                    const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
+                    if (sub == 0) {
+                        ads16[4 * (b >> 1) + (b & 1)] = dh;
+                        ads16[4 * (b >> 1) + 2 + (b & 1)] = sh;
+                    }
+                    if (out) {
+                        reinterpret_cast<uint2 *>(p.q8out.qs + 32 * b)[sub] = make_uint2(word[0], word[1]);
+                        if (sub == 0) {
+                            reinterpret_cast<__half *>(p.q8out.d)[b] = dh;
+                            reinterpret_cast<__half *>(p.q8out.s)[b] = sh;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    named_bar(1, kConsumers);
+
+    // Work of a stage: each row's blocks are split into nseg strided segments
+    // (segment s takes blocks s, s + nseg, ...); a task is one (row, segment)
+    // and runs on one group of four lanes, which accumulates in registers.
+    // Neighbouring groups take neighbouring segments, i.e. neighbouring blocks,
+    // so their shared-memory reads fall in different bank groups.
+    const int G = warp * 8 + (lane >> 2);   // task group, 128 per CTA
+    const int pp = lane & 3;                // Q8_1 block pair 2pp, 2pp+1
+    const unsigned gmask = 0xFu << (4 * (lane >> 2));
+    uint32_t it = 0;
+    for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
+        const int mat = group_mat(p, g);
+        const int row0 = (g - p.gstart[mat]) * p.R;
+        const int rows = min(p.R, p.N[mat] - row0);
+        float *yv = p.y[mat];
+        const size_t ytok = (size_t)p.N[mat];
+        float row_acc[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) row_acc[t] = 0.0f;
+        for (int pc = 0; pc < p.P; ++pc, ++it) {
+            const uint32_t slot = it % kStages, round = it / kStages;
+            // one lane polls; then every lane observes the completed phase
+            // itself (acquire) before reading the stage
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&full[slot], round & 1, p.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok) ok = mbar_wait(&full[slot], round & 1, p.status);
+            if (!ok) abort_s = 1;
+            // the tile starts (start mod 16) bytes into the stage
+            const size_t start = (size_t)row0 * p.rowbytes + (size_t)pc * p.CB * kBytes;
+            const uint8_t *stage = ring + (size_t)slot * p.stage_alloc + (kAligned ? 0 : (start & 15));
+            float *cb = contrib + slot * kMaxBlk;
+            // blocks per row in this stage and where they start in the row
+            const int rowblk = (p.P == 1) ? p.nb : min(p.CB, p.nb - pc * p.CB);
+            const int bbase = pc * p.CB;
+            const int nrows = (p.P == 1) ? rows : 1;
+            const int nseg = (rowblk + kSeg - 1) / kSeg;
+            const int ntask = nrows * nseg;
+            if (ok) {
+                for (int t = G; t < ntask; t += kGroups) {
+                    const int r = t / nseg;
+                    const int sg = t - r * nseg;
+                    const uint8_t *rowp = stage + (size_t)r * rowblk * kBytes;
+                    // all of the segment's blocks are read unconditionally (a
+                    // block past the row end re-reads the first one and is
+                    // dropped), so their shared-memory loads can all be in
+                    // flight together; the sum keeps the segment order
+                    float part[kSeg][NT];
+#pragma unroll
+                    for (int i = 0; i < kSeg; ++i) {
+                        const int lb0 = sg + i * nseg;   // block within this stage's row
+                        const int lb = lb0 < rowblk ? lb0 : sg;
+                        const uint8_t *blk = rowp + (size_t)lb * kBytes;
+                        const int b = bbase + lb;        // super-block index in the row
+                        if constexpr (FMT == kFmtQ4K) {
+                            part[i][0] = q4k_block_part(blk, pp, b, aq, ads);
+                        } else {
+                            typename std::conditional<FMT == kFmtQ5K, Q5Lane, Q6Lane>::type w;
+                            if constexpr (FMT == kFmtQ5K) q5k_decode(blk, pp, w);
+                            else q6k_decode(blk, pp, w);
+#pragma unroll
+                            for (int tk = 0; tk < NT; ++tk) {
+                                if (tk < p.ntok) {
+                                    const uint8_t *ap = aq + tk * tq + 80 * (4 * b + pp);
+                                    const uint4 a[4] = {*reinterpret_cast<const uint4 *>(ap),
+                                                        *reinterpret_cast<const uint4 *>(ap + 16),
+                                                        *reinterpret_cast<const uint4 *>(ap + 32),
+                                                        *reinterpret_cast<const uint4 *>(ap + 48)};
+                                    const uint2 ds = ads[tk * tds + 4 * b + pp];
+                                    if constexpr (FMT == kFmtQ5K) part[i][tk] = q5k_dot(w, a, ds);
+                                    else part[i][tk] = q6k_dot(w, a, ds);
+                                } else {
+                                    part[i][tk] = 0.0f;
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int tk = 0; tk < NT; ++tk) {
+                        float c = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < kSeg; ++i)
+                            if (sg + i * nseg < rowblk) c += part[i][tk];
+                        c += __shfl_xor_sync(gmask, c, 1);
+                        c += __shfl_xor_sync(gmask, c, 2);
+                        if (pp == 0) cb[(size_t)tk * kStages * kMaxBlk + t] = c;
+                    }
+                }
+            }
+            named_bar(1, kConsumers);
+            if (abort_s) return;
+            if (tid == 0) mbar_arrive(&empty[slot]);
+            if (p.P == 1) {
+                for (int r = warp; r < rows; r += kConsumerWarps) {
+                    for (int tk = 0; tk < p.ntok; ++tk) {
+                        const float *cbt = cb + (size_t)tk * kStages * kMaxBlk;
+                        float v = lane < nseg ? cbt[r * nseg + lane] : 0.0f;
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                        if (lane == 0) yv[tk * ytok + row0 + r] = v;
+                    }
+                }
+            } else if (warp == 0) {
+#pragma unroll
+                for (int tk = 0; tk < NT; ++tk) {
+                    if (tk >= p.ntok) break;
+                    const float *cbt = cb + (size_t)tk * kStages * kMaxBlk;
+                    float v = 0.0f;
+                    for (int q = lane; q < nseg; q += 32) v += cbt[q];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                    row_acc[tk] += v;
+                    if (pc == p.P - 1 && lane == 0) yv[tk * ytok + row0] = row_acc[tk];
+                }
+            }
+        }
+    }
+}
+
+// Host side: tile the job, size the stages and launch.  Returns
+// cudaErrorInvalidValue when the activation staging does not fit.
+template <int FMT, int NT>
+cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, cudaStream_t st)
+{
+    constexpr int kBytes = Fmt<FMT>::kBytes;
+    // an unaligned tile is copied from up to 14 bytes below its start to up to
+    // 14 bytes past its end; the last block's aligned loads read 2 bytes past it
+    constexpr uint32_t kSlack = (kBytes % 16) ? 32 : 0;
+    static size_t attr_bytes[64];
+    p.nmat = job.nmat;
+    p.ntok = ntok;
+    long long totalN = 0;
+    for (int m = 0; m < job.nmat; ++m) {
+        p.W[m] = static_cast<const uint8_t *>(job.W[m]);
+        p.y[m] = job.y[m];
+        p.N[m] = job.N[m];
+        totalN += job.N[m];
+    }
+    p.K = K;
+    p.nb = K / 256;
+    p.rowbytes = (uint32_t)p.nb * kBytes;
+    const int sms = num_sms();
+    // stage size: as large as shared memory allows (<= 64 KB), but small
+    // enough that every CTA gets >= 3 stages of work
+    const size_t fixed = SmemLayout(K, 0, NT).total;
+    if (fixed + (size_t)kStages * align_up(kBytes + kSlack, 128) > (size_t)kSmemLimit) return cudaErrorInvalidValue;
+    size_t cap = (kSmemLimit - fixed) / kStages / 128 * 128;
+    cap = cap > (size_t)kStageMax ? (size_t)kStageMax : cap;
+    const double total = (double)totalN * p.rowbytes;
+    size_t target = (size_t)(total / sms / 3);
+    target = target < 4096 ? 4096 : (target > cap ? cap : target);
+    // A row is split into pieces only when it does not fit in a stage at all,
+    // so a row's summation order depends on K alone, not on which other
+    // matrices share the launch.
+    if (p.rowbytes + kSlack <= cap) {
+        p.R = p.rowbytes + kSlack <= target ? (int)((target - kSlack) / p.rowbytes) : 1;
+        p.P = 1;
+        p.CB = p.nb;
+        p.stage_alloc = (uint32_t)align_up((size_t)p.R * p.rowbytes + kSlack, 128);
+    } else {
+        p.R = 1;
+        p.CB = (int)((cap - kSlack) / kBytes);
+        if (p.CB < 1) p.CB = 1;
+        p.P = (p.nb + p.CB - 1) / p.CB;
+        p.stage_alloc = (uint32_t)align_up((size_t)p.CB * kBytes + kSlack, 128);
+    }
+    p.gstart[0] = 0;
+    for (int m = 0; m < kMaxMats; ++m)
+        p.gstart[m + 1] = p.gstart[m] + (m < job.nmat ? (job.N[m] + p.R - 1) / p.R : 0);
+    p.total_groups = p.gstart[job.nmat];
+    p.status = device_status_word();
+    const SmemLayout L(K, p.stage_alloc, NT);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (attr_bytes[dev] < L.total) {
+        cudaError_t e = cudaFuncSetAttribute(kq_gemv_stream_kernel<FMT, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+        if (e != cudaSuccess) return e;
+        attr_bytes[dev] = L.total;
+    }
+    const int grid = p.total_groups < sms ? p.total_groups : sms;
+    return launch_pdl(kq_gemv_stream_kernel<FMT, NT>, dim3(grid), dim3(kThreads), L.total, st, p);
+}
+
+// B tokens of Q8_1 codes (planar [B][K]) against one matrix: one launch for
+// B = 1, else launches of up to four tokens each.
+template <int FMT>
+cudaError_t launch_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st)
+{
+    GemvJob job{};
+    job.nmat = 1;
+    job.W[0] = W;
+    job.N[0] = N;
+    for (int t0 = 0; t0 < B; t0 += 4) {
+        const int nt = B - t0 < 4 ? B - t0 : 4;
+        StreamParams p{};
+        p.qs = a.qs + (size_t)t0 * K;
+        p.d = reinterpret_cast<const __half *>(a.d) + (size_t)t0 * (K / 32);
+        p.s = reinterpret_cast<const __half *>(a.s) + (size_t)t0 * (K / 32);
+        job.y[0] = y + (size_t)t0 * N;
+        const cudaError_t e = (B == 1) ? launch_stream<FMT, 1>(p, job, K, 1, st)
+                                       : launch_stream<FMT, 4>(p, job, K, nt, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// One token given as x and gamma: RMSNorm + Q8_1 inside the launch.
+template <int FMT>
+cudaError_t launch_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps, bool silu,
+                         const zq_q8_1 *q8out, const void *pf, size_t pf_bytes, cudaStream_t st)
+{
+    StreamParams p{};
+    p.x = x;
+    p.gamma = gamma;
+    p.eps = eps;
+    p.silu = silu ? 1 : 0;
+    if (q8out) p.q8out = *q8out;
+    p.pf = static_cast<const uint8_t *>(pf);
+    p.pf_bytes = pf_bytes;
+    return launch_stream<FMT, 1>(p, job, K, 1, st);
+}
+
+}  // namespace stream
+}  // namespace zq

@@ -395,6 +395,80 @@ int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream)
     return launched(launch_q4k_dequant_f16(W, N, K, out, (cudaStream_t)stream), "zq_q4k_dequant_f16 launch");
 }
 
+size_t zq_q5k_bytes(int N, int K)
+{
+    if (N < 1 || K < 256 || K % 256) return 0;
+    return (size_t)N * (size_t)(K / 256) * 176;
+}
+
+size_t zq_q6k_bytes(int N, int K)
+{
+    if (N < 1 || K < 256 || K % 256) return 0;
+    return (size_t)N * (size_t)(K / 256) * 210;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Q5_K / Q6_K projection of B tokens (shared checks and dispatch).
+int kq_gemm(bool q6, const char *name, const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream)
+{
+    int st = check_q4k(W, N, K, name);
+    if (st) return st;
+    if (K > 32768) return fail(ZQ_ERR_SHAPE, "%s: K = %d above the staged-activation limit 32768", name, K);
+    if ((st = check_q8(a, name))) return st;
+    if (B < 1 || B > 16) return fail(ZQ_ERR_SHAPE, "%s: B = %d must be in [1, 16]", name, B);
+    if (!y) return fail(ZQ_ERR_ARG, "%s: null y", name);
+    if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "%s: y must be 16-byte aligned", name);
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    return launched(q6 ? launch_q6k_tokens(W, N, K, a, B, y, s) : launch_q5k_tokens(W, N, K, a, B, y, s), name);
+}
+
+}  // namespace
+
+extern "C" {
+
+int zq_q5k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream)
+{
+    return kq_gemm(false, "zq_q5k_gemm", W, N, K, a, B, y, stream);
+}
+
+int zq_q6k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream)
+{
+    return kq_gemm(true, "zq_q6k_gemm", W, N, K, a, B, y, stream);
+}
+
+int zq_q5k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream)
+{
+    return kq_gemm(false, "zq_q5k_gemv", W, N, K, a, 1, y, stream);
+}
+
+int zq_q6k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream)
+{
+    return kq_gemm(true, "zq_q6k_gemv", W, N, K, a, 1, y, stream);
+}
+
+int zq_rmsnorm_q6k_gemv(const float *x, const float *gamma, float eps, int K, const void *W, int N, float *y,
+                        const zq_q8_1 *q8_out, void *stream)
+{
+    const char *name = "zq_rmsnorm_q6k_gemv";
+    if (!x || !gamma) return fail(ZQ_ERR_ARG, "%s: null x or gamma", name);
+    if (!aligned16(x) || !aligned16(gamma)) return fail(ZQ_ERR_ALIGN, "%s: x and gamma must be 16-byte aligned", name);
+    if (!(eps >= 0.0f) || eps != eps) return fail(ZQ_ERR_ARG, "%s: eps must be >= 0", name);
+    GemvJob job;
+    float *ys[1] = {y};
+    int st = check_job(name, 1, &W, &N, K, ys, job);
+    if (st) return st;
+    if (K > 32768) return fail(ZQ_ERR_SHAPE, "%s: K = %d above the in-kernel normalisation limit 32768", name, K);
+    if (q8_out && (st = check_q8(*q8_out, "zq_rmsnorm_q6k_gemv (q8_out)"))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_q6k_fused(job, K, x, gamma, eps, q8_out, (cudaStream_t)stream), name);
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

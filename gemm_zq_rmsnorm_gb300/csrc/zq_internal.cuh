@@ -46,6 +46,13 @@ cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_
 cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
                                      bool silu, const zq_q8_1 *q8out, const void *pf, size_t pf_bytes,
                                      cudaStream_t st);
+// Q5_K (176-byte blocks) and Q6_K (210-byte blocks) projections of B = 1 .. 16
+// tokens of Q8_1 codes against one N x K matrix (K <= 32768); and the Q6_K
+// mat-vec of one token given as x and gamma (RMSNorm + Q8_1 in the launch).
+cudaError_t launch_q5k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
+cudaError_t launch_q6k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
+cudaError_t launch_q6k_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
+                             const zq_q8_1 *q8out, cudaStream_t st);
 cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, zq_q8_1 out, cudaStream_t st);
 
 // Launch with programmatic dependent launch: the kernel may start while the

@@ -248,6 +248,50 @@ ZQ_API int zq_silu_q4k_gemv(const float *gate, const float *up, int K, int nmat,
  */
 ZQ_API int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream);
 
+/*
+ * ---------------------------------------------------------- Q5_K and Q6_K
+ * The other k-quant blocks of a Q4_K_M checkpoint (MIInfer README, "Status":
+ * Q5_K x Q8_1 MMVQ-style recurrent output projection, MMVQ-style Q6_K x Q8_1
+ * LM head; "Current phase": Q5_K B = 4 reuse in layer-major prefill; ZINC
+ * docs "ROCm backend": packed Q8 activations feed the hot Q4_K, Q5_K and Q6_K
+ * projections).  N rows x K columns (K % 256 == 0), rows of K/256
+ * consecutive super-blocks of 256 weights, rows consecutive:
+ *   Q5_K, 176 bytes: bytes 0..15 as Q4_K (d, dmin, scales and mins);
+ *     bytes 16..47 qh, bit j of byte 16+i = bit 4 of weight i of sub-block j;
+ *     bytes 48..175 the low four bits, placed as the Q4_K nibbles;
+ *     weight = d*sc[j]*q - dmin*m[j], q in 0..31.
+ *   Q6_K, 210 bytes, sixteen sub-blocks of 16 weights; weight k has
+ *     h = k/128, c = (k%128)/32, i = k%32:
+ *     bytes 0..127 low four bits at byte 64h + 32(c%2) + i (low nibble for
+ *     c < 2, high for c >= 2); bytes 128..191 top two bits at bits 2c, 2c+1
+ *     of byte 128 + 32h + i; bytes 192..207 int8 scales sc[k/16];
+ *     bytes 208..209 d (binary16);  weight = d*sc[k/16]*(q - 32), q in 0..63.
+ *     Rows are 210*K/256 bytes: only the matrix start needs 16-byte alignment.
+ * Output as for Q4_K: Q5_K y = sum_{b,j} d*sc_j*d8*I_j - dmin*m_j*s8 with
+ * I_j over the 32 weights of sub-block j; Q6_K y = sum_{b,s} d*sc_s*d8*I_s
+ * with I_s = sum of (q - 32)*q8 over the 16 weights of sub-block s (d8 of the
+ * Q8_1 block holding them; s8 is not used).
+ *
+ * zq_q5k_gemm / zq_q6k_gemm: y [B][N] = W x B tokens of Q8_1 codes,
+ *   1 <= B <= 16 (launches of up to four tokens; every weight read once per
+ *   launch), 256 <= K <= 32768.  zq_q5k_gemv / zq_q6k_gemv: the same, B = 1.
+ * zq_rmsnorm_q6k_gemv: one token given as x, gamma, eps (RMSNorm + Q8_1
+ *   packing in the launch, byte for byte as zq_rmsnorm_q8_1), y [N] = W xh;
+ *   the LM head after the final norm.  q8_out as for zq_rmsnorm_q4k_gemv.
+ * Errors: as for the Q4_K calls; ZQ_ERR_SHAPE also for B outside [1, 16] or
+ * K > 32768.  No workspace.
+ */
+ZQ_API int zq_q5k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream);
+ZQ_API int zq_q6k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *stream);
+ZQ_API int zq_q5k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream);
+ZQ_API int zq_q6k_gemv(const void *W, int N, int K, zq_q8_1 a, float *y, void *stream);
+ZQ_API int zq_rmsnorm_q6k_gemv(const float *x, const float *gamma, float eps, int K,
+                               const void *W, int N, float *y, const zq_q8_1 *q8_out,
+                               void *stream);
+/* Storage sizes of N x K Q5_K and Q6_K matrices. */
+ZQ_API size_t zq_q5k_bytes(int N, int K);
+ZQ_API size_t zq_q6k_bytes(int N, int K);
+
 /* Bytes of device workspace zq_q4k_gemm needs for this shape (0 if none). */
 ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
 

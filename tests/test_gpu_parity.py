@@ -79,7 +79,8 @@ def run_gemv(W, N, K, a):
 
 
 GEMV_SHAPES = [  # (K, N): config-0 tile, ragged N, ragged super-block counts
-    (1024, 1024), (256, 1), (256, 77), (768, 1000), (1280, 333), (3072, 1024), (2048, 1024)]
+    (1024, 1024), (256, 1), (256, 77), (768, 1000), (1280, 333), (3072, 1024), (2048, 1024),
+    (32768, 1500)]   # the staging limit with full-size stages: shared memory at its maximum
 
 
 @pytest.mark.parametrize("K,N", GEMV_SHAPES)

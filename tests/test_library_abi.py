@@ -151,3 +151,32 @@ def test_rmsnorm_gemv_rejects(lib, x, eps, K, nmat, status):
 def test_silu_mul_rejects(lib, g, u, B, K, status):
     assert lib.zq_silu_mul_q8_1(g, u, B, K, q8(), None) == status
     assert lib.zq_last_error()
+
+
+def test_kquant_size_helpers(lib):
+    assert lib.zq_q5k_bytes(5120, 6144) == 5120 * 24 * 176
+    assert lib.zq_q6k_bytes(151936, 1024) == 151936 * 4 * 210
+    assert lib.zq_q5k_bytes(3, 100) == 0 and lib.zq_q6k_bytes(0, 256) == 0
+
+
+@pytest.mark.parametrize("fn", ["zq_q5k_gemm", "zq_q6k_gemm"])
+@pytest.mark.parametrize("W,N,K,B,y,status", [
+    (0, 8, 512, 1, A16, -1),          # null W
+    (A8, 8, 512, 1, A16, -3),         # misaligned W
+    (A16, 0, 512, 1, A16, -2),        # N < 1
+    (A16, 8, 500, 1, A16, -2),        # K % 256
+    (A16, 8, 33024, 1, A16, -2),      # K above 32768
+    (A16, 8, 512, 0, A16, -2),        # B < 1
+    (A16, 8, 512, 17, A16, -2),       # B > 16
+    (A16, 8, 512, 4, 0, -1),          # null y
+    (A16, 8, 512, 4, A8, -3),         # misaligned y
+])
+def test_kquant_gemm_rejects(lib, fn, W, N, K, B, y, status):
+    assert getattr(lib, fn)(W, N, K, q8(), B, y, None) == status
+
+
+@pytest.mark.parametrize("x,W,K,status", [
+    (0, A16, 1024, -1), (A8, A16, 1024, -3), (A16, A8, 1024, -3), (A16, A16, 1000, -2),
+    (A16, A16, 33024, -2)])
+def test_rmsnorm_q6k_gemv_rejects(lib, x, W, K, status):
+    assert lib.zq_rmsnorm_q6k_gemv(x, A16, 1e-6, K, W, 64, A16, None, None) == status
