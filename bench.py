@@ -469,6 +469,63 @@ def dequant_then_gemm(torch, wl, steps, warmup, stream):
                     "products; the dequantised copy is 3.6x the Q4_K bytes"}
 
 
+# Q5_K / Q6_K rows: the LM head of the small model in Q6_K (with and without
+# the final RMSNorm fused in) and the recurrent output projection of the
+# 27B-class layer (value width 48 x 128 = 6144 -> hidden 5120) in Q5_K.
+KQUANT_CASES = [  # (label, fmt, K, N, B, fused)
+    ("q6k_lm_head", "q6k", 1024, 151936, 1, False),
+    ("q6k_lm_head_fused_norm", "q6k", 1024, 151936, 1, True),
+    ("q5k_recurrent_out", "q5k", 6144, 5120, 1, False),
+    ("q5k_recurrent_out_b4", "q5k", 6144, 5120, 4, False),
+]
+KQ_BLOCK = {"q5k": 176, "q6k": 210}
+
+
+def kquant_rows(torch, steps, warmup, stream, pk):
+    """Per-launch device time of each Q5_K / Q6_K case over graphs of
+    back-to-back launches on rotating weight copies (>= 3x L2), as algorithmic
+    HBM GB/s: weights once + activations (Q8_1 codes, or x and gamma when the
+    norm is fused) + y."""
+    import gemm_zq_rmsnorm_gb300 as zq
+    out = []
+    for (label, fmt, K, N, B, fused) in KQUANT_CASES:
+        wbytes = N * K // 256 * KQ_BLOCK[fmt]
+        R = max(2, -(-3 * L2_BYTES // wbytes))
+        gen = inputs.q5k_weights if fmt == "q5k" else inputs.q6k_weights
+        w0 = torch.from_numpy(gen(0, N, K)).cuda()
+        Ws = [w0] + [w0.clone() for _ in range(R - 1)]
+        x = torch.from_numpy(inputs.activations(1, B, K)).cuda()
+        g = torch.from_numpy(inputs.gamma(1, K)).cuda()
+        a = zq.rmsnorm_q8_1(x, g, inputs.EPS)
+        y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+        per = 2 * R
+
+        def calls():
+            for i in range(per):
+                if fused:
+                    zq.rmsnorm_q6k_gemv(x[0], g, inputs.EPS, Ws[i % R], N, y=y[0])
+                else:
+                    zq.kq_gemm(fmt, Ws[i % R], N, K, a, B, y=y)
+
+        calls()
+        torch.cuda.synchronize()
+        reps = max(3, steps // 4)
+        ms = time_graphs(torch, [capture(torch, calls, stream)], reps, max(2, warmup // 2), stream)
+        ms /= per
+        act = 2 * K * 4 if fused else B * K * (1 + 4 / 32)
+        alg = wbytes + act + B * N * 4
+        launches = 1 if B == 1 else -(-B // 4)
+        gbs = alg / (ms * 1e-3) / 1e9
+        out.append({"case": label, "format": fmt.upper().replace("K", "_K"), "K": K, "N": N, "B": B,
+                    "call": ("zq_rmsnorm_q6k_gemv" if fused else f"zq_{fmt}_{'gemv' if B == 1 else 'gemm'}"),
+                    "launches": launches, "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "weight_copies_rotated": R,
+                    "timed_launches": reps * per * launches})
+        del Ws, w0
+        torch.cuda.empty_cache()
+    return out
+
+
 _ORACLE_CACHE = {}
 
 
@@ -516,7 +573,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zq", choices=["zq", "reference"])
     ap.add_argument("--workload", default="headline",
-                    choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny"])
+                    choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny", "kquants"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-l2-prefetch", action="store_true",
@@ -655,6 +712,22 @@ def main():
                 out["more"] = sub[1:]
         else:
             out["prefill_b512"] = sub[0]
+    if args.workload in ("headline", "kquants"):
+        barrier()
+        with Clocks(local_rank) as clk:
+            kq = kquant_rows(torch, args.steps, args.warmup, stream, pk)
+        if args.workload == "kquants":
+            r0 = kq[0]
+            out.update({"value": r0["gbs"], "unit": "GB/s", "ms_per_step": round(r0["us"] / 1e3, 5), "dtype": "u8",
+                        "config": {"workload": f"{r0['case']} {r0['K']}->{r0['N']} B={r0['B']}",
+                                   "l2": "inputs larger than L2: rotating weight copies"},
+                        "roofline": {"bound": "hbm", "kernel": f"{r0['call']} {r0['K']}->{r0['N']}",
+                                     "achieved": r0["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                     "frac": r0["frac_of_hbm"], "peak_source": pk["source"] + " (burst copy)",
+                                     "traffic": None, "kernel_ms": round(r0["us"] / 1e3, 5)},
+                        "gpu_launches": r0["timed_launches"], "clocks": clk.summary(), "more": kq[1:]})
+        else:
+            out["kquants"] = {"rows": kq, "clocks": clk.summary()}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -80,6 +80,8 @@ struct StreamParams {
     int R;                // rows per group
     int P;                // pieces per group (> 1 only when R == 1)
     int CB;               // blocks per piece
+    int nseg;             // segments per row when rows are whole (P == 1); a function of K only
+    int wl;               // warp-local rows (P == 1, nseg in 1, 2, 4, 8); a function of K only
     int total_groups;
     uint32_t stage_alloc; // bytes reserved per stage (multiple of 128)
     // input: Q8_1 planes, or (x, gamma, eps) normalised in the kernel
@@ -118,13 +120,16 @@ __host__ __device__ constexpr size_t ads_bytes(int K) { return (size_t)K / 64 * 
 static_assert(kStages * kMaxBlk >= kMaxK / 32 + 257, "RMSNorm scratch fits in the contribution area");
 
 struct SmemLayout {
-    size_t ring, act_qs, act_ds, contrib, bars, total;
-    __host__ __device__ SmemLayout(int K, uint32_t stage_alloc, int nt)
+    size_t ring, act_qs, act_ds, act_sum, contrib, bars, total;
+    // sums: also stage the exact code sum of every 8 activations (int16), for
+    // the Q6_K offset, in the order the Q6_K lanes read them
+    __host__ __device__ SmemLayout(int K, uint32_t stage_alloc, int nt, bool sums)
     {
         ring = 0;
         act_qs = ring + (size_t)kStages * stage_alloc;
         act_ds = align_up(act_qs + (size_t)nt * act_bytes(K), 16);
-        contrib = align_up(act_ds + (size_t)nt * ads_bytes(K), 16);
+        act_sum = align_up(act_ds + (size_t)nt * ads_bytes(K), 16);
+        contrib = align_up(act_sum + (sums ? (size_t)nt * K / 4 : 0), 16);
         bars = align_up(contrib + (size_t)nt * kStages * kMaxBlk * 4, 8);
         total = bars + 2 * kStages * 8;
     }
@@ -221,12 +226,13 @@ __device__ __forceinline__ void q5k_decode(const uint8_t *blk, int p, Q5Lane &w)
     const uint4 l1 = *reinterpret_cast<const uint4 *>(blk + 64 + 32 * p);
     const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-    // bit 2p (2p+1) of every qh byte becomes bit 4 of the quant
-    const int s0 = 2 * p, s1 = 2 * p + 1;
+    // bit 2p (2p+1) of every qh byte becomes bit 4 of the quant: a rotation
+    // moves it there within its byte (bits leaving a byte are masked off)
+    const uint32_t r0 = (uint32_t)(2 * p - 4) & 31u, r1 = (uint32_t)(2 * p - 3) & 31u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const uint32_t b0 = s0 <= 4 ? qh[k] << (4 - s0) : qh[k] >> (s0 - 4);
-        const uint32_t b1 = s1 <= 4 ? qh[k] << (4 - s1) : qh[k] >> (s1 - 4);
+        const uint32_t b0 = __funnelshift_r(qh[k], qh[k], r0);
+        const uint32_t b1 = __funnelshift_r(qh[k], qh[k], r1);
         w.q0[k] = (ql[k] & 0x0F0F0F0Fu) | (b0 & 0x10101010u);
         w.q1[k] = ((ql[k] >> 4) & 0x0F0F0F0Fu) | (b1 & 0x10101010u);
     }
@@ -267,10 +273,15 @@ __device__ __forceinline__ float q5k_dot(const Q5Lane &w, const uint4 (&a)[4], u
     return fmaf(w.d, main, -w.dmin * mins);
 }
 
-// ---- Q6_K: lane p decodes weights 64p..64p+63 (four 16-weight sub-blocks) ----
+// ---- Q6_K: lane p decodes positions i = 8p .. 8p+7 of all eight 32-weight
+// quarters (h, c) of the block: weights k = 128h + 32c + i.  Its bytes are
+// then disjoint from the other lanes' -- low bits at 64h + 32(c%2) + 8p (both
+// nibbles used), top bits at 128 + 32h + 8p (all four bit pairs used) -- and
+// each (h, c) chunk of 8 weights lies in one 16-weight sub-block (scale
+// index 8h + 2c + p/2) and one Q8_1 block (4h + c). ----
 struct Q6Lane {
-    uint32_t q[16];   // q - 32 as signed bytes, four per word; words 4u..4u+3 = sub-block 4p+u
-    uint32_t sc4;     // the four int8 scales of sub-blocks 4p..4p+3
+    uint32_t q[8][2];   // quants 0..63 of chunk (h, c) = q[4h + c], four per word
+    int sc[8];          // scale of chunk (h, c)
     float d;
 };
 
@@ -283,61 +294,72 @@ __device__ __forceinline__ uint32_t ld_w32(const uint8_t *base4, int o, uint32_t
     return __byte_perm(lo, hi, sel);
 }
 
+// 8 bytes at offset o (o = 0 mod 4 relative to the block): three aligned words
+__device__ __forceinline__ uint2 ld_w64(const uint8_t *base4, int o, uint32_t sel)
+{
+    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(base4 + o);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(base4 + o + 4);
+    const uint32_t w2 = *reinterpret_cast<const uint32_t *>(base4 + o + 8);
+    return make_uint2(__byte_perm(w0, w1, sel), __byte_perm(w1, w2, sel));
+}
+
 __device__ __forceinline__ void q6k_decode(const uint8_t *blk, int p, Q6Lane &w)
 {
-    const int h = p >> 1, odd = p & 1;
     const uint32_t mis = (uint32_t)reinterpret_cast<uintptr_t>(blk) & 2u;
     const uint8_t *base4 = blk - mis;
     const uint32_t sel = mis ? 0x5432u : 0x3210u;
-    // low bits: bytes 64h .. 64h+63 (quarter 2*odd in the first 32, quarter
-    // 2*odd+1 in the next 32), low nibble for p even, high nibble for p odd
-    uint32_t raw[17];
 #pragma unroll
-    for (int k = 0; k < 17; ++k) raw[k] = *reinterpret_cast<const uint32_t *>(base4 + 64 * h + 4 * k);
-    uint32_t rh[9];
+    for (int h = 0; h < 2; ++h) {
+        const uint2 th = ld_w64(base4, 128 + 32 * h + 8 * p, sel);
+        const uint32_t hw[2] = {th.x, th.y};
 #pragma unroll
-    for (int k = 0; k < 9; ++k) rh[k] = *reinterpret_cast<const uint32_t *>(base4 + 128 + 32 * h + 4 * k);
-    const int nsh = 4 * odd;          // nibble
+        for (int cc = 0; cc < 2; ++cc) {
+            const uint2 tl = ld_w64(base4, 64 * h + 32 * cc + 8 * p, sel);
+            const uint32_t lw[2] = {tl.x, tl.y};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t qh = __byte_perm(rh[k], rh[k + 1], sel);
-        const uint32_t la = __byte_perm(raw[k], raw[k + 1], sel);
-        const uint32_t lb = __byte_perm(raw[k + 8], raw[k + 9], sel);
-        // top-bit pairs of quarters 2*odd (bits 4*odd..) and 2*odd+1 (bits
-        // 4*odd+2..) of every qh byte, moved to bits 4..5
-        const uint32_t ta = odd ? qh : qh << 4;
-        const uint32_t tb = odd ? qh >> 2 : qh << 2;
-        const uint32_t qa = ((la >> nsh) & 0x0F0F0F0Fu) | (ta & 0x30303030u);
-        const uint32_t qb = ((lb >> nsh) & 0x0F0F0F0Fu) | (tb & 0x30303030u);
-        // q - 32 as a signed byte: q >= 32 -> q & 31; q < 32 -> (q & 31) | 0xE0
-        w.q[k] = (qa & 0x1F1F1F1Fu) | ((~qa & 0x20202020u) * 7u);
-        w.q[8 + k] = (qb & 0x1F1F1F1Fu) | ((~qb & 0x20202020u) * 7u);
+            for (int v = 0; v < 2; ++v) {
+                // top-bit pair of quarter c (bits 2c, 2c+1) moved to bits 4..5
+                const uint32_t t_lo = cc == 0 ? hw[v] << 4 : hw[v] << 2;   // quarter cc
+                const uint32_t t_hi = cc == 0 ? hw[v] : hw[v] >> 2;        // quarter cc + 2
+                w.q[4 * h + cc][v] = (lw[v] & 0x0F0F0F0Fu) | (t_lo & 0x30303030u);
+                w.q[4 * h + cc + 2][v] = ((lw[v] >> 4) & 0x0F0F0F0Fu) | (t_hi & 0x30303030u);
+            }
+        }
     }
-    w.sc4 = ld_w32(base4, 192 + 4 * p, sel);
+    // scales 8h + 2c + p/2: every second byte of the 16, from byte p/2
+    const uint32_t s0 = ld_w32(base4, 192, sel), s1 = ld_w32(base4, 196, sel);
+    const uint32_t s2 = ld_w32(base4, 200, sel), s3 = ld_w32(base4, 204, sel);
+    const uint32_t sw[4] = {s0, s1, s2, s3};
+    const int j = p >> 1;
+    // byte j (chunk even) or j + 2 (chunk odd) of word (4h + c) / 2, sign-extended
+#pragma unroll
+    for (int q = 0; q < 8; ++q) w.sc[q] = (int)(int8_t)(uint8_t)(sw[q >> 1] >> (8 * (j + 2 * (q & 1))));
     w.d = __half2float(*reinterpret_cast<const __half *>(blk + 208));
 }
 
-__device__ __forceinline__ int sext8(uint32_t v, int byte) { return (int)(int8_t)(uint8_t)(v >> (8 * byte)); }
+__device__ __forceinline__ int sext16(uint32_t v, int half) { return half ? (int)v >> 16 : (int)(int16_t)(v & 0xFFFFu); }
 
-// a[0..1]: codes of Q8_1 block 2p (sub-blocks 4p, 4p+1), a[2..3]: block 2p+1
-// (sub-blocks 4p+2, 4p+3); ds.x = d8 pair (binary16).
-__device__ __forceinline__ float q6k_dot(const Q6Lane &w, const uint4 (&a)[4], uint2 ds)
+// Token part of the lane's 64 weights.  ap: the super-block's codes in the
+// staging (80-byte pair stride), dsp: its four (d8 pair, s8 pair) words, as:
+// the exact sums of the lane's eight 8-code chunks (int16, chunk order 4h + c),
+// so that sum (q - 32) * q8 = sum q * q8 - 32 * sum q8 stays an exact integer.
+__device__ __forceinline__ float q6k_dot(const Q6Lane &w, const uint8_t *ap, const uint2 *dsp, uint4 as, int p)
 {
-    int I[4];
+    const uint32_t aw[4] = {as.x, as.y, as.z, as.w};
+    float acc = 0.0f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        int s = 0;
-        s = dp4a_ss(w.q[4 * u + 0], a[u].x, s);
-        s = dp4a_ss(w.q[4 * u + 1], a[u].y, s);
-        s = dp4a_ss(w.q[4 * u + 2], a[u].z, s);
-        s = dp4a_ss(w.q[4 * u + 3], a[u].w, s);
-        I[u] = s;
+    for (int q = 0; q < 8; ++q) {   // Q8_1 block q = 4h + c of the super-block
+        const uint2 a = *reinterpret_cast<const uint2 *>(ap + 80 * (q >> 1) + 32 * (q & 1) + 8 * p);
+        int I = dp4a_us(w.q[q][0], a.x, 0);
+        I = dp4a_us(w.q[q][1], a.y, I);
+        I -= 32 * sext16(aw[q >> 1], q & 1);
+        // exact: |sc * I| <= 128 * 8 * 32 * 127 < 2^23
+        const int J = w.sc[q] * I;
+        const __half2 d8 = *reinterpret_cast<const __half2 *>(&dsp[q >> 1].x);
+        const float d8q = (q & 1) ? __high2float(d8) : __low2float(d8);
+        acc = fmaf(d8q, (float)J, acc);
     }
-    // exact: |sc*I| <= 128*16*32*127 and the sum of two stays below 2^24
-    const int J0 = sext8(w.sc4, 0) * I[0] + sext8(w.sc4, 1) * I[1];
-    const int J1 = sext8(w.sc4, 2) * I[2] + sext8(w.sc4, 3) * I[3];
-    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
-    return w.d * fmaf(d8.y, (float)J1, d8.x * (float)J0);
+    return w.d * acc;
 }
 
 template <int FMT, int NT>
@@ -347,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     constexpr bool kAligned = (kBytes % 16) == 0;
     static_assert(FMT != kFmtQ4K || NT == 1, "Q4_K small batches run on the tensor-core kernel");
     extern __shared__ __align__(1024) uint8_t smem[];
-    const SmemLayout L(p.K, p.stage_alloc, NT);
+    const SmemLayout L(p.K, p.stage_alloc, NT, FMT == kFmtQ6K);
     uint8_t *ring = smem + L.ring;
     uint8_t *aq = smem + L.act_qs;
     uint2 *ads = reinterpret_cast<uint2 *>(smem + L.act_ds);
+    // Q6_K: int16 sums of the 8-code chunks, lane-major: [super-block][lane p][Q8_1 block q]
+    uint4 *asum = reinterpret_cast<uint4 *>(smem + L.act_sum);
     float *contrib = reinterpret_cast<float *>(smem + L.contrib);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kStages;
@@ -361,11 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const int lane = tid & 31;
     const size_t tq = act_bytes(p.K);          // staging stride of one token's codes
     const int tds = p.K / 64;                  // and of its d8/s8 pairs (uint2 units)
+    const int tas = p.K / 64;                  // and of its 8-code sums (uint4 units)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
         }
         abort_s = 0;
         fence_mbar_init();
@@ -431,8 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
         for (int t = 0; t < p.ntok; ++t) {
             const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs + (size_t)t * p.K);
             uint8_t *aqt = aq + t * tq;
-            for (int c = tid; c < p.K / 16; c += kConsumers)
-                *reinterpret_cast<uint4 *>(aqt + 80 * (c >> 2) + 16 * (c & 3)) = __ldg(gq + c);
+            int16_t *at = reinterpret_cast<int16_t *>(asum + t * tas);
+            for (int c = tid; c < p.K / 16; c += kConsumers) {
+                const uint4 v = __ldg(gq + c);
+                *reinterpret_cast<uint4 *>(aqt + 80 * (c >> 2) + 16 * (c & 3)) = v;
+                if constexpr (FMT == kFmtQ6K) {
+                    // 8-code chunks 2c and 2c+1: super-block k8 / 32, lane k8 % 4, Q8_1 block (k8 % 32) / 4
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k8 = 2 * c + e;
+                        const int sum = dp4a_ss(e ? v.w : v.y, 0x01010101u, dp4a_ss(e ? v.z : v.x, 0x01010101u, 0));
+                        at[((k8 >> 5) * 4 + (k8 & 3)) * 8 + ((k8 & 31) >> 2)] = (int16_t)sum;
+                    }
+                }
+            }
             const uint32_t *gd = reinterpret_cast<const uint32_t *>(p.d + (size_t)t * (p.K / 32));
             const uint32_t *gs = reinterpret_cast<const uint32_t *>(p.s + (size_t)t * (p.K / 32));
             for (int c = tid; c < p.K / 64; c += kConsumers)
@@ -560,6 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                     qsum += qi;
                     word[c >> 2] |= ((uint32_t)(qi & 0xFF)) << (8 * (c & 3));
                 }
+                if constexpr (FMT == kFmtQ6K) {
+                    // this lane's 8 codes are chunk k8 = 4b + sub
+                    if (b < nblk) reinterpret_cast<int16_t *>(asum)[((b >> 3) * 4 + sub) * 8 + (b & 7)] = (int16_t)qsum;
+                }
                 qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
                 qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
                 if (b < nblk) {
@@ -592,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const int pp = lane & 3;                // Q8_1 block pair 2pp, 2pp+1
     const unsigned gmask = 0xFu << (4 * (lane >> 2));
     uint32_t it = 0;
+    uint32_t rr = 0;                        // warp-local rows: slots handed out so far
     for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
         const int mat = group_mat(p, g);
         const int row0 = (g - p.gstart[mat]) * p.R;
@@ -605,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             const uint32_t slot = it % kStages, round = it / kStages;
             // one lane polls; then every lane observes the completed phase
             // itself (acquire) before reading the stage
+            if (p.wl && abort_s) return;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&full[slot], round & 1, p.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -618,62 +661,127 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             const int rowblk = (p.P == 1) ? p.nb : min(p.CB, p.nb - pc * p.CB);
             const int bbase = pc * p.CB;
             const int nrows = (p.P == 1) ? rows : 1;
-            const int nseg = (rowblk + kSeg - 1) / kSeg;
+            const int nseg = (p.P == 1) ? p.nseg : (rowblk + kSeg - 1) / kSeg;
             const int ntask = nrows * nseg;
+            // partial sums of this lane's 64 weights of block lb of a row, per token
+            auto block = [&](const uint8_t *rowp, int lb, float (&out)[NT]) {
+                const uint8_t *blk = rowp + (size_t)lb * kBytes;
+                const int b = bbase + lb;        // super-block index in the row
+                if constexpr (FMT == kFmtQ4K) {
+                    out[0] = q4k_block_part(blk, pp, b, aq, ads);
+                } else {
+                    typename std::conditional<FMT == kFmtQ5K, Q5Lane, Q6Lane>::type w;
+                    if constexpr (FMT == kFmtQ5K) q5k_decode(blk, pp, w);
+                    else q6k_decode(blk, pp, w);
+#pragma unroll
+                    for (int tk = 0; tk < NT; ++tk) {
+                        if (tk < p.ntok) {
+                            if constexpr (FMT == kFmtQ5K) {
+                                const uint8_t *ap = aq + tk * tq + 80 * (4 * b + pp);
+                                const uint4 a[4] = {*reinterpret_cast<const uint4 *>(ap),
+                                                    *reinterpret_cast<const uint4 *>(ap + 16),
+                                                    *reinterpret_cast<const uint4 *>(ap + 32),
+                                                    *reinterpret_cast<const uint4 *>(ap + 48)};
+                                out[tk] = q5k_dot(w, a, ads[tk * tds + 4 * b + pp]);
+                            } else {
+                                out[tk] = q6k_dot(w, aq + tk * tq + 320 * b, ads + tk * tds + 4 * b,
+                                                  asum[tk * tas + 4 * b + pp], pp);
+                            }
+                        } else {
+                            out[tk] = 0.0f;
+                        }
+                    }
+                }
+            };
+            if (p.wl && p.P == 1) {
+                // Warp-local rows: the nseg (1, 2, 4 or 8) task groups of a row
+                // sit in one warp, which reduces the row with shuffles and writes
+                // y; each warp releases the stage on its own.  Slots of 8/nseg
+                // rows go to the warps round-robin, continuing across stages.
+                if (!ok) return;
+                const int rpw = 8 / nseg;
+                const int nslots = (nrows + rpw - 1) / rpw;
+                const int gi = lane >> 2, sg = gi % nseg, sr = gi / nseg;
+                const int s0 = (warp - (int)(rr % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+                for (int sl = s0; sl < nslots; sl += kConsumerWarps) {
+                    const int r = sl * rpw + sr;   // row within the stage
+                    const bool live = r < nrows;
+                    const uint8_t *rowp = stage + (size_t)(live ? r : 0) * rowblk * kBytes;
+                    float c[NT];
+#pragma unroll
+                    for (int tk = 0; tk < NT; ++tk) c[tk] = 0.0f;
+                    // blocks sg, sg + nseg, ... of the row, four in flight, summed in order
+                    for (int lb = sg; live && lb < rowblk; lb += kSeg * nseg) {
+                        float part[kSeg][NT];
+#pragma unroll
+                        for (int i = 0; i < kSeg; ++i) {
+                            if (lb + i * nseg < rowblk) {
+                                block(rowp, lb + i * nseg, part[i]);
+                            } else {
+#pragma unroll
+                                for (int tk = 0; tk < NT; ++tk) part[i][tk] = 0.0f;
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < kSeg; ++i)
+#pragma unroll
+                            for (int tk = 0; tk < NT; ++tk)
+                                if (lb + i * nseg < rowblk) c[tk] += part[i][tk];
+                    }
+#pragma unroll
+                    for (int tk = 0; tk < NT; ++tk) {
+                        float v = c[tk];
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        for (int off = 4; off < 4 * nseg; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                        if (live && (lane & (4 * nseg - 1)) == 0 && tk < p.ntok) yv[tk * ytok + row0 + r] = v;
+                    }
+                }
+                rr += (uint32_t)nslots;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                continue;
+            }
             if (ok) {
                 for (int t = G; t < ntask; t += kGroups) {
                     const int r = t / nseg;
                     const int sg = t - r * nseg;
                     const uint8_t *rowp = stage + (size_t)r * rowblk * kBytes;
-                    // all of the segment's blocks are read unconditionally (a
-                    // block past the row end re-reads the first one and is
-                    // dropped), so their shared-memory loads can all be in
-                    // flight together; the sum keeps the segment order
-                    float part[kSeg][NT];
+                    float c[NT];
+                    if (nseg == rowblk) {
+                        // short rows: one block per task
+                        block(rowp, sg, c);
+                    } else {
+                        // all of the segment's blocks are read unconditionally (a
+                        // block past the row end re-reads the first one and is
+                        // dropped), so their shared-memory loads can all be in
+                        // flight together; the sum keeps the segment order
+                        float part[kSeg][NT];
 #pragma unroll
-                    for (int i = 0; i < kSeg; ++i) {
-                        const int lb0 = sg + i * nseg;   // block within this stage's row
-                        const int lb = lb0 < rowblk ? lb0 : sg;
-                        const uint8_t *blk = rowp + (size_t)lb * kBytes;
-                        const int b = bbase + lb;        // super-block index in the row
-                        if constexpr (FMT == kFmtQ4K) {
-                            part[i][0] = q4k_block_part(blk, pp, b, aq, ads);
-                        } else {
-                            typename std::conditional<FMT == kFmtQ5K, Q5Lane, Q6Lane>::type w;
-                            if constexpr (FMT == kFmtQ5K) q5k_decode(blk, pp, w);
-                            else q6k_decode(blk, pp, w);
+                        for (int i = 0; i < kSeg; ++i) {
+                            const int lb0 = sg + i * nseg;   // block within this stage's row
+                            block(rowp, lb0 < rowblk ? lb0 : sg, part[i]);
+                        }
 #pragma unroll
-                            for (int tk = 0; tk < NT; ++tk) {
-                                if (tk < p.ntok) {
-                                    const uint8_t *ap = aq + tk * tq + 80 * (4 * b + pp);
-                                    const uint4 a[4] = {*reinterpret_cast<const uint4 *>(ap),
-                                                        *reinterpret_cast<const uint4 *>(ap + 16),
-                                                        *reinterpret_cast<const uint4 *>(ap + 32),
-                                                        *reinterpret_cast<const uint4 *>(ap + 48)};
-                                    const uint2 ds = ads[tk * tds + 4 * b + pp];
-                                    if constexpr (FMT == kFmtQ5K) part[i][tk] = q5k_dot(w, a, ds);
-                                    else part[i][tk] = q6k_dot(w, a, ds);
-                                } else {
-                                    part[i][tk] = 0.0f;
-                                }
-                            }
+                        for (int tk = 0; tk < NT; ++tk) {
+                            c[tk] = 0.0f;
+#pragma unroll
+                            for (int i = 0; i < kSeg; ++i)
+                                if (sg + i * nseg < rowblk) c[tk] += part[i][tk];
                         }
                     }
 #pragma unroll
                     for (int tk = 0; tk < NT; ++tk) {
-                        float c = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < kSeg; ++i)
-                            if (sg + i * nseg < rowblk) c += part[i][tk];
-                        c += __shfl_xor_sync(gmask, c, 1);
-                        c += __shfl_xor_sync(gmask, c, 2);
-                        if (pp == 0) cb[(size_t)tk * kStages * kMaxBlk + t] = c;
+                        float v = c[tk];
+                        v += __shfl_xor_sync(gmask, v, 1);
+                        v += __shfl_xor_sync(gmask, v, 2);
+                        if (pp == 0) cb[(size_t)tk * kStages * kMaxBlk + t] = v;
                     }
                 }
             }
             named_bar(1, kConsumers);
             if (abort_s) return;
-            if (tid == 0) mbar_arrive(&empty[slot]);
+            if (lane == 0) mbar_arrive(&empty[slot]);
             if (p.P == 1) {
                 for (int r = warp; r < rows; r += kConsumerWarps) {
                     for (int tk = 0; tk < p.ntok; ++tk) {
@@ -726,7 +834,7 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
     const int sms = num_sms();
     // stage size: as large as shared memory allows (<= 64 KB), but small
     // enough that every CTA gets >= 3 stages of work
-    const size_t fixed = SmemLayout(K, 0, NT).total;
+    const size_t fixed = SmemLayout(K, 0, NT, FMT == kFmtQ6K).total;
     if (fixed + (size_t)kStages * align_up(kBytes + kSlack, 128) > (size_t)kSmemLimit) return cudaErrorInvalidValue;
     size_t cap = (kSmemLimit - fixed) / kStages / 128 * 128;
     cap = cap > (size_t)kStageMax ? (size_t)kStageMax : cap;
@@ -736,8 +844,37 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
     // A row is split into pieces only when it does not fit in a stage at all,
     // so a row's summation order depends on K alone, not on which other
     // matrices share the launch.
+    // Segments per row.  Warp-local rows: nseg of 4, 8, 2 or 1 task groups in
+    // one warp, the choice that splits the row's blocks most evenly among
+    // those for which a full stage holds rows for five or more warps (so the
+    // three stages in flight keep the sixteen warps busy).  Otherwise (long
+    // rows) segments of up to kSeg blocks reduced through shared memory.  Both
+    // depend on K (and the format and token count) only, so a row's summation
+    // order does not depend on the other matrices of a launch.
+    const long long rcap = p.rowbytes + kSlack <= cap ? (long long)((cap - kSlack) / p.rowbytes) : 0;
+    int ns_wl = 0;
+    double best_u = -1.0;
+    for (int ns : {4, 8, 2, 1}) {
+        if (rcap * ns < 40) continue;
+        const double u = (double)p.nb / (double)(ns * ((p.nb + ns - 1) / ns));
+        if (u > best_u + 1e-12) {
+            best_u = u;
+            ns_wl = ns;
+        }
+    }
+    p.wl = ns_wl > 0 ? 1 : 0;
+    p.nseg = p.wl ? ns_wl : (p.nb <= 8 ? p.nb : (p.nb + kSeg - 1) / kSeg);
     if (p.rowbytes + kSlack <= cap) {
-        p.R = p.rowbytes + kSlack <= target ? (int)((target - kSlack) / p.rowbytes) : 1;
+        const int rmax = p.rowbytes + kSlack <= target ? (int)((target - kSlack) / p.rowbytes) : 1;
+        // rows per stage: the most rows per round of task groups (a stage of
+        // R rows takes ceil(R*nseg/128) rounds), among R in [rmax/2, rmax];
+        // warp-local rows are balanced across stages, any R will do
+        p.R = rmax;
+        for (int r = rmax; !p.wl && r >= (rmax + 1) / 2; --r) {
+            const long long rounds_r = ((long long)r * p.nseg + kGroups - 1) / kGroups;
+            const long long rounds_R = ((long long)p.R * p.nseg + kGroups - 1) / kGroups;
+            if ((long long)r * rounds_R > (long long)p.R * rounds_r) p.R = r;
+        }
         p.P = 1;
         p.CB = p.nb;
         p.stage_alloc = (uint32_t)align_up((size_t)p.R * p.rowbytes + kSlack, 128);
@@ -753,7 +890,7 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
         p.gstart[m + 1] = p.gstart[m] + (m < job.nmat ? (job.N[m] + p.R - 1) / p.R : 0);
     p.total_groups = p.gstart[job.nmat];
     p.status = device_status_word();
-    const SmemLayout L(K, p.stage_alloc, NT);
+    const SmemLayout L(K, p.stage_alloc, NT, FMT == kFmtQ6K);
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -767,8 +904,19 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
     return launch_pdl(kq_gemv_stream_kernel<FMT, NT>, dim3(grid), dim3(kThreads), L.total, st, p);
 }
 
+// Whether the NT-token staging of K activations leaves room for the stages.
+template <int FMT, int NT>
+bool staging_fits(int K)
+{
+    constexpr int kBytes = Fmt<FMT>::kBytes;
+    constexpr uint32_t kSlack = (kBytes % 16) ? 32 : 0;
+    return SmemLayout(K, 0, NT, FMT == kFmtQ6K).total + (size_t)kStages * align_up(kBytes + kSlack, 128) <=
+           (size_t)kSmemLimit;
+}
+
 // B tokens of Q8_1 codes (planar [B][K]) against one matrix: one launch for
-// B = 1, else launches of up to four tokens each.
+// B = 1, else launches of up to four tokens each (one token each when four
+// tokens' staging does not fit in shared memory).
 template <int FMT>
 cudaError_t launch_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st)
 {
@@ -776,15 +924,16 @@ cudaError_t launch_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *
     job.nmat = 1;
     job.W[0] = W;
     job.N[0] = N;
-    for (int t0 = 0; t0 < B; t0 += 4) {
-        const int nt = B - t0 < 4 ? B - t0 : 4;
+    const int per = (B > 1 && staging_fits<FMT, 4>(K)) ? 4 : 1;
+    for (int t0 = 0; t0 < B; t0 += per) {
+        const int nt = B - t0 < per ? B - t0 : per;
         StreamParams p{};
         p.qs = a.qs + (size_t)t0 * K;
         p.d = reinterpret_cast<const __half *>(a.d) + (size_t)t0 * (K / 32);
         p.s = reinterpret_cast<const __half *>(a.s) + (size_t)t0 * (K / 32);
         job.y[0] = y + (size_t)t0 * N;
-        const cudaError_t e = (B == 1) ? launch_stream<FMT, 1>(p, job, K, 1, st)
-                                       : launch_stream<FMT, 4>(p, job, K, nt, st);
+        const cudaError_t e = (per == 1) ? launch_stream<FMT, 1>(p, job, K, 1, st)
+                                         : launch_stream<FMT, 4>(p, job, K, nt, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
