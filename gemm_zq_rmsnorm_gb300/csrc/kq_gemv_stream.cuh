@@ -710,23 +710,24 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                     float c[NT];
 #pragma unroll
                     for (int tk = 0; tk < NT; ++tk) c[tk] = 0.0f;
-                    // blocks sg, sg + nseg, ... of the row, four in flight, summed in order
-                    for (int lb = sg; live && lb < rowblk; lb += kSeg * nseg) {
+                    // blocks sg, sg + nseg, ... of the row, summed in order: four at
+                    // a time with no condition between them (so their loads are in
+                    // flight together) while four remain, then one at a time
+                    int lb = sg;
+                    for (; live && lb + (kSeg - 1) * nseg < rowblk; lb += kSeg * nseg) {
                         float part[kSeg][NT];
 #pragma unroll
-                        for (int i = 0; i < kSeg; ++i) {
-                            if (lb + i * nseg < rowblk) {
-                                block(rowp, lb + i * nseg, part[i]);
-                            } else {
-#pragma unroll
-                                for (int tk = 0; tk < NT; ++tk) part[i][tk] = 0.0f;
-                            }
-                        }
+                        for (int i = 0; i < kSeg; ++i) block(rowp, lb + i * nseg, part[i]);
 #pragma unroll
                         for (int i = 0; i < kSeg; ++i)
 #pragma unroll
-                            for (int tk = 0; tk < NT; ++tk)
-                                if (lb + i * nseg < rowblk) c[tk] += part[i][tk];
+                            for (int tk = 0; tk < NT; ++tk) c[tk] += part[i][tk];
+                    }
+                    for (; live && lb < rowblk; lb += nseg) {
+                        float part[NT];
+                        block(rowp, lb, part);
+#pragma unroll
+                        for (int tk = 0; tk < NT; ++tk) c[tk] += part[tk];
                     }
 #pragma unroll
                     for (int tk = 0; tk < NT; ++tk) {
