@@ -566,6 +566,23 @@ def oracle_sample(wl_shapes, B, budget_s=12.0, seed=0):
 
 
 # ----------------------------------------------------------------------------
+def reduce_max_over_ranks(dist, v, device):
+    """The slowest rank's time: max of v over the process group (v itself
+    without one)."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms_max, world):
+    """Replicas: every rank processes the same units; the job's rate is all
+    ranks' units over the slowest rank's time (units per second)."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,11 +628,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(dist, v, "cuda")
 
     wl_dec = None
     fz = args.decode_path == "fused"
@@ -634,7 +647,7 @@ def main():
         with Clocks(local_rank) as clk:
             ms, _ = bench_workload(torch, wl_dec, args.steps, args.warmup, stream)
         ms = max_over_ranks(ms)
-        gbs = wl_dec.algo_bytes() / (ms * 1e-3) / 1e9 * world
+        gbs = whole_job_rate(wl_dec.algo_bytes(), ms, world) / 1e9
         dom = "gate_up" if any(s[0] == "gate_up" for s in wl_dec.shapes) else wl_dec.shapes[0][0]
         dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl_dec, dom, args.steps, args.warmup, stream)
         achieved = dalg / (dms * 1e-3) / 1e9
@@ -680,8 +693,8 @@ def main():
             with Clocks(local_rank) as clk:
                 ms, _ = bench_workload(torch, wl, max(3, args.steps // 5), args.warmup, stream)
             ms = max_over_ranks(ms)
-            tops = wl.algo_ops() / (ms * 1e-3) / 1e12 * world
-            gbs = wl.algo_bytes() / (ms * 1e-3) / 1e9 * world
+            tops = whole_job_rate(wl.algo_ops(), ms, world) / 1e12
+            gbs = whole_job_rate(wl.algo_bytes(), ms, world) / 1e9
             dom = "gate_up" if any(s[0] == "gate_up" for s in wl.shapes) else wl.shapes[0][0]
             dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl, dom, max(3, args.steps // 5), args.warmup, stream)
             ach = dalg / (dms * 1e-3) / 1e12
