@@ -115,7 +115,7 @@ class LayerWorkload:
         # projection that reads it (zq_rmsnorm_q4k_gemv); otherwise
         # RMSNorm+Q8_1 first, then one call per projection
         self.fused = (B == 1) if fused is None else fused
-        self.prefetch = True
+        self.prefetch = False   # fused launches pulling the next launch's weights into L2 (--l2-prefetch)
         dev = "cuda"
         self.extra = list(extra or [])
         self.shapes = shapes + self.extra
@@ -593,8 +593,9 @@ def main():
                     choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny", "kquants"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-l2-prefetch", action="store_true",
-                    help="fused decode launches do not pull the next launch's weights into L2")
+    ap.add_argument("--l2-prefetch", action="store_true",
+                    help="fused decode launches pull the next launch's weights into L2 (measured slower on this kernel)")
+    ap.add_argument("--no-l2-prefetch", action="store_true", help="the default; kept for older command lines")
     ap.add_argument("--compare-dequant", action="store_true",
                     help="also time the dequantise-then-GEMM design (cuBLAS) on the 512-token layer")
     ap.add_argument("--decode-path", default="fused", choices=["fused", "two-step"],
@@ -642,7 +643,7 @@ def main():
 
     out = dict(result)
     if wl_dec is not None:
-        wl_dec.prefetch = not args.no_l2_prefetch
+        wl_dec.prefetch = args.l2_prefetch and not args.no_l2_prefetch
         barrier()
         with Clocks(local_rank) as clk:
             ms, _ = bench_workload(torch, wl_dec, args.steps, args.warmup, stream)

@@ -448,7 +448,23 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     // ---------------------------------------------------------- consumers
     // The producer streams weights (written by no kernel) from the start; the
     // activations may come from the previous kernel on the stream, and y may
-    // still be read by it: wait for that kernel before touching either.
+    // still be read by it: wait for that kernel before touching either.  The
+    // RMSNorm weight gamma is a weight too: when the input is short enough to
+    // stay in registers, it is loaded before the wait.
+    constexpr int kGroupsPerPass = kConsumers / 4;   // blocks of 32 values per prologue pass
+    constexpr int kRegPasses = 2;                    // inputs of up to this many passes stay in registers
+    const int grp = tid >> 2, sub = tid & 3;
+    const bool regs = p.x != nullptr && !p.silu && (p.K >> 5) <= kRegPasses * kGroupsPerPass;
+    float4 gr[kRegPasses][2];
+    if (regs) {
+#pragma unroll
+        for (int u = 0; u < kRegPasses; ++u) {
+            const int b = kGroupsPerPass * u + grp;
+            const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
+            gr[u][0] = b < (p.K >> 5) ? __ldg(pg) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gr[u][1] = b < (p.K >> 5) ? __ldg(pg + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     pdl_wait();
     if (p.x == nullptr) {
         // stage the activation rows: codes with the 80-byte group stride,
@@ -487,42 +503,28 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
         const int nblk = p.K >> 5;
         float *part = contrib;                // [nblk]
         float *slot = contrib + kMaxK / 32;   // [256] and r
-        const int grp = tid >> 2, sub = tid & 3;
-        constexpr int kGroupsPerPass = kConsumers / 4;   // 128 blocks per pass
-        constexpr int kUnroll = 3;                       // passes with loads in flight together
-        for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
-            float4 xv[kUnroll][2];
+        constexpr int kUnroll = 3;            // passes with loads in flight together
+        // sum of squares of this group's block: an fma chain through the four lanes in order
+        auto chain = [&](const float4 (&xv)[2]) {
+            float pr = 0.0f;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (base + kGroupsPerPass * u >= nblk) break;   // CTA-uniform
-                const int b = base + kGroupsPerPass * u + grp;
-                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
-                xv[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
-                xv[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            for (int j = 0; j < 4; ++j) {
+                if (sub == j) {
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (base + kGroupsPerPass * u >= nblk) break;
-                float pr = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (sub == j) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            pr = __fmaf_rn(xv[u][h].x, xv[u][h].x, pr);
-                            pr = __fmaf_rn(xv[u][h].y, xv[u][h].y, pr);
-                            pr = __fmaf_rn(xv[u][h].z, xv[u][h].z, pr);
-                            pr = __fmaf_rn(xv[u][h].w, xv[u][h].w, pr);
-                        }
+                    for (int h = 0; h < 2; ++h) {
+                        pr = __fmaf_rn(xv[h].x, xv[h].x, pr);
+                        pr = __fmaf_rn(xv[h].y, xv[h].y, pr);
+                        pr = __fmaf_rn(xv[h].z, xv[h].z, pr);
+                        pr = __fmaf_rn(xv[h].w, xv[h].w, pr);
                     }
-                    pr = __shfl_sync(0xffffffffu, pr, (lane & ~3) | j);
                 }
-                const int b = base + kGroupsPerPass * u + grp;
-                if (sub == 0 && b < nblk) part[b] = pr;
+                pr = __shfl_sync(0xffffffffu, pr, (lane & ~3) | j);
             }
-        }
+            return pr;
+        };
         float r = 1.0f;
-        if (!p.silu) {
+        // the 256 slots and the pairwise tree over the block sums: r
+        auto tree = [&]() {
             named_bar(1, kConsumers);
             if (tid < 256) {
                 float v = 0.0f;
@@ -543,81 +545,128 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             }
             named_bar(1, kConsumers);
             r = slot[256];
-        }
+        };
         __half *ads16 = reinterpret_cast<__half *>(ads);
         const bool out = blockIdx.x == 0 && p.q8out.qs != nullptr;
-        for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
-            float4 xv[kUnroll][2], gv[kUnroll][2];
+        // normalise (or form silu(gate) * up for) block b and pack it into the staging
+        auto pack = [&](int b, const float4 (&xv)[2], const float4 (&gv)[2]) {
+            float xh[8];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (base + kGroupsPerPass * u >= nblk) break;
-                const int b = base + kGroupsPerPass * u + grp;
-                const bool in = b < nblk;
-                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
-                const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    xv[u][h] = in ? __ldg(px + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    gv[u][h] = in ? __ldg(pg + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int h = 0; h < 2; ++h) {
+                if (p.silu) {
+                    xh[4 * h + 0] = silu_mul(xv[h].x, gv[h].x);
+                    xh[4 * h + 1] = silu_mul(xv[h].y, gv[h].y);
+                    xh[4 * h + 2] = silu_mul(xv[h].z, gv[h].z);
+                    xh[4 * h + 3] = silu_mul(xv[h].w, gv[h].w);
+                } else {
+                    xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[h].x, r), gv[h].x);
+                    xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[h].y, r), gv[h].y);
+                    xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[h].z, r), gv[h].z);
+                    xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[h].w, r), gv[h].w);
                 }
             }
+            float amax = 0.0f;
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (base + kGroupsPerPass * u >= nblk) break;
-                const int b = base + kGroupsPerPass * u + grp;
-                float xh[8];
+            for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(xh[c]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const float d = __fdiv_rn(amax, 127.0f);
+            const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+            uint32_t word[2] = {0u, 0u};
+            int qsum = 0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (p.silu) {
-                        xh[4 * h + 0] = silu_mul(xv[u][h].x, gv[u][h].x);
-                        xh[4 * h + 1] = silu_mul(xv[u][h].y, gv[u][h].y);
-                        xh[4 * h + 2] = silu_mul(xv[u][h].z, gv[u][h].z);
-                        xh[4 * h + 3] = silu_mul(xv[u][h].w, gv[u][h].w);
-                    } else {
-                        xh[4 * h + 0] = __fmul_rn(__fmul_rn(xv[u][h].x, r), gv[u][h].x);
-                        xh[4 * h + 1] = __fmul_rn(__fmul_rn(xv[u][h].y, r), gv[u][h].y);
-                        xh[4 * h + 2] = __fmul_rn(__fmul_rn(xv[u][h].z, r), gv[u][h].z);
-                        xh[4 * h + 3] = __fmul_rn(__fmul_rn(xv[u][h].w, r), gv[u][h].w);
-                    }
+            for (int c = 0; c < 8; ++c) {
+                float q = roundf(__fmul_rn(xh[c], id));
+                q = fminf(fmaxf(q, -127.0f), 127.0f);
+                const int qi = (int)q;
+                qsum += qi;
+                word[c >> 2] |= ((uint32_t)(qi & 0xFF)) << (8 * (c & 3));
+            }
+            if constexpr (FMT == kFmtQ6K) {
+                // this lane's 8 codes are chunk k8 = 4b + sub
+                if (b < nblk) reinterpret_cast<int16_t *>(asum)[((b >> 3) * 4 + sub) * 8 + (b & 7)] = (int16_t)qsum;
+            }
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+            if (b < nblk) {
+                *reinterpret_cast<uint2 *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 8 * sub) = make_uint2(word[0], word[1]);
+                const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
+                if (sub == 0) {
+                    ads16[4 * (b >> 1) + (b & 1)] = dh;
+                    ads16[4 * (b >> 1) + 2 + (b & 1)] = sh;
                 }
-                float amax = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(xh[c]));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const float d = __fdiv_rn(amax, 127.0f);
-                const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-                uint32_t word[2] = {0u, 0u};
-                int qsum = 0;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float q = roundf(__fmul_rn(xh[c], id));
-                    q = fminf(fmaxf(q, -127.0f), 127.0f);
-                    const int qi = (int)q;
-                    qsum += qi;
-                    word[c >> 2] |= ((uint32_t)(qi & 0xFF)) << (8 * (c & 3));
-                }
-                if constexpr (FMT == kFmtQ6K) {
-                    // this lane's 8 codes are chunk k8 = 4b + sub
-                    if (b < nblk) reinterpret_cast<int16_t *>(asum)[((b >> 3) * 4 + sub) * 8 + (b & 7)] = (int16_t)qsum;
-                }
-                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-                if (b < nblk) {
-                    *reinterpret_cast<uint2 *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 8 * sub) =
-                        make_uint2(word[0], word[1]);
-                    const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
+                if (out) {
+                    reinterpret_cast<uint2 *>(p.q8out.qs + 32 * b)[sub] = make_uint2(word[0], word[1]);
                     if (sub == 0) {
-                        ads16[4 * (b >> 1) + (b & 1)] = dh;
-                        ads16[4 * (b >> 1) + 2 + (b & 1)] = sh;
+                        reinterpret_cast<__half *>(p.q8out.d)[b] = dh;
+                        reinterpret_cast<__half *>(p.q8out.s)[b] = sh;
                     }
-                    if (out) {
-                        reinterpret_cast<uint2 *>(p.q8out.qs + 32 * b)[sub] = make_uint2(word[0], word[1]);
-                        if (sub == 0) {
-                            reinterpret_cast<__half *>(p.q8out.d)[b] = dh;
-                            reinterpret_cast<__half *>(p.q8out.s)[b] = sh;
-                        }
+                }
+            }
+        };
+        if (regs) {
+            // short input: x read once into registers (gamma is already there),
+            // one round trip to memory after the wait instead of two
+            float4 xr[kRegPasses][2];
+#pragma unroll
+            for (int u = 0; u < kRegPasses; ++u) {
+                const int b = kGroupsPerPass * u + grp;
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kRegPasses; ++u) {
+                if (kGroupsPerPass * u >= nblk) break;   // CTA-uniform
+                const int b = kGroupsPerPass * u + grp;
+                const float pr = chain(xr[u]);
+                if (sub == 0 && b < nblk) part[b] = pr;
+            }
+            tree();
+#pragma unroll
+            for (int u = 0; u < kRegPasses; ++u) {
+                if (kGroupsPerPass * u >= nblk) break;
+                pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
+            }
+        } else {
+            for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
+                float4 xv[kUnroll][2];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (base + kGroupsPerPass * u >= nblk) break;   // CTA-uniform
+                    const int b = base + kGroupsPerPass * u + grp;
+                    const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                    xv[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xv[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (base + kGroupsPerPass * u >= nblk) break;
+                    const int b = base + kGroupsPerPass * u + grp;
+                    const float pr = chain(xv[u]);
+                    if (sub == 0 && b < nblk) part[b] = pr;
+                }
+            }
+            if (!p.silu) tree();
+            for (int base = 0; base < nblk; base += kGroupsPerPass * kUnroll) {
+                float4 xv[kUnroll][2], gv[kUnroll][2];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (base + kGroupsPerPass * u >= nblk) break;
+                    const int b = base + kGroupsPerPass * u + grp;
+                    const bool in = b < nblk;
+                    const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                    const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        xv[u][h] = in ? __ldg(px + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        gv[u][h] = in ? __ldg(pg + h) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (base + kGroupsPerPass * u >= nblk) break;
+                    pack(base + kGroupsPerPass * u + grp, xv[u], gv[u]);
                 }
             }
         }

@@ -52,6 +52,12 @@
  *   failure on the calling thread.
  * - Calls may be captured in a CUDA graph after one uncaptured call of the
  *   same entry point on the device (the first call sets kernel attributes).
+ * - Kernels are launched with programmatic dependent launch: each may start
+ *   while the previous kernel on the stream finishes, and waits for it before
+ *   it reads activations or writes outputs.  Weights -- W, and gamma of the
+ *   fused RMSNorm calls -- are read before that wait, so they must be complete
+ *   in memory before the call is made (weights loaded at start-up are; a
+ *   kernel that rewrites them needs a stream or event synchronisation first).
  */
 #ifndef ZQ_H
 #define ZQ_H
