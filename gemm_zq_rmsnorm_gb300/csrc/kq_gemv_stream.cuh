@@ -210,6 +210,54 @@ __device__ __forceinline__ float q4k_block_part(const uint8_t *blk, int p, int b
     return fmaf(dd.x, main, -dd.y * mins);
 }
 
+// ---- Q4_K with several tokens: lane p decodes sub-blocks 2p and 2p+1 once ----
+struct Q4Lane {
+    uint4 q0, q1;            // the 32 nibble bytes (low nibbles: sub-block 2p, high: 2p+1)
+    uint32_t sc, mn;         // scales / mins of the two sub-blocks (bytes 0, 1)
+    float d, dmin;
+};
+
+__device__ __forceinline__ void q4k_decode(const uint8_t *blk, int p, Q4Lane &w)
+{
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    w.q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);
+    w.q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * p);
+    pair_scales(hdr, p, w.sc, w.mn);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2 *>(&hdr.x));
+    w.d = dd.x;
+    w.dmin = dd.y;
+}
+
+// the arithmetic of q4k_block_part for one token's activations
+__device__ __forceinline__ float q4k_dot(const Q4Lane &w, const uint4 (&a)[4], uint2 ds)
+{
+    constexpr uint32_t LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+    int I0 = 0, I1 = 0;
+    I0 = dp4a_us(w.q0.x & LO, a[0].x, I0);
+    I1 = dp4a_us(w.q0.x & HI, a[2].x, I1);
+    I0 = dp4a_us(w.q0.y & LO, a[0].y, I0);
+    I1 = dp4a_us(w.q0.y & HI, a[2].y, I1);
+    I0 = dp4a_us(w.q0.z & LO, a[0].z, I0);
+    I1 = dp4a_us(w.q0.z & HI, a[2].z, I1);
+    I0 = dp4a_us(w.q0.w & LO, a[0].w, I0);
+    I1 = dp4a_us(w.q0.w & HI, a[2].w, I1);
+    I0 = dp4a_us(w.q1.x & LO, a[1].x, I0);
+    I1 = dp4a_us(w.q1.x & HI, a[3].x, I1);
+    I0 = dp4a_us(w.q1.y & LO, a[1].y, I0);
+    I1 = dp4a_us(w.q1.y & HI, a[3].y, I1);
+    I0 = dp4a_us(w.q1.z & LO, a[1].z, I0);
+    I1 = dp4a_us(w.q1.z & HI, a[3].z, I1);
+    I0 = dp4a_us(w.q1.w & LO, a[1].w, I0);
+    I1 = dp4a_us(w.q1.w & HI, a[3].w, I1);
+    const int J0 = (int)(w.sc & 0xFFu) * I0;
+    const int J1 = (int)(w.sc >> 8) * (I1 >> 4);
+    const float2 d8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.x));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2 *>(&ds.y));
+    const float main = fmaf(d8.y, (float)J1, d8.x * (float)J0);
+    const float mins = fmaf((float)(w.mn >> 8), s8.y, (float)(w.mn & 0xFFu) * s8.x);
+    return fmaf(w.d, main, -w.dmin * mins);
+}
+
 // ---- Q5_K: lane p decodes the 5-bit quants of sub-blocks 2p and 2p+1 ----
 struct Q5Lane {
     uint32_t q0[8], q1[8];   // quants 0..31, four per word, sub-blocks 2p and 2p+1
@@ -367,7 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
 {
     constexpr int kBytes = Fmt<FMT>::kBytes;
     constexpr bool kAligned = (kBytes % 16) == 0;
-    static_assert(FMT != kFmtQ4K || NT == 1, "Q4_K small batches run on the tensor-core kernel");
     extern __shared__ __align__(1024) uint8_t smem[];
     const SmemLayout L(p.K, p.stage_alloc, NT, FMT == kFmtQ6K);
     uint8_t *ring = smem + L.ring;
@@ -716,22 +763,25 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             auto block = [&](const uint8_t *rowp, int lb, float (&out)[NT]) {
                 const uint8_t *blk = rowp + (size_t)lb * kBytes;
                 const int b = bbase + lb;        // super-block index in the row
-                if constexpr (FMT == kFmtQ4K) {
+                if constexpr (FMT == kFmtQ4K && NT == 1) {
                     out[0] = q4k_block_part(blk, pp, b, aq, ads);
                 } else {
-                    typename std::conditional<FMT == kFmtQ5K, Q5Lane, Q6Lane>::type w;
-                    if constexpr (FMT == kFmtQ5K) q5k_decode(blk, pp, w);
+                    typename std::conditional<FMT == kFmtQ4K, Q4Lane,
+                        typename std::conditional<FMT == kFmtQ5K, Q5Lane, Q6Lane>::type>::type w;
+                    if constexpr (FMT == kFmtQ4K) q4k_decode(blk, pp, w);
+                    else if constexpr (FMT == kFmtQ5K) q5k_decode(blk, pp, w);
                     else q6k_decode(blk, pp, w);
 #pragma unroll
                     for (int tk = 0; tk < NT; ++tk) {
                         if (tk < p.ntok) {
-                            if constexpr (FMT == kFmtQ5K) {
+                            if constexpr (FMT != kFmtQ6K) {
                                 const uint8_t *ap = aq + tk * tq + 80 * (4 * b + pp);
                                 const uint4 a[4] = {*reinterpret_cast<const uint4 *>(ap),
                                                     *reinterpret_cast<const uint4 *>(ap + 16),
                                                     *reinterpret_cast<const uint4 *>(ap + 32),
                                                     *reinterpret_cast<const uint4 *>(ap + 48)};
-                                out[tk] = q5k_dot(w, a, ads[tk * tds + 4 * b + pp]);
+                                if constexpr (FMT == kFmtQ4K) out[tk] = q4k_dot(w, a, ads[tk * tds + 4 * b + pp]);
+                                else out[tk] = q5k_dot(w, a, ads[tk * tds + 4 * b + pp]);
                             } else {
                                 out[tk] = q6k_dot(w, aq + tk * tq + 320 * b, ads + tk * tds + 4 * b,
                                                   asum[tk * tas + 4 * b + pp], pp);

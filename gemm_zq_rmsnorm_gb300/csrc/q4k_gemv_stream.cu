@@ -1,6 +1,7 @@
 // q4k_gemv_stream.cu -- the Q4_K instance of the streamed decode mat-vec
 // (kq_gemv_stream.cuh): plain, paired and up-to-four-matrix launches, with
-// Q8_1 input or with RMSNorm (or SiLU(gate)*up) + Q8_1 packing in the launch.
+// Q8_1 input or with RMSNorm (or SiLU(gate)*up) + Q8_1 packing in the launch;
+// and small batches of tokens (launches of four) for the chunked prefill.
 //
 // MIInfer README, "Status": Q4_K x Q8_1 MMVQ-style projections (FFN down,
 // shared gate/up; Q4_K metadata staging; packed int8 dot4).  ZINC docs "ROCm
@@ -19,6 +20,11 @@ cudaError_t launch_gemv_stream(const GemvJob &job, int K, zq_q8_1 a, cudaStream_
     p.d = reinterpret_cast<const __half *>(a.d);
     p.s = reinterpret_cast<const __half *>(a.s);
     return stream::launch_stream<stream::kFmtQ4K, 1>(p, job, K, 1, st);
+}
+
+cudaError_t launch_q4k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st)
+{
+    return stream::launch_tokens<stream::kFmtQ4K>(W, N, K, a, B, y, st);
 }
 
 cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,

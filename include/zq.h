@@ -178,8 +178,10 @@ ZQ_API int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, in
  *     tensor cores read, each Q8_1 value q8*d8 split into two binary16
  *     numbers, and a per-token scale; its contents on entry do not matter and
  *     are not preserved.
- * B = 1 runs the decode mat-vec.  B >= 2 runs the tensor cores on tiles of
- * 128 tokens x 128 weight rows (2 <= B <= 16: the chunk sizes, one partly
+ * B = 1 runs the decode mat-vec; 2 <= B <= 4 (K <= 32768) the same streamed
+ * kernel with the tokens staged together, each decoded weight used for all of
+ * them (the workspace is not touched).  B >= 5 runs the tensor cores on tiles
+ * of 128 tokens x 128 weight rows (5 <= B <= 16: the chunk sizes, one partly
  * filled token tile whose weights are unpacked once and shared).  There every
  * product of an activation part and a weight code sc*q4 is exact and the
  * products are summed in fp32 per 256-weight super-block, then scaled by

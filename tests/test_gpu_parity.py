@@ -199,7 +199,7 @@ def run_gemm(W, N, K, a, B):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("B,K,N", [(2, 512, 50), (4, 1024, 129), (5, 768, 64), (8, 256, 300),
+@pytest.mark.parametrize("B,K,N", [(2, 512, 50), (3, 2048, 257), (4, 1024, 129), (4, 17408, 40), (5, 768, 64), (8, 256, 300),
                                    (16, 1280, 130), (17, 512, 96), (130, 768, 200), (256, 1024, 256)])
 def test_gemm_small_all_outputs(B, K, N):
     x, g, W = make_layer_inputs(20 + B, B, K, N)
