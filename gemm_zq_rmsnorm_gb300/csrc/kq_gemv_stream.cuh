@@ -1,15 +1,15 @@
-// kq_gemv_stream.cuh -- decode mat-vec of k-quant weights (Q4_K, Q5_K, Q6_K)
-// against Q8_1 activations, with the weights streamed through shared memory
-// by bulk (TMA) copies.  Instantiated per weight format (and token count) in
-// q4k_gemv_stream.cu and kq_gemv_q56k.cu.
+// kq_gemv_stream.cuh -- mat-vec of k-quant weights (Q4_K, Q5_K, Q6_K) against
+// Q8_1 activations of one to a few tokens, with the weights streamed through
+// shared memory by bulk (TMA) copies.  Instantiated per weight format and
+// token count in q4k_gemv_stream.cu, kq_gemv_q5k.cu and kq_gemv_q6k.cu.
 //
 // MIInfer README, "Status": Q4_K x Q8_1 MMVQ-style projections (FFN down,
 // shared gate/up; Q4_K metadata staging; packed int8 dot4; activations reused
 // from on-chip memory), the Q5_K x Q8_1 MMVQ-style recurrent output
 // projection (scale/min hoisting, paired nibbles) and the MMVQ-style Q6_K x
-// Q8_1 LM head.  ZINC docs "ROCm backend", "Build and verify": paired Q4
-// projections; packed Q8 activations for the hot Q4_K, Q5_K and Q6_K
-// projections.
+// Q8_1 LM head; "Current phase": token-batched B = 4 projections.  ZINC docs
+// "ROCm backend", "Build and verify": paired Q4 projections; packed Q8
+// activations for the hot Q4_K, Q5_K and Q6_K projections.
 //
 // The mat-vec is bound by HBM bandwidth: every weight byte is read exactly
 // once.  To keep enough bytes in flight independently of register pressure,
@@ -17,13 +17,20 @@
 // of contiguous weight tiles (R whole rows, or a piece of one long row; rows
 // are contiguous, so a tile is one copy) into a ring of large shared-memory
 // stages, completing on mbarriers.  Sixteen consumer warps decode the
-// super-blocks from shared memory in groups of four lanes -- lane p takes the
-// 64 weights of Q8_1 blocks 2p and 2p+1 of the super-block -- and form the
-// integer sub-block sums with dp4a against the Q8_1 activation rows staged
-// once per CTA.  A group walks a strided segment of one row (up to four
-// blocks), applies the scales in fp32 and accumulates in registers; after the
-// stage the segments of each row are summed in a fixed order into y.  Up to
-// four matrices that read the same input (q/k/v, gate/up) share one launch.
+// super-blocks from shared memory in groups of four lanes, form the integer
+// sub-block sums with dp4a against the activation rows staged once per CTA,
+// apply the scales in fp32 and accumulate in registers.  Lane p of a group
+// takes sub-blocks 2p and 2p+1 of a Q4_K / Q5_K block; for Q6_K it takes
+// positions 8p..8p+7 of all eight 32-weight quarters, so the four lanes read
+// disjoint bytes of the 210-byte block.
+//
+// Rows are split into segments of task groups.  When a stage holds enough
+// rows, a row's segments sit in one warp, which reduces the row with shuffles
+// and releases the stage on its own (warp-local rows, handed out round-robin
+// across stages); long rows are split over more groups and reduced through
+// shared memory after a CTA barrier.  Either way a row's summation order is a
+// function of K, so every launch form gives the same y for a row.  Up to four
+// matrices that read the same input (q/k/v, gate/up) share one launch.
 //
 // Q6_K blocks are 210 bytes, so rows and blocks are only 2-byte aligned.  The
 // producer copies each tile from the 16-byte boundary below it (the bytes of
@@ -35,10 +42,11 @@
 // compute RMSNorm and the Q8_1 packing of x themselves, in the canonical order
 // of the RMSNorm+Q8_1 kernel (same bytes), straight into the shared-memory
 // staging, while the producer already streams weights: the normalised input
-// never goes through HBM and the separate launch disappears.
+// never goes through HBM and the separate launch disappears.  The same
+// prologue forms silu(gate) * up instead for the down projection.
 //
 // With NT > 1 the CTA stages NT tokens and every decoded weight is used for
-// all of them (Q5_K and Q6_K small-batch projections).
+// all of them (chunked-prefill batches of up to four tokens).
 #pragma once
 
 #include <type_traits>
