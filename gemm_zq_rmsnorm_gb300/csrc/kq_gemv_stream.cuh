@@ -118,10 +118,14 @@ __device__ __forceinline__ int group_mat(const StreamParams &p, int g)
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Activation codes are stored with 16 bytes of padding after every 64: the
-// 64-byte group g (Q8_1 block pair) starts at 80*g.  The eight lanes of a
-// quarter-warp (two consecutive super-blocks x four pairs) then start in
-// eight different 16-byte bank groups.
-__host__ __device__ constexpr size_t act_bytes(int K) { return (size_t)K / 64 * 80; }
+// 64-byte group (Q8_1 block pair) q of super-block b starts at sb*b + 80*q,
+// sb = 320.  The eight lanes of a quarter-warp (two consecutive super-blocks x
+// four pairs) then start in eight different 16-byte bank groups.  The Q6_K
+// lanes read 8 bytes at the same offset of four neighbouring super-blocks
+// instead; a super-block stride of 352 bytes (88 words) puts those four reads
+// on disjoint banks.
+__host__ __device__ constexpr int act_sb(bool q6) { return q6 ? 352 : 320; }
+__host__ __device__ constexpr size_t act_bytes(int K, bool q6) { return (size_t)K / 256 * act_sb(q6); }
 // d8 pair and s8 pair (binary16) per Q8_1 block pair
 __host__ __device__ constexpr size_t ads_bytes(int K) { return (size_t)K / 64 * 8; }
 
@@ -135,7 +139,7 @@ struct SmemLayout {
     {
         ring = 0;
         act_qs = ring + (size_t)kStages * stage_alloc;
-        act_ds = align_up(act_qs + (size_t)nt * act_bytes(K), 16);
+        act_ds = align_up(act_qs + (size_t)nt * act_bytes(K, sums), 16);
         act_sum = align_up(act_ds + (size_t)nt * ads_bytes(K), 16);
         contrib = align_up(act_sum + (sums ? (size_t)nt * K / 4 : 0), 16);
         bars = align_up(contrib + (size_t)nt * kStages * kMaxBlk * 4, 8);
@@ -178,10 +182,11 @@ __device__ __forceinline__ void pair_scales(const uint4 &hdr, int p, uint32_t &s
 __device__ __forceinline__ float q4k_block_part(const uint8_t *blk, int p, int b, const uint8_t *aq,
                                                 const uint2 *ads)
 {
+    // (Q4_K staging: super-block stride 320)
     const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
     const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);
     const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * p);
-    const uint8_t *ap = aq + 80 * (4 * b + p);
+    const uint8_t *ap = aq + 320 * b + 80 * p;
     const uint4 a00 = *reinterpret_cast<const uint4 *>(ap);
     const uint4 a01 = *reinterpret_cast<const uint4 *>(ap + 16);
     const uint4 a10 = *reinterpret_cast<const uint4 *>(ap + 32);
@@ -438,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const size_t tq = act_bytes(p.K);          // staging stride of one token's codes
+    constexpr int kSB = act_sb(FMT == kFmtQ6K); // staging stride of one super-block's codes
+    const size_t tq = act_bytes(p.K, FMT == kFmtQ6K);   // and of one token's
     const int tds = p.K / 64;                  // and of its d8/s8 pairs (uint2 units)
     const int tas = p.K / 64;                  // and of its 8-code sums (uint4 units)
 
@@ -530,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             int16_t *at = reinterpret_cast<int16_t *>(asum + t * tas);
             for (int c = tid; c < p.K / 16; c += kConsumers) {
                 const uint4 v = __ldg(gq + c);
-                *reinterpret_cast<uint4 *>(aqt + 80 * (c >> 2) + 16 * (c & 3)) = v;
+                *reinterpret_cast<uint4 *>(aqt + kSB * (c >> 4) + 80 * ((c >> 2) & 3) + 16 * (c & 3)) = v;
                 if constexpr (FMT == kFmtQ6K) {
                     // 8-code chunks 2c and 2c+1: super-block k8 / 32, lane k8 % 4, Q8_1 block (k8 % 32) / 4
 #pragma unroll
@@ -644,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
             qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
             if (b < nblk) {
-                *reinterpret_cast<uint2 *>(aq + 80 * (b >> 1) + 32 * (b & 1) + 8 * sub) = make_uint2(word[0], word[1]);
+                *reinterpret_cast<uint2 *>(aq + kSB * (b >> 3) + 80 * ((b >> 1) & 3) + 32 * (b & 1) + 8 * sub) =
+                    make_uint2(word[0], word[1]);
                 const __half dh = __float2half_rn(d), sh = __float2half_rn(__fmul_rn(d, (float)qsum));
                 if (sub == 0) {
                     ads16[4 * (b >> 1) + (b & 1)] = dh;
@@ -783,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                     for (int tk = 0; tk < NT; ++tk) {
                         if (tk < p.ntok) {
                             if constexpr (FMT != kFmtQ6K) {
-                                const uint8_t *ap = aq + tk * tq + 80 * (4 * b + pp);
+                                const uint8_t *ap = aq + tk * tq + kSB * b + 80 * pp;
                                 const uint4 a[4] = {*reinterpret_cast<const uint4 *>(ap),
                                                     *reinterpret_cast<const uint4 *>(ap + 16),
                                                     *reinterpret_cast<const uint4 *>(ap + 32),
@@ -791,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                                 if constexpr (FMT == kFmtQ4K) out[tk] = q4k_dot(w, a, ads[tk * tds + 4 * b + pp]);
                                 else out[tk] = q5k_dot(w, a, ads[tk * tds + 4 * b + pp]);
                             } else {
-                                out[tk] = q6k_dot(w, aq + tk * tq + 320 * b, ads + tk * tds + 4 * b,
+                                out[tk] = q6k_dot(w, aq + tk * tq + kSB * b, ads + tk * tds + 4 * b,
                                                   asum[tk * tas + 4 * b + pp], pp);
                             }
                         } else {
