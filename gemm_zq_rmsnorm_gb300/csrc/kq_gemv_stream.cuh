@@ -513,11 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     // RMSNorm weight gamma is a weight too: when the input is short enough to
     // stay in registers, it is loaded before the wait.
     constexpr int kGroupsPerPass = kConsumers / 4;   // blocks of 32 values per prologue pass
-    constexpr int kRegPasses = 2;                    // inputs of up to this many passes stay in registers
+    constexpr int kRegPasses = 2;                    // x and gamma of up to this many passes stay in registers
+    constexpr int kXPasses = 5;                      // x alone of up to this many passes stays in registers
     const int grp = tid >> 2, sub = tid & 3;
     const bool regs = p.x != nullptr && !p.silu && (p.K >> 5) <= kRegPasses * kGroupsPerPass;
+    const bool xregs = p.x != nullptr && !p.silu && !regs && (p.K >> 5) <= kXPasses * kGroupsPerPass;
     float4 gr[kRegPasses][2];
-    if (regs) {
+    if (regs || xregs) {
 #pragma unroll
         for (int u = 0; u < kRegPasses; ++u) {
             const int b = kGroupsPerPass * u + grp;
@@ -689,6 +691,43 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             for (int u = 0; u < kRegPasses; ++u) {
                 if (kGroupsPerPass * u >= nblk) break;
                 pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
+            }
+        } else if (xregs) {
+            // medium input (K <= 20480): x read once into registers; gamma of
+            // the first two passes is already there, the rest is loaded while
+            // those are packed -- two round trips after the wait instead of four
+            float4 xr[kXPasses][2];
+#pragma unroll
+            for (int u = 0; u < kXPasses; ++u) {
+                const int b = kGroupsPerPass * u + grp;
+                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kXPasses; ++u) {
+                if (kGroupsPerPass * u >= nblk) break;   // CTA-uniform
+                const int b = kGroupsPerPass * u + grp;
+                const float pr = chain(xr[u]);
+                if (sub == 0 && b < nblk) part[b] = pr;
+            }
+            tree();
+            // the first two passes first, so their registers are free before
+            // the rest of gamma arrives
+#pragma unroll
+            for (int u = 0; u < kRegPasses; ++u) pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
+            float4 g2[kXPasses - kRegPasses][2];
+#pragma unroll
+            for (int u = 0; u < kXPasses - kRegPasses; ++u) {
+                const int b = kGroupsPerPass * (u + kRegPasses) + grp;
+                const float4 *pg = reinterpret_cast<const float4 *>(p.gamma + 32 * b) + 2 * sub;
+                g2[u][0] = b < nblk ? __ldg(pg) : make_float4(0.f, 0.f, 0.f, 0.f);
+                g2[u][1] = b < nblk ? __ldg(pg + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kXPasses - kRegPasses; ++u) {
+                if (kGroupsPerPass * (u + kRegPasses) >= nblk) break;
+                pack(kGroupsPerPass * (u + kRegPasses) + grp, xr[u + kRegPasses], g2[u]);
             }
         } else {
             for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {

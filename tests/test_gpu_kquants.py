@@ -43,7 +43,7 @@ def run(fmt, W, N, K, q8):
 SMALL = [  # (N, K, B)
     (1, 256, 1), (7, 256, 1), (7, 256, 3), (300, 768, 1), (300, 768, 4), (300, 768, 5),
     (513, 1024, 2), (129, 2816, 16), (1000, 5120, 1), (64, 5120, 8), (5, 32768, 1), (5, 32768, 4),
-    (3, 32768, 6)]
+    (3, 32768, 6), (70, 29696, 4)]   # 29696: the largest K whose four-token Q6_K staging fits
 
 
 @pytest.mark.parametrize("fmt", ["q5k", "q6k"])
