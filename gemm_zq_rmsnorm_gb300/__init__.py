@@ -331,7 +331,7 @@ def debug_q4k_isums(W: torch.Tensor, N: int, K: int, a: Q8_1, path: int = 0,
     B = a.B
     dev = a.qs.device
     isums = torch.empty((B, N, K // 32), dtype=torch.int32, device=dev)
-    need = gemm_workspace_bytes(N, K, B) if path else 0
+    need = 2 * B * K if path else 0   # the binary16 copy of the codes (paths 1, 2)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -306,7 +306,7 @@ int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, in
 size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B)
 {
     if (N < 1 || K < 256 || K % 256 || B < 1) return 0;
-    return gemm_tc_workspace_bytes(N, K, B);
+    return chunk_streams(B, K) ? 0 : gemm_tc_workspace_bytes(N, K, B);
 }
 
 int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *workspace,
@@ -318,7 +318,7 @@ int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *w
     if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_q4k_gemm: B = %d must be in [1, 65536]", B);
     if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemm: null y");
     if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm: y must be 16-byte aligned");
-    const size_t need = gemm_tc_workspace_bytes(N, K, B);
+    const size_t need = chunk_streams(B, K) ? 0 : gemm_tc_workspace_bytes(N, K, B);
     if (need && (!workspace || workspace_bytes < need))
         return fail(ZQ_ERR_WORKSPACE, "zq_q4k_gemm: workspace of %zu bytes required, got %zu", need,
                     workspace ? workspace_bytes : (size_t)0);
@@ -341,7 +341,7 @@ int zq_q4k_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
     if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "zq_q4k_gemm_noalloc: B = %d must be in [1, 65536]", B);
     if (!y) return fail(ZQ_ERR_ARG, "zq_q4k_gemm_noalloc: null y");
     if (!aligned16(y)) return fail(ZQ_ERR_ALIGN, "zq_q4k_gemm_noalloc: y must be 16-byte aligned");
-    const size_t need = gemm_tc_workspace_bytes(N, K, B, false);
+    const size_t need = chunk_streams(B, K) ? 0 : gemm_tc_workspace_bytes(N, K, B, false);
     if (need > noalloc_scratch_bytes())
         return fail(ZQ_ERR_WORKSPACE,
                     "zq_q4k_gemm_noalloc: B*K = %lld needs %zu bytes of scratch, more than the built-in %zu "
@@ -502,7 +502,7 @@ int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B, int32_t *i
     if (path == 1 && B < 17) return fail(ZQ_ERR_SHAPE, "zq_debug_q4k_isums: path 1 needs B >= 17");
     if (path == 2 && (B < 2 || B > 16)) return fail(ZQ_ERR_SHAPE, "zq_debug_q4k_isums: path 2 needs 2 <= B <= 16");
     if (path != 0) {
-        const size_t need = gemm_tc_workspace_bytes(N, K, B);
+        const size_t need = (size_t)2 * B * K;   // the binary16 copy of the activation codes
         if (need && (!workspace || workspace_bytes < need))
             return fail(ZQ_ERR_WORKSPACE, "zq_debug_q4k_isums: workspace of %zu bytes required", need);
     }

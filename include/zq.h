@@ -173,7 +173,8 @@ ZQ_API int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, in
  * token-batched chunk projections and tensor-core/int8 GEMM prefill).
  *   W : Q4_K N x K;  a : Q8_1 of B tokens;  y : fp32 [B][N].
  *   workspace / workspace_bytes : caller-owned device scratch of at least
- *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0;
+ *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0,
+ *     as it is for B = 1 and for 2 <= B <= 4 with K <= 32768; at least
  *     4*B*K + 4*B rounded up to 256 otherwise).  It holds the activations the
  *     tensor cores read, each Q8_1 value q8*d8 split into two binary16
  *     numbers, and a per-token scale; its contents on entry do not matter and
@@ -327,8 +328,8 @@ ZQ_API int zq_version(void);
  * dot4 (dp4a) inner product of the mat-vec kernels, any B; paths 1 (B >= 17)
  * and 2 (2 <= B <= 16): tcgen05 MMAs on the projection's tile layout, fp16
  * operands holding q8 and q4 exactly, one K = 32 accumulator per sub-block
- * read back from tensor memory.  For paths 1 and 2 the workspace rules of
- * zq_q4k_gemm apply.
+ * read back from tensor memory.  Paths 1 and 2 need a device workspace of
+ * at least 2*B*K bytes (the binary16 copy of the codes); path 0 none.
  */
 ZQ_API int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B,
                        int32_t *isums, int path, void *workspace,

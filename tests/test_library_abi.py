@@ -180,3 +180,18 @@ def test_kquant_gemm_rejects(lib, fn, W, N, K, B, y, status):
     (A16, A16, 33024, -2)])
 def test_rmsnorm_q6k_gemv_rejects(lib, x, W, K, status):
     assert lib.zq_rmsnorm_q6k_gemv(x, A16, 1e-6, K, W, 64, A16, None, None) == status
+
+
+def test_chunk_workspace_query(lib):
+    """B = 2..4 run on the streamed mat-vec and need no workspace; from B = 5
+    the tensor-core path needs the split activations."""
+    for B in (1, 2, 3, 4):
+        assert lib.zq_q4k_gemm_workspace_bytes(64, 1024, B) == 0
+    assert lib.zq_q4k_gemm_workspace_bytes(64, 1024, 5) >= 4 * 5 * 1024 + 4 * 5
+    assert lib.zq_q4k_gemm_workspace_bytes(64, 33024, 4) > 0      # K above the staging limit
+    # no workspace needed at B = 4: validation passes, the missing device is reported
+    assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 4, A16, None, 0, None) == -5
+    assert lib.zq_q4k_gemm(A16, 64, 1024, q8(), 5, A16, None, 0, None) == -6
+    # the integer-sum hook's tensor-core paths need 2*B*K bytes
+    assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024 - 1, None) == -6
+    assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024, None) == -5
