@@ -29,7 +29,7 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
            "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
-           "zq_q5k_bytes", "zq_q6k_bytes")
+           "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan")
 
 
 class ZQError(RuntimeError):
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_rmsnorm_q6k_gemv": ([P, P, f, i, P, i, P, ctypes.POINTER(_Q8), P], i),
         "zq_q5k_bytes": ([i, i], sz),
         "zq_q6k_bytes": ([i, i], sz),
+        "zq_debug_stream_plan": ([i, i, i, ctypes.c_longlong, i, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -314,6 +315,14 @@ def rmsnorm_q6k_gemv(x: torch.Tensor, gamma: torch.Tensor, eps: float, W: torch.
     q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
     _check(lib.zq_rmsnorm_q6k_gemv(_ptr(x), _ptr(gamma), float(eps), K, _ptr(W), N, _ptr(y), q8, _stream(stream)))
     return y
+
+
+def debug_stream_plan(wtype: int, ntok: int, K: int, total_rows: int, sms: int = 152) -> dict:
+    """Launch plan of the streamed mat-vec (host-side; see zq_debug_stream_plan)."""
+    out = (ctypes.c_int32 * 8)()
+    _check(load().zq_debug_stream_plan(wtype, ntok, K, total_rows, sms, ctypes.cast(out, ctypes.c_void_p)))
+    keys = ("R", "P", "CB", "nseg", "wl", "stage_alloc", "smem", "rowbytes")
+    return dict(zip(keys, list(out)))
 
 
 def device_status(clear: bool = False) -> int:

@@ -963,33 +963,24 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     }
 }
 
-// Host side: tile the job, size the stages and launch.  Returns
-// cudaErrorInvalidValue when the activation staging does not fit.
+// The launch plan -- rows per stage, pieces, segments, warp-local mode, stage
+// size -- for K columns, totalN rows in all and sms CTAs: a pure host
+// computation (checked on the CPU through zq_debug_stream_plan).  Returns false
+// when the activation staging leaves no room for the stages.
 template <int FMT, int NT>
-cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, cudaStream_t st)
+bool plan_stream(StreamParams &p, int K, long long totalN, int sms)
 {
     constexpr int kBytes = Fmt<FMT>::kBytes;
     // an unaligned tile is copied from up to 14 bytes below its start to up to
     // 14 bytes past its end; the last block's aligned loads read 2 bytes past it
     constexpr uint32_t kSlack = (kBytes % 16) ? 32 : 0;
-    static size_t attr_bytes[64];
-    p.nmat = job.nmat;
-    p.ntok = ntok;
-    long long totalN = 0;
-    for (int m = 0; m < job.nmat; ++m) {
-        p.W[m] = static_cast<const uint8_t *>(job.W[m]);
-        p.y[m] = job.y[m];
-        p.N[m] = job.N[m];
-        totalN += job.N[m];
-    }
     p.K = K;
     p.nb = K / 256;
     p.rowbytes = (uint32_t)p.nb * kBytes;
-    const int sms = num_sms();
     // stage size: as large as shared memory allows (<= 64 KB), but small
     // enough that every CTA gets >= 3 stages of work
     const size_t fixed = SmemLayout(K, 0, NT, FMT == kFmtQ6K).total;
-    if (fixed + (size_t)kStages * align_up(kBytes + kSlack, 128) > (size_t)kSmemLimit) return cudaErrorInvalidValue;
+    if (fixed + (size_t)kStages * align_up(kBytes + kSlack, 128) > (size_t)kSmemLimit) return false;
     size_t cap = (kSmemLimit - fixed) / kStages / 128 * 128;
     cap = cap > (size_t)kStageMax ? (size_t)kStageMax : cap;
     const double total = (double)totalN * p.rowbytes;
@@ -1039,6 +1030,33 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
         p.P = (p.nb + p.CB - 1) / p.CB;
         p.stage_alloc = (uint32_t)align_up((size_t)p.CB * kBytes + kSlack, 128);
     }
+    return true;
+}
+
+// Bytes of dynamic shared memory a plan uses.
+template <int FMT, int NT>
+size_t plan_smem(const StreamParams &p)
+{
+    return SmemLayout(p.K, p.stage_alloc, NT, FMT == kFmtQ6K).total;
+}
+
+// Host side: tile the job, size the stages and launch.  Returns
+// cudaErrorInvalidValue when the activation staging does not fit.
+template <int FMT, int NT>
+cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, cudaStream_t st)
+{
+    static size_t attr_bytes[64];
+    p.nmat = job.nmat;
+    p.ntok = ntok;
+    long long totalN = 0;
+    for (int m = 0; m < job.nmat; ++m) {
+        p.W[m] = static_cast<const uint8_t *>(job.W[m]);
+        p.y[m] = job.y[m];
+        p.N[m] = job.N[m];
+        totalN += job.N[m];
+    }
+    const int sms = num_sms();
+    if (!plan_stream<FMT, NT>(p, K, totalN, sms)) return cudaErrorInvalidValue;
     p.gstart[0] = 0;
     for (int m = 0; m < kMaxMats; ++m)
         p.gstart[m + 1] = p.gstart[m] + (m < job.nmat ? (job.N[m] + p.R - 1) / p.R : 0);

@@ -34,4 +34,28 @@ cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, 
     return stream::launch_fused<stream::kFmtQ4K>(job, K, x, gamma, eps, silu, q8out, pf, pf_bytes, st);
 }
 
+// Launch plan of the streamed kernel (host only): out = R, P, CB, nseg,
+// warp-local, stage bytes, dynamic shared memory, row bytes.
+bool stream_plan_query(int fmt, int nt, int K, long long total_rows, int sms, int32_t *out)
+{
+    stream::StreamParams p{};
+    bool ok = false;
+    size_t smem = 0;
+    auto run = [&](auto plan, auto smem_of) {
+        ok = plan(p, K, total_rows, sms);
+        if (ok) smem = smem_of(p);
+    };
+    if (fmt == 4 && nt == 1) run(stream::plan_stream<stream::kFmtQ4K, 1>, stream::plan_smem<stream::kFmtQ4K, 1>);
+    else if (fmt == 4 && nt == 4) run(stream::plan_stream<stream::kFmtQ4K, 4>, stream::plan_smem<stream::kFmtQ4K, 4>);
+    else if (fmt == 5 && nt == 1) run(stream::plan_stream<stream::kFmtQ5K, 1>, stream::plan_smem<stream::kFmtQ5K, 1>);
+    else if (fmt == 5 && nt == 4) run(stream::plan_stream<stream::kFmtQ5K, 4>, stream::plan_smem<stream::kFmtQ5K, 4>);
+    else if (fmt == 6 && nt == 1) run(stream::plan_stream<stream::kFmtQ6K, 1>, stream::plan_smem<stream::kFmtQ6K, 1>);
+    else if (fmt == 6 && nt == 4) run(stream::plan_stream<stream::kFmtQ6K, 4>, stream::plan_smem<stream::kFmtQ6K, 4>);
+    else return false;
+    if (!ok) return false;
+    const int32_t v[8] = {p.R, p.P, p.CB, p.nseg, p.wl, (int32_t)p.stage_alloc, (int32_t)smem, (int32_t)p.rowbytes};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return true;
+}
+
 }  // namespace zq

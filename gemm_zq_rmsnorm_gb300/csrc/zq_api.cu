@@ -477,6 +477,18 @@ int zq_rmsnorm_q6k_gemv(const float *x, const float *gamma, float eps, int K, co
     return launched(launch_q6k_fused(job, K, x, gamma, eps, q8_out, (cudaStream_t)stream), name);
 }
 
+int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows, int sms, int32_t *out)
+{
+    if (!out) return fail(ZQ_ERR_ARG, "zq_debug_stream_plan: null out");
+    if (wtype < 4 || wtype > 6 || (ntok != 1 && ntok != 4))
+        return fail(ZQ_ERR_ARG, "zq_debug_stream_plan: wtype %d / ntok %d unknown", wtype, ntok);
+    if (K < 256 || K % 256 || K > 32768 || total_rows < 1 || sms < 1)
+        return fail(ZQ_ERR_SHAPE, "zq_debug_stream_plan: K = %d, rows = %lld, sms = %d out of range", K, total_rows, sms);
+    if (!stream_plan_query(wtype, ntok, K, total_rows, sms, out))
+        return fail(ZQ_ERR_SHAPE, "zq_debug_stream_plan: the staging of %d token(s) of K = %d does not fit", ntok, K);
+    return ZQ_OK;
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

@@ -54,6 +54,9 @@ cudaError_t launch_q5k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, flo
 cudaError_t launch_q6k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 cudaError_t launch_q6k_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,
                              const zq_q8_1 *q8out, cudaStream_t st);
+// Launch plan of the streamed mat-vec for a weight format (4, 5, 6 = Q4_K,
+// Q5_K, Q6_K) and tokens per launch (1 or 4): false when it does not fit.
+bool stream_plan_query(int fmt, int nt, int K, long long total_rows, int sms, int32_t *out);
 cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, zq_q8_1 out, cudaStream_t st);
 
 // Launch with programmatic dependent launch: the kernel may start while the

@@ -335,6 +335,18 @@ ZQ_API int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B,
                        int32_t *isums, int path, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/*
+ * Test hook: the launch plan of the streamed mat-vec kernel (host-side, no
+ * device needed) for weight format wtype (4, 5, 6 = Q4_K, Q5_K, Q6_K), ntok
+ * tokens per launch (1 or 4), K columns, total_rows rows over all matrices of
+ * the launch and sms CTAs.  out[8] (host memory) receives: rows per stage,
+ * pieces per row, blocks per piece, segments per row, warp-local rows (0/1),
+ * bytes per stage, dynamic shared memory per CTA, bytes per row.
+ * ZQ_ERR_SHAPE when the staging does not fit (the calls then use one token
+ * per launch) or the sizes are out of range.
+ */
+ZQ_API int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows, int sms, int32_t *out);
+
 #ifdef __cplusplus
 }
 #endif
