@@ -195,3 +195,19 @@ def test_chunk_workspace_query(lib):
     # the integer-sum hook's tensor-core paths need 2*B*K bytes
     assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024 - 1, None) == -6
     assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024, None) == -5
+
+
+@pytest.mark.parametrize("K,N", [(5120, 6144), (5120, 1024), (6144, 5120), (5120, 17408), (17408, 5120), (1024, 151936)])
+@pytest.mark.parametrize("B", [5, 16, 17, 512])
+def test_gemm_workspace_split_k(lib, K, N, B):
+    """The workspace holds the binary16 hi and lo activation parts, the token
+    scales and, when the launch splits K into S ranges, S partial sums of
+    y; S is at most 8 and leaves at least two super-blocks per range."""
+    ws = lib.zq_q4k_gemm_workspace_bytes(N, K, B)
+    base = 2 * (2 * B * K) + (4 * B + 255) // 256 * 256
+    assert ws >= base
+    extra = ws - base
+    assert extra % (4 * B * N) == 0
+    S = extra // (4 * B * N)
+    assert S == 0 or 2 <= S <= 8
+    assert S == 0 or (K // 256) // S >= 2
