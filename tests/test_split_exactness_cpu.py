@@ -26,3 +26,18 @@ def test_hi_lo_split_is_exact_for_every_scale_and_code():
     for part in (hi, lo):
         p = part.astype(np.float64) * 945.0
         assert np.array_equal(p.astype(np.float32).astype(np.float64), p)
+
+
+def test_nibble_to_binary16_fma_is_exact():
+    """The converter warps turn a nibble q and a 6-bit scale s into s*q with one
+    binary16 fma: low nibble in the mantissa of 1024 (h = 1024 + q), scale s,
+    offset -1024 s; high nibble in place (h = 1024 + 16 q), scale s/16, offset
+    -64 s.  Every operand is exact in binary16 and the one rounding of the fma
+    meets an exactly representable result (s*q <= 945 < 2048)."""
+    for s in range(64):
+        for q in range(16):
+            for h, scale, off in ((1024 + q, s, -1024 * s), (1024 + 16 * q, s / 16, -64 * s)):
+                for v in (h, scale, off):
+                    assert float(np.float16(v)) == v          # operands exact in binary16
+                fused = np.float16(h * scale + off)            # one rounding of the exact value
+                assert float(fused) == s * q
