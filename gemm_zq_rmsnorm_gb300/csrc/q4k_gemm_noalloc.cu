@@ -2,15 +2,13 @@
 //
 // The batched projection needs scratch device memory (the binary16 hi/lo
 // split of the activations that the tensor cores read, and a per-token
-// scale).  zq_q4k_gemm takes it from the
-// caller.  Some callers cannot hand out or obtain device memory at the point of
-// the call: code that runs while a CUDA graph is being captured (where
-// allocating would break the capture), engines that own every byte of device
-// memory in a fixed arena and forbid allocation after start-up, and plugins
-// invoked by a host framework that gives them no allocator.  For them this file
-// keeps a fixed scratch buffer in a file-scope device array, sized for the
-// largest shape the library's workloads use (a 512-token prefill of a
-// 17408-wide projection input), and never allocates anything.
+// scale).  zq_q4k_gemm takes it from the caller.  Some callers have no device
+// memory to hand over: engines that own every byte of device memory in a
+// fixed arena and forbid allocation after start-up, and plugins invoked by a
+// host framework that gives them no allocator.  For them this file keeps a
+// fixed scratch buffer in a file-scope device array, sized for the largest
+// shape the library's workloads use (a 512-token prefill of a 17408-wide
+// projection input), and never allocates anything.
 #include <mutex>
 
 #include "zq_internal.cuh"

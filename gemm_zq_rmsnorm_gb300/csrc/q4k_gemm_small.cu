@@ -87,8 +87,9 @@ struct Bars {
 struct SmallParams {
     int N, K, B, nb;
     int splits;
+    size_t split_stride;   // floats between two splits' partial sums
     const float *tscale;   // [B]
-    float *y;              // [B][N], or [splits][B][N] partials
+    float *y;              // [B][N], or [splits][split_stride] partials
     unsigned int *status;
 };
 
@@ -350,7 +351,7 @@ q4k_gemm_small_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_
             }
         }
         if (ok && !abort_s && n0 + row < p.N) {
-            float *yc = p.y + (size_t)split * p.B * p.N + n0 + row;
+            float *yc = p.y + (size_t)split * p.split_stride + n0 + row;
 #pragma unroll
             for (int t = 0; t < ST; ++t)
                 if (t < p.B) yc[(size_t)t * p.N] = acc[t] * tsc[t];
@@ -393,6 +394,7 @@ cudaError_t launch_gemm_small(const void *W, int N, int K, int B, const __half *
     p.B = B;
     p.nb = K / 256;
     p.splits = splits;
+    p.split_stride = split_stride(B, N);
     p.tscale = tscale;
     p.y = out;
     p.status = device_status_word();

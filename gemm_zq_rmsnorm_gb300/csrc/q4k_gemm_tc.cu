@@ -95,8 +95,9 @@ struct GemmParams {
     int N, K, B, nb;
     int t_tiles;
     int splits;            // K ranges (split-K); CTA = (split, token tile, weight tile)
+    size_t split_stride;   // floats between two splits' partial sums (split_stride(B, N))
     const float *tscale;   // [B] power of two that undoes the code scaling
-    float *y;              // [B][N], or [splits][B][N] partial sums when splits > 1
+    float *y;              // [B][N], or [splits][split_stride] partial sums when splits > 1
     unsigned int *status;
 };
 
@@ -410,7 +411,7 @@ q4k_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_con
         }
         if (ok && !abort_s && tvalid) {
             const int sp_now = (int)(blockIdx.x % (unsigned)p.splits);
-            float *yrow = p.y + ((size_t)sp_now * p.B + tok) * p.N + n0 + kEpiCols * cg;
+            float *yrow = p.y + (size_t)sp_now * p.split_stride + (size_t)tok * p.N + n0 + kEpiCols * cg;
             const int ncols = min(kEpiCols, p.N - (n0 + kEpiCols * cg));
             if (ncols == kEpiCols && (p.N & 3) == 0) {
 #pragma unroll
@@ -505,20 +506,32 @@ __global__ void q8_to_f16_kernel(const int8_t *__restrict__ qs, __half *__restri
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// y = sum over the splits of the partial products, in split order
-__global__ void splitk_reduce_kernel(const float4 *__restrict__ part, int splits, size_t n4, float4 *__restrict__ y)
+// y = sum over the splits of the partial products, in split order.  Thread i
+// adds group i of four consecutive outputs; the last group of a ragged B * N
+// (n % 4 != 0) is added element by element.
+__global__ void splitk_reduce_kernel(const float *__restrict__ part, int splits, size_t n, size_t stride,
+                                     float *__restrict__ y)
 {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n4) return;
-    float4 a = __ldg(part + i);
-    for (int s = 1; s < splits; ++s) {
-        const float4 b = __ldg(part + (size_t)s * n4 + i);
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
+    const size_t e0 = 4 * i;
+    if (e0 >= n) return;
+    if (e0 + 4 <= n) {
+        float4 a = __ldg(reinterpret_cast<const float4 *>(part + e0));
+        for (int s = 1; s < splits; ++s) {
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(part + (size_t)s * stride + e0));
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        *reinterpret_cast<float4 *>(y + e0) = a;
+        return;
     }
-    y[i] = a;
+    for (size_t e = e0; e < n; ++e) {
+        float a = __ldg(part + e);
+        for (int s = 1; s < splits; ++s) a += __ldg(part + (size_t)s * stride + e);
+        y[e] = a;
+    }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -544,7 +557,7 @@ size_t g_attr_bytes[64];
 }  // namespace
 
 // workspace layout: hi [B][K] fp16 | lo [B][K] fp16 | tscale [B] fp32 |
-// partial sums [splits][B][N] fp32 (when splits > 1)
+// partial sums [splits][split_stride(B, N)] fp32 (when splits > 1)
 size_t split_bytes(int K, int B) { return (size_t)B * K * sizeof(__half); }
 size_t tscale_bytes(int B) { return ((size_t)B * sizeof(float) + 255) & ~(size_t)255; }
 
@@ -583,9 +596,9 @@ cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, flo
 
 cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st)
 {
-    const size_t n4 = n / 4;
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4 *>(part),
-                                                                          splits, n4, reinterpret_cast<float4 *>(y));
+    const size_t groups = (n + 3) / 4;
+    const size_t stride = (n + 3) & ~(size_t)3;
+    splitk_reduce_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(part, splits, n, stride, y);
     return cudaGetLastError();
 }
 
@@ -615,7 +628,7 @@ size_t gemm_tc_workspace_bytes(int N, int K, int B, bool allow_split)
 {
     if (B <= 1) return 0;
     const int sp = allow_split ? choose_splits(B, N, K, num_sms()) : 1;
-    return 2 * split_bytes(K, B) + tscale_bytes(B) + (sp > 1 ? (size_t)sp * B * N * sizeof(float) : 0);
+    return 2 * split_bytes(K, B) + tscale_bytes(B) + (sp > 1 ? (size_t)sp * split_stride(B, N) * sizeof(float) : 0);
 }
 
 cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, bool allow_split,
@@ -652,6 +665,7 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
     p.nb = K / 256;
     p.t_tiles = (B + BM - 1) / BM;
     p.splits = splits;
+    p.split_stride = split_stride(B, N);
     p.tscale = tscale;
     p.y = splits > 1 ? part : y;
     p.status = device_status_word();

@@ -75,13 +75,16 @@ cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream
 
 // ---- shared by the two projection kernels (q4k_gemm_tc.cu) ---------------
 // Workspace: hi [B][K] binary16 | lo [B][K] binary16 | token scales [B] fp32
-// (padded to 256 B) | split-K partial sums [splits][B][N] fp32.
+// (padded to 256 B) | split-K partial sums [splits][split_stride(B, N)] fp32.
 size_t split_bytes(int K, int B);
 size_t tscale_bytes(int B);
 // x' = q8 * d8 of every token split into exact binary16 hi + lo, with a
 // per-token power-of-two scale that keeps the codes in binary16 range.
 cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, cudaStream_t st);
-// y[i] = sum over splits of part[s][i] (in split order), n a multiple of 4.
+// Floats between consecutive splits' partial sums: B * N rounded up to a
+// multiple of 4, so that every split starts on a 16-byte boundary.
+inline size_t split_stride(int B, int N) { return ((size_t)B * N + 3) & ~(size_t)3; }
+// y[i] = sum over splits of part[s * split_stride + i] (in split order), i < n.
 cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st);
 // split-K count for an output of B x N tiled by 128 x 128
 int choose_splits(int B, int N, int K, int sms);

@@ -195,13 +195,13 @@ ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
 /*
  * zq_q4k_gemm for callers that cannot provide device memory.  (No counterpart
  * on the pages this library follows: it is an interface for integration.)
- * Some callers cannot allocate or pass scratch memory when they call: work
- * recorded while a CUDA graph is being captured, engines that hand out device
- * memory only from a fixed arena set up at start-up, plugins run by a host
- * framework that offers them no allocator.  This entry point computes exactly
- * what zq_q4k_gemm computes (same kernels, same results) but takes its scratch
- * from a fixed device array inside the library instead of a workspace
- * argument, and never calls cudaMalloc, cudaFree or any allocating routine.
+ * Some callers have no device memory to pass when they call: engines that
+ * carve every byte of device memory out of one arena at start-up and allow
+ * no allocation afterwards, and plugins run by a host framework that offers
+ * them no allocator.  This entry point computes what zq_q4k_gemm computes
+ * (the same kernels, one K range per output tile) but takes its scratch from
+ * a fixed device array inside the library instead of a workspace argument,
+ * and never calls cudaMalloc, cudaFree or any allocating routine.
  *   - Limit: the workspace of zq_q4k_gemm (4*B*K + 4*B bytes) must fit in the
  *     array (40 MiB + 256 KiB), i.e. B*K <= 10485760 (for example B = 512
  *     with K up to 20480); larger shapes return ZQ_ERR_WORKSPACE without

@@ -209,6 +209,18 @@ def test_gemm_small_all_outputs(B, K, N):
     assert_within(y, y_ref, S, f"gemm B={B} K={K} N={N}")
 
 
+@pytest.mark.parametrize("B,K,N", [(17, 1280, 77), (5, 1280, 65), (9, 2560, 131), (130, 1280, 203)])
+def test_gemm_split_k_ragged_all_outputs(B, K, N):
+    """Split-K launches whose output size B*N is not a multiple of four: every
+    split's partial sums start on a 16-byte boundary and the reduction covers
+    the last ragged group; every output against the oracle."""
+    x, g, W = make_layer_inputs(25 + B, B, K, N)
+    qs, d, s = oracle_q8(x, g)
+    y = run_gemm(W, N, K, q8_from_oracle(qs, d, s), B)
+    y_ref, S = oracle.q4k_matmul(W, N, K, qs, d, s)
+    assert_within(y, y_ref, S, f"split-K gemm B={B} K={K} N={N}")
+
+
 @pytest.mark.parametrize("B", inputs.CHUNK_BATCHES)
 @pytest.mark.parametrize("name,K,N,paired", inputs.CHUNK_SHAPES)
 def test_chunk_prefill_sampled(B, name, K, N, paired):

@@ -197,17 +197,30 @@ def test_chunk_workspace_query(lib):
     assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024, None) == -5
 
 
-@pytest.mark.parametrize("K,N", [(5120, 6144), (5120, 1024), (6144, 5120), (5120, 17408), (17408, 5120), (1024, 151936)])
+@pytest.mark.parametrize("K,N", [(5120, 6144), (5120, 1024), (6144, 5120), (5120, 17408), (17408, 5120), (1024, 151936),
+                                 (1280, 77), (1280, 65)])
 @pytest.mark.parametrize("B", [5, 16, 17, 512])
 def test_gemm_workspace_split_k(lib, K, N, B):
     """The workspace holds the binary16 hi and lo activation parts, the token
     scales and, when the launch splits K into S ranges, S partial sums of
-    y; S is at most 8 and leaves at least two super-blocks per range."""
+    y, each padded to a multiple of four floats (16-byte aligned splits even
+    when B*N is not a multiple of 4); S is at most 8 and leaves at least two
+    super-blocks per range."""
     ws = lib.zq_q4k_gemm_workspace_bytes(N, K, B)
     base = 2 * (2 * B * K) + (4 * B + 255) // 256 * 256
     assert ws >= base
     extra = ws - base
-    assert extra % (4 * B * N) == 0
-    S = extra // (4 * B * N)
+    stride = 4 * ((B * N + 3) // 4 * 4)
+    assert extra % stride == 0
+    S = extra // stride
     assert S == 0 or 2 <= S <= 8
     assert S == 0 or (K // 256) // S >= 2
+
+
+def test_ragged_split_k_shapes_do_split(lib):
+    """The GPU parity cases for ragged split-K really split: B*N % 4 != 0 and
+    S > 1 (with the fallback SM count used when no device is present)."""
+    for (B, K, N) in [(17, 1280, 77), (5, 1280, 65)]:
+        assert (B * N) % 4 != 0
+        base = 2 * (2 * B * K) + (4 * B + 255) // 256 * 256
+        assert lib.zq_q4k_gemm_workspace_bytes(N, K, B) > base

@@ -352,4 +352,60 @@ def test_silu_mul_q8_1_zero_up_and_single_spike():
     qs, d, s = oracle.silu_mul_q8_1(g, u)
     h = oracle.silu32([g[0, 40]])[0] * np.float32(2.0)
     assert qs[0, 40] == (127 if h > 0 else -127) and np.count_nonzero(qs) == 1
-    assert d[0, 1] == oracle.f32_to_f16_bits([np.float32(abs(h)) / np.float32(127.0)])[0]
+    d32 = np.float32(abs(h)) / np.float32(127.0)
+    assert d[0, 1] == oracle.f32_to_f16_bits([d32])[0]
+    # s = fp16(d32 * sum q): the one code is +-127
+    assert s[0, 1] == oracle.f32_to_f16_bits([d32 * np.float32(127.0 if h > 0 else -127.0)])[0]
+    # the other block holds no non-zero product: d = s = 0
+    assert d[0, 0] == 0 and s[0, 0] == 0
+
+
+def test_silu_mul_q8_1_hand_blocks():
+    """Hand-derived blocks.  silu32(32) = 32 exactly (exp32(-32) < 2^-24, so
+    1 + exp32(-32) rounds to 1), so with gate = 32 the product h = 32 * up is
+    exact for dyadic up.  Block 0: h = 127, +-2.5, +-1.5, +-0.5, 63.5 (zeros
+    elsewhere): amax 127 -> d = 1, 1/d = 1, codes 127, +-3, +-2, +-1, 64 (half
+    away from zero), sum 191 -> s = 191 (binary16 0x59F8; sum h would be
+    190.5), d = 1 (0x3C00).  Block 1: h = 63.5, -1.25, 0.75, 0.25, -0.25:
+    d = 0.5 (0x3800), 1/d = 2, codes 127, -3, 2, 1, -1, sum 126 -> s = 63
+    (0x53E0)."""
+    assert oracle.silu32([32.0])[0] == np.float32(32.0)
+    K = 64
+    g = np.zeros((1, K), np.float32)
+    u = np.zeros((1, K), np.float32)
+    h0 = [127.0, 2.5, -2.5, 1.5, -1.5, 0.5, -0.5, 63.5]
+    pos0 = [3, 5, 6, 10, 11, 20, 21, 31]
+    h1 = [63.5, -1.25, 0.75, 0.25, -0.25]
+    pos1 = [32 + p for p in (0, 7, 8, 30, 31)]
+    for hv, pv in ((h0, pos0), (h1, pos1)):
+        for h, p in zip(hv, pv):
+            g[0, p] = 32.0
+            u[0, p] = h / 32.0
+    qs, d, s = oracle.silu_mul_q8_1(g, u)
+    want = np.zeros(K, np.int8)
+    want[pos0] = [127, 3, -3, 2, -2, 1, -1, 64]
+    want[pos1] = [127, -3, 2, 1, -1]
+    assert np.array_equal(qs[0], want)
+    assert d[0].tolist() == [0x3C00, 0x3800]
+    assert s[0].tolist() == [0x59F8, 0x53E0]
+
+
+def test_silu_mul_q8_1_properties_random():
+    """Random gate/up: every block reaches +-127 at its largest |h|, and the
+    stored s is fp16(d32 * sum q): within two binary16 roundings of
+    d16 * sum q (not the sum of the unquantised products)."""
+    B, K = 2, 4096
+    g = inputs.activations(17, B, K)
+    u = inputs.activations(18, B, K)
+    qs, d, s = oracle.silu_mul_q8_1(g, u)
+    qb = qs.reshape(B, K // 32, 32).astype(np.int64)
+    assert np.all(np.abs(qb).max(-1) == 127)
+    ssum = qb.sum(-1).astype(np.float64)
+    dd, ss_ = f16(d), f16(s)
+    assert np.all(np.abs(ss_ - dd * ssum) <= (2.0 ** -10) * np.abs(dd * ssum) + 1e-7)
+    # the dequantised codes approximate h = silu(g) * u within half a step
+    gd = g.astype(np.float64)
+    h = gd / (1.0 + np.exp(-gd)) * u.astype(np.float64)
+    xq = (dd[:, :, None] * qb).reshape(B, K)
+    step = np.repeat(dd, 32, axis=1)
+    assert np.all(np.abs(xq - h) <= 0.5 * step + 2e-3 * np.abs(h) + 1e-6)
