@@ -254,7 +254,8 @@ class LayerWorkload:
             else:
                 # q8 split + GEMM, + the split-K reduction when the workspace
                 # holds partial sums beyond the hi/lo activations and scales
-                base = 4 * self.B * K + (4 * self.B + 255) // 256 * 256
+                pad = lambda n: (n + 255) // 256 * 256
+                base = 4 * self.B * K + pad(4 * self.B) + (pad(self.B * K // 8) if self.B > 16 else 0)
                 per = 2 + (1 if self.zq.gemm_workspace_bytes(N, K, self.B) > base else 0)
             n += calls * per
         return n

@@ -16,9 +16,10 @@
 namespace zq {
 namespace {
 
-// Bytes of the shared scratch: 4 * B * K (hi and lo halves) plus 4 * B (the
-// token scales) for B * K <= 10 Mi and B <= 65536.
-constexpr size_t kNoAllocScratchBytes = (40u << 20) + (256u << 10);
+// Bytes of the shared scratch: 4 * B * K (hi and lo halves), B * K / 8 (the
+// scaled block sums of the 2-SM kernel) and 4 * B (the token scales), each
+// padded to 256 bytes, for B * K <= 10 Mi.
+constexpr size_t kNoAllocScratchBytes = (42u << 20) + (256u << 10);
 
 // One array per device that loads the library; it lives until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -73,24 +73,36 @@ cudaError_t make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, uint32_t esize,
 // q8 activation codes -> fp16 (exact), n codes, n a multiple of 16.
 cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream_t st);
 
-// ---- shared by the two projection kernels (q4k_gemm_tc.cu) ---------------
+// ---- shared by the projection kernels (q4k_gemm_tc.cu) -------------------
 // Workspace: hi [B][K] binary16 | lo [B][K] binary16 | token scales [B] fp32
-// (padded to 256 B) | split-K partial sums [splits][split_stride(B, N)] fp32.
+// | (B >= 17) the scaled, duplicated block sums s8x [B][K/16] binary16 |
+// split-K partial sums [splits][split_stride(B, N)] fp32; regions padded to
+// 256 bytes.
 size_t split_bytes(int K, int B);
 size_t tscale_bytes(int B);
-// x' = q8 * d8 of every token split into exact binary16 hi + lo, with a
-// per-token power-of-two scale that keeps the codes in binary16 range.
-cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, cudaStream_t st);
 // Floats between consecutive splits' partial sums: B * N rounded up to a
 // multiple of 4, so that every split starts on a 16-byte boundary.
 inline size_t split_stride(int B, int N) { return ((size_t)B * N + 3) & ~(size_t)3; }
+// x' = q8 * d8 of every token split into exact binary16 hi + lo, with a
+// per-token power-of-two scale that keeps the codes in binary16 range; with
+// s8x non-null also each super-block's eight s8 values, scaled the same way,
+// written twice ([B][K/16]).
+cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, __half *s8x,
+                            cudaStream_t st);
 // y[i] = sum over splits of part[s * split_stride + i] (in split order), i < n.
 cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st);
-// split-K count for an output of B x N tiled by 128 x 128
+// split-K count for the small-batch kernel (weight tiles of 128 rows)
 int choose_splits(int B, int N, int K, int sms);
+// split-K count for the pair kernel (256 weight rows x 256 tokens per pair)
+int choose_splits_pair(int B, int N, int K, int sms);
 
 // ---- small-batch projection (q4k_gemm_small.cu), 2 <= B <= kSmallMaxB ----
 constexpr int kSmallMaxB = 16;
+// ---- CTA-pair projection (q4k_gemm_2sm.cu), B > kSmallMaxB ----------------
+// out = y (splits == 1) or the partial-sum area; y receives the result.
+cudaError_t launch_gemm_pair(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
+                             const __half *s8x, const float *tscale, float *out, float *y, int splits,
+                             cudaStream_t st);
 // out = y (splits == 1) or the partial-sum area; y receives the result.
 cudaError_t launch_gemm_small(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
                               const __half *s8, const float *tscale, float *out, float *y, int splits,

@@ -202,11 +202,12 @@ ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
  * (the same kernels, one K range per output tile) but takes its scratch from
  * a fixed device array inside the library instead of a workspace argument,
  * and never calls cudaMalloc, cudaFree or any allocating routine.
- *   - Limit: the workspace of zq_q4k_gemm (4*B*K + 4*B bytes) must fit in the
- *     array (40 MiB + 256 KiB), i.e. B*K <= 10485760 (for example B = 512
- *     with K up to 20480); larger shapes return ZQ_ERR_WORKSPACE without
- *     launching.  B = 1 needs no scratch.
- *   - Every GPU that loads the library holds the 40 MiB array until the
+ *   - Limit: the scratch (4*B*K + B*K/8 + 4*B bytes, each part padded to
+ *     256 bytes) must fit in the array (42 MiB + 256 KiB), i.e.
+ *     B*K <= 10485760 (for example B = 512 with K up to 20480); larger
+ *     shapes return ZQ_ERR_WORKSPACE without launching.  B = 1 needs no
+ *     scratch.
+ *   - Every GPU that loads the library holds the 42 MiB array until the
  *     process exits.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any

@@ -197,17 +197,27 @@ def test_chunk_workspace_query(lib):
     assert lib.zq_debug_q4k_isums(A16, 64, 1024, q8(), 4, A16, 2, A16, 2 * 4 * 1024, None) == -5
 
 
+def _gemm_base_bytes(B, K):
+    """Workspace without split-K partial sums: the binary16 hi and lo halves,
+    the token scales and, for B >= 17 (the 2-SM kernel), the scaled block
+    sums s8 written twice per super-block ([B][K/16] binary16); each region
+    padded to 256 bytes."""
+    pad = lambda n: (n + 255) // 256 * 256
+    return 2 * (2 * B * K) + pad(4 * B) + (pad(B * (K // 16) * 2) if B > 16 else 0)
+
+
 @pytest.mark.parametrize("K,N", [(5120, 6144), (5120, 1024), (6144, 5120), (5120, 17408), (17408, 5120), (1024, 151936),
                                  (1280, 77), (1280, 65)])
 @pytest.mark.parametrize("B", [5, 16, 17, 512])
 def test_gemm_workspace_split_k(lib, K, N, B):
     """The workspace holds the binary16 hi and lo activation parts, the token
-    scales and, when the launch splits K into S ranges, S partial sums of
+    scales, the 2-SM kernel's s8 operand and, when the launch splits K into S
+    ranges, S partial sums of
     y, each padded to a multiple of four floats (16-byte aligned splits even
     when B*N is not a multiple of 4); S is at most 8 and leaves at least two
     super-blocks per range."""
     ws = lib.zq_q4k_gemm_workspace_bytes(N, K, B)
-    base = 2 * (2 * B * K) + (4 * B + 255) // 256 * 256
+    base = _gemm_base_bytes(B, K)
     assert ws >= base
     extra = ws - base
     stride = 4 * ((B * N + 3) // 4 * 4)
@@ -222,5 +232,4 @@ def test_ragged_split_k_shapes_do_split(lib):
     S > 1 (with the fallback SM count used when no device is present)."""
     for (B, K, N) in [(17, 1280, 77), (5, 1280, 65)]:
         assert (B * N) % 4 != 0
-        base = 2 * (2 * B * K) + (4 * B + 255) // 256 * 256
-        assert lib.zq_q4k_gemm_workspace_bytes(N, K, B) > base
+        assert lib.zq_q4k_gemm_workspace_bytes(N, K, B) > _gemm_base_bytes(B, K)
