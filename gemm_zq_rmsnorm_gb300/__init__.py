@@ -29,7 +29,7 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
            "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
-           "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan")
+           "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe")
 
 
 class ZQError(RuntimeError):
@@ -82,6 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_q5k_bytes": ([i, i], sz),
         "zq_q6k_bytes": ([i, i], sz),
         "zq_debug_stream_plan": ([i, i, i, ctypes.c_longlong, i, P], i),
+        "zq_debug_peak_probe": ([i, i, i, P, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -347,3 +348,23 @@ def debug_q4k_isums(W: torch.Tensor, N: int, K: int, a: Q8_1, path: int = 0,
     _check(lib.zq_debug_q4k_isums(_ptr(W), N, K, a._c(), B, _ptr(isums), path, _ptr(workspace),
                                   wbytes, _stream(stream)))
     return isums
+
+
+# operations per probe launch, by kind (zq_debug_peak_probe)
+PROBE_KINDS = {0: "dp4a", 1: "mma.sync m16n8k32 s8", 2: "tcgen05.mma kind::f16 128x256x16"}
+
+
+def probe_ops(kind: int, blocks: int, iters: int) -> int:
+    if kind == 0:
+        return blocks * 256 * iters * 8 * 8
+    if kind == 1:
+        return blocks * 8 * iters * 4 * 2 * 16 * 8 * 32
+    return blocks * iters * 2 * 128 * 256 * 16
+
+
+def debug_peak_probe(kind: int, blocks: int, iters: int, sink: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One launch of a throughput probe (see zq.h); returns the sink."""
+    if sink is None:
+        sink = torch.empty(blocks * 256, dtype=torch.int32, device="cuda")
+    _check(load().zq_debug_peak_probe(kind, blocks, iters, _ptr(sink), _stream(stream)))
+    return sink

@@ -30,14 +30,16 @@
 // columns, so the MMAs of super-block b+1 run while the epilogue folds b.
 //
 // Warp roles (16 warps, four warpgroups):
-//   0      TMA producer: raw Q4_K tiles (this CTA's 128 rows, one super-block
+//   0      TMA producer: raw Q4_K tiles (this CTA's 128 rows, two super-blocks
 //          ahead), binary16 hi/lo token tiles and s8 tiles, whose bytes are
 //          counted on the even CTA's stage barrier;
 //   1      MMA issuer (even CTA only) and tensor-memory owner (both CTAs);
-//   2, 3   idle;
-//   4-7    converters (one weight row per thread: nibbles -> sc*q binary16 in
-//          the 128-byte-swizzled K-major layout; the min operand once per
-//          super-block);
+//   2-7    converters, three sets of two warps, set j filling stage slot j
+//          (two weight rows per thread: nibbles -> sc*q binary16 in the
+//          128-byte-swizzled K-major layout; the min operand once per
+//          super-block).  The proxy fence that publishes a converted stage
+//          to the tensor cores costs about as much as the conversion, so the
+//          three sets keep three stages in flight;
 //   8-15   epilogue (TMEM lane quarter = warp % 4, 128 token columns each),
 //          holding the fp32 accumulator in registers: warpgroups 0-1 give
 //          registers to warpgroups 2-3 (56 / 200 of the 128 per thread the
@@ -62,14 +64,17 @@ constexpr int kMinAtom = 128 * 32;         // 128 rows x 16 binary16 (32 B), 32-
 constexpr int kStageBytes = 3 * kAtom + 2 * kMinAtom;   // A (weights), B hi, B lo, A' (mins), B' (s8)
 constexpr int kRawBytes = kRows * kQ4KBlockBytes;       // 128 rows x 144 B
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 4, kConvWarps = 4;
+constexpr int kConvWarp0 = 2, kConvWarps = 6;   // three sets of two warps, one set per stage slot
+constexpr int kSetWarps = kConvWarps / kStages;
+constexpr int kRawSlots = 3;               // raw Q4_K tiles, two super-blocks ahead
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8;
 constexpr int kEpiCols = kPairN / 2;       // token columns per epilogue thread
 constexpr uint32_t kIdesc = idesc_f16_f32(kPairM, kPairN);
 constexpr uint32_t kTmemCols = 512;        // two accumulators of 256 columns
 constexpr uint32_t kStageTx = 2 * 2 * kAtom;            // both CTAs' hi and lo token tiles
 constexpr uint32_t kStageTxMin = kStageTx + 2 * kMinAtom;
-static_assert(kConvWarps * 32 == kRows, "one converter thread per weight row");
+constexpr uint32_t kSigTx = 4 * kSetWarps;                 // the odd CTA's converter signals
+static_assert(kSetWarps * 32 * 2 == kRows, "a converter thread converts two weight rows of its stage");
 static_assert(kEpiWarp0 % 4 == 0 && kEpiWarps == 8, "epilogue lane quarters follow warp % 4");
 
 struct Smem {
@@ -80,9 +85,11 @@ struct Smem {
     static constexpr size_t amin(int s) { return stage(s) + 3 * kAtom; }
     static constexpr size_t bmin(int s) { return stage(s) + 3 * kAtom + kMinAtom; }
     static constexpr size_t raw(int i) { return stage(kStages) + (size_t)i * kRawBytes; }
-    static constexpr size_t bars() { return raw(2); }
-    // full[3], empty[3], raw_full[2], raw_empty[2], tfull[2], tempty[2], drain
-    static constexpr int kNumBars = 2 * kStages + 2 * 2 + 2 * 2 + 1;
+    // words the odd CTA's converter warps store into (st.async) to signal a stage
+    static constexpr size_t sig() { return raw(kRawSlots); }
+    static constexpr size_t bars() { return sig() + 64; }
+    // full[3], empty[3], raw_full[3], raw_empty[3], tfull[2], tempty[2], drain
+    static constexpr int kNumBars = 2 * kStages + 2 * kRawSlots + 2 * 2 + 1;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }   // + alignment slack
 };
@@ -233,8 +240,8 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
 
     uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
     uint64_t *full = bm, *empty = bm + kStages;
-    uint64_t *raw_full = empty + kStages, *raw_empty = raw_full + 2;
-    uint64_t *tfull = raw_empty + 2, *tempty = tfull + 2;
+    uint64_t *raw_full = empty + kStages, *raw_empty = raw_full + kRawSlots;
+    uint64_t *tfull = raw_empty + kRawSlots, *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
@@ -243,12 +250,16 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1 + 2 * kConvWarps);
+            // the even CTA's producer and the slot's converter warps; the odd
+            // CTA's converter warps signal with st.async bytes
+            mbar_init(&full[s], 1 + kSetWarps);
             mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kRawSlots; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvWarps);
+            mbar_init(&raw_empty[i], kConvWarps);   // every set converts part of every super-block
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], 2 * kEpiWarps);
         }
@@ -278,33 +289,25 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                 const int tok0 = T.t0 + kToks * (int)rank;
                 bool ok = true;
                 auto load_raw = [&](int bb) -> bool {
-                    const int slot = bb & 1, use = bb >> 1;
+                    const int slot = bb % kRawSlots, use = bb / kRawSlots;
                     if (use > 0 && !pair_wait(&raw_empty[slot], (use - 1) & 1, ctx)) return false;
                     mbar_arrive_expect_tx(&raw_full[slot], kRawBytes);
                     tma_load_2d(sm + Smem::raw(slot), &tmap_w, kQ4KBlockBytes * T.sb(bb), T.row0, &raw_full[slot]);
                     return true;
                 };
-                ok = load_raw(0);
-                if (ok && nb > 1) ok = load_raw(1);
+                for (int bb = 0; bb < kRawSlots - 1 && bb < nb && ok; ++bb) ok = load_raw(bb);
                 const int nq = 4 * nb;
                 for (int q = 0; q < nq && ok; ++q) {
                     const int b = q >> 2, i = q & 3;
-                    if (i == 0 && b >= 1 && b + 1 < nb && !(ok = load_raw(b + 1))) break;
+                    if (i == 0 && b + kRawSlots - 1 < nb && !(ok = load_raw(b + kRawSlots - 1))) break;
                     const int s = q % kStages, round = q / kStages;
                     if (round > 0 && !(ok = pair_wait(&empty[s], (round - 1) & 1, ctx))) break;
                     const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full[s], i == 3 ? kStageTxMin : kStageTx);
+                    if (leader) mbar_arrive_expect_tx(&full[s], (i == 3 ? kStageTxMin : kStageTx) + kSigTx);
                     const int kx = 256 * T.sb(b) + 64 * i;
                     tma_load_2d_pair(sm + Smem::bhi(s), &tmap_hi, kx, tok0, fb);
                     tma_load_2d_pair(sm + Smem::blo(s), &tmap_lo, kx, tok0, fb);
                     if (i == 3) tma_load_2d_pair(sm + Smem::bmin(s), &tmap_s8, 16 * T.sb(b), tok0, fb);
-                }
-                if (!ok) {
-                    // copies already issued land within microseconds; give
-                    // them time before this CTA's shared memory goes away
-                    const uint64_t tw = global_ns();
-                    while (global_ns() - tw < 200000ull) {
-                    }
                 }
             }
         } else if (warp == 1) {
@@ -352,19 +355,30 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             }
         } else if (warp >= kConvWarp0) {
             // ------------------------------------------------ converters
-            const int r = threadIdx.x - 32 * kConvWarp0;   // weight row within this CTA
-            const int sw = r & 7, s32 = (r >> 2) & 1;
-            for (int b = 0; b < nb; ++b) {
-                const int slot = b & 1;
-                if (!pair_warp_wait(&raw_full[slot], (b >> 1) & 1, ctx)) break;
-                const uint8_t *raw = sm + Smem::raw(slot) + (size_t)r * kQ4KBlockBytes;
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
-                const Fold fp = fold_params(hdr.x);
-                bool ok = true;
-                for (int i = 0; i < 4 && ok; ++i) {
-                    const int q = 4 * b + i;
-                    const int s = q % kStages, round = q / kStages;
-                    if (round > 0 && !(ok = pair_warp_wait(&empty[s], (round - 1) & 1, ctx))) break;
+            // set j fills stage slot j (stages q = j, j + 3, ...); so three
+            // stages are converted, fenced and published at once
+            const int set = (warp - kConvWarp0) / kSetWarps;
+            const int ct = ((warp - kConvWarp0) % kSetWarps) * 32 + lane;   // rows ct and ct + 64
+            int cur_b = -1;
+            bool ok = true;
+            for (int q = set; q < 4 * nb && ok; q += kStages) {
+                const int b = q >> 2, i = q & 3, round = q / kStages;
+                if (b != cur_b) {
+                    if (cur_b >= 0) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&raw_empty[cur_b % kRawSlots]);
+                    }
+                    if (!(ok = pair_warp_wait(&raw_full[b % kRawSlots], (uint32_t)(b / kRawSlots) & 1, ctx))) break;
+                    cur_b = b;
+                }
+                if (round > 0 && !(ok = pair_warp_wait(&empty[set], (round - 1) & 1, ctx))) break;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const int r = ct + 64 * h;   // weight row within this CTA
+                    const int sw = r & 7, s32 = (r >> 2) & 1;
+                    const uint8_t *raw = sm + Smem::raw(b % kRawSlots) + (size_t)r * kQ4KBlockBytes;
+                    const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
+                    const Fold fp = fold_params(hdr.x);
                     const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
                     const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
                     uint32_t sc0, sc1, md;
@@ -374,7 +388,7 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                     const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
                     const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
                     const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-                    uint8_t *arow = sm + Smem::a(s) + (size_t)r * 128;
+                    uint8_t *arow = sm + Smem::a(set) + (size_t)r * 128;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint4 lo, hi;
@@ -395,22 +409,29 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                             q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, m0v);
                             q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, scd, m1v);
                             const float v0 = -fp.r * (float)m0v, v1 = -fp.r * (float)m1v;
-                            const __half2 h = __floats2half2_rn(v0, v1);
-                            const float2 hb = __half22float2(h);
-                            hv[j >> 1] = h2_bits(h);
+                            const __half2 hh = __floats2half2_rn(v0, v1);
+                            const float2 hb = __half22float2(hh);
+                            hv[j >> 1] = h2_bits(hh);
                             lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
                         }
-                        uint8_t *mrow = sm + Smem::amin(s) + (size_t)r * 32;
+                        uint8_t *mrow = sm + Smem::amin(set) + (size_t)r * 32;
                         *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
                         *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
                     }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(cluster_addr(smem_u32(&full[s]), 0));
                 }
-                if (!ok) break;
+                fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[slot]);
+                if (lane == 0) {
+                    if (rank == 0)
+                        mbar_arrive(&full[set]);
+                    else
+                        st_async_signal(cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (warp - kConvWarp0), 0),
+                                        cluster_addr(smem_u32(&full[set]), 0));
+                }
+            }
+            if (ok && cur_b >= 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[cur_b % kRawSlots]);
             }
         }
     } else {
@@ -468,6 +489,13 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
         }
     }
     __syncwarp();
+    if (abort_s) {
+        // a role gave up: let copies and signals already issued land before
+        // the pair's shared memory goes away
+        const uint64_t tw = global_ns();
+        while (global_ns() - tw < 200000ull) {
+        }
+    }
     // back to the launch's 128 registers per thread before the roles meet
     // again (the epilogue's release lets the other warpgroups' request go on)
     if (warp < kEpiWarp0)

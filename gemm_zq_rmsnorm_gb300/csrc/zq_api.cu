@@ -489,6 +489,18 @@ int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows, int s
     return ZQ_OK;
 }
 
+int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void *stream)
+{
+    if (kind < 0 || kind > 2) return fail(ZQ_ERR_ARG, "zq_debug_peak_probe: kind %d unknown", kind);
+    if (!sink || !aligned16(sink)) return fail(ZQ_ERR_ARG, "zq_debug_peak_probe: sink null or misaligned");
+    if (blocks < 1 || blocks > 65535 || iters < 1 || iters > (1 << 24))
+        return fail(ZQ_ERR_SHAPE, "zq_debug_peak_probe: blocks = %d, iters = %d out of range", blocks, iters);
+    int dev, st;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_peak_probe(kind, blocks, iters, static_cast<int *>(sink), (cudaStream_t)stream),
+                    "zq_debug_peak_probe");
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

@@ -43,6 +43,17 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
 
+// Asynchronous 4-byte store into a CTA of the cluster whose completion is
+// counted (4 bytes) on an mbarrier of that CTA, with release semantics at
+// cluster scope.  Measured in the pair GEMM: ~125 cycles of the issuing
+// thread, against ~1200 for a release-arrive at cluster scope.
+__device__ __forceinline__ void st_async_signal(uint32_t cl_dst, uint32_t cl_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cl_dst), "r"(0u),
+                 "r"(cl_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");

@@ -58,6 +58,9 @@ cudaError_t launch_q6k_fused(const GemvJob &job, int K, const float *x, const fl
 // Q5_K, Q6_K) and tokens per launch (1 or 4): false when it does not fit.
 bool stream_plan_query(int fmt, int nt, int K, long long total_rows, int sms, int32_t *out);
 cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, zq_q8_1 out, cudaStream_t st);
+// Throughput probes (kind 0: dp4a, 1: mma.sync m16n8k32 s8, 2: tcgen05 kind::f16
+// 128 x 256 x 16); sink: device ints, one per thread (256 per block, 128 for kind 2).
+cudaError_t launch_peak_probe(int kind, int blocks, int iters, int *sink, cudaStream_t st);
 
 // Launch with programmatic dependent launch: the kernel may start while the
 // previous kernel on the stream is still running.  Every kernel launched this

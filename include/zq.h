@@ -348,6 +348,23 @@ ZQ_API int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B,
  */
 ZQ_API int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows, int sms, int32_t *out);
 
+/*
+ * Throughput probe of the arithmetic the projection kernels can use on this
+ * GPU (no counterpart on the pages; the rates are the denominators of the
+ * prefill metric, because the int8 tcgen05 MMA, kind::i8, does not exist on
+ * sm_103a).  One launch of `blocks` blocks, each thread or issuing thread
+ * running `iters` steps; the caller times it.  Operations per launch:
+ *   kind 0  dp4a (packed int8 dot products, 256 threads, 8 per step):
+ *           blocks * 256 * iters * 8 * 8;
+ *   kind 1  mma.sync m16n8k32 s8 (8 warps, 4 per step):
+ *           blocks * 8 * iters * 4 * 2 * 16 * 8 * 32;
+ *   kind 2  tcgen05.mma kind::f16 128 x 256 x 16 (one issuing thread per
+ *           block, one block per SM at most): blocks * iters * 2*128*256*16.
+ *   sink : device memory of at least blocks * 256 ints (results kept live).
+ * A kind-2 probe whose bounded wait expires sets ZQ_DEVICE_WAIT_EXPIRED.
+ */
+ZQ_API int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
