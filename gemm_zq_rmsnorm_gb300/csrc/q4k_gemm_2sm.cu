@@ -21,29 +21,47 @@
 // the ratio and folds with 1; a ratio too large for binary16 is scaled by a
 // power of two, undone in the fold.)
 //
-// Tile of a CTA pair: 256 weight rows (the MMA's M: 128 rows in each CTA's
-// shared and tensor memory) x 256 tokens (the MMA's N: each CTA stages 128
-// tokens, the MMA reads both halves).  Each CTA converts only its own 128
-// weight rows, and every converted weight meets all 256 tokens; one
-// 256 x 256 x 16 MMA keeps each SM's tensor core busy for ~128 cycles.
-// Tensor memory (512 columns) holds two super-block accumulators of 256
-// columns, so the MMAs of super-block b+1 run while the epilogue folds b.
+// Tile of a CTA pair: 256 weight rows (the MMA's M: 128 rows in each CTA) x
+// 256 tokens (the MMA's N: each CTA stages 128 tokens, the MMA reads both
+// halves).  Each CTA converts only its own 128 weight rows, and every
+// converted weight meets all 256 tokens; one 256 x 256 x 16 MMA keeps each
+// SM's tensor core busy for ~128 cycles.
+//
+// The converted weights (the MMA's A operand) go to tensor memory with
+// tcgen05.st, not to shared memory: shared memory then carries only the
+// token tiles (TMA writes, MMA reads), the raw Q4_K tiles and the small min
+// operands, and the MMA's reads of A no longer compete with the converters
+// for its bandwidth (with A in shared memory the converters were starved).
+// Tensor memory (512 columns): the accumulator (256 columns, tokens) and
+// eight A slots of 32 columns (a K = 64 stage of binary16 weights, two
+// super-blocks ahead).  The accumulator is single-buffered: the MMAs of
+// super-block b+1 wait for the epilogue to read X_b (~600 cycles per
+// super-block of ~4200 MMA cycles).
+//
+// Stage q (a quarter of a super-block, K = 64) has one "full" barrier in the
+// even CTA, in A slot q % 8: the token tiles' TMA bytes of both CTAs and the
+// converter warps of both CTAs complete it, so the MMA issuer waits once per
+// stage.  One commit per stage ("empty") frees A slot q % 8 and the token
+// slot of stage q (MMAs complete in order, so the producer waits on the
+// barrier of the stage that last used its slot).
 //
 // Warp roles (16 warps, four warpgroups):
-//   0      TMA producer: raw Q4_K tiles (this CTA's 128 rows, two super-blocks
-//          ahead), binary16 hi/lo token tiles and s8 tiles, whose bytes are
-//          counted on the even CTA's stage barrier;
+//   0      TMA producers: lane 0 the binary16 hi/lo token tiles (five stages)
+//          and the s8 tiles, whose bytes are counted on the even CTA's stage
+//          barrier; lane 1 the raw Q4_K tiles of this CTA's 128 rows (two
+//          super-block slots);
 //   1      MMA issuer (even CTA only) and tensor-memory owner (both CTAs);
-//   2-7    converters, three sets of two warps, set j filling stage slot j
-//          (two weight rows per thread: nibbles -> sc*q binary16 in the
-//          128-byte-swizzled K-major layout; the min operand once per
-//          super-block).  The proxy fence that publishes a converted stage
-//          to the tensor cores costs about as much as the conversion, so the
-//          three sets keep three stages in flight;
+//   2, 3   idle;
+//   4-7    converters, one weight row per thread (TMEM lane = row): nibbles
+//          -> sc*q binary16 in registers -> tensor memory; the odd CTA's
+//          warps signal a converted stage to the even CTA's barrier with
+//          st.async (a cluster-scope release-arrive costs ~1200 cycles);
 //   8-15   epilogue (TMEM lane quarter = warp % 4, 128 token columns each),
 //          holding the fp32 accumulator in registers: warpgroups 0-1 give
-//          registers to warpgroups 2-3 (56 / 200 of the 128 per thread the
-//          block is launched with).
+//          registers to warpgroups 2-3 (64 / 192 of the 128 per thread the
+//          block is launched with).  One lane polls the accumulator's
+//          barrier without sleeping and releases the others through a
+//          hardware named barrier.
 // Every wait is bounded; a failed wait stops both CTAs of the pair.
 #include <cuda.h>
 
@@ -56,44 +74,44 @@ namespace zq {
 namespace {
 
 constexpr int kRows = 128;                 // weight rows per CTA (MMA M / 2)
-constexpr int kToks = 128;                 // tokens staged per CTA (MMA N / 2)
-constexpr int kPairM = 2 * kRows, kPairN = 2 * kToks;
-constexpr int kStages = 3;                 // operand stages of K = 64
-constexpr int kAtom = 128 * 128;           // 128 rows x 64 binary16 (128 B), 128-byte swizzle
+constexpr int kTileN = 256;                // tokens per pair tile (MMA N, at most)
+constexpr int kToks = kTileN / 2;          // tokens staged per CTA
+constexpr int kPairM = 2 * kRows;
+constexpr int kStages = 5;                 // K = 64 token stages (a super-block is four)
+constexpr int kASlots = 8;                 // K = 64 converted-weight stages in tensor memory
+constexpr int kAtom = kToks * 128;         // 128 token rows x 64 binary16 (128 B), 128-byte swizzle
 constexpr int kMinAtom = 128 * 32;         // 128 rows x 16 binary16 (32 B), 32-byte swizzle
-constexpr int kStageBytes = 3 * kAtom + 2 * kMinAtom;   // A (weights), B hi, B lo, A' (mins), B' (s8)
+constexpr int kBStageBytes = 2 * kAtom;    // hi, lo
+constexpr int kRawSlots = 2;               // raw Q4_K tiles
 constexpr int kRawBytes = kRows * kQ4KBlockBytes;       // 128 rows x 144 B
 constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 2, kConvWarps = 6;   // three sets of two warps, one set per stage slot
-constexpr int kSetWarps = kConvWarps / kStages;
-constexpr int kRawSlots = 3;               // raw Q4_K tiles, two super-blocks ahead
+constexpr int kConvWarp0 = 4, kConvWarps = 4;
 constexpr int kEpiWarp0 = 8, kEpiWarps = 8;
-constexpr int kEpiCols = kPairN / 2;       // token columns per epilogue thread
-constexpr uint32_t kIdesc = idesc_f16_f32(kPairM, kPairN);
-constexpr uint32_t kTmemCols = 512;        // two accumulators of 256 columns
-constexpr uint32_t kStageTx = 2 * 2 * kAtom;            // both CTAs' hi and lo token tiles
-constexpr uint32_t kStageTxMin = kStageTx + 2 * kMinAtom;
-constexpr uint32_t kSigTx = 4 * kSetWarps;                 // the odd CTA's converter signals
-static_assert(kSetWarps * 32 * 2 == kRows, "a converter thread converts two weight rows of its stage");
-static_assert(kEpiWarp0 % 4 == 0 && kEpiWarps == 8, "epilogue lane quarters follow warp % 4");
+constexpr int kEpiCols = kTileN / 2;       // token columns per epilogue thread
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol0 = kTileN, kACols = 32;        // accumulator [0, 256), A slot k at 256 + 32 k
+constexpr uint32_t kConvSigTx = 4 * kConvWarps;         // the odd CTA's converter signals
+constexpr uint32_t kEpiSigTx = 4 * kEpiWarps;           // the odd CTA's epilogue signals
+static_assert(kConvWarps * 32 == kRows && kConvWarp0 % 4 == 0, "one converter thread per row, warp % 4 = quarter");
+static_assert(kEpiWarp0 % 4 == 0 && kEpiWarps == 8 && kEpiCols % 32 == 0, "epilogue lane quarters follow warp % 4");
+static_assert(kACol0 + kASlots * kACols <= kTmemCols, "tensor memory budget");
+static_assert(kToks % 8 == 0 && kTileN % 16 == 0, "MMA N and the swizzle atoms' 8-row groups");
 
 struct Smem {
-    static constexpr size_t stage(int s) { return (size_t)s * kStageBytes; }
-    static constexpr size_t a(int s) { return stage(s); }
-    static constexpr size_t bhi(int s) { return stage(s) + kAtom; }
-    static constexpr size_t blo(int s) { return stage(s) + 2 * kAtom; }
-    static constexpr size_t amin(int s) { return stage(s) + 3 * kAtom; }
-    static constexpr size_t bmin(int s) { return stage(s) + 3 * kAtom + kMinAtom; }
-    static constexpr size_t raw(int i) { return stage(kStages) + (size_t)i * kRawBytes; }
-    // words the odd CTA's converter warps store into (st.async) to signal a stage
+    static constexpr size_t bhi(int s) { return (size_t)s * kBStageBytes; }
+    static constexpr size_t blo(int s) { return bhi(s) + kAtom; }
+    static constexpr size_t bmin(int i) { return (size_t)kStages * kBStageBytes + (size_t)i * kMinAtom; }  // s8 tiles, 2 slots
+    static constexpr size_t amin(int i) { return bmin(2) + (size_t)i * kMinAtom; }     // min operand, 2 slots
+    static constexpr size_t raw(int i) { return amin(2) + (size_t)i * kRawBytes; }
+    // words the odd CTA's warps store into (st.async) to signal the even CTA
     static constexpr size_t sig() { return raw(kRawSlots); }
     static constexpr size_t bars() { return sig() + 64; }
-    // full[3], empty[3], raw_full[3], raw_empty[3], tfull[2], tempty[2], drain
-    static constexpr int kNumBars = 2 * kStages + 2 * kRawSlots + 2 * 2 + 1;
+    // full[8], empty[8], raw_full[2], raw_empty[2], tfull, tempty, drain
+    static constexpr int kNumBars = 2 * kASlots + 2 * kRawSlots + 3;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }   // + alignment slack
 };
-static_assert(kStageBytes % 1024 == 0 && kRawBytes % 16 == 0, "operand atoms stay 1024-byte aligned");
+static_assert(kBStageBytes % 1024 == 0 && kRawBytes % 16 == 0, "operand atoms aligned");
 static_assert(Smem::total() <= 227 * 1024, "shared memory budget");
 static_assert(Smem::total() < (1u << 18), "descriptor start addresses stay inside their 14-bit field");
 
@@ -109,63 +127,190 @@ struct Pair2Params {
     unsigned int *status;
 };
 
-// Per weight row and super-block: the factor applied to w = sc*q (a power of
-// two, or 0 when d = 0), the ratio r whose binary16 parts carry the min term
+// Per weight row and super-block: a power of two 2^-e applied to w = sc*q
+// (0 when d = 0), the ratio r whose binary16 parts carry the min term
 // (-r * m_j), and the fold factor of the accumulator, so that
 // fold * (wmul * w * x' - r * m * s8) = d * w * x' - dmin * m * s8.
+// e comes from the binary16 exponents alone (integer arithmetic, identical in
+// the converters and the epilogue): it keeps |r * m| < 2^14, so the parts of
+// the min operand stay in binary16 range; wmul * w stays exact while e <= 24
+// (dmin / d below 2^31).
 struct Fold {
-    float wmul, r, fold;
+    float wmul, fold;
+    int e;
 };
 
-__device__ __forceinline__ Fold fold_params(uint32_t d_dmin)
+// floor(log2 |v|) of a non-zero binary16 magnitude (subnormals included)
+__device__ __forceinline__ int f16_ilog2(uint32_t h)
+{
+    const uint32_t E = (h >> 10) & 31u, M = h & 1023u;
+    return E ? (int)E - 15 : -24 + 31 - __clz((int)M);
+}
+
+__device__ __forceinline__ Fold fold_of(uint32_t d_dmin)
+{
+    const uint32_t hd = d_dmin & 0x7FFFu, hm = (d_dmin >> 16) & 0x7FFFu;
+    int e = 0;
+    if (hm) e = max(0, f16_ilog2(hm) - (hd ? f16_ilog2(hd) : 0) - 7);
+    Fold f;
+    f.e = e;
+    f.wmul = hd ? ldexpf(1.0f, -e) : 0.0f;
+    const float d = __half2float(__ushort_as_half((unsigned short)(d_dmin & 0xFFFFu)));
+    f.fold = ldexpf(hd ? d : 1.0f, e);
+    return f;
+}
+
+// r * 2^-e: dmin / d (dmin itself when d = 0), scaled
+__device__ __forceinline__ float ratio_of(uint32_t d_dmin, int e)
 {
     const float d = __half2float(__ushort_as_half((unsigned short)(d_dmin & 0xFFFFu)));
     const float dm = __half2float(__ushort_as_half((unsigned short)(d_dmin >> 16)));
-    Fold f;
-    float r = d != 0.0f ? dm / d : dm;
-    const float base = d != 0.0f ? d : 1.0f;
-    int e = 0;
-    const float big = fabsf(r) * (63.0f / 16384.0f);   // |r * m| <= 16384 keeps the parts in binary16
-    if (big > 1.0f) frexpf(big, &e);                     // big <= 2^e
-    f.r = ldexpf(r, -e);
-    f.wmul = d != 0.0f ? ldexpf(1.0f, -e) : 0.0f;
-    f.fold = ldexpf(base, e);
-    return f;
+    return ldexpf((d_dmin & 0x7FFFu) ? dm / d : dm, -e);
+}
+
+// Eight weights sc*q*wmul of one sub-block pair's nibble word w, as two
+// binary16 pairs for the low nibbles (even sub-block) and two for the high
+// nibbles (odd sub-block), in byte order.  The nibble is placed in the
+// mantissa of 1024 (low) or 1024 + 16 q (high), so one fused binary16
+// operation with scale s, offset -1024 s (low) or s/16, -64 s (high) gives
+// s * q exactly while it fits in 11 bits.
+__device__ __forceinline__ void nib8_to_h2(uint32_t w, __half2 s_lo, __half2 o_lo, __half2 s_hi, __half2 o_hi,
+                                           uint32_t &l0, uint32_t &l1, uint32_t &h0, uint32_t &h1)
+{
+    const uint32_t p0 = __byte_perm(w, 0, 0x4140);   // [b0, 0, b1, 0]
+    const uint32_t p1 = __byte_perm(w, 0, 0x4342);   // [b2, 0, b3, 0]
+    const uint32_t a0 = (p0 & 0x000F000Fu) | 0x64006400u, a1 = (p1 & 0x000F000Fu) | 0x64006400u;
+    const uint32_t c0 = (p0 & 0x00F000F0u) | 0x64006400u, c1 = (p1 & 0x00F000F0u) | 0x64006400u;
+    l0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&a0), s_lo, o_lo));
+    l1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&a1), s_lo, o_lo));
+    h0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&c0), s_hi, o_hi));
+    h1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&c1), s_hi, o_hi));
+}
+
+// Converts stage I (sub-blocks 2I, 2I+1) of one weight row and stores it in
+// the row's lane of a tensor-memory A slot at column address `col`: binary16
+// pairs in K order, the low nibbles (sub-block 2I) in columns 0..15, the
+// high nibbles (2I+1) in 16..31; for I = 3 also the row's min operand
+// (-r * m_j as binary16 hi, then lo) in its 32-byte-swizzled shared-memory
+// row `mrow`.
+template <int I>
+__device__ __forceinline__ void convert_one(const uint8_t *raw, uint32_t col, uint8_t *mrow, int r)
+{
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
+    const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * I);
+    const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * I);
+    const Fold f = fold_of(hdr.x);
+    const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+    for (int hi = 0; hi < 2; ++hi) {
+        uint32_t sc, md;
+        q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * I + hi, sc, md);
+        const float scf = (float)sc * f.wmul;
+        const __half2 s2 = __float2half2_rn(hi ? scf * 0.0625f : scf);
+        const __half2 o2 = __float2half2_rn(hi ? -64.0f * scf : -1024.0f * scf);
+        const uint32_t m = hi ? 0x00F000F0u : 0x000F000Fu;
+        uint32_t o[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {   // nibble bytes 4c..4c+3 -> columns 2c, 2c+1
+            const uint32_t p0 = (__byte_perm(wv[c], 0, 0x4140) & m) | 0x64006400u;   // bytes 0, 1
+            const uint32_t p1 = (__byte_perm(wv[c], 0, 0x4342) & m) | 0x64006400u;   // bytes 2, 3
+            o[2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&p0), s2, o2));
+            o[2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&p1), s2, o2));
+        }
+        tmem_st16(col + 16u * hi, o);
+    }
+    if (I == 3) {
+        const float rr = ratio_of(hdr.x, f.e);
+        uint32_t hv[4], lv[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            uint32_t m0v, m1v, scd;
+            q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, m0v);
+            q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, scd, m1v);
+            const float v0 = -rr * (float)m0v, v1 = -rr * (float)m1v;
+            const __half2 hh = __floats2half2_rn(v0, v1);
+            const float2 hb = __half22float2(hh);
+            hv[j >> 1] = h2_bits(hh);
+            lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
+        }
+        const int s32 = (r >> 2) & 1;
+        *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        fence_async_smem();   // the min MMA reads this row through the async proxy
+    }
 }
 
 // Bounded wait on a barrier that may receive arrivals from the peer CTA;
 // gives up at once when either CTA of the pair has already failed.  Inline
 // throughout: a call out of a warpgroup whose register count was changed
 // would force spills around it.
+// The pair's abort flag and the device status word live in shared memory
+// (set up by thread 0), so a wait keeps only the peer's flag address in
+// registers.
+__shared__ int s_abort;
+__shared__ unsigned int *s_status;
+
 struct PairCtx {
-    volatile int *abort_local;
     uint32_t abort_peer;   // cluster address of the peer's flag
-    unsigned int *status;
 };
 
 __device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, const PairCtx &c)
 {
     if (mbar_try_wait_cl(bar, parity)) return true;
     const uint64_t t0 = global_ns();
+    volatile int *abort_flag = &s_abort;
     for (;;) {
-        if (*c.abort_local) return false;
+        if (*abort_flag) return false;
         if (mbar_try_wait_cl_sleep(bar, parity, kSleepNs)) return true;
         if (global_ns() - t0 >= kWaitLimitNs) {
-            flag_timeout(c.status);
-            *c.abort_local = 1;
+            flag_timeout(s_status);
+            *abort_flag = 1;
             st_cluster_u32(c.abort_peer, 1u);
             return false;
         }
     }
 }
 
-__device__ __forceinline__ bool pair_warp_wait(uint64_t *bar, uint32_t parity, const PairCtx &c)
+// Lane 0 waits; the warp follows it through __syncwarp (which orders the
+// other lanes after lane 0's acquire).  One barrier probe instead of 33.
+__device__ __forceinline__ bool pair_lane0_wait(uint64_t *bar, uint32_t parity, const PairCtx &c)
 {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = pair_wait(bar, parity, c);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok) ok = pair_wait(bar, parity, c);
-    return __all_sync(0xffffffffu, ok);
+    __syncwarp();
+    return ok;
+}
+
+// Latency-critical waits: up to 2000 non-suspending probes first, then the
+// sleeping bounded wait.
+__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool pair_wait_spin(uint64_t *bar, uint32_t parity, const PairCtx &c)
+{
+    for (int i = 0; i < 2000; ++i)
+        if (mbar_test_wait_cl(bar, parity)) return true;
+    return pair_wait(bar, parity, c);
+}
+
+__device__ __forceinline__ bool pair_lane0_wait_spin(uint64_t *bar, uint32_t parity, const PairCtx &c)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = pair_wait_spin(bar, parity, c);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
 }
 
 // Bounded wait that ignores the abort flags (draining work already issued).
@@ -181,7 +326,7 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity)
 // The pair's tile and K range, recomputed inside each role (after its
 // register count changes) rather than kept live across the change.
 struct Tile {
-    int split, t0, m0, row0, b_begin, nb, rot;
+    int split, t0, n, m0, row0, b_begin, nb, rot;   // n: the tile's tokens (MMA N, a multiple of 16)
     __device__ __forceinline__ int sb(int b) const { return b_begin + (b + rot < nb ? b + rot : b + rot - nb); }
 };
 
@@ -193,7 +338,8 @@ __device__ __forceinline__ Tile tile_of(const Pair2Params &p, uint32_t rank)
     const int tile = pair / p.splits;
     const int t_tile = tile % p.t_tiles;
     const int m_tile = tile / p.t_tiles;
-    t.t0 = t_tile * kPairN;
+    t.t0 = t_tile * kTileN;
+    t.n = min(kTileN, (p.B - t.t0 + 15) & ~15);
     t.m0 = m_tile * kPairM;
     t.row0 = t.m0 + kRows * (int)rank;
     t.b_begin = (int)((long long)t.split * p.nb / p.splits);
@@ -204,12 +350,10 @@ __device__ __forceinline__ Tile tile_of(const Pair2Params &p, uint32_t rank)
     return t;
 }
 
-__device__ __forceinline__ PairCtx pair_ctx(volatile int *abort_s, uint32_t rank, unsigned int *status)
+__device__ __forceinline__ PairCtx pair_ctx(uint32_t rank)
 {
     PairCtx c;
-    c.abort_local = abort_s;
-    c.abort_peer = cluster_addr(smem_u32(const_cast<int *>(abort_s)), rank ^ 1u);
-    c.status = status;
+    c.abort_peer = cluster_addr(smem_u32(&s_abort), rank ^ 1u);
     return c;
 }
 
@@ -236,35 +380,36 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    __shared__ volatile int abort_s;
 
     uint64_t *bm = reinterpret_cast<uint64_t *>(sm + Smem::bars());
-    uint64_t *full = bm, *empty = bm + kStages;
-    uint64_t *raw_full = empty + kStages, *raw_empty = raw_full + kRawSlots;
-    uint64_t *tfull = raw_empty + kRawSlots, *tempty = tfull + 2;
-    uint64_t *drain = tempty + 2;
+    // full[k]: stage q (k = q % 8) is ready: its token tiles landed (TMA bytes
+    // of both CTAs) and its weights are in tensor memory (both CTAs'
+    // converters); empty[k]: the MMAs of stage q have completed, which frees
+    // A slot k and the token slot of stage q (MMAs complete in order)
+    uint64_t *afull = bm, *aempty = bm + kASlots;
+    uint64_t *raw_full = aempty + kASlots, *raw_empty = raw_full + kRawSlots;
+    uint64_t *tfull = raw_empty + kRawSlots, *tempty = tfull + 1, *drain = tempty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            // the even CTA's producer and the slot's converter warps; the odd
-            // CTA's converter warps signal with st.async bytes
-            mbar_init(&full[s], 1 + kSetWarps);
-            mbar_init(&empty[s], 1);
+        for (int k = 0; k < kASlots; ++k) {
+            // the even CTA's token producer and converter warps (+ the TMA
+            // bytes of both CTAs and the odd CTA's st.async bytes)
+            mbar_init(&afull[k], 1 + kConvWarps);
+            mbar_init(&aempty[k], 1);
         }
         for (int i = 0; i < kRawSlots; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvWarps);   // every set converts part of every super-block
+            mbar_init(&raw_empty[i], kConvWarps);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 2 * kEpiWarps);
-        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, kEpiWarps);   // the even CTA's epilogue warps (+ the odd CTA's st.async bytes)
         mbar_init(drain, 1);
-        abort_s = 0;
+        s_abort = 0;
+        s_status = p.status;
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -273,41 +418,48 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
     tc_fence_after();
 
     if (warp < kEpiWarp0) {
-        regs_dec<56>();
+        regs_dec<64>();
         const uint32_t rank = cluster_rank();
         const Tile T = tile_of(p, rank);
-        const PairCtx ctx = pair_ctx(&abort_s, rank, p.status);
+        const PairCtx ctx = pair_ctx(rank);
         const int nb = T.nb;
         if (warp == 0) {
-            // ------------------------------------------------ TMA producer
             if (lane == 0) {
+                // ------------------------------------------ token tiles
+                // CTA r stages the tile's tokens r*n/2 .. (96 rows; the MMA
+                // reads the first n/2)
                 prefetch_tmap(&tmap_hi);
                 prefetch_tmap(&tmap_lo);
                 prefetch_tmap(&tmap_s8);
-                prefetch_tmap(&tmap_w);
-                const bool leader = rank == 0;
-                const int tok0 = T.t0 + kToks * (int)rank;
+                const int tok0 = T.t0 + (T.n >> 1) * (int)rank;
+                const uint32_t tx = 2u * (uint32_t)kBStageBytes, tx_min = tx + 2u * kToks * 32u;
                 bool ok = true;
-                auto load_raw = [&](int bb) -> bool {
-                    const int slot = bb % kRawSlots, use = bb / kRawSlots;
-                    if (use > 0 && !pair_wait(&raw_empty[slot], (use - 1) & 1, ctx)) return false;
-                    mbar_arrive_expect_tx(&raw_full[slot], kRawBytes);
-                    tma_load_2d(sm + Smem::raw(slot), &tmap_w, kQ4KBlockBytes * T.sb(bb), T.row0, &raw_full[slot]);
-                    return true;
-                };
-                for (int bb = 0; bb < kRawSlots - 1 && bb < nb && ok; ++bb) ok = load_raw(bb);
-                const int nq = 4 * nb;
-                for (int q = 0; q < nq && ok; ++q) {
+                for (int q = 0; q < 4 * nb && ok; ++q) {
                     const int b = q >> 2, i = q & 3;
-                    if (i == 0 && b + kRawSlots - 1 < nb && !(ok = load_raw(b + kRawSlots - 1))) break;
-                    const int s = q % kStages, round = q / kStages;
-                    if (round > 0 && !(ok = pair_wait(&empty[s], (round - 1) & 1, ctx))) break;
-                    const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full[s], (i == 3 ? kStageTxMin : kStageTx) + kSigTx);
+                    const int s = q % kStages, k = q % kASlots;
+                    // token slot s last held stage q - 5, whose MMAs completing
+                    // arrive on empty[(q - 5) % 8]
+                    if (q >= kStages &&
+                        !(ok = pair_wait(&aempty[(q - kStages) % kASlots], ((q - kStages) / kASlots) & 1, ctx)))
+                        break;
+                    const uint32_t fb = cluster_addr(smem_u32(&afull[k]), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&afull[k], i == 3 ? tx_min : tx);
                     const int kx = 256 * T.sb(b) + 64 * i;
                     tma_load_2d_pair(sm + Smem::bhi(s), &tmap_hi, kx, tok0, fb);
                     tma_load_2d_pair(sm + Smem::blo(s), &tmap_lo, kx, tok0, fb);
-                    if (i == 3) tma_load_2d_pair(sm + Smem::bmin(s), &tmap_s8, 16 * T.sb(b), tok0, fb);
+                    // the s8 tile of super-block b (slot b & 1): its previous
+                    // reader, the min MMA of b - 2, finished before the MMAs
+                    // of the stage this slot held last
+                    if (i == 3) tma_load_2d_pair(sm + Smem::bmin(b & 1), &tmap_s8, 16 * T.sb(b), tok0, fb);
+                }
+            } else if (lane == 1) {
+                // ------------------------------------------ raw Q4_K tiles
+                prefetch_tmap(&tmap_w);
+                for (int bb = 0; bb < nb; ++bb) {
+                    const int slot = bb % kRawSlots, use = bb / kRawSlots;
+                    if (use > 0 && !pair_wait(&raw_empty[slot], (use - 1) & 1, ctx)) break;
+                    mbar_arrive_expect_tx(&raw_full[slot], kRawBytes);
+                    tma_load_2d(sm + Smem::raw(slot), &tmap_w, kQ4KBlockBytes * T.sb(bb), T.row0, &raw_full[slot]);
                 }
             }
         } else if (warp == 1) {
@@ -315,39 +467,35 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             if (rank == 0 && lane == 0) {
                 const uint32_t tmem = *tmem_slot;
                 const uint32_t base = smem_u32(sm);
-                const uint64_t a0 = smem_desc(base + (uint32_t)Smem::a(0), 16, 1024, kLayoutSw128);
                 const uint64_t bh0 = smem_desc(base + (uint32_t)Smem::bhi(0), 16, 1024, kLayoutSw128);
                 const uint64_t bl0 = smem_desc(base + (uint32_t)Smem::blo(0), 16, 1024, kLayoutSw128);
+                const uint64_t bmn = smem_desc(base + (uint32_t)Smem::bmin(0), 16, 256, kLayoutSw32);
                 const uint64_t am0 = smem_desc(base + (uint32_t)Smem::amin(0), 16, 256, kLayoutSw32);
-                const uint64_t bm0 = smem_desc(base + (uint32_t)Smem::bmin(0), 16, 256, kLayoutSw32);
-                constexpr uint64_t kStage16 = kStageBytes >> 4;
-                int s = 0;
-                uint32_t ph = 0;
+                constexpr uint64_t kB16 = kBStageBytes >> 4, kM16 = kMinAtom >> 4;
+                const uint32_t idesc = idesc_f16_f32(kPairM, (uint32_t)T.n);
                 bool ok = true;
-                for (int b = 0; b < nb && ok; ++b) {
-                    const int buf = b & 1;
-                    const uint32_t use = (uint32_t)(b >> 1);
-                    const uint32_t d_tmem = tmem + (uint32_t)(kPairN * buf);
-                    if (use > 0 && !(ok = pair_wait(&tempty[buf], (use - 1) & 1, ctx))) break;
-                    tc_fence_after();
-                    for (int i = 0; i < 4; ++i) {
-                        if (!(ok = pair_wait(&full[s], ph, ctx))) break;
-                        tc_fence_after();
-                        const uint64_t so = (uint64_t)s * kStage16;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            mma_f16_pair(d_tmem, a0 + so + 2 * kk, bh0 + so + 2 * kk, kIdesc, (i | kk) != 0 ? 1u : 0u);
-                            mma_f16_pair(d_tmem, a0 + so + 2 * kk, bl0 + so + 2 * kk, kIdesc, 1u);
-                        }
-                        if (i == 3) mma_f16_pair(d_tmem, am0 + so, bm0 + so, kIdesc, 1u);
-                        mma_commit_pair_mc(&empty[s], 3);
-                        if (++s == kStages) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
+                for (int q = 0; q < 4 * nb && ok; ++q) {
+                    const int b = q >> 2, i = q & 3;
+                    const int k = q % kASlots;
+                    if (i == 0 && b > 0) {
+                        // the epilogue has read X_{b-1}
+                        if (!(ok = pair_wait_spin(tempty, (b - 1) & 1, ctx))) break;
                     }
-                    if (!ok) break;
-                    mma_commit_pair_mc(&tfull[buf], 3);
+                    const int s = q % kStages;
+                    if (!(ok = pair_wait_spin(&afull[k], (q / kASlots) & 1, ctx))) break;
+                    tc_fence_after();
+                    const uint32_t a_tmem = tmem + kACol0 + kACols * k;
+                    const uint64_t so = (uint64_t)s * kB16;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bh0 + so + 2 * kk, idesc, (i | kk) != 0 ? 1u : 0u);
+                        mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bl0 + so + 2 * kk, idesc, 1u);
+                    }
+                    if (i == 3) {
+                        mma_f16_pair(tmem, am0 + (uint64_t)(b & 1) * kM16, bmn + (uint64_t)(b & 1) * kM16, idesc, 1u);
+                        mma_commit_pair_mc(tfull, 3);
+                    }
+                    mma_commit_pair_mc(&aempty[k], 3);
                 }
                 // every MMA issued has completed before the pair tears down
                 mma_commit_pair_local(drain);
@@ -355,78 +503,42 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             }
         } else if (warp >= kConvWarp0) {
             // ------------------------------------------------ converters
-            // set j fills stage slot j (stages q = j, j + 3, ...); so three
-            // stages are converted, fenced and published at once
-            const int set = (warp - kConvWarp0) / kSetWarps;
-            const int ct = ((warp - kConvWarp0) % kSetWarps) * 32 + lane;   // rows ct and ct + 64
+            const uint32_t tmem = *tmem_slot;
+            const int r = threadIdx.x - 32 * kConvWarp0;   // weight row = TMEM lane
+            const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kACol0;
+            const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (warp - kConvWarp0), 0);
+            const uint32_t afull_cl0 = cluster_addr(smem_u32(&afull[0]), 0);   // barriers 8 bytes apart
             int cur_b = -1;
             bool ok = true;
-            for (int q = set; q < 4 * nb && ok; q += kStages) {
-                const int b = q >> 2, i = q & 3, round = q / kStages;
+            for (int q = 0; q < 4 * nb && ok; ++q) {
+                const int b = q >> 2, i = q & 3;
+                const int k = q % kASlots, round = q / kASlots;
                 if (b != cur_b) {
-                    if (cur_b >= 0) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&raw_empty[cur_b % kRawSlots]);
-                    }
-                    if (!(ok = pair_warp_wait(&raw_full[b % kRawSlots], (uint32_t)(b / kRawSlots) & 1, ctx))) break;
+                    if (cur_b >= 0 && lane == 0) mbar_arrive(&raw_empty[cur_b % kRawSlots]);
+                    if (!(ok = pair_lane0_wait(&raw_full[b % kRawSlots], (uint32_t)(b / kRawSlots) & 1, ctx))) break;
                     cur_b = b;
                 }
-                if (round > 0 && !(ok = pair_warp_wait(&empty[set], (round - 1) & 1, ctx))) break;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    const int r = ct + 64 * h;   // weight row within this CTA
-                    const int sw = r & 7, s32 = (r >> 2) & 1;
-                    const uint8_t *raw = sm + Smem::raw(b % kRawSlots) + (size_t)r * kQ4KBlockBytes;
-                    const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
-                    const Fold fp = fold_params(hdr.x);
-                    const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * i);
-                    const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * i);
-                    uint32_t sc0, sc1, md;
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i, sc0, md);
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * i + 1, sc1, md);
-                    const float scl = (float)sc0 * fp.wmul, sch = (float)sc1 * fp.wmul;
-                    const __half2 s_lo = __float2half2_rn(scl), o_lo = __float2half2_rn(-1024.0f * scl);
-                    const __half2 s_hi = __float2half2_rn(sch * 0.0625f), o_hi = __float2half2_rn(-64.0f * sch);
-                    const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-                    uint8_t *arow = sm + Smem::a(set) + (size_t)r * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 lo, hi;
-                        nib4_to_h2<false>(wv[2 * c], s_lo, o_lo, lo.x, lo.y);
-                        nib4_to_h2<false>(wv[2 * c + 1], s_lo, o_lo, lo.z, lo.w);
-                        nib4_to_h2<true>(wv[2 * c], s_hi, o_hi, hi.x, hi.y);
-                        nib4_to_h2<true>(wv[2 * c + 1], s_hi, o_hi, hi.z, hi.w);
-                        *reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4)) = lo;
-                        *reinterpret_cast<uint4 *>(arow + (((c + 4) ^ sw) << 4)) = hi;
-                    }
-                    if (i == 3) {
-                        // the min operand: -r * m_j as binary16 hi (columns
-                        // 0..7) and lo (8..15)
-                        uint32_t hv[4], lv[4];
-#pragma unroll
-                        for (int j = 0; j < 8; j += 2) {
-                            uint32_t m0v, m1v, scd;
-                            q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, m0v);
-                            q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, scd, m1v);
-                            const float v0 = -fp.r * (float)m0v, v1 = -fp.r * (float)m1v;
-                            const __half2 hh = __floats2half2_rn(v0, v1);
-                            const float2 hb = __half22float2(hh);
-                            hv[j >> 1] = h2_bits(hh);
-                            lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
-                        }
-                        uint8_t *mrow = sm + Smem::amin(set) + (size_t)r * 32;
-                        *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                        *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-                    }
+                if (round > 0 && !(ok = pair_lane0_wait(&aempty[k], (round - 1) & 1, ctx))) break;
+                tc_fence_after();
+                const uint8_t *raw = sm + Smem::raw(b % kRawSlots) + (size_t)r * kQ4KBlockBytes;
+                const uint32_t col = lane_base + kACols * k;
+                uint8_t *mrow = sm + Smem::amin(b & 1) + (size_t)r * 32;
+                switch (i) {
+                case 0: convert_one<0>(raw, col, mrow, r); break;
+                case 1: convert_one<1>(raw, col, mrow, r); break;
+                case 2: convert_one<2>(raw, col, mrow, r); break;
+                default: convert_one<3>(raw, col, mrow, r); break;
                 }
-                fence_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (rank == 0)
-                        mbar_arrive(&full[set]);
+                    if (rank != 0)
+                        st_async_signal(sig, afull_cl0 + 8u * (uint32_t)k);
+                    else if (warp == kConvWarp0)
+                        mbar_arrive_expect_tx(&afull[k], kConvSigTx);
                     else
-                        st_async_signal(cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (warp - kConvWarp0), 0),
-                                        cluster_addr(smem_u32(&full[set]), 0));
+                        mbar_arrive(&afull[k]);
                 }
             }
             if (ok && cur_b >= 0) {
@@ -435,11 +547,11 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             }
         }
     } else {
-        regs_inc<200>();
+        regs_inc<192>();
         // ---------------------------------------------------- epilogue
         const uint32_t rank = cluster_rank();
         const Tile T = tile_of(p, rank);
-        const PairCtx ctx = pair_ctx(&abort_s, rank, p.status);
+        const PairCtx ctx = pair_ctx(rank);
         const int nb = T.nb;
         const uint32_t tmem = *tmem_slot;
         const int e = warp - kEpiWarp0;
@@ -447,49 +559,61 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
         const int half = e >> 2;                   // token columns 128*half ..
         const int n = T.row0 + 32 * quarter + lane;  // weight row
         const bool nvalid = n < p.N;
-        const uint8_t *wrow = p.W + (size_t)(nvalid ? n : 0) * p.row_bytes;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(kEpiCols * half);
-        const uint32_t tempty_leader0 = cluster_addr(smem_u32(&tempty[0]), 0);
-        const uint32_t tempty_leader1 = cluster_addr(smem_u32(&tempty[1]), 0);
+        const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 16u + 4u * e, 0);
+        const uint32_t tempty_cl = cluster_addr(smem_u32(tempty), 0);
         float acc[kEpiCols];
 #pragma unroll
         for (int c = 0; c < kEpiCols; ++c) acc[c] = 0.0f;
-        uint32_t hd_next = nvalid ? ld_nc_u32(wrow + (size_t)kQ4KBlockBytes * T.sb(0)) : 0u;
+        uint32_t hd_next = nvalid ? ld_nc_u32(p.W + (size_t)n * p.row_bytes + (size_t)kQ4KBlockBytes * T.sb(0)) : 0u;
         bool ok = true;
         for (int b = 0; b < nb && ok; ++b) {
-            const int buf = b & 1;
             const uint32_t hd = hd_next;
-            if (nvalid && b + 1 < nb) hd_next = ld_nc_u32(wrow + (size_t)kQ4KBlockBytes * T.sb(b + 1));
-            const float fold = nvalid ? fold_params(hd).fold : 0.0f;
-            if (!(ok = pair_warp_wait(&tfull[buf], (uint32_t)(b >> 1) & 1, ctx))) break;
+            if (nvalid && b + 1 < nb)
+                hd_next = ld_nc_u32(p.W + (size_t)n * p.row_bytes + (size_t)kQ4KBlockBytes * T.sb(b + 1));
+            const float fold = nvalid ? fold_of(hd).fold : 0.0f;
+            // one lane polls without sleeping; the others wait at a hardware
+            // barrier, which wakes them within a few cycles
+            if (e == 0) ok = pair_lane0_wait_spin(tfull, (uint32_t)b & 1, ctx);
+            named_bar(1, 32 * kEpiWarps);
+            if (!(ok = !*reinterpret_cast<volatile int *>(&s_abort))) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < kEpiCols / 16; ++c) {
-                uint32_t v[16];
-                tmem_ld16(lane_base + (uint32_t)(kPairN * buf) + 16u * c, v);
+            for (int h = 0; h < kEpiCols / 32; ++h) {
+                uint32_t v[32];
+                tmem_ld16(lane_base + 32u * h, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld16(lane_base + 32u * h + 16u, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                 tmem_wait_ld();
-                if (c == kEpiCols / 16 - 1) {
+                if (h == kEpiCols / 32 - 1) {
+                    // X_b is read: the MMAs of super-block b + 1 may overwrite it
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+                    if (lane == 0) {
+                        if (rank != 0)
+                            st_async_signal(sig, tempty_cl);
+                        else if (e == 0)
+                            mbar_arrive_expect_tx(tempty, kEpiSigTx);
+                        else
+                            mbar_arrive(tempty);
+                    }
                 }
 #pragma unroll
-                for (int j = 0; j < 16; j += 2)
-                    fma2(acc[16 * c + j], acc[16 * c + j + 1], fold, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                for (int j = 0; j < 32; j += 2)
+                    fma2(acc[32 * h + j], acc[32 * h + j + 1], fold, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
             }
         }
-        if (ok && !abort_s && nvalid) {
+        if (ok && !*reinterpret_cast<volatile int *>(&s_abort) && nvalid) {
             float *ybase = p.y + (size_t)T.split * p.split_stride + n;
-            const int tc0 = T.t0 + kEpiCols * half;
+            const int tc0 = T.t0 + kEpiCols * half;   // column c <-> token t0 + c
 #pragma unroll
             for (int c = 0; c < kEpiCols; ++c) {
                 const int tok = tc0 + c;
-                if (tok < p.B) ybase[(size_t)tok * p.N] = acc[c] * __ldg(p.tscale + tok);
+                if (tok < p.B && kEpiCols * half + c < T.n) ybase[(size_t)tok * p.N] = acc[c] * __ldg(p.tscale + tok);
             }
         }
     }
     __syncwarp();
-    if (abort_s) {
+    if (*reinterpret_cast<volatile int *>(&s_abort)) {
         // a role gave up: let copies and signals already issued land before
         // the pair's shared memory goes away
         const uint64_t tw = global_ns();
@@ -503,7 +627,7 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
     else
         regs_dec<128>();
     tc_fence_before();
-    cluster_sync();   // the peer's MMAs, copies and arrivals are finished
+    cluster_sync();   // the peer's MMAs, copies and signals are finished
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(*tmem_slot, kTmemCols);
@@ -514,14 +638,14 @@ size_t g_attr_bytes[64];
 
 }  // namespace
 
-// Split-K count for 256 x 256 pair tiles on sms / 2 SM pairs: tiles that fill
+// Split-K count for 256-row x 192-token pair tiles on sms / 2 SM pairs: tiles that fill
 // the pairs unevenly waste whole waves; model the time of `s` splits as
 // waves * (super-blocks per split + a fixed cost) plus the partial-sum
 // traffic, and take the smallest s within 3 % of the best (>= 2 super-blocks
 // per split, s <= 8).
 int choose_splits_pair(int B, int N, int K, int sms)
 {
-    const long long tiles = (long long)((B + kPairN - 1) / kPairN) * ((N + kPairM - 1) / kPairM);
+    const long long tiles = (long long)((B + kTileN - 1) / kTileN) * ((N + kPairM - 1) / kPairM);
     const int pairs = sms / 2 > 0 ? sms / 2 : 1;
     const int nb = K / 256;
     const int smax = nb / 2 < 8 ? nb / 2 : 8;
@@ -564,7 +688,7 @@ cudaError_t launch_gemm_pair(const void *W, int N, int K, int B, const __half *h
     p.K = K;
     p.B = B;
     p.nb = K / 256;
-    p.t_tiles = (B + kPairN - 1) / kPairN;
+    p.t_tiles = (B + kTileN - 1) / kTileN;
     p.splits = splits;
     p.split_stride = split_stride(B, N);
     p.row_bytes = (size_t)(K / 256) * kQ4KBlockBytes;

@@ -59,14 +59,18 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
 }
 
-// Phase test with acquire at cluster scope: the arrivals may come from the
-// peer CTA (its converter warps, its TMA bytes, the pair's MMA commits).
+// Phase test of a barrier whose arrivals may come from the peer CTA (its
+// converter and epilogue warps' st.async bytes, its TMA bytes, the pair's MMA
+// commits).  Default (CTA-scope acquire) semantics: the peer's signals are
+// releases at cluster scope, and the data they publish is read by the tensor
+// cores after tcgen05 fences, not by this thread.  (An acquire at cluster
+// scope made each probe cost ~300 cycles.)
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -79,7 +83,7 @@ __device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint64_t *bar, uint32_t p
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
@@ -125,6 +129,19 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, ui
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same, with A in tensor memory: rows 0..127 from this CTA's tensor memory at
+// column address a_tmem (K along the columns, two binary16 per column), rows
+// 128..255 from the peer's at the same address.
+__device__ __forceinline__ void mma_f16_pair_ta(uint32_t tmem_d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
