@@ -588,6 +588,119 @@ def whole_job_rate(units_per_rank, ms_max, world):
     return units_per_rank * world / (ms_max * 1e-3)
 
 
+def decode_record(torch, wl, steps, warmup, stream, pk, local_rank, max_over_ranks, world, barrier):
+    """One B = 1 decode workload: the step's rate in HBM GB/s of algorithmic
+    bytes, its dominant launch against the HBM roofline, clocks."""
+    barrier()
+    with Clocks(local_rank) as clk:
+        ms, _ = bench_workload(torch, wl, steps, warmup, stream)
+    ms = max_over_ranks(ms)
+    gbs = whole_job_rate(wl.algo_bytes(), ms, world) / 1e9
+    # the dominant launch: the one moving the most weight bytes
+    dom = max(wl.shapes, key=lambda s: s[1] * s[2] * (2 if s[3] else 1))[0]
+    dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl, dom, steps, warmup, stream)
+    achieved = dalg / (dms * 1e-3) / 1e9
+    return {
+        "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+        "config": {"workload": wl.name, "B": 1, "hidden": wl.inputs_K[0][1],
+                   "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl.shapes],
+                   "layers": wl.layers, "weight_copies_rotated": wl.R,
+                   "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
+                                   + ("; each launch pulls the next one's weights into L2" if wl.prefetch else "")
+                                   if wl.fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
+                   "l2": f"inputs larger than L2: {wl.R} rotating weight copies of the step",
+                   "algorithmic_bytes_per_step": int(wl.algo_bytes())},
+        "roofline": {"bound": "hbm",
+                     "kernel": (f"rmsnorm_q4k_gemv {dK}->{dN}{' x2 (gate+up)' if dp else ''}" if wl.fused
+                                else f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}"),
+                     "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
+                     "traffic": (recorded_traffic(f"{'fused_' if wl.fused else ''}q4k_gemv_stream_pair_{dK}x{dN}")
+                                 if dp else None),
+                     "kernel_ms": round(dms, 5)},
+        "gpu_launches": wl.launches_per_step() * steps,
+        "clocks": clk.summary(),
+    }
+
+
+def batch_record(torch, B, shapes, name, steps, warmup, stream, pk, local_rank, max_over_ranks, world, barrier,
+                 compare_dequant=False):
+    """One batched workload (B tokens through every projection): effective
+    TOPS and HBM GB/s of the step; the dominant projection against the HBM
+    roofline (B <= 16: weights read once for all tokens) or the tensor
+    roofline (B > 16)."""
+    wl = LayerWorkload(name, shapes, B)
+    barrier()
+    with Clocks(local_rank) as clk:
+        ms, _ = bench_workload(torch, wl, steps, warmup, stream)
+    ms = max_over_ranks(ms)
+    tops = whole_job_rate(wl.algo_ops(), ms, world) / 1e12
+    gbs = whole_job_rate(wl.algo_bytes(), ms, world) / 1e9
+    dom = "gate_up" if any(s[0] == "gate_up" for s in wl.shapes) else wl.shapes[0][0]
+    dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl, dom, steps, warmup, stream)
+    if B <= 16:
+        (_, _, N, _) = [s for s in wl.shapes if s[0] == dom][0]
+        alg_bytes = proj_bytes(dK, dN, B)
+        ach = alg_bytes / (dms * 1e-3) / 1e9
+        path = "streamed mat-vec, tokens staged together" if B <= 4 else "small-batch tensor-core kernel"
+        roof = {"bound": "hbm", "kernel": f"q4k_gemm {dK}->{dN} B={B} ({path})",
+                "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
+                "traffic": None, "kernel_ms": round(dms, 5),
+                "algorithmic_bytes_per_launch": int(alg_bytes)}
+    else:
+        ach = dalg / (dms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": f"q4k_gemm {dK}->{dN} B={B}",
+                "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops"], 4),
+                "peak_source": pk["source"] + " bf16 dense burst (fp16 operands run at the bf16 rate; "
+                               "int8 tcgen05 is not available on sm_103a)",
+                "traffic": recorded_traffic(f"q4k_gemm_tc_{B}x{dK}x{dN}"),
+                "kernel_ms": round(dms, 5)}
+    rec = {"workload": wl.name, "B": B, "value": round(tops, 2), "unit": "TOPS",
+           "ms_per_step": round(ms, 4), "hbm_gbs": round(gbs, 1),
+           "algorithmic_ops_per_step": int(wl.algo_ops()), "algorithmic_bytes_per_step": int(wl.algo_bytes()),
+           "roofline": roof,
+           "gpu_launches": wl.launches_per_step() * steps, "clocks": clk.summary()}
+    if compare_dequant:
+        rec["dequant_then_gemm"] = dequant_then_gemm(torch, wl, steps, warmup, stream)
+    del wl
+    torch.cuda.empty_cache()
+    return rec
+
+
+def peak_probes(torch, stream, local_rank, sms):
+    """Throughput of the arithmetic the projection kernels can use (in-library
+    probes, zq_debug_peak_probe): packed int8 dot products (dp4a), the legacy
+    warp-level int8 MMA (mma.sync m16n8k32 s8) and the tcgen05 binary16 MMA
+    (kind::f16, 128 x 256 x 16, one issuing thread per SM).  Each probe is
+    one launch of about a millisecond, timed with CUDA events after one
+    warm-up launch."""
+    import gemm_zq_rmsnorm_gb300 as zq
+    out = {}
+    sink = torch.empty(sms * 8 * 256, dtype=torch.int32, device="cuda")
+    cfg = {0: (sms * 8, 40000), 1: (sms * 8, 6000), 2: (sms, 40000)}
+    with Clocks(local_rank) as clk:
+        for kind, (blocks, iters) in cfg.items():
+            with torch.cuda.stream(stream):
+                zq.debug_peak_probe(kind, blocks, max(1, iters // 8), sink, stream=stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                zq.debug_peak_probe(kind, blocks, iters, sink, stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            ops = zq.probe_ops(kind, blocks, iters)
+            out[zq.PROBE_KINDS[kind]] = {"tera_ops_per_s": round(ops / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+                                         "ops": ops, "blocks": blocks}
+    assert zq.device_status() == 0, "a probe's bounded wait expired"
+    out["clocks"] = clk.summary()
+    out["note"] = ("tcgen05.mma kind::i8 is rejected by ptxas for sm_103a, so the prefill path runs binary16 MMAs on "
+                   "exact hi/lo halves of every Q8_1 value (two MMAs per K step); its effective int8-op rate is "
+                   "compared with these measured rates")
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,14 +708,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="zq", choices=["zq", "reference"])
     ap.add_argument("--workload", default="headline",
-                    choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny", "kquants"])
+                    choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny", "kquants",
+                             "peaks"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2-prefetch", action="store_true",
                     help="fused decode launches pull the next launch's weights into L2 (measured slower on this kernel)")
     ap.add_argument("--no-l2-prefetch", action="store_true", help="the default; kept for older command lines")
     ap.add_argument("--compare-dequant", action="store_true",
-                    help="also time the dequantise-then-GEMM design (cuBLAS) on the 512-token layer")
+                    help="also time the dequantise-then-GEMM design on the 512-token layer")
     ap.add_argument("--decode-path", default="fused", choices=["fused", "two-step"],
                     help="B = 1 step: fused RMSNorm+mat-vec launches, or RMSNorm+Q8_1 then per-projection calls")
     args = ap.parse_args()
@@ -625,8 +739,9 @@ def main():
         dist.init_process_group("nccl")
     stream = torch.cuda.Stream()
     pk = peaks()
-    result = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
+    sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+    out = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic"}
 
     def barrier():
         if dist is not None:
@@ -636,48 +751,29 @@ def main():
     def max_over_ranks(v):
         return reduce_max_over_ranks(dist, v, "cuda")
 
-    wl_dec = None
+    common = dict(stream=stream, pk=pk, local_rank=local_rank, max_over_ranks=max_over_ranks, world=world,
+                  barrier=barrier)
     fz = args.decode_path == "fused"
-    if args.workload in ("headline", "decode-27b"):
-        wl_dec = LayerWorkload("decode-27b-layer", inputs.LAYER_27B, 1, fused=fz)
-    elif args.workload == "decode-small":
-        wl_dec = LayerWorkload("decode-small-28L+lm_head", inputs.SMALL_DECODE[:-1], 1, layers=28,
-                               extra=[inputs.SMALL_DECODE[-1]], fused=fz)
-    elif args.workload == "tiny":
-        wl_dec = LayerWorkload("tiny-1024x1024", inputs.TINY, 1, min_rotation_bytes=3 * L2_BYTES, fused=fz)
+    # the secondary workloads run with fewer timed steps: the line must finish in minutes
+    sub_steps = max(3, args.steps // 4)
 
-    out = dict(result)
-    if wl_dec is not None:
-        wl_dec.prefetch = args.l2_prefetch and not args.no_l2_prefetch
-        barrier()
-        with Clocks(local_rank) as clk:
-            ms, _ = bench_workload(torch, wl_dec, args.steps, args.warmup, stream)
-        ms = max_over_ranks(ms)
-        gbs = whole_job_rate(wl_dec.algo_bytes(), ms, world) / 1e9
-        dom = "gate_up" if any(s[0] == "gate_up" for s in wl_dec.shapes) else wl_dec.shapes[0][0]
-        dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl_dec, dom, args.steps, args.warmup, stream)
-        achieved = dalg / (dms * 1e-3) / 1e9
-        out.update({
-            "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5), "dtype": "u8",
-            "config": {"workload": wl_dec.name, "B": 1, "hidden": wl_dec.inputs_K[0][1],
-                       "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl_dec.shapes],
-                       "layers": wl_dec.layers, "weight_copies_rotated": wl_dec.R,
-                       "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
-                                       + ("; each launch pulls the next one's weights into L2" if wl_dec.prefetch else "")
-                                       if wl_dec.fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
-                       "l2": f"inputs larger than L2: {wl_dec.R} rotating weight copies of the step",
-                       "algorithmic_bytes_per_step": int(wl_dec.algo_bytes())},
-            "roofline": {"bound": "hbm",
-                         "kernel": (f"rmsnorm_q4k_gemv {dK}->{dN}{' x2 (gate+up)' if dp else ''}" if wl_dec.fused
-                                    else f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}"),
-                         "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
-                         "traffic": (recorded_traffic(f"{'fused_' if wl_dec.fused else ''}q4k_gemv_stream_pair_{dK}x{dN}")
-                                     if dp else None),
-                         "kernel_ms": round(dms, 5)},
-            "gpu_launches": wl_dec.launches_per_step() * args.steps,
-            "clocks": clk.summary(),
-        })
+    def decode_wl(which):
+        if which == "decode-27b":
+            wl = LayerWorkload("decode-27b-layer", inputs.LAYER_27B, 1, fused=fz)
+        elif which == "decode-small":
+            wl = LayerWorkload("decode-small-28L+lm_head", inputs.SMALL_DECODE[:-1], 1, layers=28,
+                               extra=[inputs.SMALL_DECODE[-1]], fused=fz)
+        else:
+            wl = LayerWorkload("tiny-1024x1024", inputs.TINY, 1, min_rotation_bytes=3 * L2_BYTES, fused=fz)
+        wl.prefetch = args.l2_prefetch and not args.no_l2_prefetch
+        return wl
+
+    if args.workload in ("headline", "decode-27b", "decode-small", "tiny"):
+        which = "decode-27b" if args.workload == "headline" else args.workload
+        wl_dec = decode_wl(which)
+        rec = decode_record(torch, wl_dec, args.steps, args.warmup, **common)
+        out.update(rec)
+        out["dtype"] = "u8"
         if any(sh[0] == "down" for sh in wl_dec.shapes) and any(sh[0] == "gate_up" for sh in wl_dec.shapes):
             out["silu_down"] = silu_down(torch, wl_dec, args.steps, args.warmup, stream)
         if not args.no_e2e:
@@ -688,62 +784,44 @@ def main():
                                    "cores": 1, "kind": "oracle",
                                    "sample": f"RMSNorm+Q8_1 of every input, row samples: {sample}; "
                                              f"scaled to one full step ({secs:.2f} s per step)"}
+        del wl_dec
+        torch.cuda.empty_cache()
+        if args.workload == "headline":
+            # the other configurations of the same path, each with its own
+            # roofline and clocks
+            for key, which in (("small_model_28L", "decode-small"), ("tiny", "tiny")):
+                wl = decode_wl(which)
+                out[key] = decode_record(torch, wl, sub_steps, args.warmup, **common)
+                del wl
+                torch.cuda.empty_cache()
 
-    if args.workload in ("headline", "prefill-512", "chunk"):
-        Bs = [inputs.PREFILL_B] if args.workload != "chunk" else list(inputs.CHUNK_BATCHES)
-        sub = []
-        for B in Bs:
-            shapes = inputs.LAYER_27B if B == inputs.PREFILL_B else inputs.CHUNK_SHAPES
-            wl = LayerWorkload(f"prefill-{B}" if B == inputs.PREFILL_B else f"chunk-B{B}", shapes, B)
-            barrier()
-            with Clocks(local_rank) as clk:
-                ms, _ = bench_workload(torch, wl, max(3, args.steps // 5), args.warmup, stream)
-            ms = max_over_ranks(ms)
-            tops = whole_job_rate(wl.algo_ops(), ms, world) / 1e12
-            gbs = whole_job_rate(wl.algo_bytes(), ms, world) / 1e9
-            dom = "gate_up" if any(s[0] == "gate_up" for s in wl.shapes) else wl.shapes[0][0]
-            dms, dalg, (dK, dN, dp) = bench_dominant(torch, wl, dom, max(3, args.steps // 5), args.warmup, stream)
-            if B <= 4:
-                # streamed mat-vec path: bound by HBM
-                ach = dalg / (dms * 1e-3) / 1e9
-                roof = {"bound": "hbm", "kernel": f"q4k_gemm {dK}->{dN} B={B} (streamed mat-vec, {B} tokens)",
-                        "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
-                        "traffic": None, "kernel_ms": round(dms, 5)}
-            else:
-                ach = dalg / (dms * 1e-3) / 1e12
-                roof = {"bound": "tensor", "kernel": f"q4k_gemm {dK}->{dN} B={B}",
-                        "achieved": round(ach, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": round(ach / pk["bf16_tflops"], 4),
-                        "peak_source": pk["source"] + " bf16 dense burst (fp16 operands run at the bf16 rate; "
-                                       "int8 tcgen05 is not available on sm_103a)",
-                        "traffic": recorded_traffic(f"q4k_gemm_tc_{B}x{dK}x{dN}"),
-                        "kernel_ms": round(dms, 5)}
-            rec = {"workload": wl.name, "B": B, "value": round(tops, 2), "unit": "TOPS",
-                   "ms_per_step": round(ms, 4), "hbm_gbs": round(gbs, 1),
-                   "algorithmic_ops_per_step": int(wl.algo_ops()),
-                   "roofline": roof,
-                   "gpu_launches": wl.launches_per_step() * max(3, args.steps // 5), "clocks": clk.summary()}
-            if B == inputs.PREFILL_B and args.compare_dequant:
-                rec["dequant_then_gemm"] = dequant_then_gemm(torch, wl, max(3, args.steps // 5), args.warmup, stream)
-            sub.append(rec)
-            del wl
-            torch.cuda.empty_cache()
-        if wl_dec is None:
-            r0 = sub[0]
-            out.update({"value": r0["value"], "unit": "TOPS", "ms_per_step": r0["ms_per_step"], "dtype": "u8",
-                        "config": {"workload": r0["workload"], "B": r0["B"]}, "roofline": r0["roofline"],
-                        "gpu_launches": r0["gpu_launches"], "clocks": r0["clocks"]})
-            if "dequant_then_gemm" in r0:
-                out["dequant_then_gemm"] = r0["dequant_then_gemm"]
-            if len(sub) > 1:
-                out["more"] = sub[1:]
+    if args.workload in ("headline", "prefill-512"):
+        rec = batch_record(torch, inputs.PREFILL_B, inputs.LAYER_27B, f"prefill-{inputs.PREFILL_B}",
+                           max(3, args.steps // 5), args.warmup, compare_dequant=args.compare_dequant, **common)
+        if args.workload == "prefill-512":
+            out.update({"value": rec["value"], "unit": "TOPS", "ms_per_step": rec["ms_per_step"], "dtype": "u8",
+                        "config": {"workload": rec["workload"], "B": rec["B"]}, "roofline": rec["roofline"],
+                        "gpu_launches": rec["gpu_launches"], "clocks": rec["clocks"]})
+            if "dequant_then_gemm" in rec:
+                out["dequant_then_gemm"] = rec["dequant_then_gemm"]
         else:
-            out["prefill_b512"] = sub[0]
+            out["prefill_b512"] = rec
+
+    if args.workload in ("headline", "chunk"):
+        recs = [batch_record(torch, B, inputs.CHUNK_SHAPES, f"chunk-B{B}", sub_steps, args.warmup, **common)
+                for B in inputs.CHUNK_BATCHES]
+        if args.workload == "chunk":
+            r0 = recs[0]
+            out.update({"value": r0["hbm_gbs"], "unit": "GB/s", "ms_per_step": r0["ms_per_step"], "dtype": "u8",
+                        "config": {"workload": r0["workload"], "B": r0["B"]}, "roofline": r0["roofline"],
+                        "gpu_launches": r0["gpu_launches"], "clocks": r0["clocks"], "more": recs[1:]})
+        else:
+            out["chunk"] = {f"B{r['B']}": r for r in recs}
+
     if args.workload in ("headline", "kquants"):
         barrier()
         with Clocks(local_rank) as clk:
-            kq = kquant_rows(torch, args.steps, args.warmup, stream, pk)
+            kq = kquant_rows(torch, sub_steps if args.workload == "headline" else args.steps, args.warmup, stream, pk)
         if args.workload == "kquants":
             r0 = kq[0]
             out.update({"value": r0["gbs"], "unit": "GB/s", "ms_per_step": round(r0["us"] / 1e3, 5), "dtype": "u8",
@@ -756,6 +834,17 @@ def main():
                         "gpu_launches": r0["timed_launches"], "clocks": clk.summary(), "more": kq[1:]})
         else:
             out["kquants"] = {"rows": kq, "clocks": clk.summary()}
+
+    if args.workload in ("headline", "peaks"):
+        barrier()
+        pr = peak_probes(torch, stream, local_rank, sms)
+        if args.workload == "peaks":
+            k2 = pr["tcgen05.mma kind::f16 128x256x16"]
+            out.update({"value": k2["tera_ops_per_s"], "unit": "TFLOP/s", "ms_per_step": k2["ms"], "dtype": "f16",
+                        "config": {"workload": "throughput probes"}, "clocks": pr["clocks"], "peaks": pr,
+                        "gpu_launches": 6})
+        else:
+            out["peaks"] = pr
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
