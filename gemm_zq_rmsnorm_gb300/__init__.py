@@ -20,6 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libzq.so")
 
 ZQ_OK = 0
+DEVICE_WAIT_EXPIRED = 1   # bit of the device status word: a bounded wait expired
 STATUS_NAMES = {0: "ZQ_OK", -1: "ZQ_ERR_ARG", -2: "ZQ_ERR_SHAPE", -3: "ZQ_ERR_ALIGN",
                 -4: "ZQ_ERR_CUDA", -5: "ZQ_ERR_DEVICE", -6: "ZQ_ERR_WORKSPACE"}
 
@@ -29,7 +30,8 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_device_status", "zq_q4k_gemm_noalloc", "zq_q4k_gemv_multi", "zq_rmsnorm_q4k_gemv",
            "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
-           "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe")
+           "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe",
+           "zq_debug_wait_expiry")
 
 
 class ZQError(RuntimeError):
@@ -83,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_q6k_bytes": ([i, i], sz),
         "zq_debug_stream_plan": ([i, i, i, ctypes.c_longlong, i, P], i),
         "zq_debug_peak_probe": ([i, i, i, P, P], i),
+        "zq_debug_wait_expiry": ([P, i, i, _Q8, P, i, ctypes.c_uint, i, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -348,6 +351,15 @@ def debug_q4k_isums(W: torch.Tensor, N: int, K: int, a: Q8_1, path: int = 0,
     _check(lib.zq_debug_q4k_isums(_ptr(W), N, K, a._c(), B, _ptr(isums), path, _ptr(workspace),
                                   wbytes, _stream(stream)))
     return isums
+
+
+def debug_wait_expiry(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor, withhold_stage: int,
+                      wait_us: int = 1000, ctas: int = 1, stream=None) -> None:
+    """One streamed mat-vec launch whose producers withhold a stage and whose
+    waits give up after wait_us (see zq_debug_wait_expiry); the expiry shows
+    in device_status()."""
+    _check(load().zq_debug_wait_expiry(_ptr(W), N, K, a._c(), _ptr(y), withhold_stage, wait_us, ctas,
+                                       _stream(stream)))
 
 
 # operations per probe launch, by kind (zq_debug_peak_probe)

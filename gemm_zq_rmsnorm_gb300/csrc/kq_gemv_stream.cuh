@@ -104,6 +104,12 @@ struct StreamParams {
     const uint8_t *pf;    // bytes for the next launch to pull into L2 once this one's are requested
     size_t pf_bytes;
     unsigned int *status;
+    // Failure-path test only (zero in every product launch): waits give up
+    // after wait_ns instead of the default limit, and when withhold > 0 the
+    // producer of every CTA stops before issuing its stage withhold - 1, so
+    // the consumers' wait for that stage must expire with no copy in flight.
+    uint64_t wait_ns;
+    int withhold;
 };
 
 // matrix of row group g
@@ -447,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const size_t tq = act_bytes(p.K, FMT == kFmtQ6K);   // and of one token's
     const int tds = p.K / 64;                  // and of its d8/s8 pairs (uint2 units)
     const int tas = p.K / 64;                  // and of its 8-code sums (uint4 units)
+    const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -470,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 const int rows = min(p.R, p.N[mat] - row0);
                 for (int pc = 0; pc < p.P; ++pc, ++it) {
                     const uint32_t slot = it % kStages, round = it / kStages;
-                    if (round > 0 && !mbar_wait(&empty[slot], (round & 1) ^ 1, p.status)) return;
+                    if (p.withhold > 0 && it == (uint32_t)(p.withhold - 1)) return;
+                    if (round > 0 && !mbar_wait_for(&empty[slot], (round & 1) ^ 1, p.status, wlim)) return;
                     const size_t bytes = (p.P == 1) ? (size_t)rows * p.rowbytes
                                                     : (size_t)min(p.CB, p.nb - pc * p.CB) * kBytes;
                     const size_t start = (size_t)row0 * p.rowbytes + (size_t)pc * p.CB * kBytes;
@@ -799,9 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             // itself (acquire) before reading the stage
             if (p.wl && abort_s) return;
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(&full[slot], round & 1, p.status);
+            if (lane == 0) ok = mbar_wait_for(&full[slot], round & 1, p.status, wlim);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (ok) ok = mbar_wait(&full[slot], round & 1, p.status);
+            if (ok) ok = mbar_wait_for(&full[slot], round & 1, p.status, wlim);
             if (!ok) abort_s = 1;
             // the tile starts (start mod 16) bytes into the stage
             const size_t start = (size_t)row0 * p.rowbytes + (size_t)pc * p.CB * kBytes;
@@ -1042,8 +1050,9 @@ size_t plan_smem(const StreamParams &p)
 
 // Host side: tile the job, size the stages and launch.  Returns
 // cudaErrorInvalidValue when the activation staging does not fit.
+// ctas > 0 plans and launches for that many CTAs instead of one per SM.
 template <int FMT, int NT>
-cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, cudaStream_t st)
+cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, cudaStream_t st, int ctas = 0)
 {
     static size_t attr_bytes[64];
     p.nmat = job.nmat;
@@ -1055,7 +1064,7 @@ cudaError_t launch_stream(StreamParams &p, const GemvJob &job, int K, int ntok, 
         p.N[m] = job.N[m];
         totalN += job.N[m];
     }
-    const int sms = num_sms();
+    const int sms = ctas > 0 ? ctas : num_sms();
     if (!plan_stream<FMT, NT>(p, K, totalN, sms)) return cudaErrorInvalidValue;
     p.gstart[0] = 0;
     for (int m = 0; m < kMaxMats; ++m)

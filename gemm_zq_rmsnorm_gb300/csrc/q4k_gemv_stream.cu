@@ -34,6 +34,26 @@ cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, 
     return stream::launch_fused<stream::kFmtQ4K>(job, K, x, gamma, eps, silu, q8out, pf, pf_bytes, st);
 }
 
+// Failure-path test: one matrix, one token, on `ctas` CTAs, whose producers
+// withhold stage `withhold` (counted per CTA from 0) and whose waits give up
+// after wait_ns.
+cudaError_t launch_q4k_wait_expiry(const void *W, int N, int K, zq_q8_1 a, float *y, int withhold,
+                                   uint64_t wait_ns, int ctas, cudaStream_t st)
+{
+    GemvJob job{};
+    job.nmat = 1;
+    job.W[0] = W;
+    job.N[0] = N;
+    job.y[0] = y;
+    stream::StreamParams p{};
+    p.qs = a.qs;
+    p.d = reinterpret_cast<const __half *>(a.d);
+    p.s = reinterpret_cast<const __half *>(a.s);
+    p.wait_ns = wait_ns;
+    p.withhold = withhold + 1;
+    return stream::launch_stream<stream::kFmtQ4K, 1>(p, job, K, 1, st, ctas);
+}
+
 // Launch plan of the streamed kernel (host only): out = R, P, CB, nseg,
 // warp-local, stage bytes, dynamic shared memory, row bytes.
 bool stream_plan_query(int fmt, int nt, int K, long long total_rows, int sms, int32_t *out)

@@ -501,6 +501,26 @@ int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void *strea
                     "zq_debug_peak_probe");
 }
 
+int zq_debug_wait_expiry(const void *W, int N, int K, zq_q8_1 a, float *y, int withhold_stage,
+                         unsigned int wait_us, int ctas, void *stream)
+{
+    const char *name = "zq_debug_wait_expiry";
+    int st = check_q4k(W, N, K, name);
+    if (st) return st;
+    if ((st = check_q8(a, name))) return st;
+    if (!y) return fail(ZQ_ERR_ARG, "%s: null y", name);
+    if (K > 32768) return fail(ZQ_ERR_SHAPE, "%s: K = %d above 32768", name, K);
+    if (withhold_stage < 0 || wait_us < 1 || wait_us > 2000000u)
+        return fail(ZQ_ERR_ARG, "%s: withhold_stage = %d, wait_us = %u out of range", name, withhold_stage, wait_us);
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    if (ctas < 1 || ctas > num_sms())
+        return fail(ZQ_ERR_ARG, "%s: ctas = %d out of range 1..%d", name, ctas, num_sms());
+    return launched(launch_q4k_wait_expiry(W, N, K, a, y, withhold_stage, (uint64_t)wait_us * 1000u, ctas,
+                                           (cudaStream_t)stream),
+                    name);
+}
+
 int zq_device_status(unsigned int *flags, int clear)
 {
     if (!flags) return fail(ZQ_ERR_ARG, "zq_device_status: null flags");

@@ -83,17 +83,24 @@ __device__ __forceinline__ uint64_t global_ns()
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kSleepNs = 20000;
 
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false (and raises the status flag) if it did not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status)
+// Bounded wait for the phase with the given parity to complete, giving up
+// after limit_ns.  Returns false (and raises the status flag) if it did not
+// complete in time.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, unsigned int *status,
+                                              uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     do {
         if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
-    } while (global_ns() - t0 < kWaitLimitNs);
+    } while (global_ns() - t0 < limit_ns);
     flag_timeout(status);
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned int *status)
+{
+    return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.

@@ -50,6 +50,8 @@ cudaError_t launch_gemv_stream_fused(const GemvJob &job, int K, const float *x, 
 // tokens of Q8_1 codes against one N x K matrix (K <= 32768); and the Q6_K
 // mat-vec of one token given as x and gamma (RMSNorm + Q8_1 in the launch).
 cudaError_t launch_q4k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
+cudaError_t launch_q4k_wait_expiry(const void *W, int N, int K, zq_q8_1 a, float *y, int withhold,
+                                   uint64_t wait_ns, int ctas, cudaStream_t st);
 cudaError_t launch_q5k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 cudaError_t launch_q6k_tokens(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 cudaError_t launch_q6k_fused(const GemvJob &job, int K, const float *x, const float *gamma, float eps,

@@ -365,6 +365,22 @@ ZQ_API int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows
  */
 ZQ_API int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void *stream);
 
+/*
+ * Test hook for the failure path of the bounded waits (no counterpart on the
+ * pages): one launch of the streamed Q4_K mat-vec (one token of Q8_1 codes a,
+ * N rows of K columns, y as in zq_q4k_gemv) on `ctas` CTAs (1 .. SM count)
+ * whose copy producers stop before issuing their stage `withhold_stage`
+ * (counted from 0 in each CTA), and whose waits give up after wait_us
+ * microseconds (1 .. 2000000) instead of two seconds.  Every CTA with more
+ * than withhold_stage stages of work then finds its consumers' wait expire,
+ * raises ZQ_DEVICE_WAIT_EXPIRED in the device status word and returns; no copy
+ * is in flight when it does.  Rows of the withheld and later stages of y are
+ * left unwritten.  The call itself returns ZQ_OK (the expiry is reported by
+ * zq_device_status, which the caller should then clear).  K <= 32768.
+ */
+ZQ_API int zq_debug_wait_expiry(const void *W, int N, int K, zq_q8_1 a, float *y, int withhold_stage,
+                                unsigned int wait_us, int ctas, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
