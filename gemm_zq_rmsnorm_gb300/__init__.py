@@ -31,7 +31,7 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
            "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe",
-           "zq_debug_wait_expiry")
+           "zq_debug_wait_expiry", "zq_q8_1_dequant_f16", "zq_f16_gemm_workspace_bytes", "zq_f16_gemm")
 
 
 class ZQError(RuntimeError):
@@ -86,6 +86,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_debug_stream_plan": ([i, i, i, ctypes.c_longlong, i, P], i),
         "zq_debug_peak_probe": ([i, i, i, P, P], i),
         "zq_debug_wait_expiry": ([P, i, i, _Q8, P, i, ctypes.c_uint, i, P], i),
+        "zq_q8_1_dequant_f16": ([_Q8, i, i, P, P], i),
+        "zq_f16_gemm_workspace_bytes": ([i, i, i], sz),
+        "zq_f16_gemm": ([P, i, i, P, i, P, P, sz, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -205,6 +208,35 @@ def q4k_dequant_f16(W: torch.Tensor, N: int, K: int, out: torch.Tensor | None = 
         out = torch.empty((N, K), dtype=torch.float16, device=W.device)
     _check(lib.zq_q4k_dequant_f16(_ptr(W), N, K, _ptr(out), _stream(stream)))
     return out
+
+
+def q8_1_dequant_f16(a: Q8_1, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Q8_1 planes of B tokens -> binary16 [B][K], x = q8 * d8 (see zq_q8_1_dequant_f16)."""
+    lib = load()
+    B, K = a.B, a.K
+    if out is None:
+        out = torch.empty((B, K), dtype=torch.float16, device=a.qs.device)
+    _check(lib.zq_q8_1_dequant_f16(a._c(), B, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def f16_gemm_workspace_bytes(N: int, K: int, B: int) -> int:
+    return int(load().zq_f16_gemm_workspace_bytes(N, K, B))
+
+
+def f16_gemm(W16: torch.Tensor, N: int, K: int, X16: torch.Tensor, B: int, y: torch.Tensor | None = None,
+             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[B][N] = X16 @ W16^T on the tensor cores (see zq_f16_gemm)."""
+    lib = load()
+    dev = W16.device
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=dev)
+    need = f16_gemm_workspace_bytes(N, K, B)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.zq_f16_gemm(_ptr(W16), N, K, _ptr(X16), B, _ptr(y), _ptr(workspace), wbytes, _stream(stream)))
+    return y
 
 
 def silu_mul_q8_1(gate: torch.Tensor, up: torch.Tensor, out: Q8_1 | None = None, stream=None) -> Q8_1:

@@ -1,5 +1,5 @@
-// q4k_dequant.cu -- Q4_K weights dequantised to binary16, the first step of a
-// dequantise-then-GEMM prefill (MIInfer README, "Current phase": Q4_K
+// q4k_dequant.cu -- Q4_K weights (and Q8_1 activations) dequantised to
+// binary16, the first step of a dequantise-then-GEMM prefill (MIInfer README, "Current phase": Q4_K
 // dequantised to 16-bit weights ahead of a dense GEMM, its best prefill lever).
 //
 // The library's own prefill keeps the weights in Q4_K and converts them tile
@@ -57,7 +57,37 @@ __global__ void q4k_dequant_f16_kernel(const uint8_t *__restrict__ W, int nb, si
     }
 }
 
+// Q8_1 activations dequantised to binary16, x = q8 * d8 (exact in fp32,
+// then one rounding to binary16, nearest even): eight codes per thread.
+__global__ void q8_1_dequant_f16_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d, size_t groups,
+                                        __half *__restrict__ out)
+{
+    const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= groups) return;
+    const uint2 q = *reinterpret_cast<const uint2 *>(qs + 8 * t);
+    const float d8 = __half2float(d[t >> 2]);   // four groups of eight per Q8_1 block
+    const uint32_t w[2] = {q.x, q.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int8_t c0 = (int8_t)((w[i >> 1] >> (16 * (i & 1))) & 0xFFu);
+        const int8_t c1 = (int8_t)((w[i >> 1] >> (16 * (i & 1) + 8)) & 0xFFu);
+        const __half2 h = __floats2half2_rn(__fmul_rn((float)c0, d8), __fmul_rn((float)c1, d8));
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(out + 8 * t) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace
+
+cudaError_t launch_q8_1_dequant_f16(zq_q8_1 a, int B, int K, void *out, cudaStream_t st)
+{
+    const size_t groups = (size_t)B * K / 8;
+    if (groups == 0) return cudaSuccess;
+    q8_1_dequant_f16_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(
+        a.qs, reinterpret_cast<const __half *>(a.d), groups, static_cast<__half *>(out));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_q4k_dequant_f16(const void *W, int N, int K, void *out, cudaStream_t st)
 {

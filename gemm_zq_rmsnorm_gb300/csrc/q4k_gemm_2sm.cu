@@ -66,6 +66,7 @@
 #include <cuda.h>
 
 #include "zq_cluster.cuh"
+#include "zq_pair_wait.cuh"
 #include "zq_internal.cuh"
 #include "zq_tc.cuh"
 #include "zq_tc_common.cuh"
@@ -240,89 +241,6 @@ __device__ __forceinline__ void convert_one(const uint8_t *raw, uint32_t col, ui
     }
 }
 
-// Bounded wait on a barrier that may receive arrivals from the peer CTA;
-// gives up at once when either CTA of the pair has already failed.  Inline
-// throughout: a call out of a warpgroup whose register count was changed
-// would force spills around it.
-// The pair's abort flag and the device status word live in shared memory
-// (set up by thread 0), so a wait keeps only the peer's flag address in
-// registers.
-__shared__ int s_abort;
-__shared__ unsigned int *s_status;
-
-struct PairCtx {
-    uint32_t abort_peer;   // cluster address of the peer's flag
-};
-
-__device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, const PairCtx &c)
-{
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    volatile int *abort_flag = &s_abort;
-    for (;;) {
-        if (*abort_flag) return false;
-        if (mbar_try_wait_cl_sleep(bar, parity, kSleepNs)) return true;
-        if (global_ns() - t0 >= kWaitLimitNs) {
-            flag_timeout(s_status);
-            *abort_flag = 1;
-            st_cluster_u32(c.abort_peer, 1u);
-            return false;
-        }
-    }
-}
-
-// Lane 0 waits; the warp follows it through __syncwarp (which orders the
-// other lanes after lane 0's acquire).  One barrier probe instead of 33.
-__device__ __forceinline__ bool pair_lane0_wait(uint64_t *bar, uint32_t parity, const PairCtx &c)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = pair_wait(bar, parity, c);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
-}
-
-// Latency-critical waits: up to 2000 non-suspending probes first, then the
-// sleeping bounded wait.
-__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool pair_wait_spin(uint64_t *bar, uint32_t parity, const PairCtx &c)
-{
-    for (int i = 0; i < 2000; ++i)
-        if (mbar_test_wait_cl(bar, parity)) return true;
-    return pair_wait(bar, parity, c);
-}
-
-__device__ __forceinline__ bool pair_lane0_wait_spin(uint64_t *bar, uint32_t parity, const PairCtx &c)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = pair_wait_spin(bar, parity, c);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
-}
-
-// Bounded wait that ignores the abort flags (draining work already issued).
-__device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity)
-{
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait_cl_sleep(bar, parity, kSleepNs)) return true;
-        if (global_ns() - t0 >= kWaitLimitNs) return false;
-    }
-}
-
 // The pair's tile and K range, recomputed inside each role (after its
 // register count changes) rather than kept live across the change.
 struct Tile {
@@ -350,12 +268,6 @@ __device__ __forceinline__ Tile tile_of(const Pair2Params &p, uint32_t rank)
     return t;
 }
 
-__device__ __forceinline__ PairCtx pair_ctx(uint32_t rank)
-{
-    PairCtx c;
-    c.abort_peer = cluster_addr(smem_u32(&s_abort), rank ^ 1u);
-    return c;
-}
 
 __device__ __forceinline__ void fma2(float &c0, float &c1, float a, float b0, float b1)
 {

@@ -403,6 +403,44 @@ int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream)
     return launched(launch_q4k_dequant_f16(W, N, K, out, (cudaStream_t)stream), "zq_q4k_dequant_f16 launch");
 }
 
+int zq_q8_1_dequant_f16(zq_q8_1 a, int B, int K, void *out, void *stream)
+{
+    int st = check_q8(a, "zq_q8_1_dequant_f16");
+    if (st) return st;
+    if (B < 1 || K < 32 || K % 32) return fail(ZQ_ERR_SHAPE, "zq_q8_1_dequant_f16: B = %d, K = %d", B, K);
+    if (!out) return fail(ZQ_ERR_ARG, "zq_q8_1_dequant_f16: null out");
+    if (!aligned16(out)) return fail(ZQ_ERR_ALIGN, "zq_q8_1_dequant_f16: out must be 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_q8_1_dequant_f16(a, B, K, out, (cudaStream_t)stream), "zq_q8_1_dequant_f16 launch");
+}
+
+size_t zq_f16_gemm_workspace_bytes(int N, int K, int B)
+{
+    if (N < 1 || K < 64 || K % 64 || B < 1) return 0;
+    return f16_gemm_workspace_bytes(N, K, B);
+}
+
+int zq_f16_gemm(const void *W16, int N, int K, const void *X16, int B, float *y, void *workspace,
+                size_t workspace_bytes, void *stream)
+{
+    const char *name = "zq_f16_gemm";
+    if (!W16 || !X16 || !y) return fail(ZQ_ERR_ARG, "%s: null pointer", name);
+    if (!aligned16(W16) || !aligned16(X16) || !aligned16(y))
+        return fail(ZQ_ERR_ALIGN, "%s: W16, X16 and y must be 16-byte aligned", name);
+    if (N < 1 || B < 1 || B > 65536 || K < 64 || K % 64 || K > (1 << 20))
+        return fail(ZQ_ERR_SHAPE, "%s: N = %d, K = %d, B = %d out of range", name, N, K, B);
+    const size_t need = f16_gemm_workspace_bytes(N, K, B);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(ZQ_ERR_WORKSPACE, "%s: workspace of %zu bytes required, got %zu", name, need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (need && !aligned16(workspace)) return fail(ZQ_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
+    int dev, st;
+    if ((st = check_device(&dev))) return st;
+    return launched(launch_f16_gemm(W16, N, K, X16, B, y, static_cast<float *>(workspace), (cudaStream_t)stream),
+                    name);
+}
+
 size_t zq_q5k_bytes(int N, int K)
 {
     if (N < 1 || K < 256 || K % 256) return 0;

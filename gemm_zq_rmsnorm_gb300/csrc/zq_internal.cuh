@@ -28,6 +28,12 @@ cudaError_t launch_isums_tc(const void *W, int N, int K, zq_q8_1 a, int B,
 bool gemv_stream_supported(int K);
 size_t noalloc_scratch_bytes();
 cudaError_t launch_q4k_dequant_f16(const void *W, int N, int K, void *out, cudaStream_t st);
+cudaError_t launch_q8_1_dequant_f16(zq_q8_1 a, int B, int K, void *out, cudaStream_t st);
+// dense binary16 GEMM y[B][N] = X16[B][K] * W16[N][K]^T (f16_gemm_2sm.cu);
+// part: split-K partial sums of f16_gemm_workspace_bytes
+size_t f16_gemm_workspace_bytes(int N, int K, int B);
+cudaError_t launch_f16_gemm(const void *W16, int N, int K, const void *X16, int B, float *y, float *part,
+                            cudaStream_t st);
 cudaError_t launch_gemm_noalloc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, cudaStream_t st);
 // Decode mat-vec job: up to kGemvMaxMats Q4_K matrices (N[m] x K) that read
 // the same input vector.

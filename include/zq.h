@@ -259,6 +259,31 @@ ZQ_API int zq_silu_q4k_gemv(const float *gate, const float *up, int K, int nmat,
 ZQ_API int zq_q4k_dequant_f16(const void *W, int N, int K, void *out, void *stream);
 
 /*
+ * Q8_1 activations dequantised to binary16, the activation half of the
+ * dequantise-then-GEMM design (MIInfer README, "Current phase").
+ *   a : Q8_1 planes of B tokens x K;  out : binary16 [B][K] (device, 16-byte
+ *   aligned, 2*B*K bytes).  x = q8 * d8 in fp32 (exact), rounded to binary16
+ *   (nearest even).  K % 32 == 0.
+ */
+ZQ_API int zq_q8_1_dequant_f16(zq_q8_1 a, int B, int K, void *out, void *stream);
+
+/*
+ * Dense binary16 GEMM on the tensor cores, the GEMM half of the
+ * dequantise-then-GEMM design (MIInfer README, "Current phase": Q4_K
+ * dequantised to 16-bit weights ahead of a dense GEMM), measured beside the
+ * library's Q4_K x Q8_1 projection; no library GEMM is involved.
+ *   W16 : binary16 [N][K] (row-major, device);  X16 : binary16 [B][K];
+ *   y   : fp32 [B][N] (device), y[t][n] = sum_k X16[t][k] * W16[n][k], each
+ *         product exact, accumulated in fp32 (order unspecified);
+ *   workspace : device, at least zq_f16_gemm_workspace_bytes(N, K, B) bytes
+ *         (split-K partial sums; 0 bytes when the call does not split).
+ * All pointers 16-byte aligned; K % 64 == 0, 1 <= B <= 65536.
+ */
+ZQ_API size_t zq_f16_gemm_workspace_bytes(int N, int K, int B);
+ZQ_API int zq_f16_gemm(const void *W16, int N, int K, const void *X16, int B, float *y, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * ---------------------------------------------------------- Q5_K and Q6_K
  * The other k-quant blocks of a Q4_K_M checkpoint (MIInfer README, "Status":
  * Q5_K x Q8_1 MMVQ-style recurrent output projection, MMVQ-style Q6_K x Q8_1

@@ -62,6 +62,10 @@ def _load():
         lib.zqo_q4k_dequant.restype = None
         lib.zqo_q4k_dequant_f16.argtypes = [P, i, i, P]
         lib.zqo_q4k_dequant_f16.restype = None
+        lib.zqo_q8_1_dequant_f16.argtypes = [P, P, i, i, P]
+        lib.zqo_q8_1_dequant_f16.restype = None
+        lib.zqo_f16_gemm_rows.argtypes = [P, P, i, i, P, i, P]
+        lib.zqo_f16_gemm_rows.restype = None
         lib.zqo_exp32.argtypes = [f]
         lib.zqo_exp32.restype = f
         lib.zqo_silu32.argtypes = [f]
@@ -181,6 +185,31 @@ def q4k_dequant_f16(W: np.ndarray, N: int, K: int) -> np.ndarray:
     w = np.zeros((N, K), np.uint16)
     _load().zqo_q4k_dequant_f16(_p(W), N, K, _p(w))
     return w
+
+
+def q8_1_dequant_f16(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Binary16 bit patterns [B][K] of x = q8 * d8 (see zqo_q8_1_dequant_f16)."""
+    qs = np.ascontiguousarray(np.atleast_2d(qs), dtype=np.int8)
+    d = np.ascontiguousarray(np.atleast_2d(d), dtype=np.uint16)
+    B, K = qs.shape
+    assert K % 32 == 0 and d.shape == (B, K // 32)
+    x = np.zeros((B, K), np.uint16)
+    _load().zqo_q8_1_dequant_f16(_p(qs), _p(d), B, K, _p(x))
+    return x
+
+
+def f16_gemm(x16: np.ndarray, w16: np.ndarray, rows=None) -> np.ndarray:
+    """y[t][r] (fp64) = sum_k x16[t][k] * w16[rows[r]][k] of binary16 bit
+    patterns x16 [B][K] and w16 [N][K] (see zqo_f16_gemm_rows)."""
+    x16 = np.ascontiguousarray(np.atleast_2d(x16), dtype=np.uint16)
+    w16 = np.ascontiguousarray(w16, dtype=np.uint16)
+    B, K = x16.shape
+    N = w16.shape[0]
+    assert w16.shape == (N, K)
+    r = np.arange(N, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    y = np.zeros((B, r.size), np.float64)
+    _load().zqo_f16_gemm_rows(_p(x16), _p(w16), B, K, _p(r), r.size, _p(y))
+    return y
 
 
 def q4k_isums(W: np.ndarray, N: int, K: int, qs: np.ndarray) -> np.ndarray:

@@ -313,6 +313,35 @@ void zqo_q4k_dequant_f16(const uint8_t *W, int N, int K, uint16_t *w16)
         }
 }
 
+/* Binary16 dequantised activations, the other input of the dequantise-then-
+ * GEMM design: x = q8 * d8 in fp32 (exact: 8 x 11 significant bits), then
+ * rounded to binary16. */
+void zqo_q8_1_dequant_f16(const int8_t *qs, const uint16_t *d16, int B, int K, uint16_t *x16)
+{
+    for (int t = 0; t < B; ++t)
+        for (int k = 0; k < K; ++k) {
+            float d = zqo_f16_to_f32(d16[(size_t)t * (K / 32) + k / 32]);
+            x16[(size_t)t * K + k] = zqo_f32_to_f16((float)qs[(size_t)t * K + k] * d);
+        }
+}
+
+/* The dense GEMM of that design on binary16 inputs, by its definition:
+ * y[t][r] = sum_k x[t][k] * w[rows[r]][k] in fp64 (each product of two
+ * binary16 values is exact in fp64; the fp64 sum rounds at 2^-53 relative,
+ * far below the fp32 accumulation it is compared with). */
+void zqo_f16_gemm_rows(const uint16_t *x16, const uint16_t *w16, int B, int K, const int *rows, int nrows,
+                       double *y)
+{
+    for (int t = 0; t < B; ++t)
+        for (int r = 0; r < nrows; ++r) {
+            const uint16_t *wr = w16 + (size_t)rows[r] * K;
+            const uint16_t *xt = x16 + (size_t)t * K;
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += (double)zqo_f16_to_f32(xt[k]) * (double)zqo_f16_to_f32(wr[k]);
+            y[(size_t)t * nrows + r] = acc;
+        }
+}
+
 /* ------------------------------------------------------------------------
  * Sub-block integer dot sums I[t][n][b*8+j] = sum_i q4 * q8 over the 32
  * weights of sub-block j of super-block b (MIInfer README, "Status": the

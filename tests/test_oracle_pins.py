@@ -313,6 +313,75 @@ def test_dequant_f16_within_half_ulp_of_fp64():
     assert np.all(np.abs(w16 - w64) <= 0.5 * ulp16 + a * 2.0 ** -24 + 1e-30)
 
 
+# ------------------------------------------- dequantise-then-GEMM (binary16)
+def test_q8_1_dequant_f16_hand_values():
+    """x = q8 * d8 rounded to binary16, worked by hand:
+    127 * 0.0625 = 7.9375 = 1.984375 * 2^2 -> 0x4400 | 1008 = 0x47F0 (exact);
+    -127 * 0.0625 -> 0xC7F0;
+    127 * (1 + 2^-10) = 127.1240234375, binary16 step 2^-4 in [64, 128):
+      nearest is 127.125 = 1.986328125 * 2^6 -> 0x5400 | 1010 = 0x57F2;
+    3 * (1 + 3 * 2^-10) = 3.0087890625 = 1540.5 steps of 2^-9: a tie, to the
+      even 1540 -> 3.0078125 = 1.50390625 * 2 -> 0x4000 | 516 = 0x4204;
+    1 * 2^-24 (the smallest subnormal d8) -> 0x0001; 0 * anything -> 0."""
+    qs = np.zeros((1, 64), np.int8)
+    d = np.zeros((1, 2), np.uint16)
+    d[0, 0] = 0x2C00
+    qs[0, 0], qs[0, 1] = 127, -127
+    d[0, 1] = 0x3C01
+    qs[0, 32] = 127
+    got = oracle.q8_1_dequant_f16(qs, d)
+    assert got[0, 0] == 0x47F0 and got[0, 1] == 0xC7F0 and got[0, 32] == 0x57F2
+    assert np.all(got[0, 2:32] == 0) and np.all(got[0, 33:] == 0)
+    qs2 = np.zeros((2, 32), np.int8)
+    qs2[0, 5] = 3
+    qs2[1, 7] = 1
+    d2 = np.array([[0x3C03], [0x0001]], np.uint16)
+    got2 = oracle.q8_1_dequant_f16(qs2, d2)
+    assert got2[0, 5] == 0x4204 and got2[1, 7] == 0x0001
+    assert np.count_nonzero(got2) == 2
+
+
+def test_q8_1_dequant_f16_matches_numpy():
+    """Random codes and scales: numpy's float32 product and float16 rounding,
+    with the block index k // 32 taken per token."""
+    rng = np.random.default_rng(5)
+    B, K = 3, 256
+    qs = rng.integers(-127, 128, size=(B, K)).astype(np.int8)
+    d = (rng.random((B, K // 32)) * 0.05).astype(np.float16).view(np.uint16)
+    want = (qs.astype(np.float32) * np.repeat(d.view(np.float16).astype(np.float32), 32, axis=1)).astype(
+        np.float16).view(np.uint16)
+    assert np.array_equal(oracle.q8_1_dequant_f16(qs, d), want)
+
+
+def test_f16_gemm_brute_force_exact():
+    """y = x w^T against exact rational sums on a tiny shape (distinct rows
+    and tokens, so a transposed operand or a dropped term shows)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(6)
+    B, N, K = 2, 3, 64
+    x = (rng.standard_normal((B, K)) * 4).astype(np.float16)
+    w = (rng.standard_normal((N, K)) / 8).astype(np.float16)
+    y = oracle.f16_gemm(x.view(np.uint16), w.view(np.uint16))
+    for t in range(B):
+        for n in range(N):
+            exact = sum(Fraction(float(x[t, k])) * Fraction(float(w[n, k])) for k in range(K))
+            assert abs(Fraction(y[t, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 60)
+    rows = [2, 0]
+    assert np.array_equal(oracle.f16_gemm(x.view(np.uint16), w.view(np.uint16), rows=rows), y[:, rows])
+
+
+def test_f16_gemm_selector_rows():
+    """w with one 1 per row picks a column of x: y[t][n] = x[t][perm[n]]."""
+    B, N, K = 4, 5, 64
+    x = np.arange(B * K, dtype=np.float32).reshape(B, K).astype(np.float16) - 100
+    perm = [7, 0, 63, 31, 2]
+    w = np.zeros((N, K), np.float16)
+    for n, k in enumerate(perm):
+        w[n, k] = 1
+    y = oracle.f16_gemm(x.view(np.uint16), w.view(np.uint16))
+    assert np.array_equal(y, x.astype(np.float64)[:, perm])
+
+
 # ---------------------------------------------------------------- SiLU * up
 def test_exp32_within_two_ulp_of_fp64():
     """exp32 against numpy's fp64 exponential on a dense grid of the clamped
