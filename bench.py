@@ -700,7 +700,8 @@ def peak_probes(torch, stream, local_rank, sms):
     import gemm_zq_rmsnorm_gb300 as zq
     out = {}
     sink = torch.empty(sms * 8 * 256, dtype=torch.int32, device="cuda")
-    cfg = {0: (sms * 8, 40000), 1: (sms * 8, 6000), 2: (sms, 40000)}
+    cfg = {0: (sms * 8, 40000), 1: (sms * 8, 6000), 2: (sms, 40000), 3: (sms, 40000), 4: (sms, 40000),
+           5: (sms, 40000), 6: (sms, 40000), 7: (sms, 40000), 8: (sms, 40000), 9: (sms, 40000)}
     with Clocks(local_rank) as clk:
         for kind, (blocks, iters) in cfg.items():
             with torch.cuda.stream(stream):
@@ -714,6 +715,8 @@ def peak_probes(torch, stream, local_rank, sms):
             ops = zq.probe_ops(kind, blocks, iters)
             out[zq.PROBE_KINDS[kind]] = {"tera_ops_per_s": round(ops / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
                                          "ops": ops, "blocks": blocks}
+            if kind >= 2:   # one issuing thread per SM: time per MMA instruction
+                out[zq.PROBE_KINDS[kind]]["ns_per_mma"] = round(ms * 1e6 / iters, 2)
     assert zq.device_status() == 0, "a probe's bounded wait expired"
     out["clocks"] = clk.summary()
     out["note"] = ("tcgen05.mma kind::i8 is rejected by ptxas for sm_103a, so the prefill path runs binary16 MMAs on "
@@ -867,7 +870,7 @@ def main():
             k2 = pr["tcgen05.mma kind::f16 128x256x16"]
             out.update({"value": k2["tera_ops_per_s"], "unit": "TFLOP/s", "ms_per_step": k2["ms"], "dtype": "f16",
                         "config": {"workload": "throughput probes"}, "clocks": pr["clocks"], "peaks": pr,
-                        "gpu_launches": 6})
+                        "gpu_launches": 20})
         else:
             out["peaks"] = pr
     if dist is not None:

@@ -395,7 +395,13 @@ def debug_wait_expiry(W: torch.Tensor, N: int, K: int, a: Q8_1, y: torch.Tensor,
 
 
 # operations per probe launch, by kind (zq_debug_peak_probe)
-PROBE_KINDS = {0: "dp4a", 1: "mma.sync m16n8k32 s8", 2: "tcgen05.mma kind::f16 128x256x16"}
+PROBE_KINDS = {0: "dp4a", 1: "mma.sync m16n8k32 s8", 2: "tcgen05.mma kind::f16 128x256x16",
+               3: "tcgen05.mma kind::f16 128x32x16", 4: "tcgen05.mma kind::f16 128x16x16",
+               5: "tcgen05.mma kind::f16 128x32x16, A in tensor memory",
+               6: "tcgen05.mma kind::f16 128x32x16, two issuing warps per SM",
+               7: "tcgen05.mma kind::f16 256x32x16, CTA pair",
+               8: "tcgen05.mma kind::f16 128x32x16, warp-wide loop, elected lane",
+               9: "tcgen05.mma kind::f16 256x32x16, CTA pair, warp-wide loop, elected lane"}
 
 
 def probe_ops(kind: int, blocks: int, iters: int) -> int:
@@ -403,7 +409,12 @@ def probe_ops(kind: int, blocks: int, iters: int) -> int:
         return blocks * 256 * iters * 8 * 8
     if kind == 1:
         return blocks * 8 * iters * 4 * 2 * 16 * 8 * 32
-    return blocks * iters * 2 * 128 * 256 * 16
+    if kind == 6:
+        return blocks * 2 * iters * 2 * 128 * 32 * 16
+    if kind in (7, 9):
+        return (blocks // 2) * iters * 2 * 256 * 32 * 16
+    n = {2: 256, 4: 16}.get(kind, 32)
+    return blocks * iters * 2 * 128 * n * 16
 
 
 def debug_peak_probe(kind: int, blocks: int, iters: int, sink: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -149,7 +149,8 @@ f16_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_con
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
-        if (rank == 0 && lane == 0) {
+        // (the whole warp runs the loop and waits; one elected lane issues)
+        if (rank == 0) {
             const uint32_t tmem = *tmem_slot;
             const uint32_t base = smem_u32(sm);
             const uint64_t a0 = smem_desc(base + (uint32_t)Smem::a(0), 16, 1024, kLayoutSw128);
@@ -162,24 +163,30 @@ f16_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_con
                 const Unit U = unit_of(p, u, 0);
                 const int buf = j & 1;
                 // accumulator buf was last used by unit j - 2: both epilogues have read it
-                if (j >= 2 && !(ok = pair_wait(&tempty[buf], ((j >> 1) - 1) & 1, ctx))) break;
+                if (j >= 2 && !(ok = __all_sync(0xffffffffu, pair_wait(&tempty[buf], ((j >> 1) - 1) & 1, ctx))))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(kTileN * buf);
                 const uint32_t idesc = idesc_f16_f32(kPairM, (uint32_t)U.n);
                 for (int s = 0; s < U.ns; ++s, ++it) {
                     const uint32_t slot = it % kStages;
-                    if (!(ok = pair_wait(&full[slot], (it / kStages) & 1, ctx))) break;
+                    if (!(ok = __all_sync(0xffffffffu, pair_wait(&full[slot], (it / kStages) & 1, ctx)))) break;
                     tc_fence_after();
                     const uint64_t so = (uint64_t)slot * kS16;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < kStageK / 16; ++kk)
-                        mma_f16_pair(d, a0 + so + 2 * kk, b0 + so + 2 * kk, idesc, (s | kk) != 0 ? 1u : 0u);
-                    mma_commit_pair_mc(&empty[slot], 3);
+                        for (int kk = 0; kk < kStageK / 16; ++kk)
+                            mma_f16_pair(d, a0 + so + 2 * kk, b0 + so + 2 * kk, idesc, (s | kk) != 0 ? 1u : 0u);
+                        mma_commit_pair_mc(&empty[slot], 3);
+                    }
+                    __syncwarp();
                 }
-                if (ok) mma_commit_pair_mc(&tfull[buf], 3);
+                if (ok && elect_one()) mma_commit_pair_mc(&tfull[buf], 3);
+                __syncwarp();
             }
             // every MMA issued has completed before the pair tears down
-            mma_commit_pair_local(drain);
+            if (elect_one()) mma_commit_pair_local(drain);
+            __syncwarp();
             drain_wait(drain, 0);
         }
     } else if (warp >= kEpiWarp0) {

@@ -8,6 +8,7 @@
 // keeps its results live by writing one value per thread or CTA to `sink`.
 #include <cuda.h>
 
+#include "zq_cluster.cuh"
 #include "zq_internal.cuh"
 #include "zq_tc.cuh"
 
@@ -62,7 +63,19 @@ __global__ void __launch_bounds__(256) probe_mma_s8_kernel(int iters, int seed, 
 // memory, then waits for them (bounded) and reads one accumulator value.
 constexpr int kProbeSmem = 2 * 128 * 128 + 2 * 256 * 128 + 1024;
 
-__global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int iters, int *sink, unsigned int *status)
+// MMA shapes of the probe kinds 2.. (M = 128, K = 16): N, whether A is read
+// from tensor memory (columns 128.., written once) instead of shared memory,
+// and whether two warps issue at once (each `iters` MMAs into its own
+// accumulator: columns 0.. and 64..)
+__host__ __device__ constexpr int probe_tc_n(int kind) { return kind == 2 ? 256 : kind == 4 ? 16 : 32; }
+__host__ __device__ constexpr bool probe_tc_ta(int kind) { return kind == 5; }
+__host__ __device__ constexpr bool probe_tc_two(int kind) { return kind == 6; }
+// kinds 8 (one CTA) and 9 (a pair): the issuing loop runs on all lanes of a
+// warp and one elected lane issues each MMA
+__host__ __device__ constexpr bool probe_tc_warp(int kind) { return kind == 8 || kind == 9; }
+
+
+__global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int kind, int iters, int *sink, unsigned int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -74,7 +87,7 @@ __global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int iters, int *si
         reinterpret_cast<uint32_t *>(sm)[i] = 0x3C003C00u;   // 1.0, 1.0
     fence_async_smem();
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        mbar_init(&bar, probe_tc_two(kind) ? 2 : 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&slot, 256);
@@ -82,12 +95,46 @@ __global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int iters, int *si
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = slot;
-    if (threadIdx.x == 0) {
+    if (probe_tc_ta(kind)) {
+        // A in tensor memory: 128 lanes x 32 columns of binary16 pairs 1.0
+        uint32_t one[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) one[i] = 0x3C003C00u;
+        tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + 128u, one);
+        tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + 144u, one);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (probe_tc_warp(kind)) {
+        if (warp == 0) {
+            const uint32_t base = smem_u32(sm);
+            const uint64_t ad = smem_desc(base, 16, 1024, kLayoutSw128);
+            const uint64_t bd = smem_desc(base + 2 * 128 * 128, 16, 1024, kLayoutSw128);
+            const uint32_t idesc = idesc_f16_f32(128, 32);
+            for (int it = 0; it < iters; ++it) {
+                if (elect_one()) mma_f16(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+                __syncwarp();
+            }
+            if (elect_one()) mma_commit(&bar);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_wait(&bar, 0, status);
+            __syncwarp();
+        }
+    } else if (threadIdx.x == 0 || (probe_tc_two(kind) && threadIdx.x == 32)) {
+        const uint32_t d = tmem + (threadIdx.x ? 64u : 0u);
         const uint32_t base = smem_u32(sm);
         const uint64_t ad = smem_desc(base, 16, 1024, kLayoutSw128);
         const uint64_t bd = smem_desc(base + 2 * 128 * 128, 16, 1024, kLayoutSw128);
-        constexpr uint32_t idesc = idesc_f16_f32(128, 256);
-        for (int it = 0; it < iters; ++it) mma_f16(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+        const uint32_t idesc = idesc_f16_f32(128, (uint32_t)probe_tc_n(kind));
+        if (probe_tc_ta(kind)) {
+            for (int it = 0; it < iters; ++it)
+                mma_f16_ta(d, tmem + 128u + 8u * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+        } else {
+            for (int it = 0; it < iters; ++it)
+                mma_f16(d, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+        }
         mma_commit(&bar);
         mbar_wait(&bar, 0, status);
     }
@@ -105,7 +152,76 @@ __global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int iters, int *si
     }
 }
 
+// Kind 7: a CTA pair; one thread of the even CTA issues `iters` 256 x 32 x 16
+// MMAs (cta_group::2: 128 rows in each SM's tensor memory), operands in each
+// CTA's shared memory.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+probe_tc_pair_kernel(int iters, int warpwide, int *sink, unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t slot;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t rank = cluster_rank();
+    for (int i = threadIdx.x; i < (2 * 128 * 128 + 2 * 256 * 128) / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(sm)[i] = 0x3C003C00u;
+    fence_async_smem();
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc_pair(&slot, 256);
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = slot;
+    if (rank == 0 && warpwide && warp == 0) {
+        const uint32_t base = smem_u32(sm);
+        const uint64_t ad = smem_desc(base, 16, 1024, kLayoutSw128);
+        const uint64_t bd = smem_desc(base + 2 * 128 * 128, 16, 1024, kLayoutSw128);
+        const uint32_t idesc = idesc_f16_f32(256, 32);
+        for (int it = 0; it < iters; ++it) {
+            if (elect_one()) mma_f16_pair(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+            __syncwarp();
+        }
+        if (elect_one()) mma_commit_pair_mc(&bar, 3);
+        __syncwarp();
+    } else if (rank == 0 && !warpwide && threadIdx.x == 0) {
+        const uint32_t base = smem_u32(sm);
+        const uint64_t ad = smem_desc(base, 16, 1024, kLayoutSw128);
+        const uint64_t bd = smem_desc(base + 2 * 128 * 128, 16, 1024, kLayoutSw128);
+        const uint32_t idesc = idesc_f16_f32(256, 32);
+        for (int it = 0; it < iters; ++it)
+            mma_f16_pair(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+        mma_commit_pair_mc(&bar, 3);
+    }
+    if (threadIdx.x == 0) {
+        // both CTAs wait for the commit that reaches them (bounded)
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait_cl_sleep(&bar, 0, kSleepNs)) {
+            if (global_ns() - t0 >= kWaitLimitNs) {
+                flag_timeout(status);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    uint32_t r[16];
+    tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16), r);
+    tmem_wait_ld();
+    sink[blockIdx.x * blockDim.x + threadIdx.x] = (int)r[0];
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 256);
+    }
+}
+
 size_t g_attr_bytes[64];
+size_t g_attr_pair[64];
 
 }  // namespace
 
@@ -125,7 +241,18 @@ cudaError_t launch_peak_probe(int kind, int blocks, int iters, int *sink, cudaSt
             if (e != cudaSuccess) return e;
             g_attr_bytes[dev] = kProbeSmem;
         }
-        probe_tc_f16_kernel<<<blocks, 128, kProbeSmem, st>>>(iters, sink, device_status_word());
+        if (kind == 7 || kind == 9) {
+            if (g_attr_pair[dev] < (size_t)kProbeSmem) {
+                cudaError_t e = cudaFuncSetAttribute(probe_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     kProbeSmem);
+                if (e != cudaSuccess) return e;
+                g_attr_pair[dev] = kProbeSmem;
+            }
+            probe_tc_pair_kernel<<<2 * (blocks / 2), 128, kProbeSmem, st>>>(iters, kind == 9 ? 1 : 0, sink,
+                                                                             device_status_word());
+        } else {
+            probe_tc_f16_kernel<<<blocks, 128, kProbeSmem, st>>>(kind, iters, sink, device_status_word());
+        }
     }
     return cudaGetLastError();
 }

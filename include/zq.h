@@ -384,7 +384,18 @@ ZQ_API int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows
  *   kind 1  mma.sync m16n8k32 s8 (8 warps, 4 per step):
  *           blocks * 8 * iters * 4 * 2 * 16 * 8 * 32;
  *   kind 2  tcgen05.mma kind::f16 128 x 256 x 16 (one issuing thread per
- *           block, one block per SM at most): blocks * iters * 2*128*256*16.
+ *           block, one block per SM at most): blocks * iters * 2*128*256*16;
+ *   kinds 3, 4  the same MMA with N = 32 and N = 16 (the chunk shapes):
+ *           blocks * iters * 2*128*N*16;
+ *   kind 5  N = 32 with the A operand read from tensor memory:
+ *           blocks * iters * 2*128*32*16;
+ *   kind 6  N = 32, two warps of each block issuing at once (own
+ *           accumulators): blocks * 2 * iters * 2*128*32*16;
+ *   kind 7  CTA pairs (blocks rounded down to even), one thread per pair
+ *           issuing 256 x 32 x 16 MMAs (cta_group::2):
+ *           (blocks/2) * iters * 2*256*32*16;
+ *   kinds 8, 9  as 3 and 7, with the issuing loop run by a whole warp and
+ *           each MMA issued by one elected lane.
  *   sink : device memory of at least blocks * 256 ints (results kept live).
  * A kind-2 probe whose bounded wait expires sets ZQ_DEVICE_WAIT_EXPIRED.
  */
