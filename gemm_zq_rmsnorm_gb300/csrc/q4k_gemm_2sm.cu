@@ -46,12 +46,13 @@
 // barrier of the stage that last used its slot).
 //
 // Warp roles (16 warps, four warpgroups):
-//   0      TMA producers: lane 0 the binary16 hi/lo token tiles (five stages)
+//   0      token TMA producer: the binary16 hi/lo token tiles (five stages)
 //          and the s8 tiles, whose bytes are counted on the even CTA's stage
-//          barrier; lane 1 the raw Q4_K tiles of this CTA's 128 rows (two
-//          super-block slots);
+//          barrier;
 //   1      MMA issuer (even CTA only) and tensor-memory owner (both CTAs);
-//   2, 3   idle;
+//   2      raw-tile TMA producer: the Q4_K tiles of this CTA's 128 rows (two
+//          super-block slots);
+//   3      idle;
 //   4-7    converters, one weight row per thread (TMEM lane = row): nibbles
 //          -> sc*q binary16 in registers -> tensor memory; the odd CTA's
 //          warps signal a converted stage to the even CTA's barrier with
@@ -70,6 +71,7 @@
 #include "zq_internal.cuh"
 #include "zq_tc.cuh"
 #include "zq_tc_common.cuh"
+#include "q4k_tc_convert.cuh"
 
 namespace zq {
 namespace {
@@ -128,119 +130,6 @@ struct Pair2Params {
     unsigned int *status;
 };
 
-// Per weight row and super-block: a power of two 2^-e applied to w = sc*q
-// (0 when d = 0), the ratio r whose binary16 parts carry the min term
-// (-r * m_j), and the fold factor of the accumulator, so that
-// fold * (wmul * w * x' - r * m * s8) = d * w * x' - dmin * m * s8.
-// e comes from the binary16 exponents alone (integer arithmetic, identical in
-// the converters and the epilogue): it keeps |r * m| < 2^14, so the parts of
-// the min operand stay in binary16 range; wmul * w stays exact while e <= 24
-// (dmin / d below 2^31).
-struct Fold {
-    float wmul, fold;
-    int e;
-};
-
-// floor(log2 |v|) of a non-zero binary16 magnitude (subnormals included)
-__device__ __forceinline__ int f16_ilog2(uint32_t h)
-{
-    const uint32_t E = (h >> 10) & 31u, M = h & 1023u;
-    return E ? (int)E - 15 : -24 + 31 - __clz((int)M);
-}
-
-__device__ __forceinline__ Fold fold_of(uint32_t d_dmin)
-{
-    const uint32_t hd = d_dmin & 0x7FFFu, hm = (d_dmin >> 16) & 0x7FFFu;
-    int e = 0;
-    if (hm) e = max(0, f16_ilog2(hm) - (hd ? f16_ilog2(hd) : 0) - 7);
-    Fold f;
-    f.e = e;
-    f.wmul = hd ? ldexpf(1.0f, -e) : 0.0f;
-    const float d = __half2float(__ushort_as_half((unsigned short)(d_dmin & 0xFFFFu)));
-    f.fold = ldexpf(hd ? d : 1.0f, e);
-    return f;
-}
-
-// r * 2^-e: dmin / d (dmin itself when d = 0), scaled
-__device__ __forceinline__ float ratio_of(uint32_t d_dmin, int e)
-{
-    const float d = __half2float(__ushort_as_half((unsigned short)(d_dmin & 0xFFFFu)));
-    const float dm = __half2float(__ushort_as_half((unsigned short)(d_dmin >> 16)));
-    return ldexpf((d_dmin & 0x7FFFu) ? dm / d : dm, -e);
-}
-
-// Eight weights sc*q*wmul of one sub-block pair's nibble word w, as two
-// binary16 pairs for the low nibbles (even sub-block) and two for the high
-// nibbles (odd sub-block), in byte order.  The nibble is placed in the
-// mantissa of 1024 (low) or 1024 + 16 q (high), so one fused binary16
-// operation with scale s, offset -1024 s (low) or s/16, -64 s (high) gives
-// s * q exactly while it fits in 11 bits.
-__device__ __forceinline__ void nib8_to_h2(uint32_t w, __half2 s_lo, __half2 o_lo, __half2 s_hi, __half2 o_hi,
-                                           uint32_t &l0, uint32_t &l1, uint32_t &h0, uint32_t &h1)
-{
-    const uint32_t p0 = __byte_perm(w, 0, 0x4140);   // [b0, 0, b1, 0]
-    const uint32_t p1 = __byte_perm(w, 0, 0x4342);   // [b2, 0, b3, 0]
-    const uint32_t a0 = (p0 & 0x000F000Fu) | 0x64006400u, a1 = (p1 & 0x000F000Fu) | 0x64006400u;
-    const uint32_t c0 = (p0 & 0x00F000F0u) | 0x64006400u, c1 = (p1 & 0x00F000F0u) | 0x64006400u;
-    l0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&a0), s_lo, o_lo));
-    l1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&a1), s_lo, o_lo));
-    h0 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&c0), s_hi, o_hi));
-    h1 = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&c1), s_hi, o_hi));
-}
-
-// Converts stage I (sub-blocks 2I, 2I+1) of one weight row and stores it in
-// the row's lane of a tensor-memory A slot at column address `col`: binary16
-// pairs in K order, the low nibbles (sub-block 2I) in columns 0..15, the
-// high nibbles (2I+1) in 16..31; for I = 3 also the row's min operand
-// (-r * m_j as binary16 hi, then lo) in its 32-byte-swizzled shared-memory
-// row `mrow`.
-template <int I>
-__device__ __forceinline__ void convert_one(const uint8_t *raw, uint32_t col, uint8_t *mrow, int r)
-{
-    const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
-    const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * I);
-    const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * I);
-    const Fold f = fold_of(hdr.x);
-    const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-#pragma unroll
-    for (int hi = 0; hi < 2; ++hi) {
-        uint32_t sc, md;
-        q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * I + hi, sc, md);
-        const float scf = (float)sc * f.wmul;
-        const __half2 s2 = __float2half2_rn(hi ? scf * 0.0625f : scf);
-        const __half2 o2 = __float2half2_rn(hi ? -64.0f * scf : -1024.0f * scf);
-        const uint32_t m = hi ? 0x00F000F0u : 0x000F000Fu;
-        uint32_t o[16];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {   // nibble bytes 4c..4c+3 -> columns 2c, 2c+1
-            const uint32_t p0 = (__byte_perm(wv[c], 0, 0x4140) & m) | 0x64006400u;   // bytes 0, 1
-            const uint32_t p1 = (__byte_perm(wv[c], 0, 0x4342) & m) | 0x64006400u;   // bytes 2, 3
-            o[2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&p0), s2, o2));
-            o[2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&p1), s2, o2));
-        }
-        tmem_st16(col + 16u * hi, o);
-    }
-    if (I == 3) {
-        const float rr = ratio_of(hdr.x, f.e);
-        uint32_t hv[4], lv[4];
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            uint32_t m0v, m1v, scd;
-            q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, m0v);
-            q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, scd, m1v);
-            const float v0 = -rr * (float)m0v, v1 = -rr * (float)m1v;
-            const __half2 hh = __floats2half2_rn(v0, v1);
-            const float2 hb = __half22float2(hh);
-            hv[j >> 1] = h2_bits(hh);
-            lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
-        }
-        const int s32 = (r >> 2) & 1;
-        *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        fence_async_smem();   // the min MMA reads this row through the async proxy
-    }
-}
-
 // The pair's tile and K range, recomputed inside each role (after its
 // register count changes) rather than kept live across the change.
 struct Tile {
@@ -268,22 +157,6 @@ __device__ __forceinline__ Tile tile_of(const Pair2Params &p, uint32_t rank)
     return t;
 }
 
-
-__device__ __forceinline__ void fma2(float &c0, float &c1, float a, float b0, float b1)
-{
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%2, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%0, %1};\n\t"
-        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
-        : "+f"(c0), "+f"(c1)
-        : "f"(a), "f"(b0), "f"(b1));
-}
-
-__device__ __forceinline__ uint32_t ld_nc_u32(const void *p)
-{
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_constant__ CUtensorMap tmap_lo,
@@ -364,7 +237,11 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                     // of the stage this slot held last
                     if (i == 3) tma_load_2d_pair(sm + Smem::bmin(b & 1), &tmap_s8, 16 * T.sb(b), tok0, fb);
                 }
-            } else if (lane == 1) {
+            }
+        } else if (warp == 2) {
+            // (a warp of its own: a lane of the token producer's warp waiting
+            // on the raw ring would hold that warp's token copies back)
+            if (lane == 0) {
                 // ------------------------------------------ raw Q4_K tiles
                 prefetch_tmap(&tmap_w);
                 for (int bb = 0; bb < nb; ++bb) {
@@ -376,7 +253,8 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             }
         } else if (warp == 1) {
             // ------------------------------------------------ MMA issuer
-            if (rank == 0 && lane == 0) {
+            // (the whole warp runs the loop and waits; one elected lane issues)
+            if (rank == 0) {
                 const uint32_t tmem = *tmem_slot;
                 const uint32_t base = smem_u32(sm);
                 const uint64_t bh0 = smem_desc(base + (uint32_t)Smem::bhi(0), 16, 1024, kLayoutSw128);
@@ -391,26 +269,31 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                     const int k = q % kASlots;
                     if (i == 0 && b > 0) {
                         // the epilogue has read X_{b-1}
-                        if (!(ok = pair_wait_spin(tempty, (b - 1) & 1, ctx))) break;
+                        if (!(ok = __all_sync(0xffffffffu, pair_wait_spin(tempty, (b - 1) & 1, ctx)))) break;
                     }
                     const int s = q % kStages;
-                    if (!(ok = pair_wait_spin(&afull[k], (q / kASlots) & 1, ctx))) break;
+                    if (!(ok = __all_sync(0xffffffffu, pair_wait_spin(&afull[k], (q / kASlots) & 1, ctx)))) break;
                     tc_fence_after();
                     const uint32_t a_tmem = tmem + kACol0 + kACols * k;
                     const uint64_t so = (uint64_t)s * kB16;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bh0 + so + 2 * kk, idesc, (i | kk) != 0 ? 1u : 0u);
-                        mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bl0 + so + 2 * kk, idesc, 1u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bh0 + so + 2 * kk, idesc, (i | kk) != 0 ? 1u : 0u);
+                            mma_f16_pair_ta(tmem, a_tmem + 8 * kk, bl0 + so + 2 * kk, idesc, 1u);
+                        }
+                        if (i == 3) {
+                            mma_f16_pair(tmem, am0 + (uint64_t)(b & 1) * kM16, bmn + (uint64_t)(b & 1) * kM16, idesc,
+                                         1u);
+                            mma_commit_pair_mc(tfull, 3);
+                        }
+                        mma_commit_pair_mc(&aempty[k], 3);
                     }
-                    if (i == 3) {
-                        mma_f16_pair(tmem, am0 + (uint64_t)(b & 1) * kM16, bmn + (uint64_t)(b & 1) * kM16, idesc, 1u);
-                        mma_commit_pair_mc(tfull, 3);
-                    }
-                    mma_commit_pair_mc(&aempty[k], 3);
+                    __syncwarp();
                 }
                 // every MMA issued has completed before the pair tears down
-                mma_commit_pair_local(drain);
+                if (elect_one()) mma_commit_pair_local(drain);
+                __syncwarp();
                 drain_wait(drain, 0);
             }
         } else if (warp >= kConvWarp0) {

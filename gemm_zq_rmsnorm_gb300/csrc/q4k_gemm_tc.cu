@@ -5,7 +5,7 @@
 //
 // MIInfer README, "Current phase": token-batched chunk projections and
 // tensor-core prefill.  B >= 17 runs the CTA-pair kernel (q4k_gemm_2sm.cu),
-// 5 <= B <= 16 the small-batch kernel (q4k_gemm_small.cu); both read the
+// 5 <= B <= 16 the chunk kernel (q4k_gemm_chunk.cu); both read the
 // activations as x' = q8 * d8 split into binary16 hi + lo, so that every
 // product with a weight code sc * q4 is exact.
 #include <cuda.h>
@@ -17,14 +17,16 @@
 namespace zq {
 namespace {
 
-// One CTA per token: x' = q8 * d8 split into binary16 hi + lo.  The token's
-// codes are scaled by 2^-k, k >= 0 the least that keeps 127 * max d8 within
-// binary16 range, and tscale[t] = 2^k.
+// CTA (t, c): token t's super-blocks c*sbc .. (c+1)*sbc - 1, x' = q8 * d8
+// split into binary16 hi + lo.  The token's codes are scaled by 2^-k, k >= 0
+// the least that keeps 127 * max d8 within binary16 range (every CTA of the
+// token finds the same maximum over all its d8), and tscale[t] = 2^k.
 constexpr int kSplitThreads = 256;
 
 __global__ void __launch_bounds__(kSplitThreads)
 q8_split_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d8, const __half *__restrict__ s8, int K,
-                __half *__restrict__ hi, __half *__restrict__ lo, float *__restrict__ tscale, __half *__restrict__ s8x)
+                int sbc, __half *__restrict__ hi, __half *__restrict__ lo, float *__restrict__ tscale,
+                __half *__restrict__ s8x)
 {
     __shared__ float red[kSplitThreads / 32];
     const int t = blockIdx.x;
@@ -43,9 +45,10 @@ q8_split_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d8, co
     const float bound = 127.0f * m;   // >= every |x'| of the token
     if (bound > 65504.0f) frexpf(bound / 65504.0f, &k);   // bound / 65504 <= 2^k
     const float down = ldexpf(1.0f, -k);
-    if (threadIdx.x == 0) tscale[t] = ldexpf(1.0f, k);
+    if (threadIdx.x == 0 && blockIdx.y == 0) tscale[t] = ldexpf(1.0f, k);
     const int8_t *qt = qs + (size_t)t * K;
-    for (int g = threadIdx.x; g < (K >> 4); g += kSplitThreads) {
+    const int sb0 = blockIdx.y * sbc, sb1 = min(K >> 8, sb0 + sbc);   // this CTA's super-blocks
+    for (int g = 16 * sb0 + threadIdx.x; g < 16 * sb1; g += kSplitThreads) {
         const int4 v = __ldg(reinterpret_cast<const int4 *>(qt) + g);
         const float dv = __half2float(dt[g >> 1]) * down;
         const int w[4] = {v.x, v.y, v.z, v.w};
@@ -73,7 +76,7 @@ q8_split_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d8, co
         // twice (the B operand of the pair kernel's min-term MMA)
         const uint4 *st = reinterpret_cast<const uint4 *>(s8 + (size_t)t * nblk);
         uint4 *dx = reinterpret_cast<uint4 *>(s8x + (size_t)t * (K >> 4));
-        for (int g = threadIdx.x; g < (K >> 8); g += kSplitThreads) {
+        for (int g = sb0 + threadIdx.x; g < sb1; g += kSplitThreads) {
             const uint4 v = __ldg(st + g);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t o[4];
@@ -162,38 +165,20 @@ size_t g_attr_bytes[64];
 // fp32 (when splits > 1); each region padded to 256 bytes
 size_t split_bytes(int K, int B) { return (size_t)B * K * sizeof(__half); }
 size_t tscale_bytes(int B) { return ((size_t)B * sizeof(float) + 255) & ~(size_t)255; }
-size_t s8x_bytes(int K, int B) { return B > kSmallMaxB ? (((size_t)B * (K / 16) * sizeof(__half) + 255) & ~(size_t)255) : 0; }
-
-// Split-K count of the small-batch kernel (B <= 16: one token tile, weight
-// tiles of 128 rows): tiles that fill the SMs unevenly waste whole waves.
-// Model the time of `s` splits as waves * (super-blocks per split + a fixed
-// per-CTA cost) plus the partial-sum traffic, and take the smallest s within
-// 3 % of the best, keeping >= 2 super-blocks per split.
-int choose_splits(int B, int N, int K, int sms)
-{
-    const long long tiles = (long long)((N + 127) / 128);
-    const int nb = K / 256;
-    const int smax = nb / 2 < 8 ? nb / 2 : 8;
-    double cost[9];
-    double best = 1e300;
-    for (int sp = 1; sp <= (smax > 1 ? smax : 1); ++sp) {
-        const long long ctas = tiles * sp;
-        const double waves = (double)((ctas + sms - 1) / sms);
-        double c = waves * ((double)nb / sp + 1.5);
-        if (sp > 1) c += (double)(sp + 1) * B * N * 4.0 / 1.85e7;   // partials, in super-block times
-        cost[sp] = c;
-        if (c < best) best = c;
-    }
-    for (int sp = 1; sp <= (smax > 1 ? smax : 1); ++sp)
-        if (cost[sp] <= best * 1.03) return sp;
-    return 1;
-}
+size_t s8x_bytes(int K, int B) { return B > 1 ? (((size_t)B * (K / 16) * sizeof(__half) + 255) & ~(size_t)255) : 0; }
 
 cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, float *tscale, __half *s8x,
                             cudaStream_t st)
 {
-    q8_split_kernel<<<B, kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d),
-                                                 reinterpret_cast<const __half *>(a.s), K, hi, lo, tscale, s8x);
+    // few tokens: split each token's K over several CTAs (two or more CTAs per SM in all)
+    const int nb = K / 256;
+    int chunks = (2 * num_sms() + B - 1) / B;
+    chunks = chunks < 1 ? 1 : (chunks > nb ? nb : chunks);
+    const int sbc = (nb + chunks - 1) / chunks;
+    chunks = (nb + sbc - 1) / sbc;
+    q8_split_kernel<<<dim3(B, chunks), kSplitThreads, 0, st>>>(a.qs, reinterpret_cast<const __half *>(a.d),
+                                                               reinterpret_cast<const __half *>(a.s), K, sbc, hi, lo,
+                                                               tscale, s8x);
     return cudaGetLastError();
 }
 
@@ -229,16 +214,24 @@ cudaError_t launch_q8_to_f16(const int8_t *qs, __half *out, size_t n, cudaStream
 
 int gemm_splits(int B, int N, int K, bool allow_split)
 {
-    if (!allow_split) return 1;
-    return B > kSmallMaxB ? choose_splits_pair(B, N, K, num_sms()) : choose_splits(B, N, K, num_sms());
+    if (!allow_split || B <= kSmallMaxB) return 1;
+    return choose_splits_pair(B, N, K, num_sms());
+}
+
+// Partial-sum bytes: split-K slices (B > 16) or the pieces of tiles that
+// straddle the chunk kernel's ranges (B <= 16); none without splitting.
+static size_t part_bytes(int N, int K, int B, bool allow_split)
+{
+    if (!allow_split) return 0;
+    if (B <= kSmallMaxB) return chunk_part_bytes(N, K, B);
+    const int sp = gemm_splits(B, N, K, true);
+    return sp > 1 ? (size_t)sp * split_stride(B, N) * sizeof(float) : 0;
 }
 
 size_t gemm_tc_workspace_bytes(int N, int K, int B, bool allow_split)
 {
     if (B <= 1) return 0;
-    const int sp = gemm_splits(B, N, K, allow_split);
-    return 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B) +
-           (sp > 1 ? (size_t)sp * split_stride(B, N) * sizeof(float) : 0);
+    return 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B) + part_bytes(N, K, B, allow_split);
 }
 
 cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, bool allow_split,
@@ -248,14 +241,12 @@ cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float 
     __half *hi = reinterpret_cast<__half *>(w8);
     __half *lo = reinterpret_cast<__half *>(w8 + split_bytes(K, B));
     float *tscale = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B));
-    __half *s8x = B > kSmallMaxB ? reinterpret_cast<__half *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B)) : nullptr;
+    __half *s8x = reinterpret_cast<__half *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B));
     float *part = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B));
-    const int splits = gemm_splits(B, N, K, allow_split);
     cudaError_t e = launch_q8_split(a, K, B, hi, lo, tscale, s8x, st);
     if (e != cudaSuccess) return e;
-    if (B <= kSmallMaxB)
-        return launch_gemm_small(W, N, K, B, hi, lo, reinterpret_cast<const __half *>(a.s), tscale,
-                                 splits > 1 ? part : y, y, splits, st);
+    if (B <= kSmallMaxB) return launch_gemm_chunk(W, N, K, B, hi, lo, s8x, tscale, y, part, allow_split, st);
+    const int splits = gemm_splits(B, N, K, allow_split);
     return launch_gemm_pair(W, N, K, B, hi, lo, s8x, tscale, splits > 1 ? part : y, y, splits, st);
 }
 

@@ -115,6 +115,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
+// 16-byte copy global -> shared through the load/store path (not the TMA
+// unit, whose queue serves requests in order), L2 only; src_bytes = 0 writes
+// zeros.  Completion: cp_async_commit / cp_async_wait<n> of this thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)

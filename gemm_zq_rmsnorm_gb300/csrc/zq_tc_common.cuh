@@ -91,21 +91,22 @@ cudaError_t launch_q8_split(zq_q8_1 a, int K, int B, __half *hi, __half *lo, flo
                             cudaStream_t st);
 // y[i] = sum over splits of part[s * split_stride + i] (in split order), i < n.
 cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float *y, cudaStream_t st);
-// split-K count for the small-batch kernel (weight tiles of 128 rows)
-int choose_splits(int B, int N, int K, int sms);
 // split-K count for the pair kernel (256 weight rows x 256 tokens per pair)
 int choose_splits_pair(int B, int N, int K, int sms);
 
-// ---- small-batch projection (q4k_gemm_small.cu), 2 <= B <= kSmallMaxB ----
+// largest B of the chunk kernel (q4k_gemm_chunk.cu); larger B run the pair kernel
 constexpr int kSmallMaxB = 16;
 // ---- CTA-pair projection (q4k_gemm_2sm.cu), B > kSmallMaxB ----------------
 // out = y (splits == 1) or the partial-sum area; y receives the result.
 cudaError_t launch_gemm_pair(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
                              const __half *s8x, const float *tscale, float *out, float *y, int splits,
                              cudaStream_t st);
-// out = y (splits == 1) or the partial-sum area; y receives the result.
-cudaError_t launch_gemm_small(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
-                              const __half *s8, const float *tscale, float *out, float *y, int splits,
+// ---- chunk projection (q4k_gemm_chunk.cu), 2 <= B <= kSmallMaxB ----------
+// part: chunk_part_bytes(N, K, B) bytes of partial sums (allow_split), else
+// unused: one CTA pair per 256-row tile and no partial sums.
+size_t chunk_part_bytes(int N, int K, int B);
+cudaError_t launch_gemm_chunk(const void *W, int N, int K, int B, const __half *hi, const __half *lo,
+                              const __half *s8x, const float *tscale, float *y, float *part, bool allow_split,
                               cudaStream_t st);
 
 }  // namespace zq

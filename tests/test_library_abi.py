@@ -198,12 +198,12 @@ def test_chunk_workspace_query(lib):
 
 
 def _gemm_base_bytes(B, K):
-    """Workspace without split-K partial sums: the binary16 hi and lo halves,
-    the token scales and, for B >= 17 (the 2-SM kernel), the scaled block
-    sums s8 written twice per super-block ([B][K/16] binary16); each region
-    padded to 256 bytes."""
+    """Workspace without partial sums: the binary16 hi and lo halves, the
+    token scales and the scaled block sums s8 written twice per super-block
+    ([B][K/16] binary16, the min-term operand of both tensor-core kernels);
+    each region padded to 256 bytes."""
     pad = lambda n: (n + 255) // 256 * 256
-    return 2 * (2 * B * K) + pad(4 * B) + (pad(B * (K // 16) * 2) if B > 16 else 0)
+    return 2 * (2 * B * K) + pad(4 * B) + pad(B * (K // 16) * 2)
 
 
 @pytest.mark.parametrize("K,N", [(5120, 6144), (5120, 1024), (6144, 5120), (5120, 17408), (17408, 5120), (1024, 151936),
@@ -211,15 +211,22 @@ def _gemm_base_bytes(B, K):
 @pytest.mark.parametrize("B", [5, 16, 17, 512])
 def test_gemm_workspace_split_k(lib, K, N, B):
     """The workspace holds the binary16 hi and lo activation parts, the token
-    scales, the 2-SM kernel's s8 operand and, when the launch splits K into S
-    ranges, S partial sums of
-    y, each padded to a multiple of four floats (16-byte aligned splits even
-    when B*N is not a multiple of 4); S is at most 8 and leaves at least two
-    super-blocks per range."""
+    scales, the s8 operand and the partial sums.  B >= 17 (2-SM kernel): when
+    the launch splits K into S ranges, S partial sums of y, each padded to a
+    multiple of four floats (16-byte aligned splits even when B*N is not a
+    multiple of 4); S is at most 8 and leaves at least two super-blocks per
+    range.  B <= 16 (chunk kernel, contiguous ranges of super-blocks per CTA
+    pair): one [B][N] slot per piece of the tile split into the most pieces,
+    which is 0 or at least 2 and at most the 256-row tile's super-blocks."""
     ws = lib.zq_q4k_gemm_workspace_bytes(N, K, B)
     base = _gemm_base_bytes(B, K)
     assert ws >= base
     extra = ws - base
+    if B <= 16:
+        assert extra % (4 * B * N) == 0
+        pieces = extra // (4 * B * N)
+        assert pieces == 0 or 2 <= pieces <= K // 256 + 1
+        return
     stride = 4 * ((B * N + 3) // 4 * 4)
     assert extra % stride == 0
     S = extra // stride
