@@ -701,7 +701,7 @@ def peak_probes(torch, stream, local_rank, sms):
     out = {}
     sink = torch.empty(sms * 8 * 256, dtype=torch.int32, device="cuda")
     cfg = {0: (sms * 8, 40000), 1: (sms * 8, 6000), 2: (sms, 40000), 3: (sms, 40000), 4: (sms, 40000),
-           5: (sms, 40000), 6: (sms, 40000), 7: (sms, 40000), 8: (sms, 40000), 9: (sms, 40000)}
+           5: (sms, 40000), 6: (sms, 40000), 7: (sms, 40000), 8: (sms, 40000), 9: (sms, 40000), 10: (sms, 40000)}
     with Clocks(local_rank) as clk:
         for kind, (blocks, iters) in cfg.items():
             with torch.cuda.stream(stream):
@@ -870,7 +870,7 @@ def main():
             k2 = pr["tcgen05.mma kind::f16 128x256x16"]
             out.update({"value": k2["tera_ops_per_s"], "unit": "TFLOP/s", "ms_per_step": k2["ms"], "dtype": "f16",
                         "config": {"workload": "throughput probes"}, "clocks": pr["clocks"], "peaks": pr,
-                        "gpu_launches": 20})
+                        "gpu_launches": 22})
         else:
             out["peaks"] = pr
     if dist is not None:

@@ -401,7 +401,8 @@ PROBE_KINDS = {0: "dp4a", 1: "mma.sync m16n8k32 s8", 2: "tcgen05.mma kind::f16 1
                6: "tcgen05.mma kind::f16 128x32x16, two issuing warps per SM",
                7: "tcgen05.mma kind::f16 256x32x16, CTA pair",
                8: "tcgen05.mma kind::f16 128x32x16, warp-wide loop, elected lane",
-               9: "tcgen05.mma kind::f16 256x32x16, CTA pair, warp-wide loop, elected lane"}
+               9: "tcgen05.mma kind::f16 256x32x16, CTA pair, warp-wide loop, elected lane",
+               10: "tcgen05.mma kind::f16 256x32x16, CTA pair, warp-wide loop, A in tensor memory"}
 
 
 def probe_ops(kind: int, blocks: int, iters: int) -> int:
@@ -411,7 +412,7 @@ def probe_ops(kind: int, blocks: int, iters: int) -> int:
         return blocks * 8 * iters * 4 * 2 * 16 * 8 * 32
     if kind == 6:
         return blocks * 2 * iters * 2 * 128 * 32 * 16
-    if kind in (7, 9):
+    if kind in (7, 9, 10):
         return (blocks // 2) * iters * 2 * 256 * 32 * 16
     n = {2: 256, 4: 16}.get(kind, 32)
     return blocks * iters * 2 * 128 * n * 16

@@ -32,9 +32,12 @@
 // warp, one elected lane: the 17 MMAs of a super-block back to back) and
 // tensor-memory owner; 2 the raw-tile TMA producer (this CTA's Q4_K
 // super-block tiles, six in flight); 3 idle; 4-11 converters (warp w: rows
-// 32*(w%4).. of TMEM lane quarter w%4, stages 2h and 2h + 1 of every
-// super-block for h = (w-4)/4: per-row metadata once per two stages, about
-// 1.3 instructions per weight); 12-15 epilogue (one lane quarter each).
+// 32*(w%4).. of TMEM lane quarter w%4, half h = (w-4)/4 of every
+// super-block -- stages 2h, 2h + 1 and terms 4h .. 4h + 3 of the row's min
+// operand -- with the row's metadata decoded once per half); 12-15 epilogue
+// (one lane quarter each).  The integer pipe bounds the converters: per
+// weight one byte permute per four weights, two masks per four and one
+// half2 fused multiply-add per two.
 // Waits suspend in hardware rather than spin, leaving issue slots to the
 // converters, which share every SM sub-partition with the other roles (a
 // warp reaches only the TMEM lane quarter of its sub-partition).  Every wait
@@ -136,30 +139,39 @@ __device__ __forceinline__ void signal_leader(uint64_t *bar_local, uint32_t rank
         mbar_arrive(bar_local);
 }
 
-// Converts half a super-block of one weight row -- stages 2H and 2H + 1,
+// 2^-e of a weight row's super-block (0 when d = 0): e from the binary16
+// exponents of d and dmin alone, as in fold_of.
+__device__ __forceinline__ float weight_scale(uint32_t d_dmin, int &e)
+{
+    const uint32_t hd = d_dmin & 0x7FFFu, hm = (d_dmin >> 16) & 0x7FFFu;
+    e = hm ? max(0, f16_ilog2(hm) - (hd ? f16_ilog2(hd) : 0) - 7) : 0;
+    return hd ? __int_as_float((127 - e) << 23) : 0.0f;
+}
+
+// Converts half H of a super-block of weight row r -- stages 2H and 2H + 1,
 // sub-blocks 4H .. 4H + 3 -- to binary16 sc * q * 2^-e and stores it in the
-// row's TMEM lane at columns col .. col + 63 (binary16 pairs in K order: per
-// stage, the even sub-block's 32 weights, then the odd one's).  H = 1 also
-// writes the row's min operand (-(dmin/d) * m_j * 2^-e as binary16 hi, then
-// lo parts, 32-byte swizzled) to mrow.  The scale 2^-e comes from the
-// binary16 exponents of d and dmin alone, as in fold_of.
+// row's TMEM lane at columns col .. col + 63 (per stage, binary16 pairs in K
+// order: the even sub-block's 32 weights, then the odd one's).  Also writes
+// terms j = 4H .. 4H + 3 of the row's min operand, -(dmin/d) * m_j * 2^-e as
+// binary16 hi and lo parts, into the row's 32-byte swizzled line `mrow` (hi
+// parts in its first 16 bytes, lo parts in the second, before the swizzle).
+// The row's metadata is decoded once for both stages.
 template <int H>
 __device__ __forceinline__ void convert_half(const uint8_t *raw, uint32_t col, uint8_t *mrow, int r)
 {
     const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
-    const uint32_t hd = hdr.x & 0x7FFFu, hm = (hdr.x >> 16) & 0x7FFFu;
-    const int e = hm ? max(0, f16_ilog2(hm) - (hd ? f16_ilog2(hd) : 0) - 7) : 0;
-    const float wmul = hd ? __int_as_float((127 - e) << 23) : 0.0f;   // 2^-e
+    int e;
+    const float wmul = weight_scale(hdr.x, e);
+    uint32_t sc[4], m[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, 4 * H + j, sc[j], m[j]);
 #pragma unroll
     for (int st = 0; st < 2; ++st) {
         const int I = 2 * H + st;   // stage: nibble bytes 32 I .. 32 I + 31
         const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * I);
         const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * I);
         const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-        uint32_t sc0, sc1, md;
-        q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * I, sc0, md);
-        q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * I + 1, sc1, md);
-        const float s0 = (float)sc0 * wmul, s1 = (float)sc1 * wmul;
+        const float s0 = (float)sc[2 * st] * wmul, s1 = (float)sc[2 * st + 1] * wmul;
         // low nibble in the mantissa of 1024: s0 * (1024 + q) - 1024 s0;
         // high nibble as 1024 + 16 q: (s1 / 16) * (1024 + 16 q) - 64 s1
         const __half2 a0 = __float2half2_rn(s0), b0 = __float2half2_rn(-1024.0f * s0);
@@ -177,25 +189,22 @@ __device__ __forceinline__ void convert_half(const uint8_t *raw, uint32_t col, u
         }
         tmem_st32(col + 32u * st, o);
     }
-    if (H == 1) {
-        const float rr = ratio_of(hdr.x, e);
-        uint32_t hv[4], lv[4];
+    // min terms: r = dmin / d (dmin itself when d = 0), times 2^-e
+    const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
+    const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+    const float rr = ((hdr.x & 0x7FFFu) ? dm / d : dm) * __int_as_float((127 - e) << 23);
+    uint32_t hv[2], lv[2];
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-            uint32_t m0v, m1v, scd;
-            q4k_scale_min(hdr.y, hdr.z, hdr.w, j, scd, m0v);
-            q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, scd, m1v);
-            const float v0 = -rr * (float)m0v, v1 = -rr * (float)m1v;
-            const __half2 hh = __floats2half2_rn(v0, v1);
-            const float2 hb = __half22float2(hh);
-            hv[j >> 1] = h2_bits(hh);
-            lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
-        }
-        const int s32 = (r >> 2) & 1;
-        *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        fence_async_smem();   // the min MMA reads this row through the async proxy
+    for (int j = 0; j < 4; j += 2) {
+        const float v0 = -rr * (float)m[j], v1 = -rr * (float)m[j + 1];
+        const __half2 hh = __floats2half2_rn(v0, v1);
+        const float2 hb = __half22float2(hh);
+        hv[j >> 1] = h2_bits(hh);
+        lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
     }
+    const int s32 = (r >> 2) & 1;
+    *reinterpret_cast<uint2 *>(mrow + ((0 ^ s32) << 4) + 8 * H) = make_uint2(hv[0], hv[1]);
+    *reinterpret_cast<uint2 *>(mrow + ((1 ^ s32) << 4) + 8 * H) = make_uint2(lv[0], lv[1]);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -267,6 +276,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         // through the TMA unit they would also wait behind the raw tiles.
         const __half *src = rank == 0 ? p.hi : p.lo;
         const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (kConvWarps + kEpiWarps), 0);
+        static_assert(4 * (kConvWarps + kEpiWarps + 2) <= 128, "st.async words of the odd CTA's warps");
         const uint32_t tfull_cl0 = cluster_addr(smem_u32(&tok_full[0]), 0);
         bool ok = true;
         auto issue = [&](int l) {
@@ -379,17 +389,21 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (warp - kConvWarp0), 0);
         const uint32_t afull_cl0 = cluster_addr(smem_u32(&afull[0]), 0);   // barriers 8 bytes apart
         bool ok = true;
+        // ring positions kept as counters: raw slot rs (phase rph), A slot a (phase aph)
+        int rs = 0, a = 0;
+        uint32_t rph = 0, aph = 0;
         for (int l = 0; l < L && ok; ++l) {
-            const int rs = l % kRawSlots, a = l % kASB;
-            if (!(ok = pair_lane0_wait(&raw_full[rs], (uint32_t)(l / kRawSlots) & 1, ctx))) break;
-            if (l >= kASB && !(ok = pair_lane0_wait(&aempty[a], ((l / kASB) - 1) & 1, ctx))) break;
+            if (!(ok = pair_lane0_wait(&raw_full[rs], rph, ctx))) break;
+            if (l >= kASB && !(ok = pair_lane0_wait(&aempty[a], aph ^ 1u, ctx))) break;
             tc_fence_after();
             const uint8_t *raw = sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes;
             const uint32_t col = lane_base + kACols * a;
+            uint8_t *mrow = sm + Smem::amin(a) + (size_t)r * 32;
             if (h == 0)
-                convert_half<0>(raw, col, nullptr, r);
+                convert_half<0>(raw, col, mrow, r);
             else
-                convert_half<1>(raw, col, sm + Smem::amin(a) + (size_t)r * 32, r);
+                convert_half<1>(raw, col, mrow, r);
+            fence_async_smem();   // the min MMA reads the min operand through the async proxy
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -397,6 +411,8 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
                 signal_leader(&afull[a], rank, quarter == 0 && h == 0, kConvSigTx, sig, afull_cl0 + 8u * (uint32_t)a);
                 mbar_arrive(&raw_empty[rs]);
             }
+            if (++rs == kRawSlots) { rs = 0; rph ^= 1u; }
+            if (++a == kASB) { a = 0; aph ^= 1u; }
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------- epilogue
@@ -408,14 +424,32 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         float acc[kTok];
 #pragma unroll
         for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
+        // the row's d/dmin of super-block l, read from global memory four
+        // super-blocks ahead (under full HBM load a read takes ~1-2 us)
+        auto header = [&](int l) -> uint32_t {
+            if (l >= L) return 0u;
+            const long long g = g0 + l;
+            const int n = (int)(g / p.nb) * kPairM + kRows * (int)rank + 32 * quarter + lane;
+            return n < p.N ? ld_nc_u32(p.W + (size_t)n * p.row_bytes + (size_t)kQ4KBlockBytes * (int)(g % p.nb))
+                           : 0u;
+        };
+        uint32_t h0 = header(0), h1 = header(1), h2 = header(2), h3 = header(3);
         bool ok = true;
         for (int l = 0; l < L && ok; ++l) {
             const long long g = g0 + l;
-            const int tile = (int)(g / p.nb), b = (int)(g % p.nb);
+            const int tile = (int)(g / p.nb);
             const int n = tile * kPairM + kRows * (int)rank + 32 * quarter + lane;
             const bool nvalid = n < p.N;
-            const uint32_t hd = nvalid ? ld_nc_u32(p.W + (size_t)n * p.row_bytes + (size_t)kQ4KBlockBytes * b) : 0u;
-            const float fold = nvalid ? fold_of(hd).fold : 0.0f;
+            const uint32_t hd = h0;
+            h0 = h1;
+            h1 = h2;
+            h2 = h3;
+            h3 = header(l + 4);
+            // fold = (d, or 1 when d = 0) * 2^e, as fold_of
+            int e;
+            weight_scale(hd, e);
+            const float dv = (hd & 0x7FFFu) ? __half2float(__ushort_as_half((unsigned short)(hd & 0xFFFFu))) : 1.0f;
+            const float fold = nvalid ? dv * __int_as_float((127 + e) << 23) : 0.0f;
             const int j = l % kAcc;
             if (!(ok = pair_lane0_wait(&tfull[j], (uint32_t)(l / kAcc) & 1, ctx))) break;
             tc_fence_after();

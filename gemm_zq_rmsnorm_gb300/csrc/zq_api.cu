@@ -529,9 +529,9 @@ int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows, int s
 
 int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void *stream)
 {
-    if (kind < 0 || kind > 9) return fail(ZQ_ERR_ARG, "zq_debug_peak_probe: kind %d unknown", kind);
-    if ((kind == 7 || kind == 9) && blocks < 2)
-        return fail(ZQ_ERR_SHAPE, "zq_debug_peak_probe: kinds 7 and 9 need blocks >= 2");
+    if (kind < 0 || kind > 10) return fail(ZQ_ERR_ARG, "zq_debug_peak_probe: kind %d unknown", kind);
+    if ((kind == 7 || kind >= 9) && blocks < 2)
+        return fail(ZQ_ERR_SHAPE, "zq_debug_peak_probe: kinds 7, 9 and 10 need blocks >= 2");
     if (!sink || !aligned16(sink)) return fail(ZQ_ERR_ARG, "zq_debug_peak_probe: sink null or misaligned");
     if (blocks < 1 || blocks > 65535 || iters < 1 || iters > (1 << 24))
         return fail(ZQ_ERR_SHAPE, "zq_debug_peak_probe: blocks = %d, iters = %d out of range", blocks, iters);

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(128, 1) probe_tc_f16_kernel(int kind, int iter
 // MMAs (cta_group::2: 128 rows in each SM's tensor memory), operands in each
 // CTA's shared memory.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
-probe_tc_pair_kernel(int iters, int warpwide, int *sink, unsigned int *status)
+probe_tc_pair_kernel(int iters, int warpwide, int a_tmem, int *sink, unsigned int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -176,13 +176,30 @@ probe_tc_pair_kernel(int iters, int warpwide, int *sink, unsigned int *status)
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = slot;
+    if (a_tmem) {
+        // A in tensor memory: 128 lanes x 32 columns of binary16 pairs 1.0
+        uint32_t one[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) one[i] = 0x3C003C00u;
+        tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + 128u, one);
+        tmem_st16(tmem + ((uint32_t)(32 * warp) << 16) + 144u, one);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
     if (rank == 0 && warpwide && warp == 0) {
         const uint32_t base = smem_u32(sm);
         const uint64_t ad = smem_desc(base, 16, 1024, kLayoutSw128);
         const uint64_t bd = smem_desc(base + 2 * 128 * 128, 16, 1024, kLayoutSw128);
         const uint32_t idesc = idesc_f16_f32(256, 32);
         for (int it = 0; it < iters; ++it) {
-            if (elect_one()) mma_f16_pair(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+            if (elect_one()) {
+                if (a_tmem)
+                    mma_f16_pair_ta(tmem, tmem + 128u + 8u * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+                else
+                    mma_f16_pair(tmem, ad + 2 * (it & 3), bd + 2 * (it & 3), idesc, it > 0 ? 1u : 0u);
+            }
             __syncwarp();
         }
         if (elect_one()) mma_commit_pair_mc(&bar, 3);
@@ -241,15 +258,15 @@ cudaError_t launch_peak_probe(int kind, int blocks, int iters, int *sink, cudaSt
             if (e != cudaSuccess) return e;
             g_attr_bytes[dev] = kProbeSmem;
         }
-        if (kind == 7 || kind == 9) {
+        if (kind == 7 || kind == 9 || kind == 10) {
             if (g_attr_pair[dev] < (size_t)kProbeSmem) {
                 cudaError_t e = cudaFuncSetAttribute(probe_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      kProbeSmem);
                 if (e != cudaSuccess) return e;
                 g_attr_pair[dev] = kProbeSmem;
             }
-            probe_tc_pair_kernel<<<2 * (blocks / 2), 128, kProbeSmem, st>>>(iters, kind == 9 ? 1 : 0, sink,
-                                                                             device_status_word());
+            probe_tc_pair_kernel<<<2 * (blocks / 2), 128, kProbeSmem, st>>>(iters, kind >= 9 ? 1 : 0, kind == 10 ? 1 : 0,
+                                                                             sink, device_status_word());
         } else {
             probe_tc_f16_kernel<<<blocks, 128, kProbeSmem, st>>>(kind, iters, sink, device_status_word());
         }

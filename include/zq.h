@@ -395,7 +395,8 @@ ZQ_API int zq_debug_stream_plan(int wtype, int ntok, int K, long long total_rows
  *           issuing 256 x 32 x 16 MMAs (cta_group::2):
  *           (blocks/2) * iters * 2*256*32*16;
  *   kinds 8, 9  as 3 and 7, with the issuing loop run by a whole warp and
- *           each MMA issued by one elected lane.
+ *           each MMA issued by one elected lane;
+ *   kind 10 as 9 with the A operand read from tensor memory.
  *   sink : device memory of at least blocks * 256 ints (results kept live).
  * A kind-2 probe whose bounded wait expires sets ZQ_DEVICE_WAIT_EXPIRED.
  */
