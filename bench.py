@@ -155,11 +155,38 @@ class LayerWorkload:
         for (pname, K, N, paired) in self.shapes:
             self.y[pname] = (torch.empty((B, N), dtype=torch.float32, device=dev),
                              torch.empty((B, N), dtype=torch.float32, device=dev) if paired else None)
-        ws = max(zq.gemm_workspace_bytes(N, K, B) for (_, K, N, _) in self.shapes)
-        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         self.key_of = {p: input_key(p) for (p, _, _, _) in self.layer_shapes}
         for (p, K, N, _) in self.extra:
             self.key_of[p] = [k for k, KK in self.inputs_K if KK == K][0]
+        # B > 1: the matrices of a layer that read the same input are stored
+        # row-stacked as one Q4_K matrix ([Wq; Wk; Wv], [Wgate; Wup]: the same
+        # bytes, one activation split and one launch per input)
+        self.stacked = B > 1 and not self.fused
+        self.groups = []   # (input key, K, N_total)
+        if self.stacked:
+            for k, K in self.inputs_K:
+                n_tot = sum(N * (2 if p else 1) for (pn, KK, N, p) in self.layer_shapes if self.key_of[pn] == k)
+                if n_tot:
+                    self.groups.append((k, K, n_tot))
+            self.SW = []   # SW[copy][layer][input key]
+            for r in range(self.R):
+                layers_w, _ = self.W[r]
+                per_layer = []
+                for li in range(layers):
+                    d = {}
+                    for k, K, _ in self.groups:
+                        parts = []
+                        for (pn, KK, N, p) in self.layer_shapes:
+                            if self.key_of[pn] == k:
+                                parts += [w for w in layers_w[li][pn] if w is not None]
+                        d[k] = torch.cat(parts)
+                    per_layer.append(d)
+                self.SW.append(per_layer)
+            self.gy = {k: torch.empty((B, n), dtype=torch.float32, device=dev) for k, _, n in self.groups}
+        ws = max(zq.gemm_workspace_bytes(N, K, B) for (_, K, N, _) in self.shapes)
+        if self.stacked:
+            ws = max([ws] + [zq.gemm_workspace_bytes(n, K, B) for _, K, n in self.groups])
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
 
     def weights(self, r, pname, layer=0):
         layers_w, extra_w = self.W[r]
@@ -230,9 +257,20 @@ class LayerWorkload:
     def run(self, r=0, stream=None):
         if self.fused:
             return self._run_fused(r, stream)
+        layers_w, extra_w = self.W[r]
+        if self.stacked:
+            # one call per input: RMSNorm + Q8_1 (and, for B >= 5, the
+            # activation split) in one kernel, then the projection
+            for li in range(self.layers):
+                for k, K, n in self.groups:
+                    self.zq.rmsnorm_q4k_gemm(self.x[k], self.g[k], inputs.EPS, self.SW[r][li][k], n, y=self.gy[k],
+                                             q8_out=self.a[k], workspace=self.ws, stream=stream)
+            for (pname, K, N, paired) in self.extra:
+                w1, w2 = extra_w[pname]
+                self._proj(pname, K, N, paired, w1, w2, stream)
+            return
         for k, K in self.inputs_K:
             self.zq.rmsnorm_q8_1(self.x[k], self.g[k], inputs.EPS, out=self.a[k], stream=stream)
-        layers_w, extra_w = self.W[r]
         for li in range(self.layers):
             for (pname, K, N, paired) in self.layer_shapes:
                 w1, w2 = layers_w[li][pname]
@@ -244,18 +282,24 @@ class LayerWorkload:
     def launches_per_step(self):
         if self.fused:
             return len(self.fused_groups(0)) * self.layers + len(self.extra)
-        n = len(self.inputs_K)
-        for (pname, K, N, paired) in self.layer_shapes * self.layers + self.extra:
+        n = 0 if self.stacked else len(self.inputs_K)
+        if self.stacked:
+            calls = [(K, N, False) for _, K, N in self.groups] * self.layers + \
+                    [(K, N, p) for (_, K, N, p) in self.extra]
+        else:
+            calls = [(K, N, p) for (_, K, N, p) in self.layer_shapes * self.layers + self.extra]
+        for (K, N, paired) in calls:
             calls = 1 if (self.B == 1 or not paired) else 2
             if self.B == 1:
                 per = 1
             elif self.B <= 4:
-                per = 1   # the streamed mat-vec with the tokens staged together
+                per = 2 if self.stacked else 1   # (norm +) the streamed mat-vec with the tokens staged together
             else:
                 # q8 split + GEMM, + the split-K reduction when the workspace
                 # holds partial sums beyond the hi/lo activations and scales
                 pad = lambda n: (n + 255) // 256 * 256
-                base = 4 * self.B * K + pad(4 * self.B) + (pad(self.B * K // 8) if self.B > 16 else 0)
+                base = 4 * self.B * K + pad(4 * self.B) + pad(self.B * K // 8)
+                # (stacked: the norm writes the split) + GEMM + reduction or fixup
                 per = 2 + (1 if self.zq.gemm_workspace_bytes(N, K, self.B) > base else 0)
             n += calls * per
         return n
@@ -358,6 +402,15 @@ def bench_dominant(torch, wl, pname, steps, warmup, stream):
     (_, K, N, paired) = [s for s in wl.shapes if s[0] == pname][0]
     zq = wl.zq
     a = wl.a[wl.key_of[pname]]
+    if wl.stacked:
+        # the launch of the row-stacked matrix holding this projection
+        key = wl.key_of[pname]
+        (_, K, N) = [g for g in wl.groups if g[0] == key][0]
+        g = capture(torch, lambda: [zq.q4k_gemm(wl.SW[i % wl.R][0][key], N, K, a, wl.B, wl.gy[key], wl.ws)
+                                    for i in range(4 * wl.R)], stream)
+        ms = time_graphs(torch, [g], max(3, steps // 4), max(1, warmup // 2), stream) / (4 * wl.R)
+        alg = proj_bytes(K, N, wl.B) if wl.B <= 16 else 2 * wl.B * N * K
+        return ms, alg, (K, N, False)
 
     def one(r):
         w1, w2 = wl.weights(r, pname)
@@ -663,7 +716,7 @@ def batch_record(torch, B, shapes, name, steps, warmup, stream, pk, local_rank, 
         (_, _, N, _) = [s for s in wl.shapes if s[0] == dom][0]
         alg_bytes = proj_bytes(dK, dN, B)
         ach = alg_bytes / (dms * 1e-3) / 1e9
-        path = "streamed mat-vec, tokens staged together" if B <= 4 else "small-batch tensor-core kernel"
+        path = "streamed mat-vec, tokens staged together" if B <= 4 else "chunk kernel on CTA pairs"
         roof = {"bound": "hbm", "kernel": f"q4k_gemm {dK}->{dN} B={B} ({path})",
                 "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
@@ -680,6 +733,8 @@ def batch_record(torch, B, shapes, name, steps, warmup, stream, pk, local_rank, 
                 "kernel_ms": round(dms, 5)}
     rec = {"workload": wl.name, "B": B, "value": round(tops, 2), "unit": "TOPS",
            "ms_per_step": round(ms, 4), "hbm_gbs": round(gbs, 1),
+           "weights": "row-stacked per input: [q;k;v] (5120 -> 8192), o, [gate;up] (5120 -> 34816), down; "
+                      "one activation split and one launch per input",
            "algorithmic_ops_per_step": int(wl.algo_ops()), "algorithmic_bytes_per_step": int(wl.algo_bytes()),
            "roofline": roof,
            "gpu_launches": wl.launches_per_step() * steps, "clocks": clk.summary()}

@@ -31,7 +31,8 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q4k_dequant_f16", "zq_silu_mul_q8_1", "zq_silu_q4k_gemv",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
            "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe",
-           "zq_debug_wait_expiry", "zq_q8_1_dequant_f16", "zq_f16_gemm_workspace_bytes", "zq_f16_gemm")
+           "zq_debug_wait_expiry", "zq_q8_1_dequant_f16", "zq_f16_gemm_workspace_bytes", "zq_f16_gemm",
+           "zq_rmsnorm_q4k_gemm")
 
 
 class ZQError(RuntimeError):
@@ -89,6 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_q8_1_dequant_f16": ([_Q8, i, i, P, P], i),
         "zq_f16_gemm_workspace_bytes": ([i, i, i], sz),
         "zq_f16_gemm": ([P, i, i, P, i, P, P, sz, P], i),
+        "zq_rmsnorm_q4k_gemm": ([P, P, f, i, i, P, i, P, ctypes.POINTER(_Q8), P, sz, P], i),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -303,6 +305,27 @@ def q4k_gemm(W: torch.Tensor, N: int, K: int, a: Q8_1, B: int | None = None,
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.zq_q4k_gemm(_ptr(W), N, K, a._c(), B, _ptr(y), _ptr(workspace), wbytes,
                            _stream(stream)))
+    return y
+
+
+def rmsnorm_q4k_gemm(x: torch.Tensor, gamma: torch.Tensor, eps: float, W: torch.Tensor, N: int,
+                     y: torch.Tensor | None = None, q8_out: Q8_1 | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """RMSNorm + Q8_1 of x [B][K] and the projection y [B][N] in one call (see zq_rmsnorm_q4k_gemm)."""
+    lib = load()
+    B, K = x.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=dev)
+    if q8_out is None and 2 <= B <= 4:
+        q8_out = empty_q8_1(B, K, dev)
+    need = gemm_workspace_bytes(N, K, B)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    q8 = ctypes.byref(q8_out._c()) if q8_out is not None else None
+    _check(lib.zq_rmsnorm_q4k_gemm(_ptr(x), _ptr(gamma), float(eps), B, K, _ptr(W), N, _ptr(y), q8,
+                                   _ptr(workspace), wbytes, _stream(stream)))
     return y
 
 

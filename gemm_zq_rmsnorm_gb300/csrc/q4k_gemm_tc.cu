@@ -234,20 +234,34 @@ size_t gemm_tc_workspace_bytes(int N, int K, int B, bool allow_split)
     return 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B) + part_bytes(N, K, B, allow_split);
 }
 
+TcWorkspace tc_workspace(void *ws, int K, int B)
+{
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    TcWorkspace w;
+    w.hi = reinterpret_cast<__half *>(w8);
+    w.lo = reinterpret_cast<__half *>(w8 + split_bytes(K, B));
+    w.tscale = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B));
+    w.s8x = reinterpret_cast<__half *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B));
+    w.part = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B));
+    return w;
+}
+
+cudaError_t launch_gemm_tc_split_done(const void *W, int N, int K, int B, float *y, void *ws, bool allow_split,
+                                      cudaStream_t st)
+{
+    const TcWorkspace w = tc_workspace(ws, K, B);
+    if (B <= kSmallMaxB) return launch_gemm_chunk(W, N, K, B, w.hi, w.lo, w.s8x, w.tscale, y, w.part, allow_split, st);
+    const int splits = gemm_splits(B, N, K, allow_split);
+    return launch_gemm_pair(W, N, K, B, w.hi, w.lo, w.s8x, w.tscale, splits > 1 ? w.part : y, y, splits, st);
+}
+
 cudaError_t launch_gemm_tc(const void *W, int N, int K, zq_q8_1 a, int B, float *y, void *ws, bool allow_split,
                            cudaStream_t st)
 {
-    uint8_t *w8 = static_cast<uint8_t *>(ws);
-    __half *hi = reinterpret_cast<__half *>(w8);
-    __half *lo = reinterpret_cast<__half *>(w8 + split_bytes(K, B));
-    float *tscale = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B));
-    __half *s8x = reinterpret_cast<__half *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B));
-    float *part = reinterpret_cast<float *>(w8 + 2 * split_bytes(K, B) + tscale_bytes(B) + s8x_bytes(K, B));
-    cudaError_t e = launch_q8_split(a, K, B, hi, lo, tscale, s8x, st);
+    const TcWorkspace w = tc_workspace(ws, K, B);
+    cudaError_t e = launch_q8_split(a, K, B, w.hi, w.lo, w.tscale, w.s8x, st);
     if (e != cudaSuccess) return e;
-    if (B <= kSmallMaxB) return launch_gemm_chunk(W, N, K, B, hi, lo, s8x, tscale, y, part, allow_split, st);
-    const int splits = gemm_splits(B, N, K, allow_split);
-    return launch_gemm_pair(W, N, K, B, hi, lo, s8x, tscale, splits > 1 ? part : y, y, splits, st);
+    return launch_gemm_tc_split_done(W, N, K, B, y, ws, allow_split, st);
 }
 
 }  // namespace zq

@@ -41,13 +41,25 @@ __device__ __forceinline__ void pack_block(const float (&xh)[32], int8_t *qdst, 
     *sq = o.s;
 }
 
+// Optional outputs of the batched projection's activation split (all null,
+// or all set; only when every block has a thread of its own): x' = q8 * d8
+// as exact binary16 hi + lo parts with the token's power-of-two scale 2^-k
+// (tscale = 2^k, k >= 0 the least that keeps 127 * max d8 within binary16
+// range), and each super-block's eight s8 values scaled alike, twice.
+struct SplitOut {
+    __half *hi, *lo;
+    float *tscale;
+    __half *s8x;
+};
+
 __global__ void __launch_bounds__(kMaxThreads)
 rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma, int K, float eps,
-                    int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq)
+                    int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq, SplitOut so)
 {
     __shared__ float part_s[kMaxBlocks];   // p_b, in block order
     __shared__ float slot_s[256];
     __shared__ float r_s;
+    __shared__ float dmax_s[kMaxThreads / 32];
 
     const int t = threadIdx.x;
     const int nthr = blockDim.x;
@@ -101,6 +113,7 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
     const float r = r_s;
 
     // pass 2: normalise and pack each block
+    Q8Block pk{};
     for (int b = t; b < nblk; b += nthr) {
         if (!one) {
             const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
@@ -123,8 +136,59 @@ rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma
             xr[4 * v + 3] = __fmul_rn(__fmul_rn(xr[4 * v + 3], r), w.w);
         }
         const size_t o = (size_t)blockIdx.x * nblk + b;
-        pack_block(xr, qs + (size_t)blockIdx.x * K + 32 * b, dq + o, sq + o);
+        if (so.hi == nullptr) {
+            pack_block(xr, qs + (size_t)blockIdx.x * K + 32 * b, dq + o, sq + o);
+            continue;
+        }
+        // one block per thread here: keep the packed block for the split
+        pk = q8_1_pack(xr);
+        if (qs != nullptr) {
+            uint4 *dst = reinterpret_cast<uint4 *>(qs + (size_t)blockIdx.x * K + 32 * b);
+            dst[0] = pk.q0;
+            dst[1] = pk.q1;
+            dq[o] = pk.d;
+            sq[o] = pk.s;
+        }
     }
+    if (so.hi == nullptr) return;
+    // the token's largest |d8| (every block's thread, then the CTA)
+    float m = t < nblk ? fabsf(__half2float(pk.d)) : 0.0f;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((t & 31) == 0) dmax_s[t >> 5] = m;
+    __syncthreads();
+    m = dmax_s[0];
+    for (int w = 1; w < (nthr >> 5); ++w) m = fmaxf(m, dmax_s[w]);
+    int k = 0;
+    const float bound = 127.0f * m;   // >= every |x'| of the token
+    if (bound > 65504.0f) frexpf(bound / 65504.0f, &k);   // bound / 65504 <= 2^k
+    const float down = ldexpf(1.0f, -k);
+    if (t == 0) so.tscale[blockIdx.x] = ldexpf(1.0f, k);
+    if (t >= nblk) return;
+    const float dv = __half2float(pk.d) * down;
+    const uint32_t w[8] = {pk.q0.x, pk.q0.y, pk.q0.z, pk.q0.w, pk.q1.x, pk.q1.y, pk.q1.z, pk.q1.w};
+    uint32_t oh[16], ol[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {   // codes 2i, 2i + 1
+        const uint32_t x2 = w[i >> 1] >> (16 * (i & 1));
+        const float a0 = (float)(int8_t)(x2 & 0xFFu) * dv, a1 = (float)(int8_t)((x2 >> 8) & 0xFFu) * dv;
+        const __half2 vh = __floats2half2_rn(a0, a1);
+        const float2 back = __half22float2(vh);
+        oh[i] = *reinterpret_cast<const uint32_t *>(&vh);
+        const __half2 vl = __floats2half2_rn(a0 - back.x, a1 - back.y);
+        ol[i] = *reinterpret_cast<const uint32_t *>(&vl);
+    }
+    uint4 *dh = reinterpret_cast<uint4 *>(so.hi + (size_t)blockIdx.x * K + 32 * t);
+    uint4 *dl = reinterpret_cast<uint4 *>(so.lo + (size_t)blockIdx.x * K + 32 * t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dh[i] = make_uint4(oh[4 * i], oh[4 * i + 1], oh[4 * i + 2], oh[4 * i + 3]);
+        dl[i] = make_uint4(ol[4 * i], ol[4 * i + 1], ol[4 * i + 2], ol[4 * i + 3]);
+    }
+    const __half sv = __float2half_rn(__half2float(pk.s) * down);
+    __half *sx = so.s8x + (size_t)blockIdx.x * (K / 16) + 16 * (t >> 3) + (t & 7);
+    sx[0] = sv;
+    sx[8] = sv;
 }
 
 // Rows wider than kMaxBlocks blocks: one CTA of 256 threads per token, thread
@@ -235,9 +299,23 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     if (nblk <= kMaxBlocks) {
         int threads = nblk < kMaxThreads ? (nblk + 31) / 32 * 32 : kMaxThreads;
         if (threads < 256) threads = 256;   // the slot tree needs 256 threads
-        return launch_pdl(rmsnorm_q8_1_kernel, dim3(B), dim3(threads), 0, st, x, gamma, K, eps, out.qs, dq, sq);
+        return launch_pdl(rmsnorm_q8_1_kernel, dim3(B), dim3(threads), 0, st, x, gamma, K, eps, out.qs, dq, sq,
+                          SplitOut{});
     }
     return launch_pdl(rmsnorm_q8_1_wide_kernel, dim3(B), dim3(256), 0, st, x, gamma, K, eps, out.qs, dq, sq);
+}
+
+cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B, int K, float eps,
+                                      const zq_q8_1 *out, __half *hi, __half *lo, float *tscale, __half *s8x,
+                                      cudaStream_t st)
+{
+    const int nblk = K / 32;
+    if (nblk > kMaxThreads) return cudaErrorInvalidValue;
+    int threads = (nblk + 31) / 32 * 32;
+    if (threads < 256) threads = 256;   // the slot tree needs 256 threads
+    return launch_pdl(rmsnorm_q8_1_kernel, dim3(B), dim3(threads), 0, st, x, gamma, K, eps,
+                      out ? out->qs : (int8_t *)nullptr, out ? reinterpret_cast<__half *>(out->d) : (__half *)nullptr,
+                      out ? reinterpret_cast<__half *>(out->s) : (__half *)nullptr, SplitOut{hi, lo, tscale, s8x});
 }
 
 }  // namespace zq

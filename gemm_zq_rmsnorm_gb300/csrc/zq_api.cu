@@ -13,6 +13,7 @@
 #include <string>
 
 #include "zq_internal.cuh"
+#include "zq_tc_common.cuh"
 
 __device__ unsigned int g_zq_device_status;
 
@@ -301,6 +302,48 @@ int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, int K, in
     return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, false, q8_out, l2_prefetch,
                                              l2_prefetch ? l2_prefetch_bytes : 0, (cudaStream_t)stream),
                     "zq_rmsnorm_q4k_gemv launch");
+}
+
+int zq_rmsnorm_q4k_gemm(const float *x, const float *gamma, float eps, int B, int K, const void *W, int N, float *y,
+                        const zq_q8_1 *q8_out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const char *name = "zq_rmsnorm_q4k_gemm";
+    if (!x || !gamma || !y) return fail(ZQ_ERR_ARG, "%s: null x, gamma or y", name);
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(y))
+        return fail(ZQ_ERR_ALIGN, "%s: x, gamma and y must be 16-byte aligned", name);
+    if (!(eps >= 0.0f) || eps != eps) return fail(ZQ_ERR_ARG, "%s: eps must be >= 0", name);
+    int st = check_q4k(W, N, K, name);
+    if (st) return st;
+    if (K > 32768) return fail(ZQ_ERR_SHAPE, "%s: K = %d above the in-kernel normalisation limit 32768", name, K);
+    if (B < 1 || B > 65536) return fail(ZQ_ERR_SHAPE, "%s: B = %d must be in [1, 65536]", name, B);
+    if (q8_out && (st = check_q8(*q8_out, name))) return st;
+    const bool streamed = B > 1 && chunk_streams(B, K);
+    if (streamed && !q8_out) return fail(ZQ_ERR_ARG, "%s: B = %d needs q8_out (the codes the mat-vec reads)", name, B);
+    const size_t need = (B == 1 || streamed) ? 0 : gemm_tc_workspace_bytes(N, K, B);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(ZQ_ERR_WORKSPACE, "%s: workspace of %zu bytes required, got %zu", name, need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (need && !aligned16(workspace)) return fail(ZQ_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (B == 1) {
+        GemvJob job{};
+        job.nmat = 1;
+        job.W[0] = W;
+        job.N[0] = N;
+        job.y[0] = y;
+        return launched(launch_gemv_stream_fused(job, K, x, gamma, eps, false, q8_out, nullptr, 0, s), name);
+    }
+    cudaError_t e;
+    if (streamed) {
+        if ((e = launch_rmsnorm_q8_1(x, gamma, B, K, eps, *q8_out, s)) != cudaSuccess) return launched(e, name);
+        return launched(launch_q4k_tokens(W, N, K, *q8_out, B, y, s), name);
+    }
+    const TcWorkspace w = tc_workspace(workspace, K, B);
+    if ((e = launch_rmsnorm_q8_1_split(x, gamma, B, K, eps, q8_out, w.hi, w.lo, w.tscale, w.s8x, s)) != cudaSuccess)
+        return launched(e, name);
+    return launched(launch_gemm_tc_split_done(W, N, K, B, y, workspace, true, s), name);
 }
 
 size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B)

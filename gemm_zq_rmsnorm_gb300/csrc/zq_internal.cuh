@@ -16,6 +16,12 @@ constexpr int kQ4KBlockWeights = 256;
 // Host-side launch descriptions (defined in the kernel TUs, called by the API).
 cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K,
                                 float eps, zq_q8_1 out, cudaStream_t st);
+// RMSNorm + Q8_1 (codes to *out when non-null) that also writes the batched
+// projection's activation split: hi/lo parts, token scales, s8 operand
+// (K <= 32768).
+cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B, int K, float eps,
+                                      const zq_q8_1 *out, __half *hi, __half *lo, float *tscale, __half *s8x,
+                                      cudaStream_t st);
 cudaError_t launch_gemv(const void *W, const void *W2, int N, int K, zq_q8_1 a,
                         int B, float *y, float *y2, int32_t *isums,
                         cudaStream_t st);

@@ -94,6 +94,15 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, size_t n, float 
 // split-K count for the pair kernel (256 weight rows x 256 tokens per pair)
 int choose_splits_pair(int B, int N, int K, int sms);
 
+// the workspace's regions (layout above)
+struct TcWorkspace {
+    __half *hi, *lo, *s8x;
+    float *tscale, *part;
+};
+TcWorkspace tc_workspace(void *ws, int K, int B);
+// the projection on activations already split into the workspace
+cudaError_t launch_gemm_tc_split_done(const void *W, int N, int K, int B, float *y, void *ws, bool allow_split,
+                                      cudaStream_t st);
 // largest B of the chunk kernel (q4k_gemm_chunk.cu); larger B run the pair kernel
 constexpr int kSmallMaxB = 16;
 // ---- CTA-pair projection (q4k_gemm_2sm.cu), B > kSmallMaxB ----------------

@@ -175,18 +175,19 @@ ZQ_API int zq_rmsnorm_q4k_gemv(const float *x, const float *gamma, float eps, in
  *   workspace / workspace_bytes : caller-owned device scratch of at least
  *     zq_q4k_gemm_workspace_bytes(N, K, B) bytes (may be NULL when that is 0,
  *     as it is for B = 1 and for 2 <= B <= 4 with K <= 32768; at least
- *     4*B*K + 4*B rounded up to 256 otherwise).  It holds the activations the
- *     tensor cores read, each Q8_1 value q8*d8 split into two binary16
- *     numbers, and a per-token scale; its contents on entry do not matter and
- *     are not preserved.
+ *     4*B*K + 4*B + B*K/8, each part rounded up to 256, otherwise).  It holds
+ *     the activations the tensor cores read (each Q8_1 value q8*d8 split into
+ *     two binary16 numbers), a per-token scale, the scaled block sums and
+ *     partial sums; its contents on entry do not matter and are not
+ *     preserved.
  * B = 1 runs the decode mat-vec; 2 <= B <= 4 (K <= 32768) the same streamed
  * kernel with the tokens staged together, each decoded weight used for all of
- * them (the workspace is not touched).  B >= 5 runs the tensor cores on tiles
- * of 128 tokens x 128 weight rows (5 <= B <= 16: the chunk sizes, one partly
- * filled token tile whose weights are unpacked once and shared).  There every
- * product of an activation part and a weight code sc*q4 is exact and the
- * products are summed in fp32 per 256-weight super-block, then scaled by
- * d_b (and the min term by dmin_b) in fp32.
+ * them (the workspace is not touched).  5 <= B <= 16 runs the chunk kernel
+ * (CTA pairs: 256 weight rows x the 16 tokens' hi and lo parts per MMA),
+ * B >= 17 the prefill kernel (CTA pairs: 256 weight rows x 256 tokens).
+ * There every product of an activation part and a weight code sc*q4 is exact
+ * and the products are summed in fp32 per 256-weight super-block, then
+ * scaled by d_b (the min term, by dmin_b, enters the same sum) in fp32.
  * Shapes: 1 <= B <= 65536, N >= 1, K % 256 == 0, K >= 256.
  */
 ZQ_API int zq_q4k_gemm(const void *W, int N, int K, zq_q8_1 a, int B, float *y,
@@ -329,6 +330,24 @@ ZQ_API size_t zq_q6k_bytes(int N, int K);
 
 /* Bytes of device workspace zq_q4k_gemm needs for this shape (0 if none). */
 ZQ_API size_t zq_q4k_gemm_workspace_bytes(int N, int K, int B);
+
+/*
+ * RMSNorm + Q8_1 of B tokens and the batched projection in one call (ZINC
+ * docs "ROCm backend", "Build and verify": RMS normalisation and Q8
+ * activation packing in one per-token kernel; MIInfer README, "Current
+ * phase": batched Q4_K projections).  y equals zq_rmsnorm_q8_1 followed by
+ * zq_q4k_gemm on the same workspace, bit for bit; for B >= 5 the
+ * normalisation kernel also writes the binary16 activation parts the tensor
+ * cores read, saving a launch and a pass over the codes.
+ *   x : fp32 [B][K];  gamma : fp32 [K];  eps >= 0;  W, N, y : as zq_q4k_gemm.
+ *   q8_out : optional Q8_1 destination of the codes (required for
+ *     2 <= B <= 4, where the streamed mat-vec reads them).
+ *   workspace : zq_q4k_gemm_workspace_bytes(N, K, B) bytes.
+ * Shapes: K % 256 == 0, 256 <= K <= 32768, 1 <= B <= 65536.
+ */
+ZQ_API int zq_rmsnorm_q4k_gemm(const float *x, const float *gamma, float eps, int B, int K, const void *W, int N,
+                               float *y, const zq_q8_1 *q8_out, void *workspace, size_t workspace_bytes,
+                               void *stream);
 
 /* Storage sizes: N x K Q4_K matrix; Q8_1 planes of B x K (qs + d + s). */
 ZQ_API size_t zq_q4k_bytes(int N, int K);
