@@ -263,8 +263,10 @@ class LayerWorkload:
             # activation split) in one kernel, then the projection
             for li in range(self.layers):
                 for k, K, n in self.groups:
+                    # the codes themselves are needed only by the streamed path (B <= 4)
                     self.zq.rmsnorm_q4k_gemm(self.x[k], self.g[k], inputs.EPS, self.SW[r][li][k], n, y=self.gy[k],
-                                             q8_out=self.a[k], workspace=self.ws, stream=stream)
+                                             q8_out=self.a[k] if self.B <= 4 else None, workspace=self.ws,
+                                             stream=stream)
             for (pname, K, N, paired) in self.extra:
                 w1, w2 = extra_w[pname]
                 self._proj(pname, K, N, paired, w1, w2, stream)

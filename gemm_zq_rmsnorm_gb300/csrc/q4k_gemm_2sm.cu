@@ -196,6 +196,7 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
         s_abort = 0;
         s_status = p.status;
         fence_mbar_init();
+        pdl_launch_dependents();
     }
     if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -212,7 +213,10 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
             if (lane == 0) {
                 // ------------------------------------------ token tiles
                 // CTA r stages the tile's tokens r*n/2 .. (96 rows; the MMA
-                // reads the first n/2)
+                // reads the first n/2).  The tokens may come from the
+                // previous kernel on the stream (programmatic launch): wait
+                // for it first; the weights, set-up and conversion do not.
+                pdl_wait();
                 prefetch_tmap(&tmap_hi);
                 prefetch_tmap(&tmap_lo);
                 prefetch_tmap(&tmap_s8);
@@ -344,6 +348,9 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
     } else {
         regs_inc<192>();
         // ---------------------------------------------------- epilogue
+        // (y, the partial sums and the token scales belong to the stream's
+        // previous kernels until they complete)
+        pdl_wait();
         const uint32_t rank = cluster_rank();
         const Tile T = tile_of(p, rank);
         const PairCtx ctx = pair_ctx(rank);
@@ -501,9 +508,10 @@ cudaError_t launch_gemm_pair(const void *W, int N, int K, int B, const __half *h
         g_attr_bytes[dev] = smem;
     }
     const long long pairs = (long long)p.t_tiles * ((N + kPairM - 1) / kPairM) * splits;
-    q4k_gemm_2sm_kernel<<<(unsigned)(2 * pairs), kThreads, smem, st>>>(th, tl, ts, tw, p);
-    if (splits == 1) return cudaGetLastError();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(q4k_gemm_2sm_kernel, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, st, th, tl, ts, tw,
+                        p)) != cudaSuccess)
+        return e;
+    if (splits == 1) return cudaSuccess;
     return launch_splitk_reduce(out, splits, (size_t)B * N, y, st);
 }
 

@@ -252,6 +252,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         s_abort = 0;
         s_status = p.status;
         fence_mbar_init();
+        pdl_launch_dependents();
     }
     if (rank != 0) {
         // the odd CTA's s8 slots are the zero rows (lo columns) of the min MMA's B
@@ -276,6 +277,9 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         // through the TMA unit they would also wait behind the raw tiles.
         const __half *src = rank == 0 ? p.hi : p.lo;
         const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (kConvWarps + kEpiWarps), 0);
+        // the tokens may come from the previous kernel on the stream
+        // (programmatic launch): wait for it; weights and set-up do not
+        pdl_wait();
         static_assert(4 * (kConvWarps + kEpiWarps + 2) <= 128, "st.async words of the odd CTA's warps");
         const uint32_t tfull_cl0 = cluster_addr(smem_u32(&tok_full[0]), 0);
         bool ok = true;
@@ -416,6 +420,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         }
     } else if (warp >= kEpiWarp0) {
         // ---------------------------------------------------- epilogue
+        pdl_wait();   // y, the partial sums and the token scales
         const uint32_t tmem = *tmem_slot;
         const int quarter = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
@@ -622,8 +627,9 @@ cudaError_t launch_gemm_chunk(const void *W, int N, int K, int B, const __half *
         g_attr_bytes[dev] = smem;
     }
     const int P = chunk_plan(N, K, allow_split);
-    q4k_gemm_chunk_kernel<<<(unsigned)(2 * P), kThreads, smem, st>>>(tw, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(q4k_gemm_chunk_kernel, dim3((unsigned)(2 * P)), dim3(kThreads), smem, st, tw, p)) !=
+        cudaSuccess)
+        return e;
     if (P == p.tiles || chunk_pieces(N, K, P) == 0) return cudaSuccess;
     chunk_fixup_kernel<<<dim3(p.tiles, B), kPairM, 0, st>>>(part, B, N, p.nb, p.total, P, y);
     return cudaGetLastError();
