@@ -722,7 +722,7 @@ def batch_record(torch, B, shapes, name, steps, warmup, stream, pk, local_rank, 
         roof = {"bound": "hbm", "kernel": f"q4k_gemm {dK}->{dN} B={B} ({path})",
                 "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4), "peak_source": pk["source"] + " (burst copy)",
-                "traffic": None, "kernel_ms": round(dms, 5),
+                "traffic": recorded_traffic(f"q4k_gemm_chunk_{B}x{dK}x{dN}"), "kernel_ms": round(dms, 5),
                 "algorithmic_bytes_per_launch": int(alg_bytes)}
     else:
         ach = dalg / (dms * 1e-3) / 1e12
@@ -791,6 +791,8 @@ def main():
     ap.add_argument("--workload", default="headline",
                     choices=["headline", "decode-27b", "decode-small", "chunk", "prefill-512", "tiny", "kquants",
                              "peaks"])
+    ap.add_argument("--chunk-batch", type=int, default=0,
+                    help="--workload chunk: run only this chunk size (one of %s)" % (inputs.CHUNK_BATCHES,))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--l2-prefetch", action="store_true",
@@ -893,8 +895,10 @@ def main():
             out["prefill_b512"] = rec
 
     if args.workload in ("headline", "chunk"):
+        batches = [b for b in inputs.CHUNK_BATCHES if args.workload == "headline" or not args.chunk_batch
+                   or b == args.chunk_batch]
         recs = [batch_record(torch, B, inputs.CHUNK_SHAPES, f"chunk-B{B}", sub_steps, args.warmup, **common)
-                for B in inputs.CHUNK_BATCHES]
+                for B in batches]
         if args.workload == "chunk":
             r0 = recs[0]
             out.update({"value": r0["hbm_gbs"], "unit": "GB/s", "ms_per_step": r0["ms_per_step"], "dtype": "u8",

@@ -11,6 +11,7 @@
 #include <cuda.h>
 
 #include "zq_internal.cuh"
+#include "zq_q8_1_pack.cuh"
 #include "zq_tc.cuh"
 #include "zq_tc_common.cuh"
 
@@ -41,11 +42,9 @@ q8_split_kernel(const int8_t *__restrict__ qs, const __half *__restrict__ d8, co
     m = red[0];
 #pragma unroll
     for (int w = 1; w < kSplitThreads / 32; ++w) m = fmaxf(m, red[w]);
-    int k = 0;
-    const float bound = 127.0f * m;   // >= every |x'| of the token
-    if (bound > 65504.0f) frexpf(bound / 65504.0f, &k);   // bound / 65504 <= 2^k
-    const float down = ldexpf(1.0f, -k);
-    if (threadIdx.x == 0 && blockIdx.y == 0) tscale[t] = ldexpf(1.0f, k);
+    const int k = split_scale_exp(m);   // 127 * m bounds every |x'| of the token
+    const float down = pow2_exact(-k);
+    if (threadIdx.x == 0 && blockIdx.y == 0) tscale[t] = pow2_exact(k);
     const int8_t *qt = qs + (size_t)t * K;
     const int sb0 = blockIdx.y * sbc, sb1 = min(K >> 8, sb0 + sbc);   // this CTA's super-blocks
     for (int g = 16 * sb0 + threadIdx.x; g < 16 * sb1; g += kSplitThreads) {

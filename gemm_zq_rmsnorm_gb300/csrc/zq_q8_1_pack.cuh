@@ -49,6 +49,21 @@ __device__ __forceinline__ Q8Block q8_1_pack(const float (&xh)[32])
     return o;
 }
 
+// The batched projection's power-of-two scale for one token's activations:
+// k = 0 when 127 * max|d8| fits binary16 (<= 65504), else the exponent e of
+// 127 * max|d8| / 65504 = f * 2^e with f in [0.5, 1), so every |q8 * d8| *
+// 2^-k stays within binary16 range.  Read from the quotient's exponent field
+// (the quotient is >= 1, a normal number).
+__device__ __forceinline__ int split_scale_exp(float dmax)
+{
+    const float bound = 127.0f * dmax;
+    if (!(bound > 65504.0f)) return 0;
+    return (int)((__float_as_uint(__fdiv_rn(bound, 65504.0f)) >> 23) & 0xFFu) - 126;
+}
+
+// 2^e for e in [-126, 127], built from its exponent field
+__device__ __forceinline__ float pow2_exact(int e) { return __int_as_float((127 + e) << 23); }
+
 // p_b of the canonical order: a fused multiply-add chain over the squares of
 // one 32-value block, in index order, from +0.
 __device__ __forceinline__ float block_sumsq(const float *xb)

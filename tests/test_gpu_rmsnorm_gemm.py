@@ -26,8 +26,11 @@ def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
 
 
+# rows of one block per thread and of two, three and four (K = 8448 leaves
+# all but eight threads with one block; K = 32768 is the widest row allowed)
 @pytest.mark.parametrize("B,K,N", [(1, 1280, 333), (2, 1280, 333), (4, 2048, 512), (5, 1280, 333),
-                                   (16, 5120, 700), (17, 1280, 77), (130, 768, 300), (512, 1024, 512)])
+                                   (16, 5120, 700), (17, 1280, 77), (130, 768, 300), (512, 1024, 512),
+                                   (5, 8448, 96), (8, 17408, 64), (6, 32768, 40), (40, 17408, 130)])
 def test_fused_equals_two_step(B, K, N):
     x, g, W = make_layer_inputs(300 + B, B, K, N)
     xd, gd, Wd = to_dev(x), to_dev(g), to_dev(W)
@@ -44,10 +47,11 @@ def test_fused_equals_two_step(B, K, N):
     assert np.array_equal(q8.s.cpu().numpy().view(np.uint16), s)
 
 
-def test_fused_without_codes_and_oracle_prefill():
-    """B = 512 at the attention input width: no q8_out, y against the oracle
-    on sampled rows."""
-    B, K, N = 512, 5120, 1024
+@pytest.mark.parametrize("K,N", [(5120, 1024), (17408, 256)])
+def test_fused_without_codes_and_oracle_prefill(K, N):
+    """B = 512 at the attention and down-projection input widths: no q8_out,
+    y against the oracle on sampled rows."""
+    B = 512
     x, g, W = make_layer_inputs(310, B, K, N)
     y = zq.rmsnorm_q4k_gemm(to_dev(x), to_dev(g), inputs.EPS, to_dev(W), N)
     torch.cuda.synchronize()
@@ -55,7 +59,7 @@ def test_fused_without_codes_and_oracle_prefill():
     qs, d, s = oracle_q8(x, g)
     rows = sample_rows(N, 37)
     y_ref, S = oracle.q4k_matmul(W, N, K, qs, d, s, rows=rows)
-    assert_within(y.cpu().numpy()[:, rows], y_ref, S, "rmsnorm_q4k_gemm B=512")
+    assert_within(y.cpu().numpy()[:, rows], y_ref, S, f"rmsnorm_q4k_gemm B=512 K={K}")
 
 
 def test_fused_argument_checks():
