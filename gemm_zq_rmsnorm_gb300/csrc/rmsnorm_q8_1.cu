@@ -11,18 +11,26 @@
 // fp32 operation (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so
 // codes and scales are reproducible bit for bit.
 //
-// One CTA per token with one thread per 32-element block (up to 1024
-// threads): every block's fma chain runs in parallel, the partials go through
-// shared memory in block order, the block stays in registers between the two
+// Many tokens (and the batched projection's activation split): one CTA per
+// token with the row staged in shared memory by TMA, one thread per block
+// for the sums of squares and eight lanes per block for the rest, so every
+// global access is coalesced (rmsnorm_q8_1_rows_kernel).  A few tokens: one
+// CTA per token with one thread per 32-element block (up to 1024 threads):
+// every block's fma chain runs in parallel, the partials go through shared
+// memory in block order, the block stays in registers between the two
 // passes, and only the 256-slot sums and the tree are serial.  Rows of up to
-// 2048 blocks (K <= 65536) give a thread two blocks; wider rows use a 256-thread
-// kernel in which thread t owns the blocks of slot t.
+// 2048 blocks (K <= 65536) give a thread two blocks; wider rows use a
+// 256-thread kernel in which thread t owns the blocks of slot t.
 //
 // HBM roofline: reads B*K*4 bytes of x (+ K*4 of gamma, cached), writes
 // B*K*(1 + 4/32) bytes.  At B = 1 the kernel is latency-bound.
+#include <cuda.h>
+
 #include "zq_async.cuh"
 #include "zq_internal.cuh"
 #include "zq_q8_1_pack.cuh"
+#include "zq_tc.cuh"
+#include "zq_tc_common.cuh"
 
 namespace zq {
 namespace {
@@ -42,48 +50,15 @@ __device__ __forceinline__ void pack_block(const float (&xh)[32], int8_t *qdst, 
 }
 
 // Optional outputs of the batched projection's activation split (all null,
-// or all set; only when every block has a thread of its own): x' = q8 * d8
-// as exact binary16 hi + lo parts with the token's power-of-two scale 2^-k
-// (tscale = 2^k, k >= 0 the least that keeps 127 * max d8 within binary16
-// range), and each super-block's eight s8 values scaled alike, twice.
+// or all set): x' = q8 * d8 as exact binary16 hi + lo parts with the token's
+// power-of-two scale 2^-k (tscale = 2^k, k from split_scale_exp, so that
+// 127 * max d8 * 2^-k stays within binary16 range), and each super-block's
+// eight s8 values scaled alike, twice.
 struct SplitOut {
     __half *hi, *lo;
     float *tscale;
     __half *s8x;
 };
-
-// One block's share of the activation split, with the token's scale
-// down = 2^-k applied: its 32 values x' = q8 * d8 * 2^-k as exact binary16
-// hi + lo parts, and its scaled s8 value in both halves of its super-block's
-// 16-entry s8x row (the same numbers as q8_split_kernel derives from the
-// stored codes).
-__device__ __forceinline__ void split_block(const Q8Block &pk, int b, float down, int K, SplitOut so)
-{
-    const float dv = __half2float(pk.d) * down;
-    const uint32_t w[8] = {pk.q0.x, pk.q0.y, pk.q0.z, pk.q0.w, pk.q1.x, pk.q1.y, pk.q1.z, pk.q1.w};
-    uint4 *dh = reinterpret_cast<uint4 *>(so.hi + (size_t)blockIdx.x * K + 32 * b);
-    uint4 *dl = reinterpret_cast<uint4 *>(so.lo + (size_t)blockIdx.x * K + 32 * b);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {   // codes 8q .. 8q + 7
-        uint32_t oh[4], ol[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {   // codes 8q + 2j, 8q + 2j + 1
-            const uint32_t x2 = w[2 * q + (j >> 1)] >> (16 * (j & 1));
-            const float a0 = (float)(int8_t)(x2 & 0xFFu) * dv, a1 = (float)(int8_t)((x2 >> 8) & 0xFFu) * dv;
-            const __half2 vh = __floats2half2_rn(a0, a1);
-            const float2 back = __half22float2(vh);
-            oh[j] = *reinterpret_cast<const uint32_t *>(&vh);
-            const __half2 vl = __floats2half2_rn(a0 - back.x, a1 - back.y);
-            ol[j] = *reinterpret_cast<const uint32_t *>(&vl);
-        }
-        dh[q] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-        dl[q] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-    }
-    const __half sv = __float2half_rn(__half2float(pk.s) * down);
-    __half *sx = so.s8x + (size_t)blockIdx.x * (K / 16) + 16 * (b >> 3) + (b & 7);
-    sx[0] = sv;
-    sx[8] = sv;
-}
 
 __global__ void __launch_bounds__(kMaxThreads)
 rmsnorm_q8_1_kernel(const float *__restrict__ x, const float *__restrict__ gamma, int K, float eps,
@@ -234,70 +209,84 @@ rmsnorm_q8_1_wide_kernel(const float *__restrict__ x, const float *__restrict__ 
     }
 }
 
-// RMSNorm + Q8_1 + the activation split for the batched projection, rows
-// of up to 256 * MB blocks.  One CTA of 256 threads per token, thread t
-// owning the blocks of slot t (t, t + 256, ...), so its running sum of their
-// p_b in increasing b is the slot sum itself; at most 64 registers a thread,
-// so four tokens' CTAs share an SM and 512 tokens run in one wave.  A single
-// block stays in registers between the passes; with more, all of them are
-// prefetched into L2 while the first loads and read again in pass 2.  The
-// packed codes wait in shared memory until the token's largest d8 is known.
-template <int MB>
-__global__ void __launch_bounds__(256, 4)
-rmsnorm_q8_1_split_kernel(const float *__restrict__ x, const float *__restrict__ gamma, int K, float eps,
-                          int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq, SplitOut so)
+// RMSNorm + Q8_1 (+ the activation split of the batched projection) with
+// the token's row staged in shared memory: one CTA of 256 threads per token.
+//  - One thread issues TMA copies of the row, 32 blocks (4 KB) each, as rows
+//    of 128 bytes with the 128-byte swizzle (16-byte piece v of block b at
+//    piece v ^ (b & 7)), each on its own mbarrier.
+//  - Pass 1, one block per thread: thread t owns the blocks of slot t (t,
+//    t + 256, ...) and reads each block's 32 values in order from shared
+//    memory (the swizzle spreads a warp's reads over all banks); its running
+//    sum is the slot sum itself.
+//  - Pass 2, eight lanes per block (four values each), so that the reads of
+//    gamma and every store are coalesced: (a) normalise in place and find
+//    each block's amax and d8, and the token's largest d8; (b) after the
+//    token's scale is known, quantise, sum the codes over the eight lanes,
+//    and write the codes and, with the split, the binary16 hi/lo parts, the
+//    token scale and s8x.
+// Every value equals the thread-per-block kernels' (amax, the code sum and
+// the element-wise steps do not depend on the order).
+constexpr int kRowChunk = 32;      // blocks per TMA copy
+constexpr int kRowsMinTokens = 5;  // codes-only calls with at least this many tokens use it
+
+__global__ void __launch_bounds__(256)
+rmsnorm_q8_1_rows_kernel(const __grid_constant__ CUtensorMap tmap_x, const float *__restrict__ gamma, int K,
+                         float eps, int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq,
+                         SplitOut so, unsigned int *status)
 {
+    extern __shared__ uint8_t smem_raw[];
+    float *xs = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar[kMaxThreads / kRowChunk];
     __shared__ float slot_s[256];
+    __shared__ float red_s[8];
     __shared__ float r_s;
-    __shared__ float dmax_s[8];
-    __shared__ uint4 kq_s[MB][2][256];   // codes of block t + 256 i
-    __shared__ __half2 kds_s[MB][256];   // its (d, s)
+    __shared__ int fail_s;
     const int t = threadIdx.x;
-    const int nblk = K >> 5;
-    const int mine = t < nblk ? (nblk - 1 - t) / 256 + 1 : 0;
-    const float *xt = x + (size_t)blockIdx.x * K;
+    const int nblk = K >> 5, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
+    float *d_s = xs + (size_t)nchunk * kRowChunk * 32;   // d8 of each block, fp32
+    const size_t tok = blockIdx.x;
+    if (t == 0) {
+        for (int c = 0; c < nchunk; ++c) mbar_init(&bar[c], 1);
+        fail_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
     pdl_wait();   // x may come from the previous kernel; the outputs may still be read by it
     pdl_launch_dependents();
-#pragma unroll
-    for (int i = 0; i < MB; ++i)
-        if (i < mine) {
-            if (i > 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(xt + 32 * (t + 256 * i)));
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(gamma + 32 * (t + 256 * i)));
+    if (t == 0) {
+        prefetch_tmap(&tmap_x);
+        for (int c = 0; c < nchunk; ++c) {
+            mbar_arrive_expect_tx(&bar[c], kRowChunk * 128);
+            tma_load_2d(xs + (size_t)c * kRowChunk * 32, &tmap_x, 0, (int)(tok * nblk) + kRowChunk * c, &bar[c]);
         }
+    }
 
     // pass 1: the slot sum of p_b
-    float xr[32];
     float slot = 0.0f;
-#pragma unroll
-    for (int i = 0; i < MB; ++i) {
-        if (i >= mine) break;
-        const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * (t + 256 * i));
+    bool ok = true;
+    for (int b = t; b < nblk; b += 256) {
+        if (!(ok = mbar_wait(&bar[b / kRowChunk], 0, status))) break;
+        const float4 *row = reinterpret_cast<const float4 *>(xs + 32 * b);
         float part = 0.0f;
-        if (MB == 1) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 f = __ldg(p + v);
-                xr[4 * v + 0] = f.x;
-                xr[4 * v + 1] = f.y;
-                xr[4 * v + 2] = f.z;
-                xr[4 * v + 3] = f.w;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) part = __fmaf_rn(xr[j], xr[j], part);
-        } else {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 f = __ldg(p + v);
-                part = __fmaf_rn(f.x, f.x, part);
-                part = __fmaf_rn(f.y, f.y, part);
-                part = __fmaf_rn(f.z, f.z, part);
-                part = __fmaf_rn(f.w, f.w, part);
-            }
+        for (int v = 0; v < 8; ++v) {
+            const float4 f = row[v ^ (b & 7)];
+            part = __fmaf_rn(f.x, f.x, part);
+            part = __fmaf_rn(f.y, f.y, part);
+            part = __fmaf_rn(f.z, f.z, part);
+            part = __fmaf_rn(f.w, f.w, part);
         }
         slot = __fadd_rn(slot, part);
     }
+    if (!ok) fail_s = 1;
     slot_s[t] = slot;
     __syncthreads();
+    if (fail_s) {
+        // a copy did not land in time (status raised): let copies still in
+        // flight finish before the CTA's shared memory goes away
+        for (int c = 0; c < nchunk; ++c) mbar_wait_for(&bar[c], 0, nullptr, 1000000ull);
+        return;
+    }
 #pragma unroll
     for (int off = 128; off >= 32; off >>= 1) {
         if (t < off) slot_s[t] = __fadd_rn(slot_s[t], slot_s[t + off]);
@@ -315,70 +304,105 @@ rmsnorm_q8_1_split_kernel(const float *__restrict__ x, const float *__restrict__
     __syncthreads();
     const float r = r_s;
 
-    // pass 2: normalise and pack, tracking the largest |d8|
+    // pass 2a: lanes 8g .. 8g + 7 of warp w take block 4w + g (+ 32 j),
+    // piece `sub` of it; the warp's four blocks are 512 contiguous bytes
+    // (nblk is a multiple of 8, so a warp's blocks are all in range or none)
+    const int warp = t >> 5, lane = t & 31, sub = lane & 7;
+    const int b0 = 4 * warp + (lane >> 3);
+    // gamma of the lane's next four blocks stays in flight (an L2 round trip
+    // per block would otherwise set the pace)
+    float4 gq[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        gq[u] = b0 + 32 * u < nblk ? __ldg(reinterpret_cast<const float4 *>(gamma + 32 * (b0 + 32 * u)) + sub)
+                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float m = 0.0f;
+    for (int j = 0; b0 + 32 * j < nblk; j += 4) {
 #pragma unroll
-    for (int i = 0; i < MB; ++i) {
-        if (i >= mine) break;
-        const int b = t + 256 * i;
-        if (MB > 1) {
-            const float4 *p = reinterpret_cast<const float4 *>(xt + 32 * b);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const float4 f = __ldg(p + v);
-                xr[4 * v + 0] = f.x;
-                xr[4 * v + 1] = f.y;
-                xr[4 * v + 2] = f.z;
-                xr[4 * v + 3] = f.w;
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int b = b0 + 32 * (j + u);
+            if (b >= nblk) break;
+            const float4 g = gq[u];
+            if (b + 128 < nblk) gq[u] = __ldg(reinterpret_cast<const float4 *>(gamma + 32 * (b + 128)) + sub);
+            float4 *cell = reinterpret_cast<float4 *>(xs + 32 * b) + (sub ^ (b & 7));
+            float4 f = *cell;
+            f.x = __fmul_rn(__fmul_rn(f.x, r), g.x);
+            f.y = __fmul_rn(__fmul_rn(f.y, r), g.y);
+            f.z = __fmul_rn(__fmul_rn(f.z, r), g.z);
+            f.w = __fmul_rn(__fmul_rn(f.w, r), g.w);
+            *cell = f;
+            float a = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const float d = __fdiv_rn(a, 127.0f);
+            if (sub == 0) d_s[b] = d;
+            m = fmaxf(m, __half2float(__float2half_rn(d)));
         }
-        const float4 *g = reinterpret_cast<const float4 *>(gamma + 32 * b);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const float4 w = __ldg(g + v);
-            xr[4 * v + 0] = __fmul_rn(__fmul_rn(xr[4 * v + 0], r), w.x);
-            xr[4 * v + 1] = __fmul_rn(__fmul_rn(xr[4 * v + 1], r), w.y);
-            xr[4 * v + 2] = __fmul_rn(__fmul_rn(xr[4 * v + 2], r), w.z);
-            xr[4 * v + 3] = __fmul_rn(__fmul_rn(xr[4 * v + 3], r), w.w);
-        }
-        const Q8Block pk = q8_1_pack(xr);
-        m = fmaxf(m, fabsf(__half2float(pk.d)));
-        if (qs != nullptr) {
-            const size_t o = (size_t)blockIdx.x * nblk + b;
-            uint4 *dst = reinterpret_cast<uint4 *>(qs + (size_t)blockIdx.x * K + 32 * b);
-            dst[0] = pk.q0;
-            dst[1] = pk.q1;
-            dq[o] = pk.d;
-            sq[o] = pk.s;
-        }
-        kq_s[i][0][t] = pk.q0;
-        kq_s[i][1][t] = pk.q1;
-        kds_s[i][t] = __halves2half2(pk.d, pk.s);
     }
-
     // the token's power-of-two scale 2^-k from its largest d8
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((t & 31) == 0) dmax_s[t >> 5] = m;
+    if (lane == 0) red_s[warp] = m;
     __syncthreads();
-    m = dmax_s[0];
+    m = red_s[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) m = fmaxf(m, dmax_s[w]);
-    const int k = split_scale_exp(m);   // 127 * m bounds every |x'| of the token
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red_s[w]);
+    const int k = split_scale_exp(m);
     const float down = pow2_exact(-k);
-    if (t == 0) so.tscale[blockIdx.x] = pow2_exact(k);
+    if (so.hi != nullptr && t == 0) so.tscale[tok] = pow2_exact(k);
+
+    // pass 2b: the codes of the lane's four values, the block's code sum, s8
+#pragma unroll 2
+    for (int b = b0; b < nblk; b += 32) {
+        const float4 f = reinterpret_cast<const float4 *>(xs + 32 * b)[sub ^ (b & 7)];
+        const float d = d_s[b];
+        const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+        const float xv[4] = {f.x, f.y, f.z, f.w};
+        int q[4];
+        uint32_t word = 0;
+        int sum = 0;
 #pragma unroll
-    for (int i = 0; i < MB; ++i) {
-        if (i >= mine) break;
-        Q8Block pk;
-        pk.q0 = kq_s[i][0][t];
-        pk.q1 = kq_s[i][1][t];
-        const __half2 ds = kds_s[i][t];
-        pk.d = __low2half(ds);
-        pk.s = __high2half(ds);
-        split_block(pk, t + 256 * i, down, K, so);
+        for (int c = 0; c < 4; ++c) {
+            const float qf = fminf(fmaxf(roundf(__fmul_rn(xv[c], id)), -127.0f), 127.0f);
+            q[c] = (int)qf;
+            sum += q[c];
+            word |= ((uint32_t)(q[c] & 0xFF)) << (8 * c);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        const __half dh = __float2half_rn(d);
+        const __half sh = __float2half_rn(__fmul_rn(d, (float)sum));
+        const size_t e0 = tok * K + 32 * (size_t)b + 4 * sub;   // the lane's first element
+        if (qs != nullptr) {
+            *reinterpret_cast<uint32_t *>(qs + e0) = word;
+            if (sub == 0) {
+                dq[tok * nblk + b] = dh;
+                sq[tok * nblk + b] = sh;
+            }
+        }
+        if (so.hi != nullptr) {
+            // x' = q8 * d8 * 2^-k (exact in fp32) as binary16 hi + lo
+            const float dv = __fmul_rn(__half2float(dh), down);
+            const float a0 = __fmul_rn((float)q[0], dv), a1 = __fmul_rn((float)q[1], dv);
+            const float a2 = __fmul_rn((float)q[2], dv), a3 = __fmul_rn((float)q[3], dv);
+            const __half2 h01 = __floats2half2_rn(a0, a1), h23 = __floats2half2_rn(a2, a3);
+            const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);
+            const __half2 l01 = __floats2half2_rn(__fsub_rn(a0, b01.x), __fsub_rn(a1, b01.y));
+            const __half2 l23 = __floats2half2_rn(__fsub_rn(a2, b23.x), __fsub_rn(a3, b23.y));
+            *reinterpret_cast<uint2 *>(so.hi + e0) = make_uint2(h2_bits(h01), h2_bits(h23));
+            *reinterpret_cast<uint2 *>(so.lo + e0) = make_uint2(h2_bits(l01), h2_bits(l23));
+            if (sub == 0) {
+                const __half sv = __float2half_rn(__fmul_rn(__half2float(sh), down));
+                __half *sx = so.s8x + tok * (K / 16) + 16 * (b >> 3) + (b & 7);
+                sx[0] = sv;
+                sx[8] = sv;
+            }
+        }
     }
 }
+
 // h = silu(g) * u packed to Q8_1: one thread per 32-value block
 __global__ void __launch_bounds__(256)
 silu_mul_q8_1_kernel(const float *__restrict__ g, const float *__restrict__ u, int K, int8_t *__restrict__ qs,
@@ -421,6 +445,10 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     const int nblk = K / 32;
     __half *dq = reinterpret_cast<__half *>(out.d);
     __half *sq = reinterpret_cast<__half *>(out.s);
+    // many tokens: the row-staged kernel (coalesced global accesses); a few:
+    // one thread per block, no staging
+    if (B >= kRowsMinTokens && nblk <= kMaxThreads)
+        return launch_rmsnorm_q8_1_split(x, gamma, B, K, eps, &out, nullptr, nullptr, nullptr, nullptr, st);
     if (nblk <= kMaxBlocks) {
         int threads = nblk < kMaxThreads ? (nblk + 31) / 32 * 32 : kMaxThreads;
         if (threads < 256) threads = 256;   // the slot tree needs 256 threads
@@ -429,22 +457,36 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     return launch_pdl(rmsnorm_q8_1_wide_kernel, dim3(B), dim3(256), 0, st, x, gamma, K, eps, out.qs, dq, sq);
 }
 
+size_t rows_smem_bytes(int K)
+{
+    const int nblk = K / 32, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
+    return 1024 + (size_t)nchunk * kRowChunk * 128 + (size_t)nblk * 4;
+}
+
 cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B, int K, float eps,
                                       const zq_q8_1 *out, __half *hi, __half *lo, float *tscale, __half *s8x,
                                       cudaStream_t st)
 {
     const int nblk = K / 32;
+    if (nblk > kMaxThreads) return cudaErrorInvalidValue;   // K > 32768
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return cudaErrorInvalidValue;
+    CUtensorMap tx;
+    cudaError_t e = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, 32, (uint64_t)B * nblk, 32, kRowChunk,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    const size_t smem = rows_smem_bytes(K);
+    static size_t attr = 0;
+    if (smem > attr) {
+        if ((e = cudaFuncSetAttribute(rmsnorm_q8_1_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)rows_smem_bytes(32768))) != cudaSuccess)
+            return e;
+        attr = rows_smem_bytes(32768);
+    }
     int8_t *qs = out ? out->qs : nullptr;
     __half *dq = out ? reinterpret_cast<__half *>(out->d) : nullptr;
     __half *sq = out ? reinterpret_cast<__half *>(out->s) : nullptr;
-    const SplitOut so{hi, lo, tscale, s8x};
-    switch ((nblk + 255) / 256) {
-    case 1: return launch_pdl(rmsnorm_q8_1_split_kernel<1>, dim3(B), dim3(256), 0, st, x, gamma, K, eps, qs, dq, sq, so);
-    case 2: return launch_pdl(rmsnorm_q8_1_split_kernel<2>, dim3(B), dim3(256), 0, st, x, gamma, K, eps, qs, dq, sq, so);
-    case 3: return launch_pdl(rmsnorm_q8_1_split_kernel<3>, dim3(B), dim3(256), 0, st, x, gamma, K, eps, qs, dq, sq, so);
-    case 4: return launch_pdl(rmsnorm_q8_1_split_kernel<4>, dim3(B), dim3(256), 0, st, x, gamma, K, eps, qs, dq, sq, so);
-    default: return cudaErrorInvalidValue;   // K > 32768
-    }
+    return launch_pdl(rmsnorm_q8_1_rows_kernel, dim3(B), dim3(256), smem, st, tx, gamma, K, eps, qs, dq, sq,
+                      SplitOut{hi, lo, tscale, s8x}, device_status_word());
 }
 
 }  // namespace zq

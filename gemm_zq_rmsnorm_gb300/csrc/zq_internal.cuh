@@ -16,9 +16,10 @@ constexpr int kQ4KBlockWeights = 256;
 // Host-side launch descriptions (defined in the kernel TUs, called by the API).
 cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K,
                                 float eps, zq_q8_1 out, cudaStream_t st);
-// RMSNorm + Q8_1 (codes to *out when non-null) that also writes the batched
-// projection's activation split: hi/lo parts, token scales, s8 operand
-// (K <= 32768).
+// RMSNorm + Q8_1 with the token's row staged in shared memory (codes to *out
+// when non-null) that also writes the batched projection's activation split
+// when hi is non-null: hi/lo parts, token scales, s8 operand (K <= 32768,
+// x 16-byte aligned).
 cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B, int K, float eps,
                                       const zq_q8_1 *out, __half *hi, __half *lo, float *tscale, __half *s8x,
                                       cudaStream_t st);
