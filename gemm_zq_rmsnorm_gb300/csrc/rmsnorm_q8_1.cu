@@ -11,20 +11,25 @@
 // fp32 operation (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn), so
 // codes and scales are reproducible bit for bit.
 //
-// Many tokens (and the batched projection's activation split): one CTA per
-// token with the row staged in shared memory by TMA, one thread per block
-// for the sums of squares and eight lanes per block for the rest, so every
-// global access is coalesced (rmsnorm_q8_1_rows_kernel).  A few tokens: one
-// CTA per token with one thread per 32-element block (up to 1024 threads):
-// every block's fma chain runs in parallel, the partials go through shared
-// memory in block order, the block stays in registers between the two
-// passes, and only the 256-slot sums and the tree are serial.  Rows of up to
-// 2048 blocks (K <= 65536) give a thread two blocks; wider rows use a
-// 256-thread kernel in which thread t owns the blocks of slot t.
+// Rows of up to 576 blocks (K <= 18432): a persistent kernel, one block per
+// thread, the token rows and gamma staged in shared memory by TMA (the next
+// token's row loading during the current one) and, with the batched
+// projection's activation split, the binary16 rows stored back by TMA
+// (rmsnorm_q8_1_staged_kernel).  Wider rows of many tokens: one CTA per token
+// with the row staged by TMA, one thread per block for the sums of squares
+// and eight lanes per block for the rest, so every global access is
+// coalesced (rmsnorm_q8_1_rows_kernel).  Otherwise one CTA per token with one
+// thread per 32-element block (up to 1024 threads): every block's fma chain
+// runs in parallel, the partials go through shared memory in block order, the
+// block stays in registers between the two passes, and only the 256-slot
+// sums and the tree are serial; rows of up to 2048 blocks (K <= 65536) give a
+// thread two blocks, wider rows use a 256-thread kernel in which thread t
+// owns the blocks of slot t.
 //
 // HBM roofline: reads B*K*4 bytes of x (+ K*4 of gamma, cached), writes
 // B*K*(1 + 4/32) bytes.  At B = 1 the kernel is latency-bound.
 #include <cuda.h>
+#include <string.h>
 
 #include "zq_async.cuh"
 #include "zq_internal.cuh"
@@ -227,7 +232,7 @@ rmsnorm_q8_1_wide_kernel(const float *__restrict__ x, const float *__restrict__ 
 // Every value equals the thread-per-block kernels' (amax, the code sum and
 // the element-wise steps do not depend on the order).
 constexpr int kRowChunk = 32;      // blocks per TMA copy
-constexpr int kRowsMinTokens = 5;  // codes-only calls with at least this many tokens use it
+constexpr int kRowsMinTokens = 5;  // codes-only calls with wider rows and at least this many tokens use it
 
 __global__ void __launch_bounds__(256)
 rmsnorm_q8_1_rows_kernel(const __grid_constant__ CUtensorMap tmap_x, const float *__restrict__ gamma, int K,
@@ -403,6 +408,242 @@ rmsnorm_q8_1_rows_kernel(const __grid_constant__ CUtensorMap tmap_x, const float
     }
 }
 
+// Persistent RMSNorm + Q8_1 (+ the activation split) for rows of up to
+// kStagedMaxBlocks blocks (K <= 18432), one block per thread throughout:
+//  - a TMA warp copies γ once and the tokens' rows into two row buffers
+//    (4 KB per copy, 128-byte rows, 128-byte swizzle), the next token's row
+//    loading while the CTA works on the current one; with the split it also
+//    stores the token's binary16 hi and lo rows from shared memory (64-byte
+//    rows, 64-byte swizzle: 16-byte piece q of block b at q ^ ((b >> 1) & 3));
+//  - compute thread t owns block t: its fma chain, then the slot sums and
+//    the tree in the canonical order, then normalisation and packing from
+//    shared memory (the swizzles keep a warp's 128-byte rows on distinct
+//    banks), codes and s8x to global memory, hi/lo into the row buffer it
+//    has finished reading.
+// All global traffic of the row is whole TMA boxes; the thread-per-block
+// arithmetic is the same as rmsnorm_q8_1_kernel's, so the bytes are too.
+constexpr int kStagedMaxBlocks = 576;
+constexpr int kStagedMaxChunks = kStagedMaxBlocks / kRowChunk;
+
+struct StagedMaps {
+    CUtensorMap x, g;            // x [B * nblk][32] fp32, γ [nblk][32] fp32; boxes of 32 rows
+    CUtensorMap hi32, lo32;      // hi, lo [B * nblk][32] binary16; boxes of 32 rows
+    CUtensorMap hi8, lo8;        // the same, boxes of 8 rows (a row's last blocks)
+};
+
+__global__ void __launch_bounds__(kStagedMaxBlocks + 32)
+rmsnorm_q8_1_staged_kernel(const __grid_constant__ StagedMaps maps, int B, int K, float eps,
+                           int8_t *__restrict__ qs, __half *__restrict__ dq, __half *__restrict__ sq, SplitOut so,
+                           unsigned int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t gbar[kStagedMaxChunks], xbar[2][kStagedMaxChunks], sfree[2];
+    __shared__ float part_s[kStagedMaxBlocks];
+    __shared__ float slot_s[256];
+    __shared__ float red_s[kStagedMaxBlocks / 32];
+    __shared__ float r_s;
+    __shared__ int fail_s;
+
+    const int t = threadIdx.x;
+    const int nblk = K >> 5, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
+    const int nc = (int)blockDim.x - 32, ncw = nc >> 5;   // compute threads; the last warp moves data
+    const size_t buf_bytes = (size_t)nchunk * kRowChunk * 128;
+    uint8_t *const gs = sm;
+    uint8_t *const xb0 = sm + buf_bytes;
+    const bool split = so.hi != nullptr;
+    const int G = (int)gridDim.x;
+
+    if (t == 0) {
+        for (int c = 0; c < nchunk; ++c) {
+            mbar_init(&gbar[c], 1);
+            mbar_init(&xbar[0][c], 1);
+            mbar_init(&xbar[1][c], 1);
+        }
+        mbar_init(&sfree[0], (uint32_t)ncw);   // buffer s read (and, with the split, staged) by every compute warp
+        mbar_init(&sfree[1], (uint32_t)ncw);
+        fail_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();   // x may come from the previous kernel; the outputs may still be read by it
+    pdl_launch_dependents();
+
+    if (t >= nc) {
+        // ---------------------------------------------------- TMA warp
+        if (t == nc) {
+            prefetch_tmap(&maps.x);
+            prefetch_tmap(&maps.g);
+            for (int c = 0; c < nchunk; ++c) {
+                mbar_arrive_expect_tx(&gbar[c], kRowChunk * 128);
+                tma_load_2d(gs + (size_t)c * kRowChunk * 128, &maps.g, 0, kRowChunk * c, &gbar[c]);
+            }
+            auto load_x = [&](int j) {
+                const int tok = (int)blockIdx.x + j * G, s = j & 1;
+                uint8_t *xb = xb0 + (size_t)s * buf_bytes;
+                for (int c = 0; c < nchunk; ++c) {
+                    mbar_arrive_expect_tx(&xbar[s][c], kRowChunk * 128);
+                    tma_load_2d(xb + (size_t)c * kRowChunk * 128, &maps.x, 0, tok * nblk + kRowChunk * c,
+                                &xbar[s][c]);
+                }
+            };
+            load_x(0);
+            if ((int)blockIdx.x + G < B) load_x(1);
+            for (int j = 0;; ++j) {
+                const int tok = (int)blockIdx.x + j * G, s = j & 1;
+                if (tok >= B) break;
+                if (!wait_fast(&sfree[s], (uint32_t)(j >> 1) & 1u, &fail_s, status)) break;
+                if (split) {
+                    const uint8_t *hs = xb0 + (size_t)s * buf_bytes, *ls = hs + buf_bytes / 2;
+                    const int full = nblk / kRowChunk;
+                    for (int c = 0; c < full; ++c) {
+                        tma_store_2d(&maps.hi32, 0, tok * nblk + kRowChunk * c, hs + (size_t)c * kRowChunk * 64);
+                        tma_store_2d(&maps.lo32, 0, tok * nblk + kRowChunk * c, ls + (size_t)c * kRowChunk * 64);
+                    }
+                    for (int r0 = kRowChunk * full; r0 < nblk; r0 += 8) {
+                        tma_store_2d(&maps.hi8, 0, tok * nblk + r0, hs + (size_t)r0 * 64);
+                        tma_store_2d(&maps.lo8, 0, tok * nblk + r0, ls + (size_t)r0 * 64);
+                    }
+                    bulk_commit();
+                    bulk_wait_read<0>();   // the buffer may take the next row
+                }
+                if (tok + 2 * G < B) load_x(j + 2);
+            }
+            bulk_wait<0>();
+        }
+    } else {
+        // ---------------------------------------------------- compute threads
+        const int warp = t >> 5, lane = t & 31;
+        const bool own = t < nblk;
+        for (int j = 0;; ++j) {
+            const int tok = (int)blockIdx.x + j * G, s = j & 1;
+            if (tok >= B) break;
+            uint8_t *const xb = xb0 + (size_t)s * buf_bytes;
+            bool ok = true;
+            float xr[32];
+            if (own) {
+                ok = wait_fast(&xbar[s][t >> 5], (uint32_t)(j >> 1) & 1u, &fail_s, status);
+                if (ok && j == 0) ok = wait_fast(&gbar[t >> 5], 0, &fail_s, status);
+                if (ok) {
+                    const float4 *row = reinterpret_cast<const float4 *>(xb + (size_t)128 * t);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float4 f = row[v ^ (t & 7)];
+                        xr[4 * v + 0] = f.x;
+                        xr[4 * v + 1] = f.y;
+                        xr[4 * v + 2] = f.z;
+                        xr[4 * v + 3] = f.w;
+                    }
+                    float part = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) part = __fmaf_rn(xr[i], xr[i], part);
+                    part_s[t] = part;
+                }
+            }
+            // one decision for every compute thread: a copy that did not land
+            // in time ends the CTA's work (the status word is raised)
+            if (named_bar_or(1, (uint32_t)nc, !ok)) {
+                fail_s = 1;
+                break;
+            }
+            if (t < 256) {
+                float slot = 0.0f;
+                for (int b = t; b < nblk; b += 256) slot = __fadd_rn(slot, part_s[b]);
+                slot_s[t] = slot;
+            }
+            named_bar(1, (uint32_t)nc);
+#pragma unroll
+            for (int off = 128; off >= 32; off >>= 1) {
+                if (t < off) slot_s[t] = __fadd_rn(slot_s[t], slot_s[t + off]);
+                named_bar(1, (uint32_t)nc);
+            }
+            if (t < 32) {
+                float v = slot_s[t];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
+                if (t == 0) {
+                    const float mean = __fdiv_rn(v, (float)K);
+                    r_s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+                }
+            }
+            named_bar(1, (uint32_t)nc);
+            const float r = r_s;
+            Q8Block pk{};
+            if (own) {
+                const float4 *grow = reinterpret_cast<const float4 *>(gs + (size_t)128 * t);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const float4 w = grow[v ^ (t & 7)];
+                    xr[4 * v + 0] = __fmul_rn(__fmul_rn(xr[4 * v + 0], r), w.x);
+                    xr[4 * v + 1] = __fmul_rn(__fmul_rn(xr[4 * v + 1], r), w.y);
+                    xr[4 * v + 2] = __fmul_rn(__fmul_rn(xr[4 * v + 2], r), w.z);
+                    xr[4 * v + 3] = __fmul_rn(__fmul_rn(xr[4 * v + 3], r), w.w);
+                }
+                pk = q8_1_pack(xr);
+                if (qs != nullptr) {
+                    const size_t o = (size_t)tok * nblk + t;
+                    uint4 *dst = reinterpret_cast<uint4 *>(qs + (size_t)tok * K + 32 * t);
+                    dst[0] = pk.q0;
+                    dst[1] = pk.q1;
+                    dq[o] = pk.d;
+                    sq[o] = pk.s;
+                }
+            }
+            if (split) {
+                // the token's power-of-two scale 2^-k from its largest d8
+                float m = own ? fabsf(__half2float(pk.d)) : 0.0f;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                if (lane == 0) red_s[warp] = m;
+                named_bar(1, (uint32_t)nc);   // (also: every compute thread has read its x from the buffer)
+                m = red_s[0];
+                for (int w = 1; w < ncw; ++w) m = fmaxf(m, red_s[w]);
+                const int k = split_scale_exp(m);
+                const float down = pow2_exact(-k);
+                if (t == 0) so.tscale[tok] = pow2_exact(k);
+                if (own) {
+                    // x' = q8 * d8 * 2^-k (exact in fp32) as binary16 hi + lo,
+                    // into the buffer's hi and lo halves (64-byte swizzle)
+                    const float dv = __fmul_rn(__half2float(pk.d), down);
+                    const uint32_t w[8] = {pk.q0.x, pk.q0.y, pk.q0.z, pk.q0.w, pk.q1.x, pk.q1.y, pk.q1.z, pk.q1.w};
+                    uint8_t *hrow = xb + (size_t)64 * t, *lrow = hrow + buf_bytes / 2;
+                    const int sw = (t >> 1) & 3;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {   // values 8q .. 8q + 7
+                        uint32_t oh[4], ol[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const uint32_t x2 = w[2 * q + (jj >> 1)] >> (16 * (jj & 1));
+                            const float a0 = __fmul_rn((float)(int8_t)(x2 & 0xFFu), dv);
+                            const float a1 = __fmul_rn((float)(int8_t)((x2 >> 8) & 0xFFu), dv);
+                            const __half2 vh = __floats2half2_rn(a0, a1);
+                            const float2 back = __half22float2(vh);
+                            oh[jj] = h2_bits(vh);
+                            ol[jj] = h2_bits(__floats2half2_rn(__fsub_rn(a0, back.x), __fsub_rn(a1, back.y)));
+                        }
+                        *reinterpret_cast<uint4 *>(hrow + 16 * (q ^ sw)) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                        *reinterpret_cast<uint4 *>(lrow + 16 * (q ^ sw)) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    }
+                    const __half sv = __float2half_rn(__fmul_rn(__half2float(pk.s), down));
+                    __half *sx = so.s8x + (size_t)tok * (K / 16) + 16 * (t >> 3) + (t & 7);
+                    sx[0] = sv;
+                    sx[8] = sv;
+                    fence_async_smem();   // the TMA store reads the staging through the async proxy
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[s]);
+        }
+    }
+    if (*reinterpret_cast<volatile int *>(&fail_s)) {
+        // a role gave up: let copies already issued land before the CTA's
+        // shared memory goes away
+        const uint64_t tw = global_ns();
+        while (global_ns() - tw < 200000ull) {
+        }
+    }
+}
+
 // h = silu(g) * u packed to Q8_1: one thread per 32-value block
 __global__ void __launch_bounds__(256)
 silu_mul_q8_1_kernel(const float *__restrict__ g, const float *__restrict__ u, int K, int8_t *__restrict__ qs,
@@ -439,14 +680,77 @@ cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, z
                       reinterpret_cast<__half *>(out.d), reinterpret_cast<__half *>(out.s));
 }
 
+static size_t rows_smem_bytes(int K)
+{
+    const int nblk = K / 32, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
+    return 1024 + (size_t)nchunk * kRowChunk * 128 + (size_t)nblk * 4;
+}
+
+static size_t staged_smem_bytes(int K)
+{
+    const int nblk = K / 32, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
+    return 1024 + 3 * (size_t)nchunk * kRowChunk * 128;   // γ and two row buffers
+}
+
+static cudaError_t launch_staged(const float *x, const float *gamma, int B, int K, float eps, int8_t *qs,
+                                 __half *dq, __half *sq, SplitOut so, cudaStream_t st)
+{
+    const int nblk = K / 32;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(gamma)) & 15u) return cudaErrorInvalidValue;
+    StagedMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const uint64_t rows = (uint64_t)B * nblk;
+    cudaError_t e;
+    if ((e = make_tmap_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, 32, rows, 32, kRowChunk,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess ||
+        (e = make_tmap_2d(&maps.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, gamma, 32, (uint64_t)nblk, 32, kRowChunk,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        return e;
+    if (so.hi != nullptr) {
+        const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        if ((e = make_tmap_2d(&maps.hi32, f16, 2, so.hi, 32, rows, 32, kRowChunk, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+                cudaSuccess ||
+            (e = make_tmap_2d(&maps.lo32, f16, 2, so.lo, 32, rows, 32, kRowChunk, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+                cudaSuccess ||
+            (e = make_tmap_2d(&maps.hi8, f16, 2, so.hi, 32, rows, 32, 8, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess ||
+            (e = make_tmap_2d(&maps.lo8, f16, 2, so.lo, 32, rows, 32, 8, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess)
+            return e;
+    }
+    const int threads = (nblk > 256 ? (nblk + 31) / 32 * 32 : 256) + 32;
+    const size_t smem = staged_smem_bytes(K);
+    static bool attr = false;
+    if (!attr) {
+        if ((e = cudaFuncSetAttribute(rmsnorm_q8_1_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)staged_smem_bytes(32 * kStagedMaxBlocks))) != cudaSuccess)
+            return e;
+        attr = true;
+    }
+    // CTAs per SM for this row width, found once per width
+    static int occ_of[kStagedMaxBlocks / 8 + 1];
+    int &occ = occ_of[nblk / 8];
+    if (occ == 0) {
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, rmsnorm_q8_1_staged_kernel, threads, smem)) !=
+            cudaSuccess)
+            return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+    }
+    const long long cap = (long long)num_sms() * occ;
+    const int grid = (int)(B < cap ? B : cap);
+    return launch_pdl(rmsnorm_q8_1_staged_kernel, dim3(grid), dim3(threads), smem, st, maps, B, K, eps, qs, dq, sq, so,
+                      device_status_word());
+}
+
 cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K, float eps, zq_q8_1 out,
                                 cudaStream_t st)
 {
     const int nblk = K / 32;
     __half *dq = reinterpret_cast<__half *>(out.d);
     __half *sq = reinterpret_cast<__half *>(out.s);
-    // many tokens: the row-staged kernel (coalesced global accesses); a few:
-    // one thread per block, no staging
+    // rows of up to kStagedMaxBlocks blocks: the persistent staged kernel;
+    // wider rows of many tokens: the row-staged kernel (coalesced global
+    // accesses); otherwise one thread per block, no staging
+    if (nblk <= kStagedMaxBlocks)
+        return launch_staged(x, gamma, B, K, eps, out.qs, dq, sq, SplitOut{nullptr, nullptr, nullptr, nullptr}, st);
     if (B >= kRowsMinTokens && nblk <= kMaxThreads)
         return launch_rmsnorm_q8_1_split(x, gamma, B, K, eps, &out, nullptr, nullptr, nullptr, nullptr, st);
     if (nblk <= kMaxBlocks) {
@@ -457,18 +761,16 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     return launch_pdl(rmsnorm_q8_1_wide_kernel, dim3(B), dim3(256), 0, st, x, gamma, K, eps, out.qs, dq, sq);
 }
 
-size_t rows_smem_bytes(int K)
-{
-    const int nblk = K / 32, nchunk = (nblk + kRowChunk - 1) / kRowChunk;
-    return 1024 + (size_t)nchunk * kRowChunk * 128 + (size_t)nblk * 4;
-}
-
 cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B, int K, float eps,
                                       const zq_q8_1 *out, __half *hi, __half *lo, float *tscale, __half *s8x,
                                       cudaStream_t st)
 {
     const int nblk = K / 32;
     if (nblk > kMaxThreads) return cudaErrorInvalidValue;   // K > 32768
+    if (nblk <= kStagedMaxBlocks)
+        return launch_staged(x, gamma, B, K, eps, out ? out->qs : nullptr,
+                             out ? reinterpret_cast<__half *>(out->d) : nullptr,
+                             out ? reinterpret_cast<__half *>(out->s) : nullptr, SplitOut{hi, lo, tscale, s8x}, st);
     if (reinterpret_cast<uintptr_t>(x) & 15u) return cudaErrorInvalidValue;
     CUtensorMap tx;
     cudaError_t e = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, 32, (uint64_t)B * nblk, 32, kRowChunk,

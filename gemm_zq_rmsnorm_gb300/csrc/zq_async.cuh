@@ -178,6 +178,22 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads)
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also tells every participant whether any of them
+// passed pred = true (one decision for all, whatever else changes meanwhile).
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.or.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(threads), "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the next grid to start its prologue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
