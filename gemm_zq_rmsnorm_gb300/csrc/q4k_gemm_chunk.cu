@@ -26,18 +26,21 @@
 // of weight bytes whatever the shape; a tile that straddles ranges leaves
 // partial sums per range, which a fixup kernel adds in range order.
 //
-// Warp roles (16 warps): 0 the token loader (cp.async copies of each
-// super-block's token tiles and s8 tile into a ten-super-block ring,
+// Warp roles (28 warps): 0 the token loader (cp.async copies of each
+// super-block's token tiles and s8 tile into an eight-super-block ring,
 // signalled to the even CTA's barrier); 1 the MMA issuer (even CTA, whole
 // warp, one elected lane: the 17 MMAs of a super-block back to back) and
 // tensor-memory owner; 2 the raw-tile TMA producer (this CTA's Q4_K
-// super-block tiles, six in flight); 3 idle; 4-11 converters (warp w: rows
-// 32*(w%4).. of TMEM lane quarter w%4, half h = (w-4)/4 of every
-// super-block -- stages 2h, 2h + 1 and terms 4h .. 4h + 3 of the row's min
-// operand -- with the row's metadata decoded once per half); 12-15 epilogue
-// (one lane quarter each).  The integer pipe bounds the converters: per
-// weight one byte permute per four weights, two masks per four and one
-// half2 fused multiply-add per two.
+// super-block tiles, six in flight); 3 idle; 4-19 converters, one per (TMEM
+// lane quarter w % 4, K = 64 stage (w - 4) / 4): the stage's two sub-block
+// scales come from shared memory, so a converter only turns nibbles into
+// binary16 products; 20-23 one per lane quarter: they decode each row's
+// super-block metadata once (sub-block scales, the min operand, the fold)
+// into a ring of their own as soon as the raw tile lands, so the converters
+// find it ready; 24-27 the epilogue, one per lane quarter.  The integer pipe bounds the converters:
+// one byte permute per four weights, two masks per four and one half2 fused
+// multiply-add per two; sixteen of them keep enough independent work in
+// flight on each SM sub-partition.
 // Waits suspend in hardware rather than spin, leaving issue slots to the
 // converters, which share every SM sub-partition with the other roles (a
 // warp reaches only the TMEM lane quarter of its sub-partition).  Every wait
@@ -61,21 +64,21 @@ constexpr int kN = 2 * kTok;
 constexpr int kASB = 3;                     // super-blocks of converted weights in TMEM (four K = 64 stages each)
 constexpr int kAcc = 4;                     // super-block accumulators
 constexpr int kRawSlots = 6;                // raw Q4_K tiles (110 KB in flight)
-constexpr int kMinSlots = kASB;             // min operands (A side), reused with the A slots
-constexpr int kTokSB = 10;                  // token ring, in super-blocks (four K = 64 stages and an s8 tile each)
-constexpr int kTokAhead = 8;                // super-blocks of token copies in flight (cp.async groups)
+constexpr int kMetaSlots = 6;               // decoded row metadata (sub-block scales, min operand) ring
+constexpr int kTokSB = 8;                   // token ring, in super-blocks (four K = 64 stages and an s8 tile each)
 constexpr int kTokAtom = kTok * 128;        // 16 rows x 64 binary16, 128-byte swizzle
 constexpr int kAMinAtom = kRows * 32;       // 128 rows x 16 binary16, 32-byte swizzle
 constexpr int kBMinAtom = kTok * 32;        // 16 rows x 16 binary16, 32-byte swizzle
 constexpr int kRawBytes = kRows * kQ4KBlockBytes;
-constexpr int kThreads = 512;
-constexpr int kConvWarp0 = 4, kConvWarps = 8;   // two sets of four: set h converts stages 2h, 2h + 1
-constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
+constexpr int kThreads = 896;
+constexpr int kConvWarp0 = 4, kConvWarps = 16;  // one per (TMEM lane quarter, K = 64 stage)
+constexpr int kMetaWarp0 = 20, kMetaWarps = 4;  // row metadata, one per lane quarter
+constexpr int kEpiWarp0 = 24, kEpiWarps = 4;    // epilogue, one per lane quarter
+constexpr int kScaleRow = 16;                   // bytes per row of a super-block's sub-block scales
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = kAcc * kN, kACols = 128;  // accumulators [0, 128), A slot a at 128 + 128 a
 constexpr uint32_t kConvSigTx = 4 * kConvWarps;        // the odd CTA's converter warps
-constexpr uint32_t kTokSigTx = 4;                      // the odd CTA's token warp
-static_assert(kTokAhead - 1 < kTokSB, "a super-block's tokens are published before its slot is waited for again");
+constexpr uint32_t kTokSigTx = 4;                      // the odd CTA's token relay (warp 1)
 constexpr uint32_t kEpiSigTx = 4 * kEpiWarps;          // the odd CTA's epilogue warps
 static_assert(kACol0 + kASB * kACols <= kTmemCols, "tensor memory budget");
 
@@ -84,12 +87,16 @@ struct Smem {
     static constexpr size_t tok(int ts, int i) { return ((size_t)ts * 4 + i) * kTokAtom; }
     static constexpr size_t bmin(int ts) { return tok(kTokSB, 0) + (size_t)ts * kBMinAtom; }
     static constexpr size_t amin(int i) { return bmin(kTokSB) + (size_t)i * kAMinAtom; }
-    static constexpr size_t raw(int i) { return amin(kMinSlots) + (size_t)i * kRawBytes; }
+    // the eight sub-block scales sc_j * 2^-e of each row (binary16), per metadata slot
+    static constexpr size_t scales(int i) { return amin(kMetaSlots) + (size_t)i * kRows * kScaleRow; }
+    // each row's accumulator fold (fp32), per metadata slot
+    static constexpr size_t fold(int i) { return scales(kMetaSlots) + (size_t)i * kRows * 4; }
+    static constexpr size_t raw(int i) { return fold(kMetaSlots) + (size_t)i * kRawBytes; }
     static constexpr size_t sig() { return raw(kRawSlots); }   // st.async targets of the odd CTA's warps
     static constexpr size_t bars() { return sig() + 128; }
     // afull[3], aempty[3], raw_full[6], raw_empty[6], tfull[4], tempty[4],
-    // tok_full[10], tok_empty[10], drain
-    static constexpr int kNumBars = 2 * kASB + 2 * kRawSlots + 2 * kAcc + 2 * kTokSB + 1;
+    // tok_full[8], tok_empty[8], drain, meta_full[6], meta_empty[6], tok_land[8]
+    static constexpr int kNumBars = 2 * kASB + 2 * kRawSlots + 2 * kAcc + 3 * kTokSB + 1 + 2 * kMetaSlots;
     static constexpr size_t tmem_slot() { return bars() + kNumBars * 8; }
     static constexpr size_t total() { return tmem_slot() + 16 + 1024; }   // + alignment slack
 };
@@ -148,63 +155,69 @@ __device__ __forceinline__ float weight_scale(uint32_t d_dmin, int &e)
     return hd ? __int_as_float((127 - e) << 23) : 0.0f;
 }
 
-// Converts half H of a super-block of weight row r -- stages 2H and 2H + 1,
-// sub-blocks 4H .. 4H + 3 -- to binary16 sc * q * 2^-e and stores it in the
-// row's TMEM lane at columns col .. col + 63 (per stage, binary16 pairs in K
-// order: the even sub-block's 32 weights, then the odd one's).  Also writes
-// terms j = 4H .. 4H + 3 of the row's min operand, -(dmin/d) * m_j * 2^-e as
-// binary16 hi and lo parts, into the row's 32-byte swizzled line `mrow` (hi
-// parts in its first 16 bytes, lo parts in the second, before the swizzle).
-// The row's metadata is decoded once for both stages.
-template <int H>
-__device__ __forceinline__ void convert_half(const uint8_t *raw, uint32_t col, uint8_t *mrow, int r)
+// Decodes the super-block metadata of one weight row: the eight sub-block
+// scales sc_j * 2^-e as binary16 into `srow` (s_j at half j), the min
+// operand -(dmin/d) * m_j * 2^-e as binary16 hi and lo parts into the row's
+// 32-byte swizzled line `mrow` (hi parts in its first 16 bytes, lo parts in
+// the second, before the swizzle), and returns the accumulator's fold
+// (d, or 1 when d = 0) * 2^e.
+__device__ __forceinline__ float decode_row(const uint8_t *raw, uint8_t *srow, uint8_t *mrow, int r)
 {
     const uint4 hdr = *reinterpret_cast<const uint4 *>(raw);
     int e;
     const float wmul = weight_scale(hdr.x, e);
-    uint32_t sc[4], m[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) q4k_scale_min(hdr.y, hdr.z, hdr.w, 4 * H + j, sc[j], m[j]);
-#pragma unroll
-    for (int st = 0; st < 2; ++st) {
-        const int I = 2 * H + st;   // stage: nibble bytes 32 I .. 32 I + 31
-        const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * I);
-        const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * I);
-        const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-        const float s0 = (float)sc[2 * st] * wmul, s1 = (float)sc[2 * st + 1] * wmul;
-        // low nibble in the mantissa of 1024: s0 * (1024 + q) - 1024 s0;
-        // high nibble as 1024 + 16 q: (s1 / 16) * (1024 + 16 q) - 64 s1
-        const __half2 a0 = __float2half2_rn(s0), b0 = __float2half2_rn(-1024.0f * s0);
-        const __half2 a1 = __float2half2_rn(s1 * 0.0625f), b1 = __float2half2_rn(-64.0f * s1);
-        uint32_t o[32];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {   // nibble bytes 4c..4c+3 -> columns 2c, 2c+1 of each sub-block
-            const uint32_t p0 = __byte_perm(wv[c], 0, 0x4140), p1 = __byte_perm(wv[c], 0, 0x4342);
-            const uint32_t l0 = (p0 & 0x000F000Fu) | 0x64006400u, l1 = (p1 & 0x000F000Fu) | 0x64006400u;
-            const uint32_t u0 = (p0 & 0x00F000F0u) | 0x64006400u, u1 = (p1 & 0x00F000F0u) | 0x64006400u;
-            o[2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&l0), a0, b0));
-            o[2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&l1), a0, b0));
-            o[16 + 2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&u0), a1, b1));
-            o[16 + 2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&u1), a1, b1));
-        }
-        tmem_st32(col + 32u * st, o);
-    }
     // min terms: r = dmin / d (dmin itself when d = 0), times 2^-e
     const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xFFFFu)));
     const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
     const float rr = ((hdr.x & 0x7FFFu) ? dm / d : dm) * __int_as_float((127 - e) << 23);
-    uint32_t hv[2], lv[2];
+    uint32_t sv[4], hv[4], lv[4];
 #pragma unroll
-    for (int j = 0; j < 4; j += 2) {
-        const float v0 = -rr * (float)m[j], v1 = -rr * (float)m[j + 1];
+    for (int j = 0; j < 8; j += 2) {
+        uint32_t sc0, m0, sc1, m1;
+        q4k_scale_min(hdr.y, hdr.z, hdr.w, j, sc0, m0);
+        q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, sc1, m1);
+        sv[j >> 1] = h2_bits(__floats2half2_rn((float)sc0 * wmul, (float)sc1 * wmul));
+        const float v0 = -rr * (float)m0, v1 = -rr * (float)m1;
         const __half2 hh = __floats2half2_rn(v0, v1);
         const float2 hb = __half22float2(hh);
         hv[j >> 1] = h2_bits(hh);
         lv[j >> 1] = h2_bits(__floats2half2_rn(v0 - hb.x, v1 - hb.y));
     }
+    *reinterpret_cast<uint4 *>(srow) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
     const int s32 = (r >> 2) & 1;
-    *reinterpret_cast<uint2 *>(mrow + ((0 ^ s32) << 4) + 8 * H) = make_uint2(hv[0], hv[1]);
-    *reinterpret_cast<uint2 *>(mrow + ((1 ^ s32) << 4) + 8 * H) = make_uint2(lv[0], lv[1]);
+    *reinterpret_cast<uint4 *>(mrow + ((0 ^ s32) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4 *>(mrow + ((1 ^ s32) << 4)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    return ((hdr.x & 0x7FFFu) ? d : 1.0f) * __int_as_float((127 + e) << 23);
+}
+
+// Converts stage I (nibble bytes 32 I .. 32 I + 31: sub-blocks 2I, low
+// nibbles, and 2I + 1, high nibbles) of one weight row to binary16
+// sc * q * 2^-e and stores it in the row's TMEM lane at columns col ..
+// col + 31 (binary16 pairs in K order: sub-block 2I's 32 weights, then
+// 2I + 1's).  s01: the two sub-blocks' scales as binary16 (2I low, 2I + 1
+// high).  Low nibble in the mantissa of 1024: s * (1024 + q) - 1024 s; high
+// nibble as 1024 + 16 q: (s / 16) * (1024 + 16 q) - 64 s (every step exact).
+__device__ __forceinline__ void convert_stage(const uint8_t *raw, int I, uint32_t s01, uint32_t col)
+{
+    const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * I);
+    const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + 32 + 32 * I);
+    const uint32_t wv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+    const __half2 s2 = *reinterpret_cast<const __half2 *>(&s01);
+    const __half2 a0 = __low2half2(s2), sh = __high2half2(s2);
+    const __half2 b0 = __hmul2(a0, __float2half2_rn(-1024.0f));
+    const __half2 a1 = __hmul2(sh, __float2half2_rn(0.0625f)), b1 = __hmul2(sh, __float2half2_rn(-64.0f));
+    uint32_t o[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {   // nibble bytes 4c..4c+3 -> columns 2c, 2c+1 of each sub-block
+        const uint32_t p0 = __byte_perm(wv[c], 0, 0x4140), p1 = __byte_perm(wv[c], 0, 0x4342);
+        const uint32_t l0 = (p0 & 0x000F000Fu) | 0x64006400u, l1 = (p1 & 0x000F000Fu) | 0x64006400u;
+        const uint32_t u0 = (p0 & 0x00F000F0u) | 0x64006400u, u1 = (p1 & 0x00F000F0u) | 0x64006400u;
+        o[2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&l0), a0, b0));
+        o[2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&l1), a0, b0));
+        o[16 + 2 * c] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&u0), a1, b1));
+        o[16 + 2 * c + 1] = h2_bits(__hfma2(*reinterpret_cast<const __half2 *>(&u1), a1, b1));
+    }
+    tmem_st32(col, o);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -222,6 +235,12 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
     uint64_t *raw_full = aempty + kASB, *raw_empty = raw_full + kRawSlots;
     uint64_t *tfull = raw_empty + kRawSlots, *tempty = tfull + kAcc;
     uint64_t *tok_full = tempty + kAcc, *tok_empty = tok_full + kTokSB, *drain = tok_empty + kTokSB;
+    // meta_full[m]: the rows' scales, min operand and fold of super-block l
+    // (m = l % 6) are in this CTA's shared memory; meta_empty[m]: its
+    // epilogue has read the folds (after its MMAs completed), freeing slot m
+    uint64_t *meta_full = drain + 1, *meta_empty = meta_full + kMetaSlots;
+    // tok_land[ts] (odd CTA): its token copies of slot ts have landed
+    uint64_t *tok_land = meta_empty + kMetaSlots;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + Smem::tmem_slot());
 
     const int warp = threadIdx.x >> 5;
@@ -237,12 +256,19 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
             mbar_init(&aempty[a], 1);
         }
         for (int ts = 0; ts < kTokSB; ++ts) {
-            mbar_init(&tok_full[ts], 1);   // the even CTA's token warp (+ the odd CTA's st.async bytes)
+            // the token warp's 32 lanes, each once its copies landed (+ in the
+            // even CTA the odd CTA's st.async bytes)
+            mbar_init(&tok_full[ts], 32);
             mbar_init(&tok_empty[ts], 1);
+            mbar_init(&tok_land[ts], 32);
         }
         for (int i = 0; i < kRawSlots; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvWarps);
+            mbar_init(&raw_empty[i], kConvWarps + kMetaWarps);
+        }
+        for (int m = 0; m < kMetaSlots; ++m) {
+            mbar_init(&meta_full[m], kMetaWarps);
+            mbar_init(&meta_empty[m], kEpiWarps);
         }
         for (int j = 0; j < kAcc; ++j) {
             mbar_init(&tfull[j], 1);
@@ -271,20 +297,22 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         // The whole warp copies each super-block's token tiles (four 16 x 64
         // stages, hi in the even CTA, lo in the odd, 128-byte swizzle; and
         // in the even CTA the s8 tile) into its slot of a ring of kTokSB
-        // super-blocks with cp.async, kTokAhead super-blocks in flight, and
-        // signals a super-block once its copies have landed.  Under full HBM
-        // load a copy takes ~3-4 us, so the copies run far ahead of the MMAs;
-        // through the TMA unit they would also wait behind the raw tiles.
+        // super-blocks with cp.async.  Each lane's arrival on the slot's
+        // barrier follows its copies by hardware, so the warp never waits
+        // for a copy, only for a free slot: under full HBM load a copy takes
+        // ~3-4 us, and through the TMA unit it would also wait behind the raw
+        // tiles.  The odd CTA's slots complete locally (tok_land); its warp 1
+        // forwards each to the even CTA's tok_full.
         const __half *src = rank == 0 ? p.hi : p.lo;
-        const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (kConvWarps + kEpiWarps), 0);
         // the tokens may come from the previous kernel on the stream
         // (programmatic launch): wait for it; weights and set-up do not
         pdl_wait();
-        static_assert(4 * (kConvWarps + kEpiWarps + 2) <= 128, "st.async words of the odd CTA's warps");
-        const uint32_t tfull_cl0 = cluster_addr(smem_u32(&tok_full[0]), 0);
         bool ok = true;
-        auto issue = [&](int l) {
+        for (int l = 0; l < L && ok; ++l) {
             const int ts = l % kTokSB;
+            if (l >= kTokSB && !(ok = pair_lane0_wait(&tok_empty[ts], ((l / kTokSB) - 1) & 1, ctx))) break;
+            // the odd CTA's forwarded signal, counted in bytes
+            if (rank == 0 && lane == 0) mbar_expect_tx(&tok_full[ts], kTokSigTx);
             const int b = (int)((g0 + l) % p.nb);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -302,31 +330,9 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
                 const __half *g = p.s8x + (size_t)(t < p.B ? t : 0) * (p.K / 16) + 16 * b + 8 * ch;
                 cp_async16(sm + Smem::bmin(ts) + 32 * t + ((ch ^ ((t >> 2) & 1)) << 4), g, t < p.B ? 16u : 0u);
             }
-            cp_async_commit();
-        };
-        auto publish = [&](int l) {
-            const int ts = l % kTokSB;
-            fence_async_smem();   // the MMA reads the copies through the async proxy
-            __syncwarp();
-            if (lane == 0) {
-                if (rank != 0)
-                    st_async_signal(sig, tfull_cl0 + 8u * (uint32_t)ts);
-                else
-                    mbar_arrive_expect_tx(&tok_full[ts], kTokSigTx);
-            }
-        };
-        for (int l = 0; l < L && ok; ++l) {
-            const int ts = l % kTokSB;
-            if (l >= kTokSB && !(ok = pair_lane0_wait(&tok_empty[ts], ((l / kTokSB) - 1) & 1, ctx))) break;
-            issue(l);
-            if (l >= kTokAhead - 1) {
-                cp_async_wait<kTokAhead - 1>();
-                publish(l - (kTokAhead - 1));
-            }
+            cp_async_mbar_arrive(rank == 0 ? &tok_full[ts] : &tok_land[ts]);
         }
-        cp_async_wait<0>();   // (also: no copy in flight when the pair tears down)
-        if (ok)
-            for (int l = L - (kTokAhead - 1) > 0 ? L - (kTokAhead - 1) : 0; l < L; ++l) publish(l);
+        cp_async_wait<0>();   // no copy in flight when the pair tears down
     } else if (warp == 2) {
         // (a warp of its own: a lane of the token producer's warp waiting
         // on the raw ring would hold that warp's token copies back)
@@ -344,6 +350,18 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
             }
         }
     } else if (warp == 1) {
+        if (rank != 0) {
+            // ------------------------- odd CTA: forward landed token slots
+            const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (kConvWarps + kEpiWarps), 0);
+            static_assert(4 * (kConvWarps + kEpiWarps + 2) <= 128, "st.async words of the odd CTA's warps");
+            const uint32_t tfull_cl0 = cluster_addr(smem_u32(&tok_full[0]), 0);
+            for (int l = 0; l < L; ++l) {
+                const int ts = l % kTokSB;
+                if (!pair_lane0_wait(&tok_land[ts], (uint32_t)(l / kTokSB) & 1u, ctx)) break;
+                fence_async_smem();   // the MMA reads the copies through the async proxy
+                if (lane == 0) st_async_signal(sig, tfull_cl0 + 8u * (uint32_t)ts);
+            }
+        }
         // ---------------------------------------------------- MMA issuer
         // (the whole warp runs the loop and waits; one elected lane issues)
         if (rank == 0) {
@@ -356,13 +374,14 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
             constexpr uint32_t idesc = idesc_f16_f32(kPairM, kN);
             bool ok = true;
             for (int l = 0; l < L && ok; ++l) {
-                const int j = l % kAcc, ts = l % kTokSB, a = l % kASB;
+                const int j = l % kAcc, ts = l % kTokSB, a = l % kASB, m = l % kMetaSlots;
                 // the epilogues have read accumulator j (super-block l - 4)
                 if (l >= kAcc && !(ok = __all_sync(0xffffffffu, pair_wait(&tempty[j], ((l / kAcc) - 1) & 1, ctx))))
                     break;
                 // the super-block's token tiles and converted weights are in both CTAs
                 if (!(ok = __all_sync(0xffffffffu, pair_wait(&tok_full[ts], (l / kTokSB) & 1, ctx)))) break;
                 if (!(ok = __all_sync(0xffffffffu, pair_wait(&afull[a], (l / kASB) & 1, ctx)))) break;
+                fence_async_smem();   // this CTA's token copies landed (cp.async): order them before the MMAs
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(kN * j);
                 const uint32_t a_tmem = tmem + kACol0 + kACols * a;
@@ -372,7 +391,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
                     for (int kk = 0; kk < 16; ++kk)   // K = 16 steps of the super-block
                         mma_f16_pair_ta(d, a_tmem + 8 * kk, bt + (uint64_t)(kk >> 2) * kT16 + 2 * (kk & 3), idesc,
                                         kk != 0 ? 1u : 0u);
-                    mma_f16_pair(d, amn + (uint64_t)a * kAM16, bmn + (uint64_t)ts * kBM16, idesc, 1u);
+                    mma_f16_pair(d, amn + (uint64_t)m * kAM16, bmn + (uint64_t)ts * kBM16, idesc, 1u);
                     mma_commit_pair_mc(&tfull[j], 3);
                     mma_commit_pair_mc(&tok_empty[ts], 3);
                     mma_commit_pair_mc(&aempty[a], 3);
@@ -387,96 +406,101 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
         // ---------------------------------------------------- converters
         const uint32_t tmem = *tmem_slot;
-        const int quarter = warp & 3, h = (warp - kConvWarp0) >> 2;   // lane quarter, stages 2h, 2h + 1
+        const int quarter = warp & 3, st = (warp - kConvWarp0) >> 2;   // lane quarter, K = 64 stage
         const int r = 32 * quarter + lane;   // weight row = TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + kACol0 + 64u * (uint32_t)h;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16) + kACol0 + 32u * (uint32_t)st;
         const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * (warp - kConvWarp0), 0);
         const uint32_t afull_cl0 = cluster_addr(smem_u32(&afull[0]), 0);   // barriers 8 bytes apart
         bool ok = true;
-        // ring positions kept as counters: raw slot rs (phase rph), A slot a (phase aph)
+        // ring positions kept as counters: raw and metadata slot rs (phase
+        // rph; both rings have kRawSlots slots), A slot a (phase aph)
         int rs = 0, a = 0;
         uint32_t rph = 0, aph = 0;
+        static_assert(kMetaSlots == kRawSlots, "one counter for both rings");
         for (int l = 0; l < L && ok; ++l) {
             if (!(ok = pair_lane0_wait(&raw_full[rs], rph, ctx))) break;
+            if (!(ok = pair_lane0_wait(&meta_full[rs], rph, ctx))) break;   // the rows' scales
             if (l >= kASB && !(ok = pair_lane0_wait(&aempty[a], aph ^ 1u, ctx))) break;
             tc_fence_after();
-            const uint8_t *raw = sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes;
-            const uint32_t col = lane_base + kACols * a;
-            uint8_t *mrow = sm + Smem::amin(a) + (size_t)r * 32;
-            if (h == 0)
-                convert_half<0>(raw, col, mrow, r);
-            else
-                convert_half<1>(raw, col, mrow, r);
-            fence_async_smem();   // the min MMA reads the min operand through the async proxy
+            const uint32_t s01 =
+                *reinterpret_cast<const uint32_t *>(sm + Smem::scales(rs) + (size_t)r * kScaleRow + 4 * st);
+            convert_stage(sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes, st, s01, lane_base + kACols * a);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                signal_leader(&afull[a], rank, quarter == 0 && h == 0, kConvSigTx, sig, afull_cl0 + 8u * (uint32_t)a);
+                signal_leader(&afull[a], rank, quarter == 0 && st == 0, kConvSigTx, sig, afull_cl0 + 8u * (uint32_t)a);
                 mbar_arrive(&raw_empty[rs]);
             }
             if (++rs == kRawSlots) { rs = 0; rph ^= 1u; }
             if (++a == kASB) { a = 0; aph ^= 1u; }
         }
+    } else if (warp >= kMetaWarp0 && warp < kMetaWarp0 + kMetaWarps) {
+        // ----------------------------------------------------- row metadata
+        // Super-block l's row metadata (scales, min operand, fold), decoded
+        // once its raw tile has landed and the epilogue of l - 6 has
+        // released metadata slot l % 6.
+        const int r = 32 * (warp & 3) + lane;
+        bool ok = true;
+        int rs = 0;   // raw and metadata slot (phase rph)
+        uint32_t rph = 0;
+        for (int l = 0; l < L && ok; ++l) {
+            if (!(ok = pair_lane0_wait(&raw_full[rs], rph, ctx))) break;
+            if (l >= kMetaSlots && !(ok = pair_lane0_wait(&meta_empty[rs], rph ^ 1u, ctx))) break;
+            const float f = decode_row(sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes,
+                                       sm + Smem::scales(rs) + (size_t)r * kScaleRow,
+                                       sm + Smem::amin(rs) + (size_t)r * 32, r);
+            reinterpret_cast<float *>(sm + Smem::fold(rs))[r] = f;
+            fence_async_smem();   // the min MMA reads the min operand through the async proxy
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&meta_full[rs]);
+                mbar_arrive(&raw_empty[rs]);
+            }
+            if (++rs == kRawSlots) { rs = 0; rph ^= 1u; }
+        }
     } else if (warp >= kEpiWarp0) {
-        // ---------------------------------------------------- epilogue
+        // ---------------------------------------------------------- epilogue
         pdl_wait();   // y, the partial sums and the token scales
         const uint32_t tmem = *tmem_slot;
         const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
         const uint32_t sig = cluster_addr(smem_u32(sm + Smem::sig()) + 4u * kConvWarps + 4u * quarter, 0);
         const uint32_t tempty_cl0 = cluster_addr(smem_u32(&tempty[0]), 0);
         float acc[kTok];
 #pragma unroll
         for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
-        // the row's d/dmin of super-block l, read from global memory four
-        // super-blocks ahead (under full HBM load a read takes ~1-2 us)
-        auto header = [&](int l) -> uint32_t {
-            if (l >= L) return 0u;
-            const long long g = g0 + l;
-            const int n = (int)(g / p.nb) * kPairM + kRows * (int)rank + 32 * quarter + lane;
-            return n < p.N ? ld_nc_u32(p.W + (size_t)n * p.row_bytes + (size_t)kQ4KBlockBytes * (int)(g % p.nb))
-                           : 0u;
-        };
-        uint32_t h0 = header(0), h1 = header(1), h2 = header(2), h3 = header(3);
         bool ok = true;
+        int ms = 0;   // metadata slot of super-block l
+        int etile = (int)(g0 / p.nb), eb = (int)(g0 % p.nb);   // tile and super-block of l
         for (int l = 0; l < L && ok; ++l) {
-            const long long g = g0 + l;
-            const int tile = (int)(g / p.nb);
-            const int n = tile * kPairM + kRows * (int)rank + 32 * quarter + lane;
+            const int n = etile * kPairM + kRows * (int)rank + r;
             const bool nvalid = n < p.N;
-            const uint32_t hd = h0;
-            h0 = h1;
-            h1 = h2;
-            h2 = h3;
-            h3 = header(l + 4);
-            // fold = (d, or 1 when d = 0) * 2^e, as fold_of
-            int e;
-            weight_scale(hd, e);
-            const float dv = (hd & 0x7FFFu) ? __half2float(__ushort_as_half((unsigned short)(hd & 0xFFFFu))) : 1.0f;
-            const float fold = nvalid ? dv * __int_as_float((127 + e) << 23) : 0.0f;
             const int j = l % kAcc;
             if (!(ok = pair_lane0_wait(&tfull[j], (uint32_t)(l / kAcc) & 1, ctx))) break;
+            // (the fold was written before the converters, hence the MMAs, of l could start)
+            const float fold = nvalid ? reinterpret_cast<const float *>(sm + Smem::fold(ms))[r] : 0.0f;
             tc_fence_after();
             uint32_t v[32];
             tmem_ld32(lane_base + (uint32_t)(kN * j), v);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
                 signal_leader(&tempty[j], rank, quarter == 0, kEpiSigTx, sig, tempty_cl0 + 8u * (uint32_t)j);
+                mbar_arrive(&meta_empty[ms]);
+            }
 #pragma unroll
             for (int t = 0; t < kTok; ++t)
                 acc[t] = fmaf(fold, __uint_as_float(v[t]) + __uint_as_float(v[kTok + t]), acc[t]);
             // the tile's last super-block in this range: write its rows
-            const bool last = (l == L - 1) || ((g + 1) % p.nb == 0);
-            if (last) {
+            if (l == L - 1 || eb + 1 == p.nb) {
                 if (nvalid) {
-                    const long long t0g = (long long)tile * p.nb;
+                    const long long t0g = (long long)etile * p.nb;
                     const int pf = pair_of(t0g, p.total, P);
                     const int pl = pair_of(t0g + p.nb - 1, p.total, P);
-                    float *out = (pf == pl) ? p.y + n
-                                            : p.part + ((size_t)(pair - pf) * p.B) * p.N + n;
+                    float *out = (pf == pl) ? p.y + n : p.part + ((size_t)(pair - pf) * p.B) * p.N + n;
 #pragma unroll
                     for (int t = 0; t < kTok; ++t)
                         if (t < p.B) out[(size_t)t * p.N] = acc[t] * __ldg(p.tscale + t);
@@ -484,6 +508,11 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
 #pragma unroll
                 for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
             }
+            if (++eb == p.nb) {
+                eb = 0;
+                ++etile;
+            }
+            if (++ms == kMetaSlots) ms = 0;
         }
     }
     __syncwarp();
