@@ -687,19 +687,17 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
                 xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            // every pass runs (a block past the row is zeros and stores
+            // nothing), so the passes' dependency chains interleave
 #pragma unroll
             for (int u = 0; u < kRegPasses; ++u) {
-                if (kGroupsPerPass * u >= nblk) break;   // CTA-uniform
                 const int b = kGroupsPerPass * u + grp;
                 const float pr = chain(xr[u]);
                 if (sub == 0 && b < nblk) part[b] = pr;
             }
             tree();
 #pragma unroll
-            for (int u = 0; u < kRegPasses; ++u) {
-                if (kGroupsPerPass * u >= nblk) break;
-                pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
-            }
+            for (int u = 0; u < kRegPasses; ++u) pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
         } else if (xregs) {
             // medium input (K <= 20480): x read once into registers; gamma of
             // the first two passes is already there, the rest is loaded while
@@ -714,7 +712,6 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             }
 #pragma unroll
             for (int u = 0; u < kXPasses; ++u) {
-                if (kGroupsPerPass * u >= nblk) break;   // CTA-uniform
                 const int b = kGroupsPerPass * u + grp;
                 const float pr = chain(xr[u]);
                 if (sub == 0 && b < nblk) part[b] = pr;
@@ -733,10 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 g2[u][1] = b < nblk ? __ldg(pg + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < kXPasses - kRegPasses; ++u) {
-                if (kGroupsPerPass * (u + kRegPasses) >= nblk) break;
+            for (int u = 0; u < kXPasses - kRegPasses; ++u)
                 pack(kGroupsPerPass * (u + kRegPasses) + grp, xr[u + kRegPasses], g2[u]);
-            }
         } else {
             for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
                 float4 xv[kUnroll][2];
