@@ -594,25 +594,39 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             return pr;
         };
         float r = 1.0f;
-        // the 256 slots and the pairwise tree over the block sums: r
+        // the 256 slots and the pairwise tree over the block sums: r.  The
+        // tree's levels 128, 64 and 32 run in warp 0 from the slots in shared
+        // memory, in the tree's own association (lane l: level 128 pairs
+        // slots l + 32 j and l + 32 j + 128, level 64 pairs the results for j
+        // and j + 2, level 32 those for j = 0 and 1), then levels 16 .. 1 by
+        // shuffles: the same additions with three barriers instead of seven
+        // (two for rows of at most 256 blocks).
+        // (Rows of at most 256 blocks: a slot holds at most one block, and
+        // +0 + p = p exactly, so warp 0 reads the block sums directly.)
+        const bool one_per_slot = nblk <= 256;
         auto tree = [&]() {
             named_bar(1, kConsumers);
-            if (tid < 256) {
-                float v = 0.0f;
-                for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
-                slot[tid] = v;
-            }
-            named_bar(1, kConsumers);
-#pragma unroll
-            for (int off = 128; off >= 32; off >>= 1) {
-                if (tid < off) slot[tid] = __fadd_rn(slot[tid], slot[tid + off]);
+            if (!one_per_slot) {
+                if (tid < 256) {
+                    float v = 0.0f;
+                    for (int b = tid; b < nblk; b += 256) v = __fadd_rn(v, part[b]);
+                    slot[tid] = v;
+                }
                 named_bar(1, kConsumers);
             }
-            if (tid < 32) {
-                float v = slot[tid];
+            if (warp == 0) {
+                float sl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = lane + 32 * j;
+                    sl[j] = one_per_slot ? (t < nblk ? part[t] : 0.0f) : slot[t];
+                }
+                const float a0 = __fadd_rn(sl[0], sl[4]), a1 = __fadd_rn(sl[1], sl[5]);
+                const float a2 = __fadd_rn(sl[2], sl[6]), a3 = __fadd_rn(sl[3], sl[7]);
+                float v = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, off));
-                if (tid == 0) slot[256] = rms_scale(v, p.K, p.eps);
+                if (lane == 0) slot[256] = rms_scale(v, p.K, p.eps);
             }
             named_bar(1, kConsumers);
             r = slot[256];
