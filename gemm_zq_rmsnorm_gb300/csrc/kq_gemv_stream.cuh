@@ -75,6 +75,8 @@ constexpr int kSeg = 4;                                // max blocks per task
 constexpr int kSmemLimit = 227 * 1024 - 1024;        // dynamic bytes: the static part pads to 1 KB
 constexpr int kMaxK = 32768;                           // one row of segments per warp in the reduction
 constexpr int kMaxMats = kGemvMaxMats;
+constexpr size_t kBalanceMinStage = 32 * 1024;        // smallest stage the row balancing may choose
+constexpr long long kBalanceMinGainPct = 8;            // ... and the least it must take off the busiest CTA
 
 struct StreamParams {
     const uint8_t *W[kMaxMats];
@@ -1036,6 +1038,26 @@ bool plan_stream(StreamParams &p, int K, long long totalN, int sms)
             const long long rounds_r = ((long long)r * p.nseg + kGroups - 1) / kGroups;
             const long long rounds_R = ((long long)p.R * p.nseg + kGroups - 1) / kGroups;
             if ((long long)r * rounds_R > (long long)p.R * rounds_r) p.R = r;
+        }
+        // warp-local rows: the row groups go to the CTAs round-robin, so pick
+        // the R that leaves the fewest rows on the busiest CTA (the launch
+        // ends with it), among stages of at least half the largest and of
+        // 32 KB or more, when that takes 8 % or more off it (smaller stages
+        // cost more per byte than a small gain in balance); a row's
+        // summation order does not depend on R
+        if (p.wl) {
+            auto load = [&](int r) { return ((totalN + r - 1) / r + sms - 1) / sms * r; };
+            const long long full = load(rmax);
+            long long best = full;
+            int rb = rmax;
+            const int rlo = max((rmax + 1) / 2, (int)((kBalanceMinStage + p.rowbytes - 1) / p.rowbytes));
+            for (int r = rmax - 1; r >= rlo; --r)
+                if (load(r) < best) {
+                    best = load(r);
+                    rb = r;
+                }
+            // (measured: smaller stages pay off only for a clear gain)
+            if (best * 100 <= full * (100 - kBalanceMinGainPct)) p.R = rb;
         }
         p.P = 1;
         p.CB = p.nb;
