@@ -694,30 +694,41 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
         };
         if (regs) {
             // short input: x read once into registers (gamma is already there),
-            // one round trip to memory after the wait instead of two
-            float4 xr[kRegPasses][2];
+            // one round trip to memory after the wait instead of two.  One pass
+            // or two (a compile-time count, so both passes of a two-pass row run
+            // without a branch between them and their chains interleave, and a
+            // one-pass row, as in small models, pays for no pass of zeros).
+            auto short_prologue = [&](auto npc) {
+                constexpr int NP = decltype(npc)::value;
+                float4 xr[NP][2];
 #pragma unroll
-            for (int u = 0; u < kRegPasses; ++u) {
-                const int b = kGroupsPerPass * u + grp;
-                const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
-                xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
-                xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            // every pass runs (a block past the row is zeros and stores
-            // nothing), so the passes' dependency chains interleave
+                for (int u = 0; u < NP; ++u) {
+                    const int b = kGroupsPerPass * u + grp;
+                    const float4 *px = reinterpret_cast<const float4 *>(p.x + 32 * b) + 2 * sub;
+                    xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-            for (int u = 0; u < kRegPasses; ++u) {
-                const int b = kGroupsPerPass * u + grp;
-                const float pr = chain(xr[u]);
-                if (sub == 0 && b < nblk) part[b] = pr;
-            }
-            tree();
+                for (int u = 0; u < NP; ++u) {
+                    const int b = kGroupsPerPass * u + grp;
+                    const float pr = chain(xr[u]);
+                    if (sub == 0 && b < nblk) part[b] = pr;
+                }
+                tree();
 #pragma unroll
-            for (int u = 0; u < kRegPasses; ++u) pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
+                for (int u = 0; u < NP; ++u) pack(kGroupsPerPass * u + grp, xr[u], gr[u]);
+            };
+            static_assert(kRegPasses == 2, "one-pass and two-pass forms");
+            if (nblk <= kGroupsPerPass)   // CTA-uniform
+                short_prologue(std::integral_constant<int, 1>{});
+            else
+                short_prologue(std::integral_constant<int, 2>{});
         } else if (xregs) {
             // medium input (K <= 20480): x read once into registers; gamma of
             // the first two passes is already there, the rest is loaded while
-            // those are packed -- two round trips after the wait instead of four
+            // those are packed -- two round trips after the wait instead of
+            // four.  Every pass runs (a block past the row is zeros and stores
+            // nothing), so the passes' dependency chains interleave.
             float4 xr[kXPasses][2];
 #pragma unroll
             for (int u = 0; u < kXPasses; ++u) {
