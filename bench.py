@@ -392,7 +392,39 @@ def capture(torch, fn, stream):
     return g
 
 
+def time_steps(torch, run, R, steps, warmup, stream):
+    """ms per step over exactly `steps` timed steps (after at least `warmup`
+    untimed ones), step i on weight copy i % R.  Consecutive steps are
+    captured together, S = R * ceil(8 / R) of them per CUDA graph (a whole
+    number of passes over the copies), so they run without a graph-launch
+    gap between them, as a forward pass captured once would; a remainder
+    graph makes the count exact.  Each step is still a full pass of the
+    path over its own weight copy."""
+    S = R * max(1, -(-8 // R))
+    full = capture(torch, lambda: [run(i % R) for i in range(S)], stream)
+    tail_n = steps % S
+    tail = capture(torch, lambda: [run(i % R) for i in range(tail_n)], stream) if tail_n else None
+    for _ in range(max(1, -(-warmup // S))):
+        full.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps // S):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
 def bench_workload(torch, wl, steps, warmup, stream):
+    if wl.B == 1:
+        # decode: several consecutive steps per graph
+        return time_steps(torch, wl.run, wl.R, steps, warmup, stream), None
+    # batched steps (each several hundred microseconds to a millisecond):
+    # one graph per step
     graphs = [capture(torch, lambda r=r: wl.run(r), stream) for r in range(wl.R)]
     ms = time_graphs(torch, graphs, steps, warmup, stream)
     return ms, graphs
