@@ -976,23 +976,42 @@ def main():
 
 def e2e(torch, wl, steps, warmup):
     """Same metric through the public API with host buffers: each step copies
-    the step's activations from pinned host memory, runs every call of the path
-    and reads every output back to pinned host memory.  Measured two ways: the
+    the step's activations from pinned host memory (one copy: the inputs share
+    one device buffer), runs every call of the path and reads every output back
+    to pinned host memory (one copy).  Measured two ways: the
     step replayed from a CUDA graph holding the copies and the calls (how an
     engine runs a decode step; the copies still move every byte every step),
     and eagerly from Python (no graph).  The graph figure is the line's value."""
-    hx = {k: wl.x[k].cpu().pin_memory() for k in wl.x}
-    hy = {p: (wl.y[p][0].cpu().pin_memory(), None if wl.y[p][1] is None else wl.y[p][1].cpu().pin_memory())
-          for p in wl.y}
+    # every input of the step in one device buffer and every output in
+    # another (the calls get views of them, as an engine that owns its
+    # activation buffers would), so a step moves them with one copy each way
+    def gather(tensors):
+        flat = torch.empty(sum(t.numel() for t in tensors), dtype=torch.float32, device="cuda")
+        views, o = [], 0
+        for t in tensors:
+            v = flat[o:o + t.numel()].view_as(t)
+            v.copy_(t)
+            views.append(v)
+            o += t.numel()
+        return flat, views
+
+    keys = list(wl.x)
+    dx, xv = gather([wl.x[k] for k in keys])
+    for k, v in zip(keys, xv):
+        wl.x[k] = v
+    outs = [(p, j) for p in wl.y for j in (0, 1) if wl.y[p][j] is not None]
+    dy, yv = gather([wl.y[p][j] for p, j in outs])
+    ynew = {p: [None, None] for p in wl.y}
+    for (p, j), v in zip(outs, yv):
+        ynew[p][j] = v
+    wl.y = {p: tuple(v) for p, v in ynew.items()}
+    hx = dx.cpu().pin_memory()
+    hy = torch.empty(dy.numel(), dtype=torch.float32).pin_memory()
 
     def step(r, s):
-        for k in hx:
-            wl.x[k].copy_(hx[k], non_blocking=True)
+        dx.copy_(hx, non_blocking=True)
         wl.run(r, stream=s)
-        for p in hy:
-            hy[p][0].copy_(wl.y[p][0], non_blocking=True)
-            if hy[p][1] is not None:
-                hy[p][1].copy_(wl.y[p][1], non_blocking=True)
+        hy.copy_(dy, non_blocking=True)
 
     def timed(run_one):
         for i in range(warmup):
