@@ -751,7 +751,9 @@ cudaError_t launch_rmsnorm_q8_1(const float *x, const float *gamma, int B, int K
     // accesses); otherwise one thread per block, no staging
     if (nblk <= kStagedMaxBlocks)
         return launch_staged(x, gamma, B, K, eps, out.qs, dq, sq, SplitOut{nullptr, nullptr, nullptr, nullptr}, st);
-    if (B >= kRowsMinTokens && nblk <= kMaxThreads)
+    // (the row-staged kernel's eight-lane groups need K % 256 == 0: a warp's
+    // four blocks are then all in the row or all past it)
+    if (B >= kRowsMinTokens && nblk <= kMaxThreads && nblk % 8 == 0)
         return launch_rmsnorm_q8_1_split(x, gamma, B, K, eps, &out, nullptr, nullptr, nullptr, nullptr, st);
     if (nblk <= kMaxBlocks) {
         int threads = nblk < kMaxThreads ? (nblk + 31) / 32 * 32 : kMaxThreads;
@@ -767,6 +769,9 @@ cudaError_t launch_rmsnorm_q8_1_split(const float *x, const float *gamma, int B,
 {
     const int nblk = K / 32;
     if (nblk > kMaxThreads) return cudaErrorInvalidValue;   // K > 32768
+    // the split's 8-row stores, and the row-staged kernel's eight-lane
+    // groups, need whole groups of eight blocks (K % 256 == 0)
+    if ((hi != nullptr || nblk > kStagedMaxBlocks) && nblk % 8 != 0) return cudaErrorInvalidValue;
     if (nblk <= kStagedMaxBlocks)
         return launch_staged(x, gamma, B, K, eps, out ? out->qs : nullptr,
                              out ? reinterpret_cast<__half *>(out->d) : nullptr,
