@@ -66,6 +66,7 @@ template <> struct Fmt<kFmtQ6K> { static constexpr int kBytes = 210; };
 
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
+static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "warp round-robin by mask");
 constexpr int kThreads = kConsumers + 32;
 constexpr int kStages = 3;
 constexpr int kStageMax = 64 * 1024;
@@ -812,6 +813,12 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const int G = warp * 8 + (lane >> 2);   // task group, 128 per CTA
     const int pp = lane & 3;                // Q8_1 block pair 2pp, 2pp+1
     const unsigned gmask = 0xFu << (4 * (lane >> 2));
+    // warp-local rows: nseg (a power of two, 1..8) task groups per row, so
+    // 8 / nseg = 2^(3 - wl_lg) rows per slot of eight groups; this lane's
+    // segment and row within a slot (launch constants, hoisted out of the
+    // stage loop)
+    const int wl_lg = p.wl ? __ffs(p.nseg) - 1 : 0;
+    const int wl_sg = (lane >> 2) & (p.nseg - 1), wl_sr = (lane >> 2) >> wl_lg;
     uint32_t it = 0;
     uint32_t rr = 0;                        // warp-local rows: slots handed out so far
     for (int g = blockIdx.x; g < p.total_groups; g += gridDim.x) {
@@ -882,12 +889,11 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 // y; each warp releases the stage on its own.  Slots of 8/nseg
                 // rows go to the warps round-robin, continuing across stages.
                 if (!ok) return;
-                const int rpw = 8 / nseg;
-                const int nslots = (nrows + rpw - 1) / rpw;
-                const int gi = lane >> 2, sg = gi % nseg, sr = gi / nseg;
-                const int s0 = (warp - (int)(rr % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+                const int nslots = (nrows + (8 >> wl_lg) - 1) >> (3 - wl_lg);
+                const int sg = wl_sg;
+                const int s0 = (int)((uint32_t)(warp - (int)rr) & (kConsumerWarps - 1));
                 for (int sl = s0; sl < nslots; sl += kConsumerWarps) {
-                    const int r = sl * rpw + sr;   // row within the stage
+                    const int r = (sl << (3 - wl_lg)) + wl_sr;   // row within the stage
                     const bool live = r < nrows;
                     const uint8_t *rowp = stage + (size_t)(live ? r : 0) * rowblk * kBytes;
                     float c[NT];
