@@ -152,7 +152,7 @@ struct SmemLayout {
         act_sum = align_up(act_ds + (size_t)nt * ads_bytes(K), 16);
         contrib = align_up(act_sum + (sums ? (size_t)nt * K / 4 : 0), 16);
         bars = align_up(contrib + (size_t)nt * kStages * kMaxBlk * 4, 8);
-        total = bars + 2 * kStages * 8;
+        total = bars + (2 * kStages + 1) * 8;   // full, empty, inputs-issued
     }
 };
 
@@ -447,6 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     float *contrib = reinterpret_cast<float *>(smem + L.contrib);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kStages;
+    uint64_t *xbar = empty + kStages;      // every consumer warp has issued its input loads
     __shared__ volatile int abort_s;
 
     const int tid = threadIdx.x;
@@ -457,12 +458,26 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     const int tds = p.K / 64;                  // and of its d8/s8 pairs (uint2 units)
     const int tas = p.K / 64;                  // and of its 8-code sums (uint4 units)
     const uint64_t wlim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+    // fused input: RMSNorm prologue forms (see the consumers)
+    constexpr int kGroupsPerPass = kConsumers / 4;   // blocks of 32 values per prologue pass
+    constexpr int kRegPasses = 2;                    // x and gamma of up to this many passes stay in registers
+    constexpr int kXPasses = 5;                      // x alone of up to this many passes stays in registers
+    const bool regs = p.x != nullptr && !p.silu && (p.K >> 5) <= kRegPasses * kGroupsPerPass;
+    // Stages the producer issues before the consumers' input loads are out:
+    // the input (x, or the Q8_1 rows) is read after the programmatic-launch
+    // wait, and a request issued behind the ring's first copies waits for
+    // them.  One stage when the prologue reads its input once; two when it
+    // loads again after its first loads (gamma of the later passes of a long
+    // row, or x and gamma pass by pass), so that its second round trip has
+    // fewer copies ahead of it.
+    const uint32_t early = (p.x == nullptr || regs) ? 1u : 2u;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(xbar, kConsumerWarps);
         abort_s = 0;
         fence_mbar_init();
         pdl_launch_dependents();
@@ -481,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 for (int pc = 0; pc < p.P; ++pc, ++it) {
                     const uint32_t slot = it % kStages, round = it / kStages;
                     if (p.withhold > 0 && it == (uint32_t)(p.withhold - 1)) return;
+                    if (it == early && !mbar_wait_for(xbar, 0, p.status, wlim)) return;
                     if (round > 0 && !mbar_wait_for(&empty[slot], (round & 1) ^ 1, p.status, wlim)) return;
                     const size_t bytes = (p.P == 1) ? (size_t)rows * p.rowbytes
                                                     : (size_t)min(p.CB, p.nb - pc * p.CB) * kBytes;
@@ -518,16 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
     }
 
     // ---------------------------------------------------------- consumers
-    // The producer streams weights (written by no kernel) from the start; the
-    // activations may come from the previous kernel on the stream, and y may
-    // still be read by it: wait for that kernel before touching either.  The
+    // The producer streams weights (written by no kernel) from the start (its
+    // first one or two stages; the rest once every consumer warp has issued
+    // its input loads); the activations may come from the previous kernel on
+    // the stream, and y may still be read by it: wait for that kernel before
+    // touching either.  The
     // RMSNorm weight gamma is a weight too: when the input is short enough to
     // stay in registers, it is loaded before the wait.
-    constexpr int kGroupsPerPass = kConsumers / 4;   // blocks of 32 values per prologue pass
-    constexpr int kRegPasses = 2;                    // x and gamma of up to this many passes stay in registers
-    constexpr int kXPasses = 5;                      // x alone of up to this many passes stays in registers
     const int grp = tid >> 2, sub = tid & 3;
-    const bool regs = p.x != nullptr && !p.silu && (p.K >> 5) <= kRegPasses * kGroupsPerPass;
     const bool xregs = p.x != nullptr && !p.silu && !regs && (p.K >> 5) <= kXPasses * kGroupsPerPass;
     float4 gr[kRegPasses][2];
     if (regs || xregs) {
@@ -540,7 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
         }
     }
     pdl_wait();
+    // this warp's input loads are issued: the producer may stream the rest
+    auto inputs_out = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+    };
     if (p.x == nullptr) {
+        inputs_out();
         // stage the activation rows: codes with the 80-byte group stride,
         // scales and sums as they are (pairs of binary16 per 32-bit word)
         for (int t = 0; t < p.ntok; ++t) {
@@ -709,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                     xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
                     xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                inputs_out();
 #pragma unroll
                 for (int u = 0; u < NP; ++u) {
                     const int b = kGroupsPerPass * u + grp;
@@ -738,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
                 xr[u][0] = b < nblk ? __ldg(px) : make_float4(0.f, 0.f, 0.f, 0.f);
                 xr[u][1] = b < nblk ? __ldg(px + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            inputs_out();
 #pragma unroll
             for (int u = 0; u < kXPasses; ++u) {
                 const int b = kGroupsPerPass * u + grp;
@@ -761,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) kq_gemv_stream_kernel(const Strea
             for (int u = 0; u < kXPasses - kRegPasses; ++u)
                 pack(kGroupsPerPass * (u + kRegPasses) + grp, xr[u + kRegPasses], g2[u]);
         } else {
+            inputs_out();
             for (int base = 0; base < (p.silu ? 0 : nblk); base += kGroupsPerPass * kUnroll) {
                 float4 xv[kUnroll][2];
 #pragma unroll
