@@ -198,7 +198,7 @@ f16_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_con
         for (int u = pair; u < p.units; u += npairs, ++j) {
             const Unit U = unit_of(p, u, rank);
             const int buf = j & 1;
-            if (!pair_lane0_wait(&tfull[buf], (uint32_t)(j >> 1) & 1, ctx)) break;
+            if (!pair_warp_wait(&tfull[buf], (uint32_t)(j >> 1) & 1, ctx)) break;
             tc_fence_after();
             const int n = U.row0 + 32 * quarter + lane;   // weight row
             const bool nvalid = n < p.N;

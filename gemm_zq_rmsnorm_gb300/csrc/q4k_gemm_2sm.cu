@@ -314,10 +314,10 @@ q4k_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_hi, const __grid_co
                 const int k = q % kASlots, round = q / kASlots;
                 if (b != cur_b) {
                     if (cur_b >= 0 && lane == 0) mbar_arrive(&raw_empty[cur_b % kRawSlots]);
-                    if (!(ok = pair_lane0_wait(&raw_full[b % kRawSlots], (uint32_t)(b / kRawSlots) & 1, ctx))) break;
+                    if (!(ok = pair_warp_wait(&raw_full[b % kRawSlots], (uint32_t)(b / kRawSlots) & 1, ctx))) break;
                     cur_b = b;
                 }
-                if (round > 0 && !(ok = pair_lane0_wait(&aempty[k], (round - 1) & 1, ctx))) break;
+                if (round > 0 && !(ok = pair_warp_wait(&aempty[k], (round - 1) & 1, ctx))) break;
                 tc_fence_after();
                 const uint8_t *raw = sm + Smem::raw(b % kRawSlots) + (size_t)r * kQ4KBlockBytes;
                 const uint32_t col = lane_base + kACols * k;

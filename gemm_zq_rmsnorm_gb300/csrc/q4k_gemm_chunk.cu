@@ -310,7 +310,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         bool ok = true;
         for (int l = 0; l < L && ok; ++l) {
             const int ts = l % kTokSB;
-            if (l >= kTokSB && !(ok = pair_lane0_wait(&tok_empty[ts], ((l / kTokSB) - 1) & 1, ctx))) break;
+            if (l >= kTokSB && !(ok = pair_warp_wait(&tok_empty[ts], ((l / kTokSB) - 1) & 1, ctx))) break;
             // the odd CTA's forwarded signal, counted in bytes
             if (rank == 0 && lane == 0) mbar_expect_tx(&tok_full[ts], kTokSigTx);
             const int b = (int)((g0 + l) % p.nb);
@@ -357,7 +357,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
             const uint32_t tfull_cl0 = cluster_addr(smem_u32(&tok_full[0]), 0);
             for (int l = 0; l < L; ++l) {
                 const int ts = l % kTokSB;
-                if (!pair_lane0_wait(&tok_land[ts], (uint32_t)(l / kTokSB) & 1u, ctx)) break;
+                if (!pair_warp_wait(&tok_land[ts], (uint32_t)(l / kTokSB) & 1u, ctx)) break;
                 fence_async_smem();   // the MMA reads the copies through the async proxy
                 if (lane == 0) st_async_signal(sig, tfull_cl0 + 8u * (uint32_t)ts);
             }
@@ -418,9 +418,9 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         uint32_t rph = 0, aph = 0;
         static_assert(kMetaSlots == kRawSlots, "one counter for both rings");
         for (int l = 0; l < L && ok; ++l) {
-            if (!(ok = pair_lane0_wait(&raw_full[rs], rph, ctx))) break;
-            if (!(ok = pair_lane0_wait(&meta_full[rs], rph, ctx))) break;   // the rows' scales
-            if (l >= kASB && !(ok = pair_lane0_wait(&aempty[a], aph ^ 1u, ctx))) break;
+            if (!(ok = pair_warp_wait(&raw_full[rs], rph, ctx))) break;
+            if (!(ok = pair_warp_wait(&meta_full[rs], rph, ctx))) break;   // the rows' scales
+            if (l >= kASB && !(ok = pair_warp_wait(&aempty[a], aph ^ 1u, ctx))) break;
             tc_fence_after();
             const uint32_t s01 =
                 *reinterpret_cast<const uint32_t *>(sm + Smem::scales(rs) + (size_t)r * kScaleRow + 4 * st);
@@ -445,8 +445,8 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
         int rs = 0;   // raw and metadata slot (phase rph)
         uint32_t rph = 0;
         for (int l = 0; l < L && ok; ++l) {
-            if (!(ok = pair_lane0_wait(&raw_full[rs], rph, ctx))) break;
-            if (l >= kMetaSlots && !(ok = pair_lane0_wait(&meta_empty[rs], rph ^ 1u, ctx))) break;
+            if (!(ok = pair_warp_wait(&raw_full[rs], rph, ctx))) break;
+            if (l >= kMetaSlots && !(ok = pair_warp_wait(&meta_empty[rs], rph ^ 1u, ctx))) break;
             const float f = decode_row(sm + Smem::raw(rs) + (size_t)r * kQ4KBlockBytes,
                                        sm + Smem::scales(rs) + (size_t)r * kScaleRow,
                                        sm + Smem::amin(rs) + (size_t)r * 32, r);
@@ -478,7 +478,7 @@ q4k_gemm_chunk_kernel(const __grid_constant__ CUtensorMap tmap_w, const ChunkPar
             const int n = etile * kPairM + kRows * (int)rank + r;
             const bool nvalid = n < p.N;
             const int j = l % kAcc;
-            if (!(ok = pair_lane0_wait(&tfull[j], (uint32_t)(l / kAcc) & 1, ctx))) break;
+            if (!(ok = pair_warp_wait(&tfull[j], (uint32_t)(l / kAcc) & 1, ctx))) break;
             // (the fold was written before the converters, hence the MMAs, of l could start)
             const float fold = nvalid ? reinterpret_cast<const float *>(sm + Smem::fold(ms))[r] : 0.0f;
             tc_fence_after();
