@@ -32,7 +32,7 @@ EXPORTS = ("zq_rmsnorm_q8_1", "zq_q4k_gemv", "zq_q4k_gemv_pair", "zq_q4k_gemm",
            "zq_q5k_gemm", "zq_q6k_gemm", "zq_q5k_gemv", "zq_q6k_gemv", "zq_rmsnorm_q6k_gemv",
            "zq_q5k_bytes", "zq_q6k_bytes", "zq_debug_stream_plan", "zq_debug_peak_probe",
            "zq_debug_wait_expiry", "zq_q8_1_dequant_f16", "zq_f16_gemm_workspace_bytes", "zq_f16_gemm",
-           "zq_rmsnorm_q4k_gemm")
+           "zq_rmsnorm_q4k_gemm", "zq_copy")
 
 
 class ZQError(RuntimeError):
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "zq_rmsnorm_q4k_gemv": ([P, P, f, i, i, P, P, P, ctypes.POINTER(_Q8), P, sz, P], i),
         "zq_q5k_gemm": ([P, i, i, _Q8, i, P, P], i),
         "zq_q6k_gemm": ([P, i, i, _Q8, i, P, P], i),
+        "zq_copy": ([P, P, sz, P], i),
         "zq_q5k_gemv": ([P, i, i, _Q8, P, P], i),
         "zq_q6k_gemv": ([P, i, i, _Q8, P, P], i),
         "zq_rmsnorm_q6k_gemv": ([P, P, f, i, P, i, P, ctypes.POINTER(_Q8), P], i),
@@ -382,6 +383,18 @@ def debug_stream_plan(wtype: int, ntok: int, K: int, total_rows: int, sms: int =
     _check(load().zq_debug_stream_plan(wtype, ntok, K, total_rows, sms, ctypes.cast(out, ctypes.c_void_p)))
     keys = ("R", "P", "CB", "nseg", "wl", "stage_alloc", "smem", "rowbytes")
     return dict(zip(keys, list(out)))
+
+
+def copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy src into dst (same byte size, both contiguous) with the GPU's SMs
+    (zq_copy): each may live on this GPU or in pinned host memory."""
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy: dst and src must be contiguous")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("copy: dst and src differ in size")
+    _check(load().zq_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)))
+    return dst
 
 
 def device_status(clear: bool = False) -> int:

@@ -74,6 +74,28 @@ int check_device(int *dev_out)
     return ZQ_OK;
 }
 
+// The device address of p when the device may access it: memory of this
+// device (or managed memory), or pinned host memory mapped into the device's
+// address space; anything else is refused before a kernel could touch it.
+int device_address(const void *p, int dev, void **out, const char *what)
+{
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ZQ_ERR_ARG, "%s: pointer unknown to CUDA (%s)", what, cudaGetErrorString(e));
+    }
+    if ((a.type == cudaMemoryTypeDevice && a.device == dev) || a.type == cudaMemoryTypeManaged) {
+        *out = a.devicePointer ? a.devicePointer : const_cast<void *>(p);
+        return ZQ_OK;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+        *out = a.devicePointer;
+        return ZQ_OK;
+    }
+    return fail(ZQ_ERR_ARG, "%s: neither memory of device %d nor pinned host memory mapped into it", what, dev);
+}
+
 int launched(cudaError_t e, const char *what)
 {
     if (e != cudaSuccess) return fail(ZQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -615,6 +637,18 @@ int zq_device_status(unsigned int *flags, int clear)
         e = cudaMemcpyToSymbol(g_zq_device_status, &zero, sizeof zero);
     }
     return launched(e, "zq_device_status");
+}
+
+int zq_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (bytes == 0) return ZQ_OK;
+    if (!dst || !src) return fail(ZQ_ERR_ARG, "zq_copy: null pointer");
+    int dev, st;
+    if ((st = check_device(&dev))) return st;
+    void *d = nullptr, *s = nullptr;
+    if ((st = device_address(dst, dev, &d, "zq_copy: dst"))) return st;
+    if ((st = device_address(src, dev, &s, "zq_copy: src"))) return st;
+    return launched(launch_copy(d, s, bytes, g_sms[dev], (cudaStream_t)stream), "zq_copy");
 }
 
 int zq_debug_q4k_isums(const void *W, int N, int K, zq_q8_1 a, int B, int32_t *isums, int path,

@@ -76,6 +76,8 @@ cudaError_t launch_silu_mul_q8_1(const float *g, const float *u, int B, int K, z
 // Throughput probes (kind 0: dp4a, 1: mma.sync m16n8k32 s8, 2: tcgen05 kind::f16
 // 128 x 256 x 16); sink: device ints, one per thread (256 per block, 128 for kind 2).
 cudaError_t launch_peak_probe(int kind, int blocks, int iters, int *sink, cudaStream_t st);
+// Copy by the SMs (zq_copy): dst and src are device addresses.
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int sms, cudaStream_t st);
 
 // Launch with programmatic dependent launch: the kernel may start while the
 // previous kernel on the stream is still running.  Every kernel launched this

@@ -437,6 +437,23 @@ ZQ_API int zq_debug_peak_probe(int kind, int blocks, int iters, void *sink, void
 ZQ_API int zq_debug_wait_expiry(const void *W, int N, int K, zq_q8_1 a, float *y, int withhold_stage,
                                 unsigned int wait_us, int ctas, void *stream);
 
+/*
+ * Copy `bytes` bytes from src to dst with the GPU's SMs, on `stream`, ordered
+ * after the stream's previous kernel (no counterpart on the pages: the host <->
+ * device plumbing of a decode step, whose activations are a few hundred KB a
+ * step and for which a copy engine's start-up latency dominates).  Each
+ * pointer may be device memory of the current device, or pinned host memory
+ * that the driver maps into the device's address space (cudaHostAlloc,
+ * cudaHostRegister; on a Grace-coupled GPU the SMs reach it over the
+ * chip-to-chip link).  Both are checked with cudaPointerGetAttributes before
+ * anything runs: any other pointer (pageable host memory, another device's
+ * memory, an unknown address) returns ZQ_ERR_ARG.  The caller owns both
+ * buffers, which must hold `bytes` bytes and must not overlap; any alignment
+ * works (16-byte aligned pointers copy 16 bytes per access).  bytes = 0 does
+ * nothing and returns ZQ_OK.
+ */
+ZQ_API int zq_copy(void *dst, const void *src, size_t bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
