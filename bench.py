@@ -93,6 +93,27 @@ def layer_algo_bytes(shapes, B, layers=1, extra=()):
     return b
 
 
+def rotation_copies(shapes, layers=1, extra=(), min_rotation_bytes=3 * L2_BYTES):
+    """Distinct weight copies a benchmark rotates through so that each step
+    reads its weights from HBM, not from L2."""
+    per_copy = (sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in shapes) * layers
+                + sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in extra))
+    return max(1, -(-min_rotation_bytes // per_copy))
+
+
+def decode_config(name, shapes, layers=1, extra=(), R=None, fused=True, prefetch=False):
+    """The `config` of a B = 1 decode line (both arms print the same one)."""
+    R = rotation_copies(shapes, layers, extra) if R is None else R
+    return {"workload": name, "B": 1, "hidden": layer_inputs(shapes)[0][1],
+            "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in list(shapes) + list(extra)],
+            "layers": layers, "weight_copies_rotated": R,
+            "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
+                            + ("; each launch pulls the next one's weights into L2" if prefetch else "")
+                            if fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
+            "l2": f"inputs larger than L2: {R} rotating weight copies of the step",
+            "algorithmic_bytes_per_step": int(layer_algo_bytes(shapes, 1, layers, extra))}
+
+
 def proj_bytes(K, N, B):
     """Algorithmic bytes of one projection: weights once, Q8_1 input, fp32 y."""
     return N * K * 144 // 256 + B * K * (1 + 4 / 32) + B * N * 4
@@ -129,9 +150,7 @@ class LayerWorkload:
         self.a = {k: zq.empty_q8_1(B, K, dev) for k, K in self.inputs_K}
         # weights: generate once per shape, clone to distinct device copies
         self.layer_shapes = list(shapes)
-        per_copy = (sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in self.layer_shapes) * layers
-                    + sum(N * K * 144 // 256 * (2 if p else 1) for (_, K, N, p) in self.extra))
-        self.R = max(1, -(-min_rotation_bytes // per_copy))
+        self.R = rotation_copies(self.layer_shapes, layers, self.extra, min_rotation_bytes)
         self.layers = layers
         base = {}
         for si, (pname, K, N, paired) in enumerate(self.shapes):
@@ -710,14 +729,7 @@ def decode_record(torch, wl, steps, warmup, stream, pk, local_rank, max_over_ran
     achieved = dalg / (dms * 1e-3) / 1e9
     return {
         "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
-        "config": {"workload": wl.name, "B": 1, "hidden": wl.inputs_K[0][1],
-                   "projections": [f"{p} {K}->{N}{' x2' if pr else ''}" for (p, K, N, pr) in wl.shapes],
-                   "layers": wl.layers, "weight_copies_rotated": wl.R,
-                   "decode_path": ("fused: one launch per layer input (RMSNorm + Q8_1 in the mat-vec kernel)"
-                                   + ("; each launch pulls the next one's weights into L2" if wl.prefetch else "")
-                                   if wl.fused else "two-step: RMSNorm+Q8_1, then one launch per projection"),
-                   "l2": f"inputs larger than L2: {wl.R} rotating weight copies of the step",
-                   "algorithmic_bytes_per_step": int(wl.algo_bytes())},
+        "config": decode_config(wl.name, wl.layer_shapes, wl.layers, wl.extra, wl.R, wl.fused, wl.prefetch),
         "roofline": {"bound": "hbm",
                      "kernel": (f"rmsnorm_q4k_gemv {dK}->{dN}{' x2 (gate+up)' if dp else ''}" if wl.fused
                                 else f"q4k_gemv{'_pair' if dp else ''} {dK}->{dN}"),
@@ -1075,7 +1087,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-            "data": "synthetic", "config": {"workload": "decode-27b-layer", "B": 1},
+            "data": "synthetic", "config": decode_config("decode-27b-layer", shapes),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"per step: {sample}, scaled to a full step"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
