@@ -41,9 +41,11 @@
 // With x and gamma instead of Q8_1 codes (one token) the consumers first
 // compute RMSNorm and the Q8_1 packing of x themselves, in the canonical order
 // of the RMSNorm+Q8_1 kernel (same bytes), straight into the shared-memory
-// staging, while the producer already streams weights: the normalised input
-// never goes through HBM and the separate launch disappears.  The same
-// prologue forms silu(gate) * up instead for the down projection.
+// staging, while the producer already streams weights (one or two stages
+// before the consumers' input loads are out, the rest after, so those loads
+// do not queue behind the ring's copies): the normalised input never goes
+// through HBM and the separate launch disappears.  The same prologue forms
+// silu(gate) * up instead for the down projection.
 //
 // With NT > 1 the CTA stages NT tokens and every decoded weight is used for
 // all of them (chunked-prefill batches of up to four tokens).
